@@ -1,0 +1,227 @@
+"""Seeded synthetic inputs for the block-scaled GEMM workloads.
+
+This module holds random draws and workload recipes only: shapes, value
+distributions, expert routing counts and the 256-row padding of each expert's
+row range.  It contains none of the method's arithmetic (no quantisation, no
+scale-factor layout, no GEMM, no epilogue); the float64 oracle and the CUDA
+library each derive everything else from the fp32 tensors produced here.
+
+Every value is a pure function of ``(seed, stream, flat index)``: the flat range
+of a tensor is cut into chunks of ``CHUNK`` elements and chunk ``c`` is drawn by
+its own PCG64 generator seeded with ``SeedSequence([seed, stream, c])``.  So a
+few rows of a multi-gigabyte operand can be regenerated alone (for sampled
+parity checks) and the full tensor can be filled by several threads with the
+same result.
+
+The five workloads follow the shapes named by the pages' dense GEMM + Amax and
+grouped GEMM + sReLU operations (both "Shapes" sections); the recipes
+(distributions, routing, padding) are the ones stated for each workload below.
+"""
+from __future__ import annotations
+
+import concurrent.futures as _cf
+import dataclasses
+import math
+import os
+
+import numpy as np
+
+CHUNK = 1 << 20
+
+# stream ids: one per tensor kind so tensors never share random numbers
+S_A, S_B, S_ALPHA, S_PROB, S_ROUTE = 1, 2, 3, 4, 5
+
+PAD = 256  # expert row ranges are padded to multiples of 256 rows
+
+
+def _chunk_rng(seed: int, stream: int, chunk: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, stream, chunk])))
+
+
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def normal_f32(seed: int, stream: int, start: int, stop: int) -> np.ndarray:
+    """Standard normal float32 values for flat indices ``[start, stop)``."""
+    n = stop - start
+    out = np.empty(n, dtype=np.float32)
+    if n <= 0:
+        return out
+    c0, c1 = start // CHUNK, (stop - 1) // CHUNK
+
+    def fill(c: int) -> None:
+        lo, hi = c * CHUNK, (c + 1) * CHUNK
+        buf = _chunk_rng(seed, stream, c).standard_normal(CHUNK, dtype=np.float32)
+        a, b = max(lo, start), min(hi, stop)
+        out[a - start:b - start] = buf[a - lo:b - lo]
+
+    chunks = range(c0, c1 + 1)
+    if len(chunks) == 1:
+        fill(c0)
+    else:
+        with _cf.ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(fill, chunks))
+    return out
+
+
+def uniform_f32(seed: int, stream: int, n: int, lo: float, hi: float) -> np.ndarray:
+    """``n`` float32 values uniform in [lo, hi) (one generator; n is small)."""
+    u = _chunk_rng(seed, stream, 0).random(n, dtype=np.float32)
+    return (np.float32(lo) + np.float32(hi - lo) * u).astype(np.float32)
+
+
+# ----------------------------------------------------------------------------
+# dense workloads
+
+
+@dataclasses.dataclass(frozen=True)
+class Dense:
+    """Batched dense block-scaled GEMM + amax workload: A (L,M,K), B (L,N,K)."""
+    name: str
+    m: int
+    n: int
+    k: int
+    l: int
+    fmt: str            # "mxfp8" (E4M3 codes, E8M0 scales, v=32) or "nvfp4" (E2M1, UE4M3, v=16)
+    c_dtype: str        # "f32" or "bf16"
+    boost_every: int = 0  # if >0: K-blocks kb with kb % boost_every == boost_every-1 of A are x2^6
+    seed: int = 0
+
+    @property
+    def sf_vec(self) -> int:
+        return 32 if self.fmt == "mxfp8" else 16
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.m * self.n * self.k * self.l
+
+    def a_rows(self, rows: np.ndarray | None = None) -> np.ndarray:
+        """fp32 A as (L, M, K); with ``rows`` (flat indices l*M+m) only those rows."""
+        return self._rows(S_A, self.m, rows, boost=True)
+
+    def b_rows(self, rows: np.ndarray | None = None) -> np.ndarray:
+        return self._rows(S_B, self.n, rows, boost=False)
+
+    def _rows(self, stream, nrows, rows, boost):
+        k = self.k
+        if rows is None:
+            x = normal_f32(self.seed, stream, 0, self.l * nrows * k).reshape(self.l, nrows, k)
+        else:
+            x = np.stack([normal_f32(self.seed, stream, int(r) * k, (int(r) + 1) * k) for r in rows])
+        if boost and self.boost_every:
+            v, e = self.sf_vec, self.boost_every
+            kb = np.arange(k) // v
+            x[..., (kb % e) == e - 1] *= np.float32(64.0)
+        return x
+
+
+# ----------------------------------------------------------------------------
+# grouped (MoE) workloads
+
+
+@dataclasses.dataclass(frozen=True)
+class Grouped:
+    """Grouped block-scaled GEMM + sReLU workload over 256-padded expert row ranges."""
+    name: str
+    experts: int
+    k: int
+    n: int
+    routed_rows: int
+    skew: str              # "uniform" or "zipf1.2"
+    d_dtype: str           # "bf16" or "e4m3"
+    tanh_clamp: float | None = None
+    seed: int = 0
+    fmt: str = "mxfp8"
+
+    @property
+    def sf_vec(self) -> int:
+        return 32 if self.fmt == "mxfp8" else 16
+
+    def counts(self) -> np.ndarray:
+        """Routed rows per expert: one seeded multinomial draw."""
+        g = np.arange(self.experts, dtype=np.float64)
+        if self.skew == "uniform":
+            p = np.full(self.experts, 1.0 / self.experts)
+        elif self.skew.startswith("zipf"):
+            s = float(self.skew[4:])
+            w = (g + 1.0) ** (-s)
+            p = w / w.sum()
+        elif self.skew.startswith("fixed:"):
+            return np.array([int(c) for c in self.skew[6:].split(",")], dtype=np.int64)
+        else:
+            raise ValueError(self.skew)
+        rng = _chunk_rng(self.seed, S_ROUTE, 0)
+        return rng.multinomial(self.routed_rows, p).astype(np.int64)
+
+    def padded_offsets(self) -> np.ndarray:
+        """int32 cumulative ends of each expert's range, each padded up to 256 rows."""
+        c = self.counts()
+        padded = (c + PAD - 1) // PAD * PAD
+        return np.cumsum(padded).astype(np.int32)
+
+    @property
+    def valid_m(self) -> int:
+        return int(self.padded_offsets()[-1])
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.valid_m * self.n * self.k
+
+    def routed_mask(self) -> np.ndarray:
+        """Boolean (valid_m,): True for routed rows, False for padding rows."""
+        c = self.counts()
+        ends = self.padded_offsets().astype(np.int64)
+        mask = np.zeros(int(ends[-1]), dtype=bool)
+        begin = 0
+        for g in range(self.experts):
+            mask[begin:begin + c[g]] = True
+            begin = int(ends[g])
+        return mask
+
+    def a_rows(self, rows: np.ndarray | None = None) -> np.ndarray:
+        """fp32 A (valid_m, K): N(0,1)/sqrt(K) on routed rows, zero on padding rows."""
+        k, vm = self.k, self.valid_m
+        scale = np.float32(1.0 / math.sqrt(k))
+        mask = self.routed_mask()
+        if rows is None:
+            x = normal_f32(self.seed, S_A, 0, vm * k).reshape(vm, k)
+            x *= scale
+            x[~mask] = 0.0
+        else:
+            x = np.stack([normal_f32(self.seed, S_A, int(r) * k, (int(r) + 1) * k) for r in rows])
+            x *= scale
+            x[~mask[np.asarray(rows)]] = 0.0
+        return x
+
+    def b_rows(self, rows: np.ndarray | None = None) -> np.ndarray:
+        """fp32 B (L, N, K) as N(0,1)/sqrt(K); with ``rows`` (flat g*N+n) only those rows."""
+        k = self.k
+        scale = np.float32(1.0 / math.sqrt(k))
+        if rows is None:
+            x = normal_f32(self.seed, S_B, 0, self.experts * self.n * k).reshape(self.experts, self.n, k)
+        else:
+            x = np.stack([normal_f32(self.seed, S_B, int(r) * k, (int(r) + 1) * k) for r in rows])
+        x *= scale
+        return x
+
+    def alpha(self) -> np.ndarray:
+        return uniform_f32(self.seed, S_ALPHA, self.experts, 0.5, 2.0)
+
+    def prob(self) -> np.ndarray:
+        return uniform_f32(self.seed, S_PROB, self.valid_m, 0.0, 1.0)
+
+
+# The five named workloads.  The first is small enough for the oracle to finish
+# in seconds; the second is the large batched dense one throughput is quoted on.
+DENSE_MXFP8_256 = Dense("dense_mxfp8_m256_n256_k256_l1", 256, 256, 256, 1, "mxfp8", "f32")
+DENSE_MXFP8_8192 = Dense("dense_mxfp8_m8192_n8192_k8192_l4", 8192, 8192, 8192, 4, "mxfp8", "bf16",
+                         boost_every=7)
+DENSE_NVFP4_16384 = Dense("dense_nvfp4_m16384_n16384_k8192_l1", 16384, 16384, 8192, 1, "nvfp4", "bf16")
+GROUPED_SRELU_E32 = Grouped("grouped_mxfp8_srelu_e32_k7168_n2048", 32, 7168, 2048, 32768, "uniform", "bf16")
+GROUPED_SRELU_E32_CLAMP = dataclasses.replace(GROUPED_SRELU_E32, name=GROUPED_SRELU_E32.name + "_tanh32",
+                                              tanh_clamp=32.0)
+GROUPED_FP8D_E128 = Grouped("grouped_mxfp8_fp8d_e128_k4096_n4096", 128, 4096, 4096, 65536, "zipf1.2", "e4m3")
+
+ALL = {w.name: w for w in (DENSE_MXFP8_256, DENSE_MXFP8_8192, DENSE_NVFP4_16384, GROUPED_SRELU_E32,
+                           GROUPED_SRELU_E32_CLAMP, GROUPED_FP8D_E128)}
