@@ -14,7 +14,8 @@ float8_e8m0fnu and float8_e4m3fn):
 Decoders are the formulas above.  Encoders round to nearest, ties to the even
 code, saturating to the largest finite magnitude ("satfinite"); the decision is
 taken on the exact input value, so a float64 input that is itself exact gives
-the correctly rounded code.
+the correctly rounded code.  As in IEEE rounding the sign is kept, so a negative
+value that rounds to zero encodes as -0.
 """
 from __future__ import annotations
 
@@ -72,7 +73,8 @@ def encode_e4m3(x) -> np.ndarray:
     q = np.where(carry, 8, q)
     code_norm = ((big_e + 7) << 3) | (q.astype(np.int64) - 8)
     code = np.where(a < 2.0 ** -6, q_sub.astype(np.int64), code_norm)
-    code = np.where(neg & (code != 0), code | 0x80, code)
+    # rounding keeps the sign: a negative value that rounds to zero gives -0 (0x80)
+    code = np.where(neg, code | 0x80, code)
     return code.astype(np.uint8)
 
 
@@ -94,8 +96,10 @@ def encode_e2m1_scaled(x, s) -> np.ndarray:
         # on a tie the even of (i, i+1) wins
         even_up = (i + 1) % 2 == 0
         idx = idx + np.where(above | (tie & even_up), 1, 0)
+    # rounding keeps the sign (a negative value that rounds to zero gives -0, nibble 0x8);
+    # a zero scale gives the code +0 for every element
+    neg = np.signbit(x) & (s > 0)
     idx = np.where(s > 0, idx, 0)
-    neg = np.signbit(x) & (idx != 0)
     return (idx | np.where(neg, 8, 0)).astype(np.uint8)
 
 

@@ -1,0 +1,89 @@
+"""GPU parity of bsg_gemm_amax (dense / batched block-scaled GEMM + global amax) against the oracle.
+
+Both paths start from the same seeded fp32 operands; each quantises them with its own
+quantiser (asserted bit-identical first), then the GPU GEMM is compared element by
+element with the float64 oracle on shapes that span several tiles and ragged tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import gemm as og, quantize as oq
+from parity import check_amax, check_c
+
+pytestmark = pytest.mark.gpu
+
+
+def _operands(seed, fmt, m, n, k, l, boost=False, spread=False):
+    a = W.normal_f32(seed, W.S_A, 0, l * m * k).reshape(l, m, k)
+    b = W.normal_f32(seed, W.S_B, 0, l * n * k).reshape(l, n, k)
+    if boost:
+        v = 32 if fmt == "mxfp8" else 16
+        kb = np.arange(k) // v
+        a[..., kb % 7 == 6] *= np.float32(64.0)
+    if spread:
+        e = np.clip(np.round(W.normal_f32(seed, 21, 0, l * m) * 6), -30, 30).reshape(l, m, 1)
+        a = (a * np.exp2(e)).astype(np.float32)
+    return a, b
+
+
+def run_dense(fmt, m, n, k, l, c_kind, tile_n=0, seed=1, boost=False, spread=False, max_ctas=0):
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    a, b = _operands(seed, fmt, m, n, k, l, boost, spread)
+    qa, sfa = torch_ops.quantize(torch.from_numpy(a).cuda(), fmt)
+    qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), fmt)
+    c_dtype = torch.float32 if c_kind == "f32" else torch.bfloat16
+    ws = torch_ops.new_workspace()
+    c, amax = torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, m, n, k, l, c_dtype=c_dtype, workspace=ws,
+                                  tile_n=tile_n, max_ctas=max_ctas)
+    torch.cuda.synchronize()
+    import nvfp4_gemm_moe_gb300 as bsg
+    assert bsg.bsg_read_device_error(ws) == 0
+    # oracle side
+    qa_ref, sfa_ref = oq.quantize(a, fmt)
+    qb_ref, sfb_ref = oq.quantize(b, fmt)
+    assert np.array_equal(qa.cpu().numpy().reshape(qa_ref.shape), qa_ref)
+    assert np.array_equal(qb.cpu().numpy().reshape(qb_ref.shape), qb_ref)
+    assert np.array_equal(sfa.cpu().numpy(), sfa_ref) and np.array_equal(sfb.cpu().numpy(), sfb_ref)
+    ref, amax_ref = og.dense_gemm_amax(qa_ref, qb_ref, sfa_ref, sfb_ref, fmt, m, n, k, l)
+    s = og.dense_abs_sum(qa_ref, qb_ref, sfa_ref, sfb_ref, fmt, m, n, k, l)
+    check_c(c.float().cpu().numpy(), ref, s, c_kind)
+    check_amax(amax.cpu().numpy()[0], amax_ref)
+    return c, amax
+
+
+@pytest.mark.parametrize("fmt,m,n,k,l,c_kind,tile_n", [
+    ("mxfp8", 256, 256, 256, 1, "f32", 0),      # the small dense workload's shape
+    ("mxfp8", 256, 256, 256, 1, "f32", 256),
+    ("mxfp8", 300, 264, 384, 2, "bf16", 0),     # ragged M and N, batch 2
+    ("mxfp8", 384, 520, 1024, 1, "bf16", 256),  # several N tiles, ragged last one
+    ("mxfp8", 384, 520, 1024, 1, "f32", 128),
+    ("mxfp8", 128, 128, 160, 1, "f32", 128),    # K tail: one 32-wide MMA in the last stage
+    ("mxfp8", 1, 8, 32, 1, "f32", 128),         # minimal
+    ("nvfp4", 256, 256, 512, 1, "bf16", 256),
+    ("nvfp4", 300, 264, 320, 2, "f32", 128),    # K tail: one MMA in the last stage
+    ("nvfp4", 130, 136, 96, 1, "f32", 0),       # K = 96: half of the second MMA is zero fill
+    ("nvfp4", 640, 768, 2048, 1, "bf16", 256),
+])
+def test_dense_parity(lib, fmt, m, n, k, l, c_kind, tile_n):
+    run_dense(fmt, m, n, k, l, c_kind, tile_n)
+
+
+def test_dense_scale_range_boosted_blocks(lib):
+    """Every 7th K block of A x2^6 and rows spread over 2^+-30 (E8M0 scale range)."""
+    run_dense("mxfp8", 512, 384, 2048, 2, "bf16", 256, boost=True, spread=True)
+    run_dense("nvfp4", 256, 384, 1024, 1, "f32", 128, boost=True)
+
+
+def test_dense_persistent_loop_few_ctas(lib):
+    """Few CTAs: each walks many tiles, exercising stage / accumulator phase wrap-around."""
+    run_dense("mxfp8", 1024, 1024, 1024, 1, "bf16", 256, max_ctas=3)
+    run_dense("mxfp8", 1024, 1024, 512, 1, "f32", 128, max_ctas=5)
+    run_dense("nvfp4", 512, 768, 1024, 1, "bf16", 256, max_ctas=2)
+
+
+def test_dense_repeat_calls_are_identical(lib):
+    c1, a1 = run_dense("mxfp8", 256, 512, 512, 1, "bf16", 256, seed=7)
+    c2, a2 = run_dense("mxfp8", 256, 512, 512, 1, "bf16", 256, seed=7)
+    assert torch.equal(c1, c2) and torch.equal(a1, a2)

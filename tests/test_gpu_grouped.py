@@ -1,0 +1,147 @@
+"""GPU parity of bsg_grouped_gemm_srelu (grouped MoE GEMM + prob-gated sReLU) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import formats, gemm as og, quantize as oq, sf_layout
+from parity import check_amax, check_c, check_d_bf16, check_e4m3_blocks, d_tolerance, TOL_C
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(counts, n, k, seed=3, a_scale=1.0):
+    wl = W.Grouped("t", len(counts), k, n, int(sum(counts)), "fixed:" + ",".join(str(c) for c in counts), "bf16",
+                   seed=seed)
+    offs = wl.padded_offsets()
+    a = wl.a_rows() * np.float32(a_scale)
+    b = wl.b_rows()
+    return wl, offs, a.astype(np.float32), b, wl.alpha(), wl.prob()
+
+
+def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0, tile_n=0, seed=3, a_scale=1.0,
+                tanh_approx=False, max_ctas=0):
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    wl, offs, a, b, alpha, prob = _case(counts, n, k, seed, a_scale)
+    vm = int(offs[-1])
+    qa, sfa = torch_ops.quantize(torch.from_numpy(a).cuda(), "mxfp8")
+    qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), "mxfp8")
+    ws = torch_ops.new_workspace()
+    c_dtype = {"bf16": torch.bfloat16, "f32": torch.float32, None: None}[c_kind]
+    out = torch_ops.grouped_gemm_srelu(
+        qa[0], qb, sfa, sfb, "mxfp8", torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
+        torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=clamp, d_dtype=d_dtype, c_dtype=c_dtype,
+        norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
+        tanh_approx=tanh_approx, max_ctas=max_ctas)
+    torch.cuda.synchronize()
+    assert bsg.bsg_read_device_error(ws) == 0
+    qa_ref, sfa_ref = oq.quantize(a, "mxfp8")
+    qb_ref, sfb_ref = oq.quantize(b, "mxfp8")
+    assert np.array_equal(qa.cpu().numpy(), qa_ref) and np.array_equal(qb.cpu().numpy(), qb_ref)
+    assert np.array_equal(sfa.cpu().numpy(), sfa_ref) and np.array_equal(sfb.cpu().numpy(), sfb_ref)
+    ref = og.grouped_srelu(qa_ref[0], qb_ref, sfa_ref, sfb_ref, "mxfp8", offs, alpha, prob, k, n,
+                           tanh_clamp_scale=clamp, d_fp8=(d_dtype == "e4m3"), norm_const=nc)
+    # sum_k |Ahat||Bhat| per element for the tolerance, with each row's expert
+    ahat = np.abs(oq.dequantize(qa_ref, sfa_ref, "mxfp8", vm, k, 1)[0])
+    bhat = np.abs(oq.dequantize(qb_ref, sfb_ref, "mxfp8", n, k, len(counts)))
+    g_of = og.expert_of_rows(offs, vm)
+    s = np.zeros((vm, n))
+    for g in range(len(counts)):
+        rows = g_of == g
+        if rows.any():
+            s[rows] = float(alpha[g]) * (ahat[rows] @ bhat[g].T)
+    c_tol = TOL_C * s
+    if c_kind is not None:
+        check_c(out["c"].float().cpu().numpy(), ref["c"], s, c_kind)
+    d_tol = d_tolerance(ref["c"], prob, c_tol) + 2.0 ** -20 * ref["d"]
+    if tanh_approx and clamp is not None:
+        # the approximate tanh (max abs error 7.7e-6 on the pages' sweep) through d(c^2) = 2c dc
+        d_tol = d_tol + np.asarray(prob, np.float64)[:, None] * 2 * clamp * clamp * 7.7e-6
+    if d_dtype == "bf16":
+        d_gpu = out["d"].float().cpu().numpy()
+        if tanh_approx and clamp is not None:
+            err = np.abs(d_gpu - ref["d"])
+            assert np.all(err <= formats.bf16_ulp(ref["d"]) + d_tol)
+        else:
+            check_d_bf16(d_gpu, ref["d"], ref["c"], prob, c_tol)
+        amax = out["amax"].cpu().numpy()
+        assert np.all(amax[ref["amax"] == 0] == 0)
+        nz = ref["amax"] > 0
+        if tanh_approx and clamp is not None:
+            assert np.allclose(amax[nz], ref["amax"][nz], rtol=2e-5)
+        else:
+            check_amax(amax[nz], ref["amax"][nz])
+    else:
+        sfd_row = sf_layout.unpack(out["sfd_row"].cpu().numpy(), vm, n // 32)[0]
+        sfd_col = sf_layout.unpack(out["sfd_col"].cpu().numpy(), n, vm // 32)[0]
+        nr = check_e4m3_blocks(out["d"].cpu().numpy(), sfd_row, ref["d"], d_tol, nc, axis=1, what="D_row")
+        nc_ = check_e4m3_blocks(out["d_col"].cpu().numpy(), sfd_col, ref["d"], d_tol, nc, axis=0, what="D_col")
+        # padding bytes of the SF buffers are zero
+        full_row = out["sfd_row"].cpu().numpy()
+        full_col = out["sfd_col"].cpu().numpy()
+        assert (full_row != 0).sum() <= vm * (n // 32) and (full_col != 0).sum() <= n * (vm // 32)
+        assert np.array_equal(sf_layout.pack(sfd_row[None]), full_row)
+        assert np.array_equal(sf_layout.pack(sfd_col[None]), full_col)
+        return out, ref, (nr, nc_)
+    return out, ref, None
+
+
+EDGE = [0, 300, 0, 0, 1, 256, 0]  # empty experts first, in a run and last; one 1-row expert
+
+
+@pytest.mark.parametrize("counts,n,k,tile_n", [
+    (EDGE, 256, 256, 0),
+    (EDGE, 264, 512, 256),    # ragged N tile
+    ([200, 200, 200, 200], 512, 384, 128),
+    ([512], 384, 256, 256),   # single expert
+    ([1, 2, 3, 700, 4], 256, 1024, 256),
+])
+def test_grouped_bf16_d(lib, counts, n, k, tile_n):
+    run_grouped(counts, n, k, "bf16", None, "bf16", tile_n=tile_n)
+
+
+def test_grouped_bf16_c_f32_and_no_c(lib):
+    run_grouped(EDGE, 256, 256, "bf16", None, "f32")
+    run_grouped(EDGE, 256, 256, "bf16", None, None)
+
+
+@pytest.mark.parametrize("approx", [False, True])
+def test_grouped_tanh_clamp(lib, approx):
+    # inputs scaled so that |C| reaches well past s = 32 and the clamp saturates
+    run_grouped([300, 500, 0, 220], 256, 512, "bf16", 32.0, "bf16", a_scale=700.0, tanh_approx=approx)
+
+
+@pytest.mark.parametrize("nc,tile_n", [(1.0, 256), (1.0, 128), (0.75, 256)])
+def test_grouped_fp8_d(lib, nc, tile_n):
+    run_grouped(EDGE, 384, 512, "e4m3", None, "bf16", nc=nc, tile_n=tile_n)
+
+
+def test_grouped_fp8_d_ragged_n_and_clamp(lib):
+    run_grouped([257, 0, 511], 160, 256, "e4m3", 32.0, None, a_scale=700.0)
+
+
+def test_grouped_few_ctas(lib):
+    run_grouped([600, 900, 0, 300], 512, 512, "bf16", None, "bf16", tile_n=256, max_ctas=3)
+    run_grouped([600, 900, 0, 300], 512, 512, "e4m3", None, "bf16", tile_n=128, max_ctas=2)
+
+
+def test_grouped_bad_offsets_detected_on_device(lib):
+    """Offsets that are not multiples of 256 are flagged on the device, nothing is computed."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    k, n, vm = 256, 256, 512
+    qa = torch.zeros((vm, k), dtype=torch.uint8, device="cuda")
+    qb = torch.zeros((2, n, k), dtype=torch.uint8, device="cuda")
+    sfa = torch.zeros(bsg.bsg_sf_bytes(1, vm, k, 32), dtype=torch.uint8, device="cuda")
+    sfb = torch.zeros(bsg.bsg_sf_bytes(2, n, k, 32), dtype=torch.uint8, device="cuda")
+    ws = torch_ops.new_workspace()
+    offs = torch.tensor([100, 512], dtype=torch.int32, device="cuda")
+    ones = torch.ones(2, device="cuda")
+    prob = torch.ones(vm, device="cuda")
+    torch_ops.grouped_gemm_srelu(qa, qb, sfa, sfb, "mxfp8", offs, ones, prob, n, k, workspace=ws)
+    assert bsg.bsg_read_device_error(ws) == bsg.DEVERR_BAD_OFFSETS
+    with pytest.raises(bsg.BsgError) as ei:
+        torch_ops.grouped_gemm_srelu(qa, qb, sfa, sfb, "mxfp8", offs, ones, prob, n, k, workspace=ws,
+                                     validate_offsets=True)
+    assert ei.value.status == 7

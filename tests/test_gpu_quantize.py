@@ -1,0 +1,94 @@
+"""GPU parity of bsg_quantize_mx against the oracle quantiser: codes and scale bytes bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import formats, quantize as oq
+
+pytestmark = pytest.mark.gpu
+
+
+def _wide_range(seed, batch, rows, k, v):
+    """N(0,1) values with a per-block power-of-two spread of 2^-40 .. 2^40 and some zero blocks."""
+    x = W.normal_f32(seed, 11, 0, batch * rows * k).reshape(batch, rows, k)
+    e = W.normal_f32(seed, 12, 0, batch * rows * (k // v)).reshape(batch, rows, k // v)
+    e = np.clip(np.round(e * 12), -40, 40).astype(np.float32)
+    x = x * np.repeat(np.exp2(e), v, axis=-1).astype(np.float32)
+    x[..., :v][np.abs(e[..., 0]) > 25] = 0.0  # a few all-zero blocks
+    return x.astype(np.float32)
+
+
+def _ties(fmt, batch, rows, k):
+    """Values sitting exactly on rounding midpoints of the code grid (after the block scale)."""
+    rng_vals = W.normal_f32(5, 13, 0, batch * rows * k).reshape(batch, rows, k)
+    if fmt == "mxfp8":
+        grid = formats.decode_e4m3(np.arange(0, 0x7F))
+        mids = (grid[:-1] + grid[1:]) / 2
+        idx = (np.abs(rng_vals) * 1000).astype(np.int64) % len(mids)
+        x = np.where(rng_vals < 0, -mids[idx], mids[idx])
+        x[..., ::32] = 448.0  # pins every block's scale to 2^0
+    else:
+        mids = formats.E2M1_MIDS
+        idx = (np.abs(rng_vals) * 1000).astype(np.int64) % len(mids)
+        x = np.where(rng_vals < 0, -mids[idx], mids[idx])
+        x[..., ::16] = 6.0  # block scale 1.0
+    return x.astype(np.float32)
+
+
+def _run(lib, x, fmt):
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    xg = torch.from_numpy(x).cuda()
+    q, sf = torch_ops.quantize(xg, fmt)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), sf.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt,batch,rows,k", [
+    ("mxfp8", 1, 256, 256), ("mxfp8", 2, 130, 160), ("mxfp8", 1, 1, 32), ("mxfp8", 3, 129, 4096),
+    ("nvfp4", 1, 256, 512), ("nvfp4", 2, 130, 96), ("nvfp4", 1, 3, 32), ("nvfp4", 2, 200, 2080),
+])
+def test_quantize_bit_exact_wide_range(lib, fmt, batch, rows, k):
+    v = 32 if fmt == "mxfp8" else 16
+    x = _wide_range(batch * 1000 + rows + k, batch, rows, k, v)
+    q, sf = _run(lib, x, fmt)
+    q_ref, sf_ref = oq.quantize(x, fmt)
+    assert np.array_equal(sf, sf_ref), f"{(sf != sf_ref).sum()} scale bytes differ"
+    assert np.array_equal(q.reshape(q_ref.shape), q_ref), f"{(q.reshape(q_ref.shape) != q_ref).sum()} code bytes differ"
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_quantize_bit_exact_ties(lib, fmt):
+    x = _ties(fmt, 2, 128, 256)
+    q, sf = _run(lib, x, fmt)
+    q_ref, sf_ref = oq.quantize(x, fmt)
+    assert np.array_equal(sf, sf_ref)
+    assert np.array_equal(q.reshape(q_ref.shape), q_ref)
+
+
+def test_quantize_nvfp4_scale_ties_and_saturation(lib):
+    """Block maxima at 6 * (E4M3 midpoints) test the exact scale rounding; huge maxima saturate."""
+    grid = formats.decode_e4m3(np.arange(0, 0x7F))
+    mids = (grid[:-1] + grid[1:]) / 2
+    amax = np.concatenate([6 * mids, [3000.0, 1e6, 6 * 2.0 ** -11, 6 * 2.0 ** -10]]).astype(np.float32)
+    amax = amax[np.abs(amax.astype(np.float64) - np.concatenate([6 * mids, [3000.0, 1e6, 6 * 2.0 ** -11,
+                                                                           6 * 2.0 ** -10]])) == 0]
+    rows = len(amax)
+    x = np.zeros((1, rows, 32), np.float32)
+    x[0, :, 0] = amax
+    x[0, :, 1] = -amax * np.float32(0.3)
+    x[0, :, 16] = amax * np.float32(0.5)
+    q, sf = _run(lib, x, "nvfp4")
+    q_ref, sf_ref = oq.quantize(x, "nvfp4")
+    assert np.array_equal(sf, sf_ref)
+    assert np.array_equal(q.reshape(q_ref.shape), q_ref)
+
+
+def test_quantize_workload_rows_bit_exact(lib):
+    """The recipe of the large batched dense workload (with its 2^6-boosted K blocks), on a row slice."""
+    wl = W.DENSE_MXFP8_8192
+    rows = np.arange(0, 256)
+    x = wl.a_rows(rows)[None]
+    q, sf = _run(lib, x, "mxfp8")
+    q_ref, sf_ref = oq.quantize(x, "mxfp8")
+    assert np.array_equal(sf, sf_ref) and np.array_equal(q.reshape(q_ref.shape), q_ref)
