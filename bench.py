@@ -1,0 +1,394 @@
+"""Throughput benchmark of the block-scaled GEMM hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input: quantise A and B
+(fp32 -> MXFP8 / NVFP4 codes + scale factors) and run the block-scaled GEMM with its
+fused epilogue.  Default workload: the batched dense MXFP8 GEMM + amax, L = 4,
+M = N = K = 8192, C bf16.  Inputs (2 x 1.07 GB fp32) are larger than L2, so no flush
+is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs an independent replica
+of the workload on its own GPU ("replicas only": the path has no exchange step); the
+elapsed time is the maximum over ranks and `value` counts the work of all ranks.
+`--impl reference` times the float64 CPU oracle on a bounded sample of the same
+workload on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "block-scaled GEMM TFLOPS and % of GB300 FP8/FP4 tensor peak, per config"
+UNIT = "TFLOPS"
+NOMINAL_RATIO = {"mxfp8": 4.5 / 2.25, "nvfp4": 13.5 / 2.25}  # dense fp8 / fp4 vs bf16 tensor peak
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def _dense_inputs(wl):
+    a = wl.a_rows()
+    b = wl.b_rows()
+    return a, b
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import nvfp4_gemm_moe_gb300 as bsg
+    from nvfp4_gemm_moe_gb300 import torch_ops
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = W.ALL[args.workload]
+    stream = torch.cuda.current_stream()
+    is_dense = isinstance(wl, W.Dense)
+    fmt = wl.fmt
+    flops = wl.flops
+
+    # ---------------- inputs resident in HBM
+    if is_dense:
+        a_h, b_h = _dense_inputs(wl)
+    else:
+        a_h, b_h = wl.a_rows()[None], wl.b_rows()
+    a_pin = torch.from_numpy(a_h).pin_memory()
+    b_pin = torch.from_numpy(b_h).pin_memory()
+    a_d = a_pin.to(dev)
+    b_d = b_pin.to(dev)
+    la, ma, ka = a_d.shape
+    lb, nb, _ = b_d.shape
+    v = 32 if fmt == "mxfp8" else 16
+    qcols = ka if fmt == "mxfp8" else ka // 2
+    qa = torch.empty((la, ma, qcols), dtype=torch.uint8, device=dev)
+    qb = torch.empty((lb, nb, qcols), dtype=torch.uint8, device=dev)
+    sfa = torch.empty(bsg.bsg_sf_bytes(la, ma, ka, v), dtype=torch.uint8, device=dev)
+    sfb = torch.empty(bsg.bsg_sf_bytes(lb, nb, ka, v), dtype=torch.uint8, device=dev)
+    ws = torch_ops.new_workspace(dev)
+    if is_dense:
+        c = torch.empty((wl.l, wl.m, wl.n), dtype=torch.float32 if wl.c_dtype == "f32" else torch.bfloat16,
+                        device=dev)
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+        outs = None
+    else:
+        offs = torch.from_numpy(wl.padded_offsets()).to(dev)
+        alpha = torch.from_numpy(wl.alpha()).to(dev)
+        prob = torch.from_numpy(wl.prob()).to(dev)
+        nc = torch.ones(1, dtype=torch.float32, device=dev)
+        outs = {"c": torch.empty((wl.valid_m, wl.n), dtype=torch.bfloat16, device=dev)}
+
+    def gemm():
+        if is_dense:
+            torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, wl.m, wl.n, wl.k, wl.l, c=c, amax=amax, workspace=ws)
+        else:
+            torch_ops.grouped_gemm_srelu(qa[0], qb, sfa, sfb, fmt, offs, alpha, prob, wl.n, wl.k,
+                                         tanh_clamp_scale=wl.tanh_clamp, d_dtype=wl.d_dtype, norm_const=nc,
+                                         outputs=outs, workspace=ws)
+
+    def step(ev0=None, ev1=None):
+        torch_ops.quantize(a_d, fmt, q=qa, sf=sfa)
+        torch_ops.quantize(b_d, fmt, q=qb, sf=sfb)
+        if ev0 is not None:
+            ev0.record(stream)
+        gemm()
+        if ev1 is not None:
+            ev1.record(stream)
+
+    launches_per_step = 3  # two quantiser kernels + one GEMM kernel
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if bsg.bsg_read_device_error(ws):
+        raise RuntimeError("device error during warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(g0[i], g1[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop() if clocks else None
+    elapsed_ms = t0.elapsed_time(t1)
+    gemm_ms = [g0[i].elapsed_time(g1[i]) for i in range(args.steps)]
+    if bsg.bsg_read_device_error(ws):
+        raise RuntimeError("device error in the timed region")
+
+    # ---------------- end to end through the C ABI from pinned host buffers
+    e2e_steps = max(3, min(args.steps, 20))
+    c_out = c if is_dense else outs["c"]
+    c_host = torch.empty(c_out.shape, dtype=c_out.dtype, pin_memory=True)
+    amax_t = amax if is_dense else None
+    res_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+    h2d = a_pin.numel() * 4 + b_pin.numel() * 4
+    d2h = c_out.numel() * c_out.element_size() + 4
+    if not is_dense:
+        if wl.d_dtype == "bf16":
+            d_out = outs["d"]
+        else:
+            d_out = outs["d"]
+        d_host = torch.empty(d_out.shape, dtype=d_out.dtype, pin_memory=True)
+        d2h += d_out.numel() * d_out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        a_d.copy_(a_pin, non_blocking=True)
+        b_d.copy_(b_pin, non_blocking=True)
+        step()
+        c_host.copy_(c_out, non_blocking=True)
+        if is_dense:
+            res_host.copy_(amax_t, non_blocking=True)
+        else:
+            d_host.copy_(d_out, non_blocking=True)
+            res_host.copy_(outs["amax"][:1] if "amax" in outs else outs["sfd_row"][:4].view(torch.float32),
+                           non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # ---------------- max over ranks
+    times = torch.tensor([elapsed_ms, e2e_ms, statistics.mean(gemm_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_ms, gemm_mean_ms = times.tolist()
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"] * NOMINAL_RATIO[fmt]
+    achieved = flops / (gemm_mean_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": _traffic(args.workload),
+            "kernel": "gemm_kernel", "peak_source": f"{peak_src} bf16 burst x {NOMINAL_RATIO[fmt]:g} "
+                                                   f"(dense {fmt} / bf16 nominal ratio)"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3" if fmt == "mxfp8" else "e2m1", "data": "synthetic",
+        "config": _config(wl),
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "gemm_ms": round(gemm_mean_ms, 4),
+    }
+    return line
+
+
+def _traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if one exists for this workload."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(workload)
+    return None
+
+
+def _config(wl):
+    if isinstance(wl, W.Dense):
+        return {"workload": wl.name, "format": wl.fmt, "m": wl.m, "n": wl.n, "k": wl.k, "l": wl.l,
+                "c_dtype": wl.c_dtype, "flops_per_step": wl.flops,
+                "l2": "no flush: fp32 inputs of 2 x %.2f GB exceed L2" % (wl.l * wl.m * wl.k * 4 / 1e9),
+                "step": "quantise A + quantise B + GEMM/amax"}
+    return {"workload": wl.name, "format": wl.fmt, "experts": wl.experts, "n": wl.n, "k": wl.k,
+            "valid_m": wl.valid_m, "routed_rows": wl.routed_rows, "d_dtype": wl.d_dtype, "tanh_clamp": wl.tanh_clamp,
+            "flops_per_step": wl.flops, "l2": "no flush: fp32 inputs exceed L2",
+            "step": "quantise A + quantise B + grouped GEMM/sReLU"}
+
+
+# --------------------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args):
+    from oracle import gemm as og, quantize as oq
+    wl = W.ALL[args.workload]
+    cores = os.cpu_count() or 1
+    step_times, sample_flops = [], 0.0
+
+    def one_step():
+        if isinstance(wl, W.Dense):
+            rows = np.arange(args.ref_rows)           # first rows of batch 0 of A
+            a = wl.a_rows(rows)[None]
+            b = wl.b_rows(np.arange(wl.n))[None]       # all of B for batch 0
+            qa, sfa = oq.quantize(a, wl.fmt)
+            qb, sfb = oq.quantize(b, wl.fmt)
+            c, amax = og.dense_gemm_amax(qa, qb, sfa, sfb, wl.fmt, len(rows), wl.n, wl.k, 1)
+            return 2.0 * len(rows) * wl.n * wl.k
+        offs = wl.padded_offsets()
+        rows = np.arange(args.ref_rows)
+        g = 0
+        a = wl.a_rows(rows)[None]
+        b = wl.b_rows(np.arange(wl.n))[None]  # expert 0's weights
+        qa, sfa = oq.quantize(a, wl.fmt)
+        qb, sfb = oq.quantize(b, wl.fmt)
+        o = np.array([len(rows)], np.int32)
+        og.grouped_srelu(qa[0], qb, sfa, sfb, wl.fmt, o, wl.alpha()[:1], wl.prob()[:len(rows)], wl.k, wl.n,
+                         tanh_clamp_scale=wl.tanh_clamp, d_fp8=(wl.d_dtype == "e4m3"))
+        del g, offs
+        return 2.0 * len(rows) * wl.n * wl.k
+
+    for _ in range(args.warmup):
+        one_step()
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        sample_flops = one_step()
+        step_times.append(time.perf_counter() - t)
+    total = sum(step_times)
+    value = sample_flops * args.steps / total / 1e12
+    sample = (f"oracle path (quantise, dequantise, float64 GEMM, epilogue) on the first {args.ref_rows} rows of A "
+              f"against all {wl.n} rows of B (batch/expert 0) of {wl.name}; numpy/BLAS float64 on {cores} host threads")
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": _config(wl),
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def cpu_baseline(args):
+    """The oracle timed on a bounded sample (about 10-30 s of host work) for the GPU arm's line."""
+    class A:
+        pass
+    ra = A()
+    ra.workload, ra.steps, ra.warmup, ra.ref_rows = args.workload, 1, 0, args.ref_rows
+    t = time.perf_counter()
+    line = run_reference(ra)
+    cb = line["cpu_baseline"]
+    cb["wall_s"] = round(time.perf_counter() - t, 2)
+    return cb
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=W.DENSE_MXFP8_8192.name, choices=sorted(W.ALL))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=256, help="rows of A in the oracle's timed sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            if args.steps > 3:
+                args.steps = 3  # each oracle step is a bounded host sample of several seconds
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

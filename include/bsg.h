@@ -1,0 +1,211 @@
+/*
+ * bsg.h -- C ABI of the block-scaled GEMM library for GB300 (sm_103a).
+ *
+ * Three operations, each one asynchronous launch sequence on the caller's
+ * CUDA stream:
+ *
+ *   bsg_quantize_mx         fp32 -> MXFP8 / NVFP4 codes + scale factors in the
+ *                           128x4 scale-factor atom layout (produces the GEMM operands);
+ *   bsg_gemm_amax           dense / batched block-scaled GEMM + global amax
+ *                           ("GEMM + Amax (SM100)", Overview and Equations);
+ *   bsg_grouped_gemm_srelu  grouped MoE block-scaled GEMM + prob-gated sReLU with
+ *                           optional tanh soft clamp, per-expert amax or FP8 D with
+ *                           row/column MXFP8 scale factors
+ *                           ("Grouped GEMM + sReLU (SM100)", Overview, Equations,
+ *                           Tanh soft clamp).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named as device pointers must be device memory of the current CUDA
+ *   device (or managed memory); the library never allocates, frees or retains
+ *   them.  All tensors are caller-owned.
+ * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *   stream.  Every entry point only enqueues work (memsets and kernel launches)
+ *   and returns; results are valid once the stream reaches that point.
+ * - Sizes are element counts, not bytes, unless the name says bytes.
+ * - Errors: invalid arguments are detected on the host before anything is
+ *   enqueued and reported as a bsg_status; nothing is thrown across the ABI.
+ *   Errors detected on the device (a pipeline wait that exceeded its time limit,
+ *   invalid padded_offsets contents) set bits in the caller's workspace; read
+ *   them with bsg_read_device_error.
+ * - Scale-factor (SF) layout ("GEMM + Amax (SM100)", Shapes and "Using JAX
+ *   arrays"): for a (batch, rows, K) operand with block size v the SF buffer is
+ *   the C-contiguous physical array (batch, ceil(rows/128), ceil(K/(4v)), 32, 4, 4)
+ *   of one byte per scale; the byte of row r, block kb, batch l is
+ *       ((((l*MT + r/128)*KT + kb/4)*32 + r%32)*4 + (r%128)/32)*4 + kb%4
+ *   with MT = ceil(rows/128), KT = ceil(K/(4v)).  Padding bytes (rows >= rows or
+ *   blocks >= ceil(K/v)) must hold a finite scale (bsg_quantize_mx writes 0).
+ * - Formats: MXFP8 = E4M3 codes (1 byte) with UE8M0 scales and v = 32; NVFP4 =
+ *   E2M1 codes packed two per byte (element 2j in the low nibble) with UE4M3
+ *   scales and v = 16 ("GEMM + Amax (SM100)", Support surface: E4M3 scales
+ *   only with v = 16, FP8 operands only with v = 32).
+ * - Operands A (rows, K) and B are K-major (row-major with K contiguous);
+ *   outputs C, D, D_col are N-major (row-major with N contiguous).  Every
+ *   base pointer must be 16-byte aligned and every row pitch a multiple of 16
+ *   bytes ("GEMM + Amax (SM100)", Layouts and strides).
+ * - Requires a device of compute capability 10.3 (GB300); the library carries
+ *   sm_103a code only.
+ */
+#ifndef BSG_H
+#define BSG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bsg_status {
+  BSG_OK = 0,
+  BSG_ERR_INVALID_ARG = 1,   /* null pointer, bad size or inconsistent arguments */
+  BSG_ERR_UNSUPPORTED = 2,   /* a valid combination this library does not implement */
+  BSG_ERR_ALIGNMENT = 3,     /* a pointer or pitch breaks the 16-byte rule */
+  BSG_ERR_ARCH = 4,          /* current device is not compute capability 10.3 */
+  BSG_ERR_CUDA = 5,          /* a CUDA runtime / driver call failed */
+  BSG_ERR_DEVICE = 6,        /* bsg_read_device_error found device-side error bits */
+  BSG_ERR_BAD_OFFSETS = 7,   /* host-validated padded_offsets are invalid */
+  BSG_ERR_WORKSPACE = 8      /* workspace missing or smaller than bsg_workspace_size() */
+} bsg_status;
+
+typedef enum bsg_dtype {
+  BSG_E4M3 = 0,  /* float8_e4m3fn */
+  BSG_E5M2 = 1,  /* float8_e5m2 (not implemented) */
+  BSG_E2M1 = 2,  /* float4_e2m1fn, two per byte */
+  BSG_F32 = 3,
+  BSG_BF16 = 4,
+  BSG_F16 = 5
+} bsg_dtype;
+
+typedef enum bsg_sf_dtype {
+  BSG_SF_UE8M0 = 0, /* float8_e8m0fnu: 2^(code-127) */
+  BSG_SF_UE4M3 = 1  /* float8_e4m3fn used as an unsigned scale */
+} bsg_sf_dtype;
+
+/* Device error bits written to the workspace. */
+#define BSG_DEVERR_TIMEOUT 0x1u      /* a pipeline wait exceeded its time limit; the kernel gave up */
+#define BSG_DEVERR_BAD_OFFSETS 0x2u  /* padded_offsets not non-decreasing multiples of 256 ending at valid_m */
+
+/* Optional launch options; pass NULL for the defaults (all fields 0). */
+typedef struct bsg_gemm_opts {
+  int tile_n;            /* output tile width: 0 = automatic, else 128 or 256 */
+  int max_ctas;          /* 0 = one persistent CTA per SM, else at most this many CTAs */
+  int tanh_approx;       /* grouped only: 1 = tanh.approx.f32 in the soft clamp, 0 = tanhf */
+  int validate_offsets;  /* grouped only: 1 = copy padded_offsets to the host and check them
+                            before launching (synchronises the stream) */
+  int reserved[4];
+} bsg_gemm_opts;
+
+/* Bytes of scratch the GEMM entry points need in `workspace` (device memory,
+ * 256-byte aligned).  The call overwrites it; do not share one workspace between
+ * calls that may run concurrently. */
+size_t bsg_workspace_size(void);
+
+/* Bytes of the SF buffer for a (batch, rows, K) operand with block size v. */
+size_t bsg_sf_bytes(int64_t batch, int64_t rows, int64_t k, int sf_vec_size);
+
+/*
+ * bsg_quantize_mx -- block quantiser that produces GEMM operands.
+ *
+ * x       device, fp32 (batch, rows, k) row-major (k contiguous).
+ * q       device output: E4M3 -> (batch, rows, k) bytes; E2M1 -> (batch, rows, k/2)
+ *         bytes, element 2j in the low nibble of byte j.
+ * sf      device output: bsg_sf_bytes(batch, rows, k, sf_vec_size) bytes in the SF
+ *         layout above; every byte is written, padding bytes as 0.
+ * Formats (the workloads' recipes for the operands of "GEMM + Amax (SM100)"):
+ *   q_dtype = BSG_E4M3, sf_vec_size = 32, sf_dtype = BSG_SF_UE8M0 (MXFP8): per block
+ *     of 32 the scale is 2^e, e the smallest integer with blockamax <= 448*2^e
+ *     (E8M0 code clamped to [0, 254]); code = RNE_satfinite_E4M3(x / 2^e).
+ *   q_dtype = BSG_E2M1, sf_vec_size = 16, sf_dtype = BSG_SF_UE4M3 (NVFP4): scale
+ *     s = RNE_UE4M3(blockamax / 6); code = RNE_satfinite_E2M1(x / s), decided on the
+ *     exact quotient; s = 0 gives zero codes.
+ * Requirements: k % sf_vec_size == 0, rows >= 1, batch >= 1, k >= sf_vec_size.
+ * Returns BSG_OK after enqueueing; x must not contain NaN or infinities.
+ */
+bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t k,
+                           bsg_dtype q_dtype, int sf_vec_size, bsg_sf_dtype sf_dtype,
+                           void* q, uint8_t* sf, void* stream);
+
+/*
+ * bsg_gemm_amax -- dense batched block-scaled GEMM with fused global amax
+ * ("GEMM + Amax (SM100)", Equations):
+ *     C[m, n, l] = sum_k Ahat[m, k, l] * Bhat[n, k, l],   *amax = max |C|,
+ * Ahat/Bhat the codes times their block scales, accumulated in fp32.
+ *
+ * a, b      device codes: A (l, m, k) and B (l, n, k), K-major; E4M3 one byte per
+ *           element or E2M1 packed (k/2 bytes per row).
+ * sfa, sfb  device SF buffers for A (rows m) and B (rows n).
+ * ab_dtype / sf_dtype / sf_vec_size: (BSG_E4M3, BSG_SF_UE8M0, 32) or (BSG_E2M1, BSG_SF_UE4M3, 16).
+ * c         device output (l, m, n), N-major, c_dtype BSG_F32 or BSG_BF16 (RNE from fp32).
+ * amax      device output, one float: the max of |C| taken on the fp32 accumulator
+ *           before rounding to c_dtype.  Zeroed by the call on `stream` first.
+ * workspace device scratch of bsg_workspace_size() bytes (see bsg_read_device_error).
+ * Requirements: m, n, k, l >= 1; k*bytes_per_element % 16 == 0 (k % 16 for E4M3,
+ * k % 32 for E2M1); k % sf_vec_size == 0; n*sizeof(c) % 16 == 0.
+ */
+bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
+                         bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size,
+                         int64_t m, int64_t n, int64_t k, int64_t l,
+                         void* c, bsg_dtype c_dtype, float* amax,
+                         const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * bsg_grouped_gemm_srelu -- grouped MoE block-scaled GEMM + prob-gated sReLU
+ * ("Grouped GEMM + sReLU (SM100)", Equations and Tanh soft clamp).  Rows
+ * [padded_offsets[g-1], padded_offsets[g]) (0 for g = 0) belong to expert g
+ * ("Grouped GEMM (SM100 BF16)", Operation):
+ *     C[m, n] = alpha[g] * sum_k Ahat[m, k] * Bhat[n, k, g]
+ *     D[m, n] = prob[m] * relu(C[m, n])^2                          (tanh_clamp_scale <= 0)
+ *     D[m, n] = prob[m] * (s * min(tanh(relu(C[m, n]) / s), 1))^2  (s = tanh_clamp_scale > 0)
+ * evaluated in fp32 from the fp32 accumulator.
+ *
+ * a               device codes (valid_m, k), K-major.
+ * b               device codes (num_experts, n, k), K-major.
+ * sfa, sfb        device SF buffers: A with rows valid_m, B with batch num_experts, rows n.
+ * padded_offsets  device int32 (num_experts,): cumulative ends, non-decreasing multiples
+ *                 of 256, the last equal to valid_m.  Caller's responsibility; with
+ *                 opts->validate_offsets the host checks them first (and syncs), otherwise
+ *                 the kernel checks them, sets BSG_DEVERR_BAD_OFFSETS and computes nothing.
+ * alpha           device fp32 (num_experts,).
+ * prob            device fp32 (valid_m,).
+ * norm_const      device fp32 (1,); required iff d_dtype == BSG_E4M3.
+ * c               optional device output (valid_m, n) bf16 or f32 (c_dtype); NULL skips C.
+ * d               device output (valid_m, n): d_dtype BSG_BF16 (RNE of the fp32 D) or
+ *                 BSG_E4M3 (row-quantised D).
+ * d_col           device output (valid_m, n) E4M3 (column-quantised D); required iff
+ *                 d_dtype == BSG_E4M3, else must be NULL.
+ * sfd_row         device output, SF layout with rows valid_m and K = n (blocks of 32 columns).
+ * sfd_col         device output, SF layout with rows n and K = valid_m (blocks of 32 rows).
+ *                 For E4M3 D the scale of a block is 2^e, e the smallest integer with
+ *                 norm_const * blockamax(|D|) <= 448 * 2^e, and the code is
+ *                 RNE_satfinite_E4M3(D * norm_const / 2^e) ("Grouped GEMM + dSwiGLU (SM100)",
+ *                 Step 3, with the scale rounded up to a power of two).
+ * amax            device fp32 (num_experts,): max |D| over each expert's rows (0 for an
+ *                 empty expert); required iff d_dtype == BSG_BF16.  Zeroed by the call.
+ * Requirements: valid_m % 256 == 0, 1 <= num_experts <= 1024, sf as for bsg_gemm_amax,
+ * n % 32 == 0 for E4M3 D, n*sizeof(d) % 16 == 0.
+ */
+bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
+                                  bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size,
+                                  int64_t valid_m, int64_t n, int64_t k, int64_t num_experts,
+                                  const int32_t* padded_offsets, const float* alpha, const float* prob,
+                                  float tanh_clamp_scale, const float* norm_const,
+                                  void* c, bsg_dtype c_dtype,
+                                  void* d, void* d_col, bsg_dtype d_dtype,
+                                  uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
+                                  const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/* Synchronises `stream` and returns the device error bits of the last call that
+ * used `workspace` in *error_bits; BSG_ERR_DEVICE if any bit is set. */
+bsg_status bsg_read_device_error(const void* workspace, void* stream, uint32_t* error_bits);
+
+/* Static string naming a status code. */
+const char* bsg_status_string(bsg_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSG_H */

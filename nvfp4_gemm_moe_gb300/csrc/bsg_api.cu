@@ -1,0 +1,345 @@
+// bsg_api.cu -- the C ABI: argument validation, TMA descriptor encoding, launch configuration.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/bsg.h"
+#include "internal.h"
+
+namespace {
+
+using bsg::GemmConfig;
+using bsg::GemmParams;
+
+constexpr size_t kWorkspaceBytes = 256;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  int num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+bsg_status current_device(int* dev_out, DeviceInfo* info_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSG_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return BSG_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return BSG_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    d.probed = true;
+  }
+  if (dev_out) *dev_out = dev;
+  if (info_out) *info_out = d;
+  return d.supported ? BSG_OK : BSG_ERR_ARCH;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// K-major operand (batch, rows, row_bytes) of bytes, loaded as 128-byte x box_rows boxes with
+// the 128-byte swizzle; out-of-range rows / K bytes read as zero.
+bool make_operand_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t batch,
+                      uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {row_bytes, rows, batch};
+  const cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
+  const cuuint32_t box[3] = {128, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Operand format from the (ab_dtype, sf_dtype, sf_vec_size) triple.
+bsg_status operand_format(bsg_dtype ab, bsg_sf_dtype sf, int v, int* fmt) {
+  if (ab == BSG_E4M3 && sf == BSG_SF_UE8M0 && v == 32) { *fmt = bsg::kMXFP8; return BSG_OK; }
+  if (ab == BSG_E2M1 && sf == BSG_SF_UE4M3 && v == 16) { *fmt = bsg::kNVFP4; return BSG_OK; }
+  if (v != 16 && v != 32) return BSG_ERR_INVALID_ARG;
+  if (sf != BSG_SF_UE8M0 && sf != BSG_SF_UE4M3) return BSG_ERR_INVALID_ARG;
+  // couplings the operation forbids: E4M3 scales need v = 16, FP8 operands need v = 32
+  if (sf == BSG_SF_UE4M3 && v == 32) return BSG_ERR_INVALID_ARG;
+  if ((ab == BSG_E4M3 || ab == BSG_E5M2) && v == 16) return BSG_ERR_INVALID_ARG;
+  if (ab != BSG_E4M3 && ab != BSG_E5M2 && ab != BSG_E2M1) return BSG_ERR_INVALID_ARG;
+  return BSG_ERR_UNSUPPORTED;  // E5M2 operands, MXFP4 (E2M1 with E8M0 scales)
+}
+
+bool fits_int32(int64_t v) { return v >= 0 && v < (int64_t(1) << 31); }
+
+int choose_tile_n(int64_t n, int64_t m_tiles_total, int num_sms, const bsg_gemm_opts* opts) {
+  if (opts && (opts->tile_n == 128 || opts->tile_n == 256)) return opts->tile_n;
+  if (n <= 128) return 128;
+  // prefer 256-wide tiles unless that leaves SMs idle
+  return (m_tiles_total * cdiv(n, 256) >= num_sms) ? 256 : 128;
+}
+
+int grid_size(int64_t tiles, int num_sms, const bsg_gemm_opts* opts) {
+  int64_t g = num_sms;
+  if (opts && opts->max_ctas > 0 && opts->max_ctas < g) g = opts->max_ctas;
+  if (tiles < g) g = tiles;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t bsg_workspace_size(void) { return kWorkspaceBytes; }
+
+size_t bsg_sf_bytes(int64_t batch, int64_t rows, int64_t k, int sf_vec_size) {
+  if (batch <= 0 || rows <= 0 || k <= 0 || sf_vec_size <= 0) return 0;
+  return static_cast<size_t>(batch * cdiv(rows, 128) * cdiv(cdiv(k, sf_vec_size), 4) * 512);
+}
+
+const char* bsg_status_string(bsg_status s) {
+  switch (s) {
+    case BSG_OK: return "BSG_OK";
+    case BSG_ERR_INVALID_ARG: return "BSG_ERR_INVALID_ARG";
+    case BSG_ERR_UNSUPPORTED: return "BSG_ERR_UNSUPPORTED";
+    case BSG_ERR_ALIGNMENT: return "BSG_ERR_ALIGNMENT";
+    case BSG_ERR_ARCH: return "BSG_ERR_ARCH";
+    case BSG_ERR_CUDA: return "BSG_ERR_CUDA";
+    case BSG_ERR_DEVICE: return "BSG_ERR_DEVICE";
+    case BSG_ERR_BAD_OFFSETS: return "BSG_ERR_BAD_OFFSETS";
+    case BSG_ERR_WORKSPACE: return "BSG_ERR_WORKSPACE";
+  }
+  return "BSG_ERR_UNKNOWN";
+}
+
+bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t k, bsg_dtype q_dtype,
+                           int sf_vec_size, bsg_sf_dtype sf_dtype, void* q, uint8_t* sf, void* stream) {
+  int fmt = 0;
+  bsg_status st = operand_format(q_dtype, sf_dtype, sf_vec_size, &fmt);
+  if (st != BSG_OK) return st;
+  if (!x || !q || !sf) return BSG_ERR_INVALID_ARG;
+  if (batch < 1 || rows < 1 || k < sf_vec_size || k % sf_vec_size != 0) return BSG_ERR_INVALID_ARG;
+  if ((fmt == bsg::kMXFP8 && k % 16 != 0) || (fmt == bsg::kNVFP4 && k % 32 != 0)) return BSG_ERR_ALIGNMENT;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return BSG_ERR_ALIGNMENT;
+  DeviceInfo info;
+  st = current_device(nullptr, &info);
+  if (st != BSG_OK) return st;
+  cudaError_t e = bsg::launch_quantize(fmt, x, batch, rows, k, static_cast<uint8_t*>(q), sf, info.num_sms,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+}
+
+bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb, bsg_dtype ab_dtype,
+                         bsg_sf_dtype sf_dtype, int sf_vec_size, int64_t m, int64_t n, int64_t k, int64_t l,
+                         void* c, bsg_dtype c_dtype, float* amax, const bsg_gemm_opts* opts, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  int fmt = 0;
+  bsg_status st = operand_format(ab_dtype, sf_dtype, sf_vec_size, &fmt);
+  if (st != BSG_OK) return st;
+  if (!a || !b || !sfa || !sfb || !c || !amax) return BSG_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
+  if (m < 1 || n < 1 || k < 1 || l < 1) return BSG_ERR_INVALID_ARG;
+  if (!fits_int32(m) || !fits_int32(n) || !fits_int32(k) || !fits_int32(l)) return BSG_ERR_INVALID_ARG;
+  if (k % sf_vec_size != 0) return BSG_ERR_INVALID_ARG;
+  if (c_dtype != BSG_F32 && c_dtype != BSG_BF16) return BSG_ERR_UNSUPPORTED;
+  const int64_t row_bytes = fmt == bsg::kMXFP8 ? k : k / 2;
+  const int64_t c_size = c_dtype == BSG_F32 ? 4 : 2;
+  if (row_bytes % 16 != 0 || (n * c_size) % 16 != 0) return BSG_ERR_ALIGNMENT;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(c) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || (reinterpret_cast<uintptr_t>(amax) & 3u) != 0)
+    return BSG_ERR_ALIGNMENT;
+  DeviceInfo info;
+  st = current_device(nullptr, &info);
+  if (st != BSG_OK) return st;
+
+  const int64_t m_tiles = cdiv(m, 128);
+  const int bn = choose_tile_n(n, m_tiles * l, info.num_sms, opts);
+  const int64_t n_tiles = cdiv(n, bn);
+  const int64_t tiles = l * m_tiles * n_tiles;
+  const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
+  if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
+
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, a, row_bytes, m, l, 128) || !make_operand_map(&tb, b, row_bytes, n, l, bn))
+    return BSG_ERR_CUDA;
+
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.m = static_cast<int>(m);
+  p.n = static_cast<int>(n);
+  p.k = static_cast<int>(k);
+  p.l = static_cast<int>(l);
+  p.m_tiles = static_cast<int>(m_tiles);
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.k_tiles = static_cast<int>(cdiv(k, elems_per_ktile));
+  p.num_tiles = static_cast<int>(tiles);
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.sfa_mt = static_cast<int>(m_tiles);
+  p.sfb_mt = static_cast<int>(cdiv(n, 128));
+  p.sf_kt = static_cast<int>(cdiv(k / sf_vec_size, 4));
+  p.c = c;
+  p.c_kind = c_dtype == BSG_F32 ? bsg::kOutF32 : bsg::kOutBF16;
+  p.amax = amax;
+  p.err = static_cast<uint32_t*>(workspace);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
+  if (cudaMemsetAsync(amax, 0, sizeof(float), s) != cudaSuccess) return BSG_ERR_CUDA;
+  GemmConfig cfg{fmt, bn, bsg::kEpiDense};
+  cudaError_t e = bsg::launch_gemm_dense(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
+  return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+}
+
+bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
+                                  bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size, int64_t valid_m,
+                                  int64_t n, int64_t k, int64_t num_experts, const int32_t* padded_offsets,
+                                  const float* alpha, const float* prob, float tanh_clamp_scale,
+                                  const float* norm_const, void* c, bsg_dtype c_dtype, void* d, void* d_col,
+                                  bsg_dtype d_dtype, uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
+                                  const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  int fmt = 0;
+  bsg_status st = operand_format(ab_dtype, sf_dtype, sf_vec_size, &fmt);
+  if (st != BSG_OK) return st;
+  if (!a || !b || !sfa || !sfb || !padded_offsets || !alpha || !prob || !d) return BSG_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
+  if (valid_m < 0 || valid_m % 256 != 0 || n < 1 || k < 1 || num_experts < 1 || num_experts > 1024)
+    return BSG_ERR_INVALID_ARG;
+  if (!fits_int32(valid_m) || !fits_int32(n) || !fits_int32(k)) return BSG_ERR_INVALID_ARG;
+  if (k % sf_vec_size != 0) return BSG_ERR_INVALID_ARG;
+  const bool fp8_d = d_dtype == BSG_E4M3;
+  if (d_dtype != BSG_BF16 && !fp8_d) return BSG_ERR_UNSUPPORTED;
+  if (fp8_d) {
+    if (fmt != bsg::kMXFP8) return BSG_ERR_UNSUPPORTED;
+    if (!d_col || !sfd_row || !sfd_col || !norm_const) return BSG_ERR_INVALID_ARG;
+    if (n % 32 != 0) return BSG_ERR_INVALID_ARG;
+  } else {
+    if (!amax || d_col || sfd_row || sfd_col) return BSG_ERR_INVALID_ARG;
+  }
+  if (c && c_dtype != BSG_BF16 && c_dtype != BSG_F32) return BSG_ERR_UNSUPPORTED;
+  if (!(tanh_clamp_scale == tanh_clamp_scale)) return BSG_ERR_INVALID_ARG;  // NaN
+  const int64_t row_bytes = fmt == bsg::kMXFP8 ? k : k / 2;
+  const int64_t d_size = fp8_d ? 1 : 2;
+  const int64_t c_size = c_dtype == BSG_F32 ? 4 : 2;
+  if (row_bytes % 16 != 0 || (n * d_size) % 16 != 0 || (c && (n * c_size) % 16 != 0)) return BSG_ERR_ALIGNMENT;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d) ||
+      (c && !aligned16(c)) || (d_col && !aligned16(d_col)) || (sfd_row && !aligned16(sfd_row)) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || (reinterpret_cast<uintptr_t>(padded_offsets) & 3u))
+    return BSG_ERR_ALIGNMENT;
+  DeviceInfo info;
+  st = current_device(nullptr, &info);
+  if (st != BSG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (opts && opts->validate_offsets) {
+    std::vector<int32_t> h(static_cast<size_t>(num_experts));
+    if (cudaMemcpyAsync(h.data(), padded_offsets, h.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return BSG_ERR_CUDA;
+    int32_t prev = 0;
+    for (size_t i = 0; i < h.size(); ++i) {
+      if (h[i] % 256 != 0 || h[i] < prev || h[i] > valid_m) return BSG_ERR_BAD_OFFSETS;
+      prev = h[i];
+    }
+    if (prev != valid_m) return BSG_ERR_BAD_OFFSETS;
+  }
+
+  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
+  if (!fp8_d && cudaMemsetAsync(amax, 0, sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
+  if (fp8_d && n % 128 != 0) {
+    // SFD_col rows n .. ceil(n/128)*128 are padding the kernel never touches
+    if (cudaMemsetAsync(sfd_col, 0, bsg_sf_bytes(1, n, valid_m, 32), s) != cudaSuccess) return BSG_ERR_CUDA;
+  }
+  if (valid_m == 0) return BSG_OK;
+
+  const int64_t m_tiles = valid_m / 128;
+  const int bn = choose_tile_n(n, m_tiles, info.num_sms, opts);
+  const int64_t n_tiles = cdiv(n, bn);
+  const int64_t tiles = m_tiles * n_tiles;
+  if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
+  const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
+
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128) ||
+      !make_operand_map(&tb, b, row_bytes, n, num_experts, bn))
+    return BSG_ERR_CUDA;
+
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.m = static_cast<int>(valid_m);
+  p.n = static_cast<int>(n);
+  p.k = static_cast<int>(k);
+  p.l = static_cast<int>(num_experts);
+  p.m_tiles = static_cast<int>(m_tiles);
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.k_tiles = static_cast<int>(cdiv(k, elems_per_ktile));
+  p.num_tiles = static_cast<int>(tiles);
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.sfa_mt = static_cast<int>(m_tiles);
+  p.sfb_mt = static_cast<int>(cdiv(n, 128));
+  p.sf_kt = static_cast<int>(cdiv(k / sf_vec_size, 4));
+  p.c = c;
+  p.c_kind = !c ? bsg::kOutNone : (c_dtype == BSG_F32 ? bsg::kOutF32 : bsg::kOutBF16);
+  p.amax = amax;
+  p.offsets = padded_offsets;
+  p.alpha = alpha;
+  p.prob = prob;
+  p.clamp_s = tanh_clamp_scale > 0.0f ? tanh_clamp_scale : 0.0f;
+  p.tanh_approx = (opts && opts->tanh_approx) ? 1 : 0;
+  p.norm_const = norm_const;
+  p.d = d;
+  p.d_col = d_col;
+  p.sfd_row = sfd_row;
+  p.sfd_col = sfd_col;
+  p.sfd_row_kt = static_cast<int>(cdiv(n, 128));
+  p.sfd_col_mt = static_cast<int>(cdiv(n, 128));
+  p.sfd_col_kt = static_cast<int>(cdiv(valid_m, 128));
+  p.err = static_cast<uint32_t*>(workspace);
+
+  GemmConfig cfg{fmt, bn, fp8_d ? bsg::kEpiGroupedFP8 : bsg::kEpiGroupedBF16};
+  cudaError_t e = bsg::launch_gemm_grouped(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
+  if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+}
+
+bsg_status bsg_read_device_error(const void* workspace, void* stream, uint32_t* error_bits) {
+  if (!workspace || !error_bits) return BSG_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BSG_ERR_CUDA;
+  uint32_t bits = 0;
+  if (cudaMemcpy(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return BSG_ERR_CUDA;
+  *error_bits = bits;
+  return bits ? BSG_ERR_DEVICE : BSG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,537 @@
+// gemm_kernel.cuh -- persistent, warp-specialised block-scaled GEMM for sm_103a.
+//
+// One CTA per SM walks a static list of 128 x BN output tiles (dense: batch-major, then
+// groups of 16 M-tiles swept along N; grouped: M-tile-major over the experts' padded row
+// ranges).  Six warps:
+//   warp 0     TMA producer: per 128-byte K slice, A (128 rows) and B (BN rows) tiles with
+//              128-byte swizzle via cp.async.bulk.tensor, and the scale-factor atoms via
+//              cp.async.bulk, into a STAGES-deep shared-memory ring (full/empty mbarriers);
+//   warp 1     TMEM owner and MMA issuer: one thread copies the stage's scale factors to
+//              TMEM (tcgen05.cp 32x128b.warpx4) and issues four block-scaled tcgen05.mma
+//              (kind::mxf8f6f4 scale_vec::1X for MXFP8, kind::mxf4nvf4 scale_vec::4X for
+//              NVFP4) into an fp32 accumulator in TMEM, then tcgen05.commit frees the stage;
+//   warps 2-5  epilogue: each warp owns one 32-lane quadrant of TMEM (= 32 rows of the
+//              tile), reads 32-column chunks with tcgen05.ld and applies the dense (C + amax)
+//              or grouped (alpha, C, sReLU / tanh clamp, D, per-expert amax or MXFP8 row and
+//              column re-quantisation) epilogue.
+// ACC accumulator buffers let the epilogue of one tile overlap the MMAs of the next.
+// Every wait is bounded: a wait longer than kWaitLimitNs records a device error, the CTA
+// drains its own in-flight copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsg {
+
+constexpr int kThreadsGemm = 192;
+constexpr int kTileM = 128;
+constexpr int kTileKBytes = 128;  // one 128-byte swizzle row of K per stage
+
+template <int FMT, int BN>
+struct GemmTraits {
+  static constexpr int kElemsPerKTile = FMT == kMXFP8 ? 128 : 256;
+  static constexpr int kMmaK = FMT == kMXFP8 ? 32 : 64;  // elements per tcgen05.mma (32 bytes)
+  static constexpr int kMmasPerStage = 4;
+  static constexpr int kAtomsPerStage = FMT == kMXFP8 ? 1 : 4;  // SF atoms (128 rows x 4 blocks) along K
+  static constexpr int kBRowGroups = BN / 128;
+  static constexpr int kABytes = kTileM * kTileKBytes;
+  static constexpr int kBBytes = BN * kTileKBytes;
+  static constexpr int kSfaBytes = kAtomsPerStage * 512;
+  static constexpr int kSfbBytes = kBRowGroups * kAtomsPerStage * 512;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kStages = (BN == 256) ? 4 : (FMT == kMXFP8 ? 6 : 5);
+  static constexpr int kAcc = (BN == 256) ? 1 : 2;
+  static constexpr int kSfaCols = kAtomsPerStage * 4;
+  static constexpr int kSfbCols = kBRowGroups * kAtomsPerStage * 4;
+  static constexpr int kSfStride = ((kSfaCols + kSfbCols + 15) / 16) * 16;
+  static constexpr int kSfBase = kAcc * BN;
+  static constexpr int kTmemUsed = kSfBase + kStages * kSfStride;
+  static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                   : kTmemUsed <= 256 ? 256 : 512;
+  static_assert(kTmemUsed <= 512, "TMEM budget");
+  // barrier / scalar area after the stages
+  static constexpr int kBarBytes = 1024;
+  static constexpr int kOffsetsBytes = 4096;  // padded_offsets of up to 1024 experts (grouped)
+  static constexpr int kAmaxBytes = 4096;     // per-expert amax staging (grouped bf16 D)
+  static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarBytes +
+                                    kOffsetsBytes + kAmaxBytes;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+  // Instruction descriptor: A/B formats (bits 7-12), K-major A and B, N >> 3 (bits 17-22),
+  // scale format (bit 23: 1 = UE8M0, 0 = UE4M3), M >> 4 (bits 24-28).
+  static constexpr uint32_t kIdesc = (FMT == kMXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))
+                                                    : ((1u << 7) | (1u << 10) | (0u << 23))) |
+                                     (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     (static_cast<uint32_t>(kTileM >> 4) << 24);
+};
+
+struct TileCoord {
+  int l;   // batch (dense) or expert (grouped)
+  int mt;  // 128-row tile index
+  int nt;  // BN-column tile index
+};
+
+__device__ __forceinline__ int find_expert(const int32_t* offs, int num_experts, int row) {
+  int lo = 0, hi = num_experts - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (offs[mid] > row) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+template <int EPI>
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t, const int32_t* offs) {
+  TileCoord tc;
+  if (EPI == kEpiDense) {
+    const int per_batch = p.m_tiles * p.n_tiles;
+    tc.l = t / per_batch;
+    const int idx = t - tc.l * per_batch;
+    constexpr int kGroupM = 16;
+    const int group = idx / (kGroupM * p.n_tiles);
+    const int first_m = group * kGroupM;
+    const int gm = min(kGroupM, p.m_tiles - first_m);
+    const int loc = idx - group * kGroupM * p.n_tiles;
+    tc.mt = first_m + loc % gm;
+    tc.nt = loc / gm;
+  } else {
+    tc.mt = t / p.n_tiles;
+    tc.nt = t - tc.mt * p.n_tiles;
+    tc.l = find_expert(offs, p.l, tc.mt * kTileM);
+  }
+  return tc;
+}
+
+__device__ __forceinline__ void store16(void* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  *reinterpret_cast<uint4*>(dst) = make_uint4(a, b, c, d);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
+  atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
+}
+
+// sReLU with optional tanh soft clamp: s * min(tanh(relu(c) / s), 1) (or relu(c)), squared, times prob.
+__device__ __forceinline__ float srelu_clamp(float c, float prob, float s, int tanh_approx) {
+  float r = fmaxf(c, 0.0f);
+  if (s > 0.0f) {
+    const float u = __fdiv_rn(r, s);
+    float t;
+    if (tanh_approx) {
+      asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(u));
+    } else {
+      t = tanhf(u);
+    }
+    r = s * fminf(t, 1.0f);
+  }
+  return prob * (r * r);
+}
+
+// Butterfly reduce-scatter of 32 values across the warp: afterwards v[0] of lane i holds the
+// maximum over all 32 lanes of the original v[i].
+__device__ __forceinline__ void warp_colmax_scatter(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float send = upper ? v[j] : v[j + w];
+      const float keep = upper ? v[j + w] : v[j];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+      v[j] = fmaxf(keep, recv);
+    }
+  }
+}
+
+template <int FMT, int BN, int EPI>
+__global__ void __launch_bounds__(kThreadsGemm, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                const __grid_constant__ GemmParams p) {
+  using T = GemmTraits<FMT, BN>;
+  constexpr int S = T::kStages;
+  constexpr int ACC = T::kAcc;
+
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzled TMA tiles need 1024-byte aligned shared addresses
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* s_a = smem;
+  uint8_t* s_b = s_a + S * T::kABytes;
+  uint8_t* s_sfa = s_b + S * T::kBBytes;
+  uint8_t* s_sfb = s_sfa + S * T::kSfaBytes;
+  uint8_t* s_bar = s_sfb + S * T::kSfbBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_bar);
+  uint64_t* empty = full + S;
+  uint64_t* tmem_full = empty + S;
+  uint64_t* tmem_empty = tmem_full + ACC;
+  uint64_t* drain = tmem_empty + ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* bad_flag = const_cast<int*>(abort_flag) + 1;
+  int32_t* s_offs = reinterpret_cast<int32_t*>(s_bar + T::kBarBytes);
+  float* s_amax = reinterpret_cast<float*>(s_bar + T::kBarBytes + T::kOffsetsBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *bad_flag = 0;
+    fence_mbar_init();
+  }
+  if (EPI != kEpiDense) {
+    for (int i = threadIdx.x; i < 1024; i += kThreadsGemm) s_amax[i] = 0.0f;
+  } else if (threadIdx.x == 0) {
+    s_amax[0] = 0.0f;
+  }
+  __syncthreads();
+  if (EPI != kEpiDense) {
+    // stage padded_offsets and check: multiples of 256, non-decreasing, last == valid_m
+    for (int i = threadIdx.x; i < p.l; i += kThreadsGemm) {
+      const int32_t o = p.offsets[i];
+      const int32_t prev = i == 0 ? 0 : p.offsets[i - 1];
+      s_offs[i] = o;
+      if ((o & 255) != 0 || o < prev || o > p.m || (i == p.l - 1 && o != p.m)) atomicOr(bad_flag, 1);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, T::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const bool bad = *bad_flag != 0;
+  if (bad && blockIdx.x == 0 && threadIdx.x == 0) report_error(p.err, kErrBadOffsets);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && !bad) {
+      uint32_t stage = 0, phase = 0;
+      uint64_t issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
+        const int a_batch = EPI == kEpiDense ? tc.l : 0;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          const int k_left = p.k - kt * T::kElemsPerKTile;
+          const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
+          const int atoms = FMT == kMXFP8 ? 1 : n_mma;
+          const uint32_t sf_bytes = static_cast<uint32_t>(atoms * 512 * (1 + T::kBRowGroups));
+          mbar_arrive_expect_tx(&full[stage], T::kABytes + T::kBBytes + sf_bytes);
+          tma_load_3d(s_a + stage * T::kABytes, &tmap_a, &full[stage], kt * kTileKBytes, tc.mt * kTileM, a_batch);
+          tma_load_3d(s_b + stage * T::kBBytes, &tmap_b, &full[stage], kt * kTileKBytes, tc.nt * BN, tc.l);
+          const uint8_t* sfa_src =
+              p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + tc.mt) * p.sf_kt +
+                       static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+          bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, &full[stage]);
+#pragma unroll
+          for (int i = 0; i < T::kBRowGroups; ++i) {
+            // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
+            const int rb = min(tc.nt * T::kBRowGroups + i, p.sfb_mt - 1);
+            const uint8_t* sfb_src =
+                p.sfb + ((static_cast<uint64_t>(tc.l) * p.sfb_mt + rb) * p.sf_kt +
+                         static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+            bulk_load(s_sfb + stage * T::kSfbBytes + i * T::kAtomsPerStage * 512, sfb_src, atoms * 512,
+                      &full[stage]);
+          }
+          ++issued;
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // drain: every load issued must land before the CTA leaves
+        for (int s = 0; s < S; ++s) {
+          if (issued > static_cast<uint64_t>(s)) {
+            const uint32_t ph = (s < static_cast<int>(stage)) ? phase : (phase ^ 1u);
+            wait_bounded_plain(&full[s], ph);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (!bad) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
+      const uint32_t sfa_base = smem_u32(s_sfa), sfb_base = smem_u32(s_sfb);
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!wait_bounded(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const int k_left = p.k - kt * T::kElemsPerKTile;
+            const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
+            const int atoms = FMT == kMXFP8 ? 1 : n_mma;
+            const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
+            const uint32_t sfb_t = sfa_t + T::kSfaCols;
+            for (int a = 0; a < atoms; ++a) {
+              tc_cp_32x128b_warpx4(sfa_t + a * 4,
+                                   smem_desc(sfa_base + stage * T::kSfaBytes + a * 512, 0, 128, kSwizzleNone));
+#pragma unroll
+              for (int i = 0; i < T::kBRowGroups; ++i) {
+                tc_cp_32x128b_warpx4(
+                    sfb_t + (a * T::kBRowGroups + i) * 4,
+                    smem_desc(sfb_base + stage * T::kSfbBytes + (i * T::kAtomsPerStage + a) * 512, 0, 128,
+                              kSwizzleNone));
+              }
+            }
+            const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
+            const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
+            for (int j = 0; j < n_mma; ++j) {
+              const uint32_t accumulate = (kt > 0 || j > 0) ? 1u : 0u;
+              // advance the start address by 32 bytes of K per MMA (encoded >> 4)
+              if (FMT == kMXFP8) {
+                const uint32_t idesc = T::kIdesc | (static_cast<uint32_t>(j) << 29) | (static_cast<uint32_t>(j) << 4);
+                tc_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t, sfb_t, accumulate);
+              } else {
+                tc_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
+                                sfb_t + j * T::kBRowGroups * 4, accumulate);
+              }
+            }
+            tc_commit(&empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit(&tmem_full[acc]);
+        __syncwarp();
+        if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) {
+        // drain: wait for every MMA issued so far before TMEM is released
+        if (lane == 0) {
+          tc_commit(drain);
+          wait_bounded_plain(drain, 0);
+        }
+        __syncwarp();
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps 2..5
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    float run_max = 0.0f;       // dense amax, or grouped per-expert segment max
+    int run_expert = -1;
+    uint32_t acc = 0, acc_phase = 0;
+    const float s_clamp = p.clamp_s;
+    const float nc = (EPI == kEpiGroupedFP8) ? *p.norm_const : 1.0f;
+    for (int t = blockIdx.x; !bad && t < p.num_tiles; t += gridDim.x) {
+      const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
+      if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int row = tc.mt * kTileM + quad * 32 + lane;
+      const bool row_ok = row < p.m;
+      float alpha_g = 1.0f, prob_r = 0.0f;
+      if (EPI != kEpiDense) {
+        alpha_g = p.alpha[tc.l];
+        prob_r = p.prob[row];
+        if (tc.l != run_expert) {
+          if (run_expert >= 0) {
+            float v = run_max;
+            for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0 && EPI == kEpiGroupedBF16) atomic_max_nonneg(&s_amax[run_expert], v);
+          }
+          run_expert = tc.l;
+          run_max = 0.0f;
+        }
+      }
+      uint32_t sfd_row_word = 0;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = tc.nt * BN + c * 32;
+        if (col0 >= p.n) break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + c * 32, r);
+        tmem_ld_wait(r);
+        if (EPI == kEpiDense) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(__uint_as_float(r[j])));
+          if (row_ok) {
+            if (p.c_kind == kOutF32) {
+              float* dst = reinterpret_cast<float*>(p.c) +
+                           (static_cast<uint64_t>(tc.l) * p.m + row) * static_cast<uint64_t>(p.n) + col0;
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                if (col0 + j < p.n) store16(dst + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
+            } else {
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.c) +
+                                   (static_cast<uint64_t>(tc.l) * p.m + row) * static_cast<uint64_t>(p.n) + col0;
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                if (col0 + j < p.n) {
+                  store16(dst + j, pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                          pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                          pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                          pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+                }
+              }
+            }
+          }
+        } else {
+          float d[32];
+          const uint64_t rc = static_cast<uint64_t>(row) * p.n + col0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float cv = alpha_g * __uint_as_float(r[j]);
+            r[j] = __float_as_uint(cv);
+            d[j] = srelu_clamp(cv, prob_r, s_clamp, p.tanh_approx);
+          }
+          // a chunk may run past N (N % 8 == 0 for 16-bit outputs, % 4 for fp32): 16-byte granules
+          if (p.c_kind == kOutBF16) {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.c) + rc;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8)
+              if (col0 + j < p.n)
+                store16(dst + j, pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                        pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                        pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                        pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+          } else if (p.c_kind == kOutF32) {
+            float* dst = reinterpret_cast<float*>(p.c) + rc;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              if (col0 + j < p.n) store16(dst + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
+          }
+          if (EPI == kEpiGroupedBF16) {
+            // columns past N hold zeros (zero-filled B rows), so they cannot raise the maximum
+#pragma unroll
+            for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(d[j]));
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.d) + rc;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8)
+              if (col0 + j < p.n)
+                store16(dst + j, pack_bf16x2(d[j], d[j + 1]), pack_bf16x2(d[j + 2], d[j + 3]),
+                        pack_bf16x2(d[j + 4], d[j + 5]), pack_bf16x2(d[j + 6], d[j + 7]));
+          } else {
+            // row MXFP8: this thread's 32 columns form one block
+            float bmax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, fabsf(d[j]));
+            const uint32_t code_r = e8m0_ceil_code(nc * bmax);
+            const float inv_r = e8m0_inv_scale(code_r);
+            uint32_t q[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j], nc), inv_r),
+                                             __fmul_rn(__fmul_rn(d[4 * j + 1], nc), inv_r));
+              const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j + 2], nc), inv_r),
+                                             __fmul_rn(__fmul_rn(d[4 * j + 3], nc), inv_r));
+              q[j] = lo | (hi << 16);
+            }
+            uint8_t* drow = reinterpret_cast<uint8_t*>(p.d) + rc;
+            store16(drow, q[0], q[1], q[2], q[3]);
+            store16(drow + 16, q[4], q[5], q[6], q[7]);
+            const int nb = col0 >> 5;
+            sfd_row_word |= code_r << (8 * (nb & 3));
+            if ((nb & 3) == 3 || col0 + 32 >= p.n || c == BN / 32 - 1) {
+              const uint64_t off = sf_offset(row, nb & ~3, 0, p.m_tiles, p.sfd_row_kt);
+              *reinterpret_cast<uint32_t*>(p.sfd_row + off) = sfd_row_word;
+              sfd_row_word = 0;
+            }
+            // column MXFP8: the warp's 32 lanes are 32 consecutive rows (one block per column)
+            float cm[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cm[j] = fabsf(d[j]);
+            warp_colmax_scatter(cm, lane);
+            const uint32_t code_c = e8m0_ceil_code(nc * cm[0]);
+            const float inv_c = e8m0_inv_scale(code_c);
+            const int mblk = row >> 5;  // same for the whole warp
+            p.sfd_col[sf_offset(col0 + lane, mblk, 0, p.sfd_col_mt, p.sfd_col_kt)] = static_cast<uint8_t>(code_c);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float i0 = __shfl_sync(0xffffffffu, inv_c, 4 * j);
+              const float i1 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 1);
+              const float i2 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 2);
+              const float i3 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 3);
+              const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j], nc), i0),
+                                             __fmul_rn(__fmul_rn(d[4 * j + 1], nc), i1));
+              const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j + 2], nc), i2),
+                                             __fmul_rn(__fmul_rn(d[4 * j + 3], nc), i3));
+              q[j] = lo | (hi << 16);
+            }
+            uint8_t* dcol = reinterpret_cast<uint8_t*>(p.d_col) + rc;
+            store16(dcol, q[0], q[1], q[2], q[3]);
+            store16(dcol + 16, q[4], q[5], q[6], q[7]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
+    }
+    // fold this warp's running maximum into shared memory
+    float v = run_max;
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) {
+      if (EPI == kEpiDense) atomic_max_nonneg(&s_amax[0], v);
+      else if (EPI == kEpiGroupedBF16 && run_expert >= 0) atomic_max_nonneg(&s_amax[run_expert], v);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (!bad && *abort_flag == 0) {
+    // one global atomicMax per CTA (dense) or per CTA and expert touched (grouped bf16 D)
+    if (EPI == kEpiDense) {
+      if (threadIdx.x == 0 && s_amax[0] > 0.0f) atomic_max_nonneg(p.amax, s_amax[0]);
+    } else if (EPI == kEpiGroupedBF16) {
+      for (int g = threadIdx.x; g < p.l; g += kThreadsGemm)
+        if (s_amax[g] > 0.0f) atomic_max_nonneg(&p.amax[g], s_amax[g]);
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, T::kTmemCols);
+  }
+}
+
+template <int FMT, int BN, int EPI>
+cudaError_t launch_gemm_t(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const GemmParams& p, int grid,
+                          cudaStream_t stream) {
+  using T = GemmTraits<FMT, BN>;
+  auto kern = gemm_kernel<FMT, BN, EPI>;
+  static bool attr_set[64] = {};  // per instantiation and device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  kern<<<grid, kThreadsGemm, T::kSmemBytes, stream>>>(tmap_a, tmap_b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace bsg

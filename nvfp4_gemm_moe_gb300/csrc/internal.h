@@ -1,0 +1,67 @@
+// internal.h -- launch interfaces between the C ABI (bsg_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bsg {
+
+enum Fmt : int { kMXFP8 = 0, kNVFP4 = 1 };
+enum OutKind : int { kOutNone = 0, kOutF32 = 1, kOutBF16 = 2, kOutE4M3 = 3 };
+enum EpiKind : int { kEpiDense = 0, kEpiGroupedBF16 = 1, kEpiGroupedFP8 = 2 };
+
+// Everything a GEMM kernel needs besides the two tensor maps.
+struct GemmParams {
+  // problem
+  int m, n, k;           // rows of A, rows of B (N), K in elements
+  int l;                 // batch (dense) or number of experts (grouped)
+  int m_tiles, n_tiles;  // ceil(m/128), ceil(n/BN)
+  int k_tiles;           // ceil(K / elements per 128-byte K tile)
+  int num_tiles;         // l*m_tiles*n_tiles (dense) or m_tiles*n_tiles (grouped)
+  // scale factors
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int sfa_mt, sfb_mt;    // ceil(m/128), ceil(n/128)
+  int sf_kt;             // ceil(K / (4 v)) atoms along K
+  // dense epilogue
+  void* c;
+  int c_kind;            // OutKind
+  float* amax;           // dense: 1 float; grouped bf16 D: num_experts floats
+  // grouped epilogue
+  const int32_t* offsets;
+  const float* alpha;
+  const float* prob;
+  float clamp_s;         // <= 0: no tanh clamp
+  int tanh_approx;
+  const float* norm_const;
+  void* d;
+  void* d_col;
+  uint8_t* sfd_row;
+  uint8_t* sfd_col;
+  int sfd_row_kt;        // ceil(n / 128): atoms along N of SFD_row
+  int sfd_col_mt;        // ceil(n / 128): 128-row groups of SFD_col
+  int sfd_col_kt;        // ceil(valid_m / 128): atoms along M of SFD_col
+  // device error word (workspace)
+  uint32_t* err;
+};
+
+struct GemmConfig {
+  int fmt;       // Fmt
+  int bn;        // 128 or 256
+  int epi;       // EpiKind
+};
+
+// Launches the persistent GEMM kernel for `cfg`; returns cudaSuccess or the launch error.
+cudaError_t launch_gemm(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                        const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_dense(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                              const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_grouped(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                                const GemmParams& p, int grid, cudaStream_t stream);
+
+// Launches the block quantiser.
+cudaError_t launch_quantize(int fmt, const float* x, int64_t batch, int64_t rows, int64_t k, uint8_t* q,
+                            uint8_t* sf, int num_sms, cudaStream_t stream);
+
+}  // namespace bsg
