@@ -1,0 +1,127 @@
+"""The C ABI library loads, exports every declared entry point, and validates arguments on the host.
+
+These tests need no GPU: every rejected call returns its status before any CUDA call, and
+the pointers passed are fake values that are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_gemm_moe_gb300 as bsg
+from nvfp4_gemm_moe_gb300 import build as bsg_build
+
+OK, INVALID, UNSUPPORTED, ALIGN, ARCH, CUDA, DEVICE, BAD_OFFS, WORKSPACE = range(9)
+P = 0x10000  # a fake, 16-byte aligned "device pointer" (never dereferenced by a rejected call)
+
+
+def _declared_functions():
+    src = open(bsg.HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:bsg_status|size_t|const char\s*\*)\s*(bsg_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert {"bsg_quantize_mx", "bsg_gemm_amax", "bsg_grouped_gemm_srelu"} <= set(names)
+    lib = ctypes.CDLL(bsg_build.build())
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+    assert os.path.dirname(bsg.LIBRARY_PATH) == os.path.dirname(os.path.abspath(bsg.__file__))
+
+
+def test_sizes_and_strings():
+    assert bsg.bsg_workspace_size() == 256
+    # (batch, ceil(rows/128), ceil(K/(4v)), 32, 4, 4)
+    assert bsg.bsg_sf_bytes(1, 256, 256, 32) == 1 * 2 * 2 * 512
+    assert bsg.bsg_sf_bytes(4, 8192, 8192, 32) == 4 * 64 * 64 * 512
+    assert bsg.bsg_sf_bytes(1, 130, 96, 16) == 2 * 2 * 512
+    assert bsg.bsg_sf_bytes(0, 1, 1, 32) == 0
+    assert bsg.bsg_status_string(0) == "BSG_OK"
+    assert bsg.bsg_status_string(7) == "BSG_ERR_BAD_OFFSETS"
+
+
+def _quant(**kw):
+    a = dict(x=P, batch=1, rows=128, k=256, q=0x1, v=32, sf=0, qp=P, sfp=P, stream=None)
+    a.update(kw)
+    return bsg.raw_status("bsg_quantize_mx", a["x"], a["batch"], a["rows"], a["k"], a["q"], a["v"], a["sf"],
+                          a["qp"], a["sfp"], a["stream"])
+
+
+def test_quantize_validation():
+    E4M3, E2M1, E5M2 = bsg.E4M3, bsg.E2M1, bsg.E5M2
+    assert _quant(q=E4M3, v=32, sf=bsg.SF_UE8M0, x=None) == INVALID
+    assert _quant(q=E4M3, v=16, sf=bsg.SF_UE8M0) == INVALID         # FP8 needs v = 32
+    assert _quant(q=E2M1, v=32, sf=bsg.SF_UE4M3) == INVALID         # E4M3 scales need v = 16
+    assert _quant(q=E5M2, v=32, sf=bsg.SF_UE8M0) == UNSUPPORTED
+    assert _quant(q=E2M1, v=32, sf=bsg.SF_UE8M0) == UNSUPPORTED     # MXFP4
+    assert _quant(q=E4M3, v=32, sf=bsg.SF_UE8M0, k=48) == INVALID   # K not a whole number of blocks
+    assert _quant(q=E2M1, v=16, sf=bsg.SF_UE4M3, k=48) == ALIGN     # K/2 bytes not a multiple of 16
+    assert _quant(q=E4M3, v=32, sf=bsg.SF_UE8M0, x=P + 4) == ALIGN
+    assert _quant(q=E4M3, v=32, sf=bsg.SF_UE8M0, rows=0) == INVALID
+
+
+def _opts():
+    return ctypes.byref(bsg.bsg_gemm_opts())
+
+
+def _dense(**kw):
+    a = dict(a=P, b=P, sfa=P, sfb=P, ab=bsg.E4M3, sf=bsg.SF_UE8M0, v=32, m=256, n=256, k=256, l=1, c=P,
+             ck=bsg.BF16, amax=P, ws=P, wsb=256)
+    a.update(kw)
+    return bsg.raw_status("bsg_gemm_amax", a["a"], a["b"], a["sfa"], a["sfb"], a["ab"], a["sf"], a["v"], a["m"],
+                          a["n"], a["k"], a["l"], a["c"], a["ck"], a["amax"], _opts(), a["ws"], a["wsb"], None)
+
+
+def test_dense_validation():
+    assert _dense(a=None) == INVALID
+    assert _dense(amax=None) == INVALID
+    assert _dense(ws=None) == WORKSPACE
+    assert _dense(wsb=128) == WORKSPACE
+    assert _dense(m=0) == INVALID
+    assert _dense(k=48) == INVALID
+    assert _dense(k=16 * 33) == INVALID                # not a multiple of 32
+    assert _dense(ck=bsg.F16) == UNSUPPORTED
+    assert _dense(n=4) == ALIGN                         # 4 bf16 = 8 bytes per row of C
+    assert _dense(c=P + 8) == ALIGN
+    assert _dense(ws=P + 16) == ALIGN                   # workspace is 256-byte aligned
+    assert _dense(ab=bsg.E2M1, sf=bsg.SF_UE4M3, v=16, k=48) == ALIGN  # 24-byte rows
+    assert _dense(m=1 << 31) == INVALID
+    # a valid call on a machine without a usable sm_103 device stops at the device check
+    st = _dense()
+    assert st in (OK, ARCH, CUDA)
+
+
+def _grouped(**kw):
+    a = dict(a=P, b=P, sfa=P, sfb=P, ab=bsg.E4M3, sf=bsg.SF_UE8M0, v=32, vm=512, n=256, k=256, L=2, offs=P,
+             alpha=P, prob=P, s=0.0, nc=None, c=P, ck=bsg.BF16, d=P, dcol=None, dk=bsg.BF16, sfr=None, sfc=None,
+             amax=P, ws=P, wsb=256)
+    a.update(kw)
+    return bsg.raw_status("bsg_grouped_gemm_srelu", a["a"], a["b"], a["sfa"], a["sfb"], a["ab"], a["sf"], a["v"],
+                          a["vm"], a["n"], a["k"], a["L"], a["offs"], a["alpha"], a["prob"], ctypes.c_float(a["s"]),
+                          a["nc"], a["c"], a["ck"], a["d"], a["dcol"], a["dk"], a["sfr"], a["sfc"], a["amax"],
+                          _opts(), a["ws"], a["wsb"], None)
+
+
+def test_grouped_validation():
+    assert _grouped(prob=None) == INVALID                # prob is required
+    assert _grouped(vm=300) == INVALID                   # valid_m must be a multiple of 256
+    assert _grouped(L=0) == INVALID and _grouped(L=1025) == INVALID
+    assert _grouped(amax=None) == INVALID                # bf16 D needs the per-expert amax
+    assert _grouped(dcol=P) == INVALID                   # D_col only with E4M3 D
+    assert _grouped(dk=bsg.E4M3) == INVALID              # E4M3 D needs d_col, SFD and norm_const
+    assert _grouped(dk=bsg.E4M3, dcol=P, sfr=P, sfc=P, nc=P, amax=None, n=48) == INVALID  # n % 32
+    assert _grouped(dk=bsg.F32) == UNSUPPORTED
+    assert _grouped(ck=bsg.F16) == UNSUPPORTED
+    assert _grouped(s=float("nan")) == INVALID
+    assert _grouped(ws=None) == WORKSPACE
+    assert _grouped(offs=P + 2) == ALIGN
+    st = _grouped()
+    assert st in (OK, ARCH, CUDA)
+
+
+def test_binding_raises_on_bad_status():
+    with pytest.raises(bsg.BsgError) as ei:
+        bsg.bsg_quantize_mx(P, 1, 128, 48, bsg.E4M3, 32, bsg.SF_UE8M0, P, P, stream=0)
+    assert ei.value.status == INVALID
