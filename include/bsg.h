@@ -197,6 +197,31 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
                                   const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
                                   void* stream);
 
+/*
+ * bsg_gemm_amax_noalloc -- bsg_gemm_amax for callers that cannot provide device memory.
+ *
+ * The pages have no counterpart of this call.  It exists for callers that cannot hand the
+ * library device memory of their own at the call site: code running under a memory plan
+ * fixed at start-up that forbids later allocations, and latency-critical paths that cannot
+ * afford cudaMalloc's implicit device synchronisation.  Arguments and results are those of
+ * bsg_gemm_amax without `workspace` / `workspace_bytes`; the call allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine) and instead uses a static device
+ * array of BSG_NOALLOC_SCRATCH_BYTES bytes owned by the library (every GPU that loads the
+ * library holds it until the process exits).
+ * - The first call on a device looks up that array's address on the current device; make
+ *   that first call before any stream capture.
+ * - All calls on a device share the one array: calls that may overlap on the GPU (other
+ *   streams, other threads) race on it.  Each call clears it before its kernel runs.
+ * - Returns BSG_ERR_WORKSPACE if the GEMM's scratch (bsg_workspace_size()) is larger than
+ *   BSG_NOALLOC_SCRATCH_BYTES.  Device-side errors of these calls are not reported.
+ */
+#define BSG_NOALLOC_SCRATCH_BYTES 256
+bsg_status bsg_gemm_amax_noalloc(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
+                                 bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size,
+                                 int64_t m, int64_t n, int64_t k, int64_t l,
+                                 void* c, bsg_dtype c_dtype, float* amax,
+                                 const bsg_gemm_opts* opts, void* stream);
+
 /* Synchronises `stream` and returns the device error bits of the last call that
  * used `workspace` in *error_bits; BSG_ERR_DEVICE if any bit is set. */
 bsg_status bsg_read_device_error(const void* workspace, void* stream, uint32_t* error_bits);

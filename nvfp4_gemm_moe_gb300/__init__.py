@@ -58,6 +58,9 @@ def _load():
     lib.bsg_grouped_gemm_srelu.restype = I
     lib.bsg_grouped_gemm_srelu.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, P, P, F, P, P, I, P, P, I,
                                            P, P, P, ctypes.POINTER(bsg_gemm_opts), P, SZ, P]
+    lib.bsg_gemm_amax_noalloc.restype = I
+    lib.bsg_gemm_amax_noalloc.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, I, P,
+                                          ctypes.POINTER(bsg_gemm_opts), P]
     lib.bsg_read_device_error.restype = I
     lib.bsg_read_device_error.argtypes = [P, P, U32P]
     return lib
@@ -119,6 +122,16 @@ def bsg_gemm_amax(a, b, sfa, sfb, ab_dtype, sf_dtype, sf_vec_size, m, n, k, l, c
     _check(_lib.bsg_gemm_amax(_ptr(a), _ptr(b), _ptr(sfa), _ptr(sfb), ab_dtype, sf_dtype, sf_vec_size, m, n, k, l,
                               _ptr(c), c_dtype, _ptr(amax), ctypes.byref(o), _ptr(workspace), ws_bytes,
                               _stream(stream)), "bsg_gemm_amax")
+
+
+def bsg_gemm_amax_noalloc(a, b, sfa, sfb, ab_dtype, sf_dtype, sf_vec_size, m, n, k, l, c, c_dtype, amax,
+                          stream=None, **opts):
+    """bsg_gemm_amax without a workspace argument: its scratch lives in a static device array
+    of the library (for callers that cannot provide device memory; see include/bsg.h)."""
+    o = _opts(**opts)
+    _check(_lib.bsg_gemm_amax_noalloc(_ptr(a), _ptr(b), _ptr(sfa), _ptr(sfb), ab_dtype, sf_dtype, sf_vec_size, m, n,
+                                      k, l, _ptr(c), c_dtype, _ptr(amax), ctypes.byref(o), _stream(stream)),
+           "bsg_gemm_amax_noalloc")
 
 
 def bsg_grouped_gemm_srelu(a, b, sfa, sfb, ab_dtype, sf_dtype, sf_vec_size, valid_m, n, k, num_experts,

@@ -121,6 +121,16 @@ def test_grouped_validation():
     assert st in (OK, ARCH, CUDA)
 
 
+def test_noalloc_validation():
+    def call(**kw):
+        a = dict(a=P, c=P, amax=P, n=256)
+        a.update(kw)
+        return bsg.raw_status("bsg_gemm_amax_noalloc", a["a"], P, P, P, bsg.E4M3, bsg.SF_UE8M0, 32, 256, a["n"],
+                              256, 1, a["c"], bsg.BF16, a["amax"], _opts(), None)
+    assert call(a=None) in (INVALID, CUDA)
+    assert call(n=4) in (ALIGN, CUDA)
+
+
 def test_binding_raises_on_bad_status():
     with pytest.raises(bsg.BsgError) as ei:
         bsg.bsg_quantize_mx(P, 1, 128, 48, bsg.E4M3, 32, bsg.SF_UE8M0, P, P, stream=0)
