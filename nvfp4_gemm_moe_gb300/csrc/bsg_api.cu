@@ -7,7 +7,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/bsg.h"
+#include "bsg.h"
 #include "internal.h"
 
 namespace {

@@ -10,7 +10,7 @@
 
 #include <mutex>
 
-#include "../../include/bsg.h"
+#include "bsg.h"
 
 namespace {
 
