@@ -38,8 +38,10 @@ class bsg_gemm_opts(ctypes.Structure):
 
 
 def _load():
-    path = _build_mod.LIB
-    if not os.path.exists(path) or os.environ.get("BSG_AUTOBUILD", "1") == "1":
+    # BSG_LIBRARY names a prebuilt library file to load instead of the in-tree build
+    path = os.environ.get("BSG_LIBRARY") or _build_mod.LIB
+    if not os.environ.get("BSG_LIBRARY") and (not os.path.exists(path) or
+                                              os.environ.get("BSG_AUTOBUILD", "1") == "1"):
         path = _build_mod.build()
     lib = ctypes.CDLL(path)
     P, I64, I, F, SZ, U32P = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
