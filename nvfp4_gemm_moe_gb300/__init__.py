@@ -34,7 +34,7 @@ class BsgError(RuntimeError):
 
 class bsg_gemm_opts(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("max_ctas", ctypes.c_int), ("tanh_approx", ctypes.c_int),
-                ("validate_offsets", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
+                ("validate_offsets", ctypes.c_int), ("cta_pair", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 def _load():
@@ -89,9 +89,10 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _opts(tile_n=0, max_ctas=0, tanh_approx=False, validate_offsets=False):
+def _opts(tile_n=0, max_ctas=0, tanh_approx=False, validate_offsets=False, cta_pair=0):
     o = bsg_gemm_opts()
     o.tile_n, o.max_ctas, o.tanh_approx, o.validate_offsets = tile_n, max_ctas, int(tanh_approx), int(validate_offsets)
+    o.cta_pair = cta_pair
     return o
 
 

@@ -80,6 +80,19 @@ bool make_operand_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale-factor buffer viewed as rows of one 512-byte atom (128 x u32), loaded `atoms` rows at a time.
+bool make_sf_map(CUtensorMap* m, const void* base, uint64_t total_atoms, uint32_t atoms) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {128, total_atoms};
+  const cuuint64_t strides[1] = {512};
+  const cuuint32_t box[2] = {128, atoms};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -104,6 +117,21 @@ int choose_tile_n(int64_t n, int64_t m_tiles_total, int num_sms, const bsg_gemm_
   if (n <= 128) return 128;
   // prefer 256-wide tiles unless that leaves SMs idle
   return (m_tiles_total * cdiv(n, 256) >= num_sms) ? 256 : 128;
+}
+
+// CTA pairs (256 x 256 tiles) when asked for, or when the problem still gives every pair a tile.
+bool use_pairs(int64_t tiles256, int64_t m, int64_t n, int num_sms, const bsg_gemm_opts* opts) {
+  if (opts && opts->cta_pair == 1) return false;
+  if (opts && opts->cta_pair == 2) return true;
+  if (opts && opts->tile_n == 128) return false;
+  return m >= 256 && n > 128 && tiles256 >= num_sms / 2;
+}
+
+int max_pairs(int64_t tiles, int num_sms, const bsg_gemm_opts* opts) {
+  int64_t pairs = num_sms / 2;
+  if (opts && opts->max_ctas > 0 && opts->max_ctas / 2 < pairs) pairs = opts->max_ctas / 2;
+  if (tiles < pairs) pairs = tiles;
+  return static_cast<int>(pairs < 1 ? 1 : pairs);
 }
 
 int grid_size(int64_t tiles, int num_sms, const bsg_gemm_opts* opts) {
@@ -179,15 +207,22 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   st = current_device(nullptr, &info);
   if (st != BSG_OK) return st;
 
-  const int64_t m_tiles = cdiv(m, 128);
-  const int bn = choose_tile_n(n, m_tiles * l, info.num_sms, opts);
+  const bool pairs = use_pairs(l * cdiv(m, 256) * cdiv(n, 256), m, n, info.num_sms, opts);
+  const int64_t m_tiles = pairs ? cdiv(m, 256) : cdiv(m, 128);
+  const int bn = pairs ? 256 : choose_tile_n(n, m_tiles * l, info.num_sms, opts);
   const int64_t n_tiles = cdiv(n, bn);
   const int64_t tiles = l * m_tiles * n_tiles;
   const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
 
-  CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, a, row_bytes, m, l, 128) || !make_operand_map(&tb, b, row_bytes, n, l, bn))
+  CUtensorMap ta, tb, tsfa, tsfb;
+  if (!make_operand_map(&ta, a, row_bytes, m, l, 128) ||
+      !make_operand_map(&tb, b, row_bytes, n, l, pairs ? 128 : bn))
+    return BSG_ERR_CUDA;
+  const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
+  const uint32_t atoms_per_stage = fmt == bsg::kMXFP8 ? 1 : 4;
+  if (pairs && (!make_sf_map(&tsfa, sfa, l * cdiv(m, 128) * sf_kt, atoms_per_stage) ||
+                !make_sf_map(&tsfb, sfb, l * cdiv(n, 128) * sf_kt, atoms_per_stage)))
     return BSG_ERR_CUDA;
 
   GemmParams p;
@@ -202,9 +237,9 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   p.num_tiles = static_cast<int>(tiles);
   p.sfa = sfa;
   p.sfb = sfb;
-  p.sfa_mt = static_cast<int>(m_tiles);
+  p.sfa_mt = static_cast<int>(cdiv(m, 128));
   p.sfb_mt = static_cast<int>(cdiv(n, 128));
-  p.sf_kt = static_cast<int>(cdiv(k / sf_vec_size, 4));
+  p.sf_kt = static_cast<int>(sf_kt);
   p.c = c;
   p.c_kind = c_dtype == BSG_F32 ? bsg::kOutF32 : bsg::kOutBF16;
   p.amax = amax;
@@ -214,7 +249,8 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (cudaMemsetAsync(amax, 0, sizeof(float), s) != cudaSuccess) return BSG_ERR_CUDA;
   GemmConfig cfg{fmt, bn, bsg::kEpiDense};
-  cudaError_t e = bsg::launch_gemm_dense(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
+  cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, tsfa, tsfb, p, max_pairs(tiles, info.num_sms, opts), s)
+                        : bsg::launch_gemm_dense(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }
 
@@ -281,16 +317,22 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   }
   if (valid_m == 0) return BSG_OK;
 
-  const int64_t m_tiles = valid_m / 128;
-  const int bn = choose_tile_n(n, m_tiles, info.num_sms, opts);
+  const bool pairs = use_pairs((valid_m / 256) * cdiv(n, 256), valid_m, n, info.num_sms, opts);
+  const int64_t m_tiles = pairs ? valid_m / 256 : valid_m / 128;
+  const int bn = pairs ? 256 : choose_tile_n(n, m_tiles, info.num_sms, opts);
   const int64_t n_tiles = cdiv(n, bn);
   const int64_t tiles = m_tiles * n_tiles;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
   const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
 
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tsfa, tsfb;
   if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128) ||
-      !make_operand_map(&tb, b, row_bytes, n, num_experts, bn))
+      !make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? 128 : bn))
+    return BSG_ERR_CUDA;
+  const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
+  const uint32_t atoms_per_stage = fmt == bsg::kMXFP8 ? 1 : 4;
+  if (pairs && (!make_sf_map(&tsfa, sfa, (valid_m / 128) * sf_kt, atoms_per_stage) ||
+                !make_sf_map(&tsfb, sfb, num_experts * cdiv(n, 128) * sf_kt, atoms_per_stage)))
     return BSG_ERR_CUDA;
 
   GemmParams p;
@@ -305,9 +347,9 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   p.num_tiles = static_cast<int>(tiles);
   p.sfa = sfa;
   p.sfb = sfb;
-  p.sfa_mt = static_cast<int>(m_tiles);
+  p.sfa_mt = static_cast<int>(valid_m / 128);
   p.sfb_mt = static_cast<int>(cdiv(n, 128));
-  p.sf_kt = static_cast<int>(cdiv(k / sf_vec_size, 4));
+  p.sf_kt = static_cast<int>(sf_kt);
   p.c = c;
   p.c_kind = !c ? bsg::kOutNone : (c_dtype == BSG_F32 ? bsg::kOutF32 : bsg::kOutBF16);
   p.amax = amax;
@@ -327,7 +369,8 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   p.err = static_cast<uint32_t*>(workspace);
 
   GemmConfig cfg{fmt, bn, fp8_d ? bsg::kEpiGroupedFP8 : bsg::kEpiGroupedBF16};
-  cudaError_t e = bsg::launch_gemm_grouped(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
+  cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, tsfa, tsfb, p, max_pairs(tiles, info.num_sms, opts), s)
+                        : bsg::launch_gemm_grouped(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
   if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }

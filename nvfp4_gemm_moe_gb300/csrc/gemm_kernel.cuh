@@ -86,7 +86,9 @@ __device__ __forceinline__ int find_expert(const int32_t* offs, int num_experts,
   return lo;
 }
 
-template <int EPI>
+// Tile t -> (batch or expert, M tile of TM rows, N tile).  Dense: batch-major, then groups of 16
+// M tiles swept along N (neighbouring CTAs share A and B in L2); grouped: M-tile-major.
+template <int EPI, int TM = kTileM>
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t, const int32_t* offs) {
   TileCoord tc;
   if (EPI == kEpiDense) {
@@ -103,7 +105,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t, con
   } else {
     tc.mt = t / p.n_tiles;
     tc.nt = t - tc.mt * p.n_tiles;
-    tc.l = find_expert(offs, p.l, tc.mt * kTileM);
+    tc.l = find_expert(offs, p.l, tc.mt * TM);
   }
   return tc;
 }
@@ -149,6 +151,137 @@ __device__ __forceinline__ void warp_colmax_scatter(float (&v)[32], int lane) {
       const float keep = upper ? v[j + w] : v[j];
       const float recv = __shfl_xor_sync(0xffffffffu, send, w);
       v[j] = fmaxf(keep, recv);
+    }
+  }
+}
+
+// Epilogue of one tile for the rows of one warp: reads the fp32 accumulator chunk by chunk
+// (32 columns of this thread's row per tcgen05.ld) from `tmem_acc` (this warp's lane
+// quadrant, first accumulator column) and writes the outputs of row `row`, columns
+// col_base .. col_base + BN - 1 (clipped at N).  `l` is the batch (dense) or expert (grouped).
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int row, int col_base, uint32_t tmem_acc,
+                                              int lane, float alpha_g, float prob_r, float nc, float& run_max) {
+  const bool row_ok = row < p.m;
+  const float s_clamp = p.clamp_s;
+  uint32_t sfd_row_word = 0;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int col0 = col_base + c * 32;
+    if (col0 >= p.n) break;  // warp-uniform
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tmem_acc + c * 32, r);
+    tmem_ld_wait(r);
+    if (EPI == kEpiDense) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(__uint_as_float(r[j])));
+      if (row_ok) {
+        if (p.c_kind == kOutF32) {
+          float* dst = reinterpret_cast<float*>(p.c) +
+                       (static_cast<uint64_t>(l) * p.m + row) * static_cast<uint64_t>(p.n) + col0;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            if (col0 + j < p.n) store16(dst + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
+        } else {
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.c) +
+                               (static_cast<uint64_t>(l) * p.m + row) * static_cast<uint64_t>(p.n) + col0;
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            if (col0 + j < p.n) {
+              store16(dst + j, pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                      pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                      pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                      pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+            }
+          }
+        }
+      }
+    } else {
+      float d[32];
+      const uint64_t rc = static_cast<uint64_t>(row) * p.n + col0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float cv = alpha_g * __uint_as_float(r[j]);
+        r[j] = __float_as_uint(cv);
+        d[j] = srelu_clamp(cv, prob_r, s_clamp, p.tanh_approx);
+      }
+      // a chunk may run past N (N % 8 == 0 for 16-bit outputs, % 4 for fp32): 16-byte granules
+      if (p.c_kind == kOutBF16) {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.c) + rc;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8)
+          if (col0 + j < p.n)
+            store16(dst + j, pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                    pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                    pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                    pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+      } else if (p.c_kind == kOutF32) {
+        float* dst = reinterpret_cast<float*>(p.c) + rc;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          if (col0 + j < p.n) store16(dst + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
+      }
+      if (EPI == kEpiGroupedBF16) {
+        // columns past N hold zeros (zero-filled B rows), so they cannot raise the maximum
+#pragma unroll
+        for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(d[j]));
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.d) + rc;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8)
+          if (col0 + j < p.n)
+            store16(dst + j, pack_bf16x2(d[j], d[j + 1]), pack_bf16x2(d[j + 2], d[j + 3]),
+                    pack_bf16x2(d[j + 4], d[j + 5]), pack_bf16x2(d[j + 6], d[j + 7]));
+      } else {
+        // row MXFP8: this thread's 32 columns form one block
+        float bmax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, fabsf(d[j]));
+        const uint32_t code_r = e8m0_ceil_code(nc * bmax);
+        const float inv_r = e8m0_inv_scale(code_r);
+        uint32_t q[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j], nc), inv_r),
+                                         __fmul_rn(__fmul_rn(d[4 * j + 1], nc), inv_r));
+          const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j + 2], nc), inv_r),
+                                         __fmul_rn(__fmul_rn(d[4 * j + 3], nc), inv_r));
+          q[j] = lo | (hi << 16);
+        }
+        uint8_t* drow = reinterpret_cast<uint8_t*>(p.d) + rc;
+        store16(drow, q[0], q[1], q[2], q[3]);
+        store16(drow + 16, q[4], q[5], q[6], q[7]);
+        const int nb = col0 >> 5;
+        sfd_row_word |= code_r << (8 * (nb & 3));
+        if ((nb & 3) == 3 || col0 + 32 >= p.n || c == BN / 32 - 1) {
+          const uint64_t off = sf_offset(row, nb & ~3, 0, (p.m + 127) / 128, p.sfd_row_kt);
+          *reinterpret_cast<uint32_t*>(p.sfd_row + off) = sfd_row_word;
+          sfd_row_word = 0;
+        }
+        // column MXFP8: the warp's 32 lanes are 32 consecutive rows (one block per column)
+        float cm[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) cm[j] = fabsf(d[j]);
+        warp_colmax_scatter(cm, lane);
+        const uint32_t code_c = e8m0_ceil_code(nc * cm[0]);
+        const float inv_c = e8m0_inv_scale(code_c);
+        const int mblk = row >> 5;  // same for the whole warp
+        p.sfd_col[sf_offset(col0 + lane, mblk, 0, p.sfd_col_mt, p.sfd_col_kt)] = static_cast<uint8_t>(code_c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float i0 = __shfl_sync(0xffffffffu, inv_c, 4 * j);
+          const float i1 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 1);
+          const float i2 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 2);
+          const float i3 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 3);
+          const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j], nc), i0),
+                                         __fmul_rn(__fmul_rn(d[4 * j + 1], nc), i1));
+          const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j + 2], nc), i2),
+                                         __fmul_rn(__fmul_rn(d[4 * j + 3], nc), i3));
+          q[j] = lo | (hi << 16);
+        }
+        uint8_t* dcol = reinterpret_cast<uint8_t*>(p.d_col) + rc;
+        store16(dcol, q[0], q[1], q[2], q[3]);
+        store16(dcol + 16, q[4], q[5], q[6], q[7]);
+      }
     }
   }
 }
@@ -342,14 +475,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     float run_max = 0.0f;       // dense amax, or grouped per-expert segment max
     int run_expert = -1;
     uint32_t acc = 0, acc_phase = 0;
-    const float s_clamp = p.clamp_s;
     const float nc = (EPI == kEpiGroupedFP8) ? *p.norm_const : 1.0f;
     for (int t = blockIdx.x; !bad && t < p.num_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
       if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const int row = tc.mt * kTileM + quad * 32 + lane;
-      const bool row_ok = row < p.m;
       float alpha_g = 1.0f, prob_r = 0.0f;
       if (EPI != kEpiDense) {
         alpha_g = p.alpha[tc.l];
@@ -364,126 +495,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           run_max = 0.0f;
         }
       }
-      uint32_t sfd_row_word = 0;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = tc.nt * BN + c * 32;
-        if (col0 >= p.n) break;  // warp-uniform
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + c * 32, r);
-        tmem_ld_wait(r);
-        if (EPI == kEpiDense) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(__uint_as_float(r[j])));
-          if (row_ok) {
-            if (p.c_kind == kOutF32) {
-              float* dst = reinterpret_cast<float*>(p.c) +
-                           (static_cast<uint64_t>(tc.l) * p.m + row) * static_cast<uint64_t>(p.n) + col0;
-#pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                if (col0 + j < p.n) store16(dst + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
-            } else {
-              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.c) +
-                                   (static_cast<uint64_t>(tc.l) * p.m + row) * static_cast<uint64_t>(p.n) + col0;
-#pragma unroll
-              for (int j = 0; j < 32; j += 8) {
-                if (col0 + j < p.n) {
-                  store16(dst + j, pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                          pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
-                          pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
-                          pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
-                }
-              }
-            }
-          }
-        } else {
-          float d[32];
-          const uint64_t rc = static_cast<uint64_t>(row) * p.n + col0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float cv = alpha_g * __uint_as_float(r[j]);
-            r[j] = __float_as_uint(cv);
-            d[j] = srelu_clamp(cv, prob_r, s_clamp, p.tanh_approx);
-          }
-          // a chunk may run past N (N % 8 == 0 for 16-bit outputs, % 4 for fp32): 16-byte granules
-          if (p.c_kind == kOutBF16) {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.c) + rc;
-#pragma unroll
-            for (int j = 0; j < 32; j += 8)
-              if (col0 + j < p.n)
-                store16(dst + j, pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                        pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
-                        pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
-                        pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
-          } else if (p.c_kind == kOutF32) {
-            float* dst = reinterpret_cast<float*>(p.c) + rc;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              if (col0 + j < p.n) store16(dst + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
-          }
-          if (EPI == kEpiGroupedBF16) {
-            // columns past N hold zeros (zero-filled B rows), so they cannot raise the maximum
-#pragma unroll
-            for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(d[j]));
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.d) + rc;
-#pragma unroll
-            for (int j = 0; j < 32; j += 8)
-              if (col0 + j < p.n)
-                store16(dst + j, pack_bf16x2(d[j], d[j + 1]), pack_bf16x2(d[j + 2], d[j + 3]),
-                        pack_bf16x2(d[j + 4], d[j + 5]), pack_bf16x2(d[j + 6], d[j + 7]));
-          } else {
-            // row MXFP8: this thread's 32 columns form one block
-            float bmax = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, fabsf(d[j]));
-            const uint32_t code_r = e8m0_ceil_code(nc * bmax);
-            const float inv_r = e8m0_inv_scale(code_r);
-            uint32_t q[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j], nc), inv_r),
-                                             __fmul_rn(__fmul_rn(d[4 * j + 1], nc), inv_r));
-              const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j + 2], nc), inv_r),
-                                             __fmul_rn(__fmul_rn(d[4 * j + 3], nc), inv_r));
-              q[j] = lo | (hi << 16);
-            }
-            uint8_t* drow = reinterpret_cast<uint8_t*>(p.d) + rc;
-            store16(drow, q[0], q[1], q[2], q[3]);
-            store16(drow + 16, q[4], q[5], q[6], q[7]);
-            const int nb = col0 >> 5;
-            sfd_row_word |= code_r << (8 * (nb & 3));
-            if ((nb & 3) == 3 || col0 + 32 >= p.n || c == BN / 32 - 1) {
-              const uint64_t off = sf_offset(row, nb & ~3, 0, p.m_tiles, p.sfd_row_kt);
-              *reinterpret_cast<uint32_t*>(p.sfd_row + off) = sfd_row_word;
-              sfd_row_word = 0;
-            }
-            // column MXFP8: the warp's 32 lanes are 32 consecutive rows (one block per column)
-            float cm[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) cm[j] = fabsf(d[j]);
-            warp_colmax_scatter(cm, lane);
-            const uint32_t code_c = e8m0_ceil_code(nc * cm[0]);
-            const float inv_c = e8m0_inv_scale(code_c);
-            const int mblk = row >> 5;  // same for the whole warp
-            p.sfd_col[sf_offset(col0 + lane, mblk, 0, p.sfd_col_mt, p.sfd_col_kt)] = static_cast<uint8_t>(code_c);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float i0 = __shfl_sync(0xffffffffu, inv_c, 4 * j);
-              const float i1 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 1);
-              const float i2 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 2);
-              const float i3 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 3);
-              const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j], nc), i0),
-                                             __fmul_rn(__fmul_rn(d[4 * j + 1], nc), i1));
-              const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j + 2], nc), i2),
-                                             __fmul_rn(__fmul_rn(d[4 * j + 3], nc), i3));
-              q[j] = lo | (hi << 16);
-            }
-            uint8_t* dcol = reinterpret_cast<uint8_t*>(p.d_col) + rc;
-            store16(dcol, q[0], q[1], q[2], q[3]);
-            store16(dcol + 16, q[4], q[5], q[6], q[7]);
-          }
-        }
-      }
+      epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN,
+                             lane, alpha_g, prob_r, nc, run_max);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);

@@ -28,7 +28,7 @@ def _operands(seed, fmt, m, n, k, l, boost=False, spread=False):
     return a, b
 
 
-def run_dense(fmt, m, n, k, l, c_kind, tile_n=0, seed=1, boost=False, spread=False, max_ctas=0):
+def run_dense(fmt, m, n, k, l, c_kind, tile_n=0, seed=1, boost=False, spread=False, max_ctas=0, cta_pair=0):
     from nvfp4_gemm_moe_gb300 import torch_ops
     a, b = _operands(seed, fmt, m, n, k, l, boost, spread)
     qa, sfa = torch_ops.quantize(torch.from_numpy(a).cuda(), fmt)
@@ -36,7 +36,7 @@ def run_dense(fmt, m, n, k, l, c_kind, tile_n=0, seed=1, boost=False, spread=Fal
     c_dtype = torch.float32 if c_kind == "f32" else torch.bfloat16
     ws = torch_ops.new_workspace()
     c, amax = torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, m, n, k, l, c_dtype=c_dtype, workspace=ws,
-                                  tile_n=tile_n, max_ctas=max_ctas)
+                                  tile_n=tile_n, max_ctas=max_ctas, cta_pair=cta_pair)
     torch.cuda.synchronize()
     import nvfp4_gemm_moe_gb300 as bsg
     assert bsg.bsg_read_device_error(ws) == 0
@@ -87,3 +87,22 @@ def test_dense_repeat_calls_are_identical(lib):
     c1, a1 = run_dense("mxfp8", 256, 512, 512, 1, "bf16", 256, seed=7)
     c2, a2 = run_dense("mxfp8", 256, 512, 512, 1, "bf16", 256, seed=7)
     assert torch.equal(c1, c2) and torch.equal(a1, a2)
+
+
+@pytest.mark.parametrize("fmt,m,n,k,l,c_kind", [
+    ("mxfp8", 256, 256, 256, 1, "f32"),
+    ("mxfp8", 300, 264, 384, 2, "bf16"),     # ragged M (second 256-row tile mostly empty) and N
+    ("mxfp8", 512, 768, 1024, 1, "bf16"),
+    ("mxfp8", 256, 256, 160, 1, "f32"),      # K tail
+    ("nvfp4", 256, 256, 512, 1, "bf16"),
+    ("nvfp4", 300, 264, 320, 2, "f32"),      # K tail: one MMA in the last stage
+    ("nvfp4", 512, 512, 2048, 1, "bf16"),
+])
+def test_dense_parity_cta_pairs(lib, fmt, m, n, k, l, c_kind):
+    run_dense(fmt, m, n, k, l, c_kind, cta_pair=2)
+
+
+def test_dense_cta_pairs_few_clusters(lib):
+    """Two pairs walk many 256 x 256 tiles: stage and accumulator phases wrap around."""
+    run_dense("mxfp8", 1024, 1024, 1024, 2, "bf16", cta_pair=2, max_ctas=4, boost=True)
+    run_dense("nvfp4", 768, 1024, 1024, 1, "bf16", cta_pair=2, max_ctas=2)

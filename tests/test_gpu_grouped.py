@@ -20,7 +20,7 @@ def _case(counts, n, k, seed=3, a_scale=1.0):
 
 
 def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0, tile_n=0, seed=3, a_scale=1.0,
-                tanh_approx=False, max_ctas=0):
+                tanh_approx=False, max_ctas=0, cta_pair=0):
     from nvfp4_gemm_moe_gb300 import torch_ops
     import nvfp4_gemm_moe_gb300 as bsg
     wl, offs, a, b, alpha, prob = _case(counts, n, k, seed, a_scale)
@@ -33,7 +33,7 @@ def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0,
         qa[0], qb, sfa, sfb, "mxfp8", torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
         torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=clamp, d_dtype=d_dtype, c_dtype=c_dtype,
         norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
-        tanh_approx=tanh_approx, max_ctas=max_ctas)
+        tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair)
     torch.cuda.synchronize()
     assert bsg.bsg_read_device_error(ws) == 0
     qa_ref, sfa_ref = oq.quantize(a, "mxfp8")
@@ -145,3 +145,18 @@ def test_grouped_bad_offsets_detected_on_device(lib):
         torch_ops.grouped_gemm_srelu(qa, qb, sfa, sfb, "mxfp8", offs, ones, prob, n, k, workspace=ws,
                                      validate_offsets=True)
     assert ei.value.status == 7
+
+
+@pytest.mark.parametrize("d_dtype,clamp,c_kind,n,nc", [
+    ("bf16", None, "bf16", 256, 1.0),
+    ("bf16", 32.0, "f32", 264, 1.0),    # ragged N
+    ("e4m3", None, "bf16", 384, 1.0),
+    ("e4m3", None, None, 512, 0.75),
+])
+def test_grouped_cta_pairs(lib, d_dtype, clamp, c_kind, n, nc):
+    run_grouped(EDGE, n, 512, d_dtype, clamp, c_kind, nc=nc, cta_pair=2, a_scale=700.0 if clamp else 1.0)
+
+
+def test_grouped_cta_pairs_few_clusters(lib):
+    run_grouped([600, 900, 0, 300], 512, 512, "bf16", None, "bf16", cta_pair=2, max_ctas=2)
+    run_grouped([600, 900, 0, 300], 512, 512, "e4m3", None, "bf16", cta_pair=2, max_ctas=4)
