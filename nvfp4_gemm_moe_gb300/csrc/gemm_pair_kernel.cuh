@@ -186,56 +186,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
         if (!wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
-        // Stages are consumed kBatch at a time: all of a batch's waits come first, then one thread
-        // issues the batch's copies and MMAs.  A barrier wait in the issuing warp idles the tensor
-        // pipe for about a hundred cycles, so fewer waits per MMA keep it busy.
-        for (int kt0 = 0; kt0 < p.k_tiles; kt0 += kBatch) {
-          const int nb = min(kBatch, p.k_tiles - kt0);
-          uint32_t st_end = stage, ph_end = phase;
-          for (int g = 0; g < nb; ++g) {
-            if (!wait_bounded(&full[st_end], ph_end, abort_flag, p.err)) { ok = false; break; }
-            if (++st_end == S) { st_end = 0; ph_end ^= 1u; }
-          }
-          if (!ok) break;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!wait_bounded(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
+          // operands computed by the whole warp (warp-uniform), issue confined to one lane
+          const int k_left = p.k - kt * T::kElemsPerKTile;
+          const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
+          const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
+          const uint32_t sfb_t = sfa_t + T::kSfaCols;
+          const uint32_t sfa_s = sfa_base + stage * T::kSfaBytes;
+          const uint32_t sfb_s = sfb_base + stage * T::kSfbBytes;
+          const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
+          const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
           if (lane == 0) {
-            for (int g = 0; g < nb; ++g) {
-              const int kt = kt0 + g;
-              const int k_left = p.k - kt * T::kElemsPerKTile;
-              const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
-              const int atoms = FMT == kMXFP8 ? 1 : n_mma;
-              const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
-              const uint32_t sfb_t = sfa_t + T::kSfaCols;
-              for (int a = 0; a < atoms; ++a) {
-                tc_cp_32x128b_warpx4_pair(sfa_t + a * 4,
-                                          smem_desc(sfa_base + stage * T::kSfaBytes + a * 512, 0, 128, kSwizzleNone));
-  #pragma unroll
-                for (int g = 0; g < T::kSfbGroups; ++g) {
-                  tc_cp_32x128b_warpx4_pair(
-                      sfb_t + (a * T::kSfbGroups + g) * 4,
-                      smem_desc(sfb_base + stage * T::kSfbBytes + (g * T::kAtomsPerStage + a) * 512, 0, 128,
-                                kSwizzleNone));
-                }
+#pragma unroll
+            for (int a = 0; a < T::kAtomsPerStage; ++a) {
+              if (FMT == kMXFP8 || a < n_mma) {
+                tc_cp_32x128b_warpx4_pair(sfa_t + a * 4, smem_desc(sfa_s + a * 512, 0, 128, kSwizzleNone));
+#pragma unroll
+                for (int g = 0; g < T::kSfbGroups; ++g)
+                  tc_cp_32x128b_warpx4_pair(sfb_t + (a * T::kSfbGroups + g) * 4,
+                                            smem_desc(sfb_s + (g * T::kAtomsPerStage + a) * 512, 0, 128, kSwizzleNone));
               }
-              const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
-              const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
-              for (int j = 0; j < n_mma; ++j) {
+            }
+#pragma unroll
+            for (int j = 0; j < T::kMmasPerStage; ++j) {
+              if (j < n_mma) {
                 const uint32_t accumulate = (kt > 0 || j > 0) ? 1u : 0u;
                 if (FMT == kMXFP8) {
-                  const uint32_t idesc = T::kIdesc | (static_cast<uint32_t>(j) << 29) | (static_cast<uint32_t>(j) << 4);
-                  tc_mma_mxf8f6f4_pair(tmem_base, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_t, sfb_t, accumulate);
+                  tc_mma_mxf8f6f4_pair(tmem_base, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t,
+                                       sfb_t, accumulate);
                 } else {
                   tc_mma_mxf4nvf4_pair(tmem_base, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
                                        sfb_t + j * T::kSfbGroups * 4, accumulate);
                 }
               }
-              tc_commit_pair_multicast(&empty[stage], 0x3);
-              if (++stage == S) { stage = 0; phase ^= 1u; }
             }
+            tc_commit_pair_multicast(&empty[stage], 0x3);
           }
           __syncwarp();
-          stage = st_end;
-          phase = ph_end;
+          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         if (lane == 0) tc_commit_pair_multicast(tmem_full, 0x3);
