@@ -286,6 +286,36 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
   }
 }
 
+// One stage's scale-factor copies (SMEM -> TMEM, tcgen05.cp 32x128b.warpx4) and NM block-scaled
+// MMAs into d_tmem, issued by one thread.  MXFP8 stages hold one scale atom per 128-row group
+// (four K blocks, one per MMA, selected by the instruction descriptor's scale-factor id); NVFP4
+// stages hold one atom per MMA (one TMEM column of four UE4M3 scales per row).  The first MMA
+// accumulates iff acc0.
+template <int FMT, class T, int NM>
+__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa_t,
+                                            uint32_t sfb_t, uint32_t sfa_s, uint32_t sfb_s, uint32_t acc0) {
+  constexpr int kAtoms = FMT == kMXFP8 ? 1 : NM;
+#pragma unroll
+  for (int a = 0; a < kAtoms; ++a) {
+    tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc(sfa_s + a * 512, 0, 128, kSwizzleNone));
+#pragma unroll
+    for (int i = 0; i < T::kBRowGroups; ++i)
+      tc_cp_32x128b_warpx4(sfb_t + (a * T::kBRowGroups + i) * 4,
+                           smem_desc(sfb_s + (i * T::kAtomsPerStage + a) * 512, 0, 128, kSwizzleNone));
+  }
+#pragma unroll
+  for (int j = 0; j < NM; ++j) {
+    const uint32_t accumulate = j > 0 ? 1u : acc0;
+    // advance the start address by 32 bytes of K per MMA (encoded >> 4)
+    if (FMT == kMXFP8) {
+      tc_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t, sfb_t, accumulate);
+    } else {
+      tc_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4, sfb_t + j * T::kBRowGroups * 4,
+                      accumulate);
+    }
+  }
+}
+
 template <int FMT, int BN, int EPI>
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -418,45 +448,31 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!wait_bounded(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+          // Control flow and every tcgen05 operand stay warp-uniform: the operands are computed
+          // by the whole warp and only the issue is confined to one lane, and a failed wait
+          // (timeout or abort) is recorded rather than acted on until the tile ends, so the
+          // k-loop has no data-dependent exit.  Otherwise the operands are not provably uniform
+          // and every tcgen05 instruction costs tens of cycles of extra issue work.  Issuing
+          // after a failed wait reads stale shared memory, which is harmless: the results are
+          // discarded with the error.
+          ok &= wait_bounded(&full[stage], phase, abort_flag, p.err);
           tc_fence_after();
-          // Every operand of the tcgen05 instructions is computed by the whole warp from
-          // warp-uniform values; only their issue is confined to one lane.  Values computed
-          // inside the one-lane branch would not be uniform, and each tcgen05 instruction fed
-          // from non-uniform registers costs tens of cycles of extra issue work per stage.
-          const int k_left = p.k - kt * T::kElemsPerKTile;
-          const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
           const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
           const uint32_t sfa_s = sfa_base + stage * T::kSfaBytes;
           const uint32_t sfb_s = sfb_base + stage * T::kSfbBytes;
           const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
+          const uint32_t acc0 = kt > 0 ? 1u : 0u;  // the first MMA of a tile overwrites the accumulator
+          const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
           if (lane == 0) {
-#pragma unroll
-            for (int a = 0; a < T::kAtomsPerStage; ++a) {
-              // MXFP8: one atom per stage; NVFP4: one atom per MMA
-              if (FMT == kMXFP8 || a < n_mma) {
-                tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc(sfa_s + a * 512, 0, 128, kSwizzleNone));
-#pragma unroll
-                for (int i = 0; i < T::kBRowGroups; ++i)
-                  tc_cp_32x128b_warpx4(sfb_t + (a * T::kBRowGroups + i) * 4,
-                                       smem_desc(sfb_s + (i * T::kAtomsPerStage + a) * 512, 0, 128, kSwizzleNone));
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < T::kMmasPerStage; ++j) {
-              if (j < n_mma) {
-                const uint32_t accumulate = (kt > 0 || j > 0) ? 1u : 0u;
-                // advance the start address by 32 bytes of K per MMA (encoded >> 4)
-                if (FMT == kMXFP8) {
-                  tc_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t, sfb_t,
-                                  accumulate);
-                } else {
-                  tc_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
-                                  sfb_t + j * T::kBRowGroups * 4, accumulate);
-                }
-              }
+            if (n_mma == T::kMmasPerStage) {
+              issue_stage<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+            } else {
+              // the last, partial K stage (K not a multiple of the stage depth)
+              if (n_mma == 1) issue_stage<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+              if (n_mma == 2) issue_stage<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+              if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
             }
             tc_commit(&empty[stage]);
           }

@@ -54,6 +54,33 @@ struct PairTraits {
                                      (static_cast<uint32_t>(kTileMPair >> 4) << 24);
 };
 
+// One stage's scale-factor copies into both CTAs' TMEM and NM pair MMAs (M = 256), issued by one
+// thread of the even CTA (layout as in issue_stage; each CTA holds the scales of all B rows).
+template <int FMT, class T, int NM>
+__device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa_t,
+                                                 uint32_t sfb_t, uint32_t sfa_s, uint32_t sfb_s, uint32_t acc0) {
+  constexpr int kAtoms = FMT == kMXFP8 ? 1 : NM;
+#pragma unroll
+  for (int a = 0; a < kAtoms; ++a) {
+    tc_cp_32x128b_warpx4_pair(sfa_t + a * 4, smem_desc(sfa_s + a * 512, 0, 128, kSwizzleNone));
+#pragma unroll
+    for (int g = 0; g < T::kSfbGroups; ++g)
+      tc_cp_32x128b_warpx4_pair(sfb_t + (a * T::kSfbGroups + g) * 4,
+                                smem_desc(sfb_s + (g * T::kAtomsPerStage + a) * 512, 0, 128, kSwizzleNone));
+  }
+#pragma unroll
+  for (int j = 0; j < NM; ++j) {
+    const uint32_t accumulate = j > 0 ? 1u : acc0;
+    if (FMT == kMXFP8) {
+      tc_mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t, sfb_t,
+                           accumulate);
+    } else {
+      tc_mma_mxf4nvf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
+                           sfb_t + j * T::kSfbGroups * 4, accumulate);
+    }
+  }
+}
+
 template <int FMT, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -187,40 +214,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         if (!wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!wait_bounded(&full[stage], phase, abort_flag, p.err)) { ok = false; break; }
+          // warp-uniform control flow and operands, failures acted on per tile (as in the 1-CTA
+          // kernel)
+          ok &= wait_bounded(&full[stage], phase, abort_flag, p.err);
           tc_fence_after();
-          // operands computed by the whole warp (warp-uniform), issue confined to one lane
-          const int k_left = p.k - kt * T::kElemsPerKTile;
-          const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
           const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
           const uint32_t sfa_s = sfa_base + stage * T::kSfaBytes;
           const uint32_t sfb_s = sfb_base + stage * T::kSfbBytes;
           const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
+          const uint32_t acc0 = kt > 0 ? 1u : 0u;
+          const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
           if (lane == 0) {
-#pragma unroll
-            for (int a = 0; a < T::kAtomsPerStage; ++a) {
-              if (FMT == kMXFP8 || a < n_mma) {
-                tc_cp_32x128b_warpx4_pair(sfa_t + a * 4, smem_desc(sfa_s + a * 512, 0, 128, kSwizzleNone));
-#pragma unroll
-                for (int g = 0; g < T::kSfbGroups; ++g)
-                  tc_cp_32x128b_warpx4_pair(sfb_t + (a * T::kSfbGroups + g) * 4,
-                                            smem_desc(sfb_s + (g * T::kAtomsPerStage + a) * 512, 0, 128, kSwizzleNone));
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < T::kMmasPerStage; ++j) {
-              if (j < n_mma) {
-                const uint32_t accumulate = (kt > 0 || j > 0) ? 1u : 0u;
-                if (FMT == kMXFP8) {
-                  tc_mma_mxf8f6f4_pair(tmem_base, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t,
-                                       sfb_t, accumulate);
-                } else {
-                  tc_mma_mxf4nvf4_pair(tmem_base, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
-                                       sfb_t + j * T::kSfbGroups * 4, accumulate);
-                }
-              }
+            if (n_mma == T::kMmasPerStage) {
+              issue_stage_pair<FMT, T, T::kMmasPerStage>(tmem_base, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+            } else {
+              if (n_mma == 1) issue_stage_pair<FMT, T, 1>(tmem_base, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+              if (n_mma == 2) issue_stage_pair<FMT, T, 2>(tmem_base, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+              if (n_mma == 3) issue_stage_pair<FMT, T, 3>(tmem_base, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
             }
             tc_commit_pair_multicast(&empty[stage], 0x3);
           }
