@@ -6,14 +6,18 @@
 //   warp 0     TMA producer: per 128-byte K slice, A (128 rows) and B (BN rows) tiles with
 //              128-byte swizzle via cp.async.bulk.tensor, and the scale-factor atoms via
 //              cp.async.bulk, into a STAGES-deep shared-memory ring (full/empty mbarriers);
-//   warp 1     TMEM owner and MMA issuer: one thread copies the stage's scale factors to
-//              TMEM (tcgen05.cp 32x128b.warpx4) and issues four block-scaled tcgen05.mma
-//              (kind::mxf8f6f4 scale_vec::1X for MXFP8, kind::mxf4nvf4 scale_vec::4X for
-//              NVFP4) into an fp32 accumulator in TMEM, then tcgen05.commit frees the stage;
+//   warp 1     TMEM owner and MMA issuer: one thread issues the stage's four block-scaled
+//              tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for MXFP8, kind::mxf4nvf4 scale_vec::4X
+//              for NVFP4) into an fp32 accumulator in TMEM, then tcgen05.commit frees the stage;
 //   warps 2-5  epilogue: each warp owns one 32-lane quadrant of TMEM (= 32 rows of the
 //              tile), reads 32-column chunks with tcgen05.ld and applies the dense (C + amax)
 //              or grouped (alpha, C, sReLU / tanh clamp, D, per-expert amax or MXFP8 row and
-//              column re-quantisation) epilogue.
+//              column re-quantisation) epilogue;
+//   warps 6-9  scale-factor stagers: each warp writes its 32-lane quadrant of the stage's
+//              scale factors from shared memory into TMEM with tcgen05.st, in the layout a
+//              tcgen05.cp 32x128b.warpx4 of each atom would produce.  tcgen05.cp runs in the
+//              tensor pipe, serialised with the MMAs (about 40 cycles per 2 KB atom copy, i.e.
+//              up to twelve copies per four MMAs for NVFP4); the stores run beside it.
 // ACC accumulator buffers let the epilogue of one tile overlap the MMAs of the next.
 // Every wait is bounded: a wait longer than kWaitLimitNs records a device error, the CTA
 // drains its own in-flight copies and MMAs, frees TMEM and exits.
@@ -29,7 +33,7 @@
 
 namespace bsg {
 
-constexpr int kThreadsGemm = 192;
+constexpr int kThreadsGemm = 320;  // producer, MMA issuer, four epilogue and four scale-factor warps
 constexpr int kTileM = 128;
 constexpr int kTileKBytes = 128;  // one 128-byte swizzle row of K per stage
 
@@ -286,23 +290,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
   }
 }
 
-// One stage's scale-factor copies (SMEM -> TMEM, tcgen05.cp 32x128b.warpx4) and NM block-scaled
-// MMAs into d_tmem, issued by one thread.  MXFP8 stages hold one scale atom per 128-row group
-// (four K blocks, one per MMA, selected by the instruction descriptor's scale-factor id); NVFP4
-// stages hold one atom per MMA (one TMEM column of four UE4M3 scales per row).  The first MMA
-// accumulates iff acc0.
+// NM block-scaled MMAs of one stage into d_tmem, issued by one thread; the stage's scale factors
+// are in TMEM at sfa_t / sfb_t.  MXFP8 stages hold one scale column per row (four K blocks, one
+// per MMA, selected by the instruction descriptor's scale-factor id); NVFP4 stages hold one
+// column of four UE4M3 scales per row and MMA.  The first MMA accumulates iff acc0.
 template <int FMT, class T, int NM>
 __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa_t,
-                                            uint32_t sfb_t, uint32_t sfa_s, uint32_t sfb_s, uint32_t acc0) {
-  constexpr int kAtoms = FMT == kMXFP8 ? 1 : NM;
-#pragma unroll
-  for (int a = 0; a < kAtoms; ++a) {
-    tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc(sfa_s + a * 512, 0, 128, kSwizzleNone));
-#pragma unroll
-    for (int i = 0; i < T::kBRowGroups; ++i)
-      tc_cp_32x128b_warpx4(sfb_t + (a * T::kBRowGroups + i) * 4,
-                           smem_desc(sfb_s + (i * T::kAtomsPerStage + a) * 512, 0, 128, kSwizzleNone));
-  }
+                                            uint32_t sfb_t, uint32_t acc0) {
 #pragma unroll
   for (int j = 0; j < NM; ++j) {
     const uint32_t accumulate = j > 0 ? 1u : acc0;
@@ -314,6 +308,35 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uin
                       accumulate);
     }
   }
+}
+
+// One stager warp's share of a stage's scale factors: lane i of quadrant q (TMEM lanes 32q + i)
+// receives row i of every 512-byte atom (16 bytes: the scales of rows i, 32 + i, 64 + i and
+// 96 + i of the 128-row group, four K blocks each) as four consecutive 32-bit columns, i.e. what
+// tcgen05.cp 32x128b.warpx4 of the atom writes into every quadrant.  SFA atoms go to columns
+// sfa_t + 4a, SFB atom a of row group g to sfb_t + 4 (a * groups + g).
+template <class T>
+__device__ __forceinline__ void stage_scale_factors(const uint8_t* sfa_s, const uint8_t* sfb_s, uint32_t sfa_t,
+                                                    uint32_t sfb_t, int lane) {
+  constexpr int A = T::kAtomsPerStage, G = T::kBRowGroups;
+  uint32_t ra[4 * A];
+#pragma unroll
+  for (int a = 0; a < A; ++a) {
+    const uint4 v = *reinterpret_cast<const uint4*>(sfa_s + a * 512 + lane * 16);
+    ra[4 * a] = v.x; ra[4 * a + 1] = v.y; ra[4 * a + 2] = v.z; ra[4 * a + 3] = v.w;
+  }
+  uint32_t rb[4 * A * G];
+#pragma unroll
+  for (int a = 0; a < A; ++a) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const uint4 v = *reinterpret_cast<const uint4*>(sfb_s + (g * A + a) * 512 + lane * 16);
+      const int c = 4 * (a * G + g);
+      rb[c] = v.x; rb[c + 1] = v.y; rb[c + 2] = v.z; rb[c + 3] = v.w;
+    }
+  }
+  tmem_st_32x32b<4 * A>(sfa_t, ra);
+  tmem_st_32x32b<4 * A * G>(sfb_t, rb);
 }
 
 template <int FMT, int BN, int EPI>
@@ -337,7 +360,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   uint64_t* tmem_full = empty + S;
   uint64_t* tmem_empty = tmem_full + ACC;
   uint64_t* drain = tmem_empty + ACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_ready = drain + 1;  // the stage's scale factors are in TMEM (four stager arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_ready + S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bad_flag = const_cast<int*>(abort_flag) + 1;
   int32_t* s_offs = reinterpret_cast<int32_t*>(s_bar + T::kBarBytes);
@@ -356,6 +380,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       mbar_init(&tmem_empty[a], 4);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < S; ++s) mbar_init(&sf_ready[s], 4);
     *abort_flag = 0;
     *bad_flag = 0;
     fence_mbar_init();
@@ -442,7 +467,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
-      const uint32_t sfa_base = smem_u32(s_sfa), sfb_base = smem_u32(s_sfb);
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
@@ -455,24 +479,23 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           // and every tcgen05 instruction costs tens of cycles of extra issue work.  Issuing
           // after a failed wait reads stale shared memory, which is harmless: the results are
           // discarded with the error.
-          ok &= wait_bounded(&full[stage], phase, abort_flag, p.err);
+          // the stagers arrive after the stage's data landed and its scale factors are in TMEM
+          ok &= wait_bounded(&sf_ready[stage], phase, abort_flag, p.err);
           tc_fence_after();
           const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
-          const uint32_t sfa_s = sfa_base + stage * T::kSfaBytes;
-          const uint32_t sfb_s = sfb_base + stage * T::kSfbBytes;
           const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
           const uint32_t acc0 = kt > 0 ? 1u : 0u;  // the first MMA of a tile overwrites the accumulator
           const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
           if (lane == 0) {
             if (n_mma == T::kMmasPerStage) {
-              issue_stage<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+              issue_stage<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
             } else {
               // the last, partial K stage (K not a multiple of the stage depth)
-              if (n_mma == 1) issue_stage<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
-              if (n_mma == 2) issue_stage<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
-              if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+              if (n_mma == 1) issue_stage<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
+              if (n_mma == 2) issue_stage<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
+              if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
             }
             tc_commit(&empty[stage]);
           }
@@ -491,6 +514,27 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           wait_bounded_plain(drain, 0);
         }
         __syncwarp();
+      }
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ scale-factor stagers 6..9
+    // A stage's TMEM scale columns are free once its smem stage has been refilled: the refill
+    // waited for the commit of the MMAs that read them.
+    const uint32_t quad_lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; !bad && ok && t < p.num_tiles; t += gridDim.x) {
+      for (int kt = 0; kt < p.k_tiles; ++kt) {
+        ok &= wait_bounded(&full[stage], phase, abort_flag, p.err);
+        tc_fence_after();
+        const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
+        stage_scale_factors<T>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t, sfa_t + T::kSfaCols,
+                               lane);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[stage]);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
       }
     }
   } else {

@@ -21,6 +21,8 @@
 
 namespace bsg {
 
+constexpr int kThreadsPair = 192;  // producer, MMA issuer, four epilogue warps
+
 template <int FMT>
 struct PairTraits {
   static constexpr int kTileMPair = 256;
@@ -82,7 +84,7 @@ __device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc
 }
 
 template <int FMT, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                      const __grid_constant__ GemmParams p) {
@@ -125,13 +127,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     fence_mbar_init();
   }
   if (EPI != kEpiDense) {
-    for (int i = threadIdx.x; i < 1024; i += kThreadsGemm) s_amax[i] = 0.0f;
+    for (int i = threadIdx.x; i < 1024; i += kThreadsPair) s_amax[i] = 0.0f;
   } else if (threadIdx.x == 0) {
     s_amax[0] = 0.0f;
   }
   __syncthreads();
   if (EPI != kEpiDense) {
-    for (int i = threadIdx.x; i < p.l; i += kThreadsGemm) {
+    for (int i = threadIdx.x; i < p.l; i += kThreadsPair) {
       const int32_t o = p.offsets[i];
       const int32_t prev = i == 0 ? 0 : p.offsets[i - 1];
       s_offs[i] = o;
@@ -303,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     if (EPI == kEpiDense) {
       if (threadIdx.x == 0 && s_amax[0] > 0.0f) atomic_max_nonneg(p.amax, s_amax[0]);
     } else if (EPI == kEpiGroupedBF16) {
-      for (int g = threadIdx.x; g < p.l; g += kThreadsGemm)
+      for (int g = threadIdx.x; g < p.l; g += kThreadsPair)
         if (s_amax[g] > 0.0f) atomic_max_nonneg(&p.amax[g], s_amax[g]);
     }
   }
@@ -330,7 +332,7 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreadsGemm, 1, 1);
+    cfg.blockDim = dim3(kThreadsPair, 1, 1);
     cfg.dynamicSmemBytes = T::kSmemBytes;
     int clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
@@ -339,7 +341,7 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
   }
   int pairs = max_pairs < resident_pairs[dev] ? max_pairs : resident_pairs[dev];
   if (pairs < 1) pairs = 1;
-  kern<<<2 * pairs, kThreadsGemm, T::kSmemBytes, stream>>>(ta, tb, tsfa, tsfb, p);
+  kern<<<2 * pairs, kThreadsPair, T::kSmemBytes, stream>>>(ta, tb, tsfa, tsfb, p);
   return cudaGetLastError();
 }
 
