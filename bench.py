@@ -360,7 +360,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=W.DENSE_MXFP8_8192.name, choices=sorted(W.ALL))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=256, help="rows of A in the oracle's timed sample")
+    ap.add_argument("--ref-rows", type=int, default=2048, help="rows of A in the oracle's timed sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
