@@ -121,7 +121,8 @@ size_t bsg_sf_bytes(int64_t batch, int64_t rows, int64_t k, int sf_vec_size);
  *   q_dtype = BSG_E2M1, sf_vec_size = 16, sf_dtype = BSG_SF_UE4M3 (NVFP4): scale
  *     s = RNE_UE4M3(blockamax / 6); code = RNE_satfinite_E2M1(x / s), decided on the
  *     exact quotient; s = 0 gives zero codes.
- * Requirements: k % sf_vec_size == 0, rows >= 1, batch >= 1, k >= sf_vec_size.
+ * Requirements: k % sf_vec_size == 0, rows >= 1, batch >= 1, sf_vec_size <= k <= 2^30
+ *   (else BSG_ERR_INVALID_ARG).
  * Returns BSG_OK after enqueueing; x must not contain NaN or infinities.
  */
 bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t k,

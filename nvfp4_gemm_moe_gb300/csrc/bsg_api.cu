@@ -177,6 +177,7 @@ bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t 
   if (st != BSG_OK) return st;
   if (!x || !q || !sf) return BSG_ERR_INVALID_ARG;
   if (batch < 1 || rows < 1 || k < sf_vec_size || k % sf_vec_size != 0) return BSG_ERR_INVALID_ARG;
+  if (k > (int64_t{1} << 30)) return BSG_ERR_INVALID_ARG;  // row offsets along K are 32-bit in the kernel
   if ((fmt == bsg::kMXFP8 && k % 16 != 0) || (fmt == bsg::kNVFP4 && k % 32 != 0)) return BSG_ERR_ALIGNMENT;
   if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return BSG_ERR_ALIGNMENT;
   DeviceInfo info;

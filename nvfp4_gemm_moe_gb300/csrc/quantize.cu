@@ -1,7 +1,7 @@
 // quantize.cu -- fp32 -> MXFP8 / NVFP4 block quantiser (memory-bound).
 //
-// Each warp step handles one "unit": 128 consecutive fp32 values of one row (512 bytes,
-// one float4 per lane, fully coalesced).  For MXFP8 a unit is 4 blocks of 32 (8 lanes per
+// A warp takes one row at a time and walks its "units": 128 consecutive fp32 values (512 bytes,
+// one float4 per lane, fully coalesced), kUnroll loads in flight.  For MXFP8 a unit is 4 blocks of 32 (8 lanes per
 // block), for NVFP4 8 blocks of 16 (4 lanes per block).  Block maxima are reduced with
 // warp shuffles, the scale bytes of 4 consecutive blocks are adjacent in the atom layout
 // and leave as one 32-bit store, the codes as one 32-bit (E4M3) or 16-bit (E2M1) store
@@ -15,15 +15,17 @@
 namespace bsg {
 namespace {
 
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;  // 512-byte loads in flight per warp
 constexpr int kThreads = 256;
 
-// RNE_UE4M3(a / 6) decided exactly: candidate from the rounded fp32 quotient, then moved
-// by at most one code after comparing a with 6 * (neighbouring midpoints), products that
-// are exact in fp32 (a midpoint has at most 5 significant bits).  Saturates at 448.
+// RNE_UE4M3(a / 6) decided exactly: candidate from an fp32 approximation of the quotient
+// (a times the rounded 1/6, within two ulps of a/6, so the candidate is at most one code
+// off), then moved by at most one code after comparing a with 6 * (neighbouring midpoints),
+// products that are exact in fp32 (a midpoint has at most 5 significant bits).  Saturates
+// at 448.
 __device__ __forceinline__ uint32_t ue4m3_code_of_amax_over_6(float a) {
   if (!(a > 0.0f)) return 0;
-  const float q = __fdiv_rn(a, 6.0f);
+  const float q = a * (1.0f / 6.0f);
   uint32_t c = cvt_e4m3x2(q, 0.0f) & 0x7Fu;
   if (c > 0x7Eu) c = 0x7Eu;
   if (c < 0x7Eu) {
@@ -48,76 +50,136 @@ __device__ __forceinline__ uint32_t e2m1_nibble(float x, const float (&t)[7]) {
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restrict__ x, int64_t rows, int64_t k,
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restrict__ x, int64_t rows, int k,
                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                            int64_t rows_padded, int64_t units_per_row,
-                                                            int64_t total_units, int64_t mt_n, int64_t kt_n) {
+                                                            int64_t rows_padded, int units_per_row, int64_t total_rows,
+                                                            int64_t mt_n, int64_t kt_n) {
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
 
-  for (int64_t u0 = warp_id * kUnroll; u0 < total_units; u0 += num_warps * kUnroll) {
-    float4 v[kUnroll];
-    int64_t row_g[kUnroll], r_[kUnroll], l_[kUnroll], kc_[kUnroll];
-    bool row_ok[kUnroll], elem_ok[kUnroll], unit_ok[kUnroll];
+  // one (padded) row per warp iteration: the row's batch and index are computed once, then
+  // the warp walks the row's units kUnroll at a time with kUnroll 512-byte loads in flight
+  for (int64_t rg = warp_id; rg < total_rows; rg += num_warps) {
+    const int64_t l = rg / rows_padded;
+    const int64_t r = rg - l * rows_padded;
+    const bool row_ok = r < rows;
+    const int64_t row_g = l * rows + r;
+    const float* xr = x + row_g * k;
+    for (int kc0 = 0; kc0 < units_per_row; kc0 += kUnroll) {
+      float4 v[kUnroll];
 #pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int64_t u = u0 + j;
-      unit_ok[j] = u < total_units;
-      const int64_t kc = u % units_per_row;
-      const int64_t rg = u / units_per_row;  // row index over batch * rows_padded
-      const int64_t l = rg / rows_padded, r = rg % rows_padded;
-      kc_[j] = kc;
-      r_[j] = r;
-      l_[j] = l;
-      row_g[j] = l * rows + r;
-      const int64_t kk = kc * 128 + lane * 4;
-      row_ok[j] = unit_ok[j] && r < rows;
-      elem_ok[j] = row_ok[j] && kk < k;
-      v[j] = elem_ok[j] ? __ldcs(reinterpret_cast<const float4*>(x + row_g[j] * k + kk))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+      for (int j = 0; j < kUnroll; ++j) {
+        const int kk = (kc0 + j) * 128 + lane * 4;
+        v[j] = (row_ok && kc0 + j < units_per_row && kk < k) ? __ldcs(reinterpret_cast<const float4*>(xr + kk))
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      if (!unit_ok[j]) continue;  // uniform across the warp
-      const int64_t kk = kc_[j] * 128 + lane * 4;
-      float a = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
-      if (FMT == kMXFP8) {
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-        const uint32_t code = e8m0_ceil_code(a);
-        const float inv = e8m0_inv_scale(code);
-        const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[j].x, inv), __fmul_rn(v[j].y, inv));
-        const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[j].z, inv), __fmul_rn(v[j].w, inv));
-        if (elem_ok[j]) *reinterpret_cast<uint32_t*>(q + row_g[j] * k + kk) = lo | (hi << 16);
-        const uint32_t c1 = __shfl_sync(0xffffffffu, code, 8);
-        const uint32_t c2 = __shfl_sync(0xffffffffu, code, 16);
-        const uint32_t c3 = __shfl_sync(0xffffffffu, code, 24);
-        if (lane == 0) {
-          const uint64_t off = sf_offset(r_[j], kc_[j] * 4, l_[j], mt_n, kt_n);
-          *reinterpret_cast<uint32_t*>(sf + off) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+      for (int j = 0; j < kUnroll; ++j) {
+        const int kc = kc0 + j;
+        if (kc >= units_per_row) break;  // uniform across the warp
+        const int kk = kc * 128 + lane * 4;
+        const bool elem_ok = row_ok && kk < k;
+        float a = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
+        if (FMT == kMXFP8) {
+          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+          const uint32_t code = e8m0_ceil_code(a);
+          const float inv = e8m0_inv_scale(code);
+          const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[j].x, inv), __fmul_rn(v[j].y, inv));
+          const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[j].z, inv), __fmul_rn(v[j].w, inv));
+          if (elem_ok) *reinterpret_cast<uint32_t*>(q + row_g * k + kk) = lo | (hi << 16);
+          const uint32_t c1 = __shfl_sync(0xffffffffu, code, 8);
+          const uint32_t c2 = __shfl_sync(0xffffffffu, code, 16);
+          const uint32_t c3 = __shfl_sync(0xffffffffu, code, 24);
+          if (lane == 0) {
+            const uint64_t off = sf_offset(r, kc * 4, l, mt_n, kt_n);
+            *reinterpret_cast<uint32_t*>(sf + off) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+          }
+        } else {
+          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+          const uint32_t code = ue4m3_code_of_amax_over_6(a);
+          const float s = ue4m3_value(code);
+          const float t[7] = {0.25f * s, 0.75f * s, 1.25f * s, 1.75f * s, 2.5f * s, 3.5f * s, 5.0f * s};
+          uint32_t nib = 0;
+          if (code != 0) {
+            nib = e2m1_nibble(v[j].x, t) | (e2m1_nibble(v[j].y, t) << 4) | (e2m1_nibble(v[j].z, t) << 8) |
+                  (e2m1_nibble(v[j].w, t) << 12);
+          }
+          if (elem_ok) *reinterpret_cast<uint16_t*>(q + (row_g * k + kk) / 2) = static_cast<uint16_t>(nib);
+          // scale bytes: blocks 0-3 from lanes 0, 4, 8, 12 and blocks 4-7 from lanes 16, 20, 24, 28
+          const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 4);
+          const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 8);
+          const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 12);
+          if ((lane & 15) == 0) {
+            const int64_t kb = static_cast<int64_t>(kc) * 8 + (lane >> 2);
+            if ((kb >> 2) < kt_n) {
+              const uint64_t off = sf_offset(r, kb, l, mt_n, kt_n);
+              *reinterpret_cast<uint32_t*>(sf + off) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+            }
+          }
         }
-      } else {
+      }
+    }
+  }
+}
+
+// NVFP4: a unit is 256 consecutive fp32 values of one row (1 KB), eight per lane (two
+// float4 loads), so a block of 16 spans two lanes and each lane's eight codes leave as one
+// 32-bit store.  The 16 scale bytes of a unit are four 32-bit words of the atom layout,
+// stored by lanes 0, 8, 16 and 24.
+__global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const float* __restrict__ x, int64_t rows, int k,
+                                                                  uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                                  int64_t rows_padded, int units_per_row,
+                                                                  int64_t total_rows, int64_t mt_n, int64_t kt_n) {
+  constexpr int kU = 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  for (int64_t rg = warp_id; rg < total_rows; rg += num_warps) {
+    const int64_t l = rg / rows_padded;
+    const int64_t r = rg - l * rows_padded;
+    const bool row_ok = r < rows;
+    const int64_t row_g = l * rows + r;
+    const float* xr = x + row_g * k;
+    for (int kc0 = 0; kc0 < units_per_row; kc0 += kU) {
+      float4 v0[kU], v1[kU];
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int kk = (kc0 + j) * 256 + lane * 8;
+        const bool ok = row_ok && kc0 + j < units_per_row && kk < k;
+        v0[j] = ok ? __ldcs(reinterpret_cast<const float4*>(xr + kk)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v1[j] = ok ? __ldcs(reinterpret_cast<const float4*>(xr + kk + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int kc = kc0 + j;
+        if (kc >= units_per_row) break;  // uniform across the warp
+        const int kk = kc * 256 + lane * 8;
+        float a = fmaxf(fmaxf(fmaxf(fabsf(v0[j].x), fabsf(v0[j].y)), fmaxf(fabsf(v0[j].z), fabsf(v0[j].w))),
+                        fmaxf(fmaxf(fabsf(v1[j].x), fabsf(v1[j].y)), fmaxf(fabsf(v1[j].z), fabsf(v1[j].w))));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
         const uint32_t code = ue4m3_code_of_amax_over_6(a);
         const float s = ue4m3_value(code);
         const float t[7] = {0.25f * s, 0.75f * s, 1.25f * s, 1.75f * s, 2.5f * s, 3.5f * s, 5.0f * s};
         uint32_t nib = 0;
         if (code != 0) {
-          nib = e2m1_nibble(v[j].x, t) | (e2m1_nibble(v[j].y, t) << 4) | (e2m1_nibble(v[j].z, t) << 8) |
-                (e2m1_nibble(v[j].w, t) << 12);
+          nib = e2m1_nibble(v0[j].x, t) | (e2m1_nibble(v0[j].y, t) << 4) | (e2m1_nibble(v0[j].z, t) << 8) |
+                (e2m1_nibble(v0[j].w, t) << 12) | (e2m1_nibble(v1[j].x, t) << 16) | (e2m1_nibble(v1[j].y, t) << 20) |
+                (e2m1_nibble(v1[j].z, t) << 24) | (e2m1_nibble(v1[j].w, t) << 28);
         }
-        if (elem_ok[j]) *reinterpret_cast<uint16_t*>(q + (row_g[j] * k + kk) / 2) = static_cast<uint16_t>(nib);
-        // scale bytes: blocks 0-3 from lanes 0, 4, 8, 12 and blocks 4-7 from lanes 16, 20, 24, 28
-        const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 4);
-        const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 8);
-        const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 12);
-        if ((lane & 15) == 0) {
-          const int64_t kb = kc_[j] * 8 + (lane >> 2);
+        if (row_ok && kk < k) *reinterpret_cast<uint32_t*>(q + (row_g * k + kk) / 2) = nib;
+        // block b of the unit is held by lanes 2b and 2b + 1; scale word w (blocks 4w..4w+3)
+        // gathers the codes of lanes 8w, 8w + 2, 8w + 4, 8w + 6
+        const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 2);
+        const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 4);
+        const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 6);
+        if ((lane & 7) == 0) {
+          const int64_t kb = static_cast<int64_t>(kc) * 16 + (lane >> 1);
           if ((kb >> 2) < kt_n) {
-            const uint64_t off = sf_offset(r_[j], kb, l_[j], mt_n, kt_n);
+            const uint64_t off = sf_offset(r, kb, l, mt_n, kt_n);
             *reinterpret_cast<uint32_t*>(sf + off) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
           }
         }
@@ -134,19 +196,18 @@ cudaError_t launch_quantize(int fmt, const float* x, int64_t batch, int64_t rows
   const int64_t mt_n = (rows + 127) / 128;
   const int64_t kt_n = (k / v + 3) / 4;
   const int64_t rows_padded = mt_n * 128;
-  const int64_t units_per_row = (k + 127) / 128;
-  const int64_t total_units = batch * rows_padded * units_per_row;
-  const int64_t warps_needed = (total_units + kUnroll - 1) / kUnroll;
-  int64_t blocks = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
+  const int units_per_row = static_cast<int>((k + 127) / 128);
+  const int64_t total_rows = batch * rows_padded;
+  int64_t blocks = (total_rows + (kThreads / 32) - 1) / (kThreads / 32);
   const int64_t max_blocks = static_cast<int64_t>(num_sms) * 8;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
   if (fmt == kMXFP8) {
     quantize_kernel<kMXFP8><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        x, rows, k, q, sf, rows_padded, units_per_row, total_units, mt_n, kt_n);
+        x, rows, static_cast<int>(k), q, sf, rows_padded, units_per_row, total_rows, mt_n, kt_n);
   } else {
-    quantize_kernel<kNVFP4><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        x, rows, k, q, sf, rows_padded, units_per_row, total_units, mt_n, kt_n);
+    quantize_nvfp4_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+        x, rows, static_cast<int>(k), q, sf, rows_padded, static_cast<int>((k + 255) / 256), total_rows, mt_n, kt_n);
   }
   return cudaGetLastError();
 }
