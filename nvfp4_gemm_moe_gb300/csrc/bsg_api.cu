@@ -112,11 +112,24 @@ bsg_status operand_format(bsg_dtype ab, bsg_sf_dtype sf, int v, int* fmt) {
 
 bool fits_int32(int64_t v) { return v >= 0 && v < (int64_t(1) << 31); }
 
-int choose_tile_n(int64_t n, int64_t m_tiles_total, int num_sms, const bsg_gemm_opts* opts) {
+int choose_tile_n(int fmt, int64_t n, int64_t m_tiles_total, int num_sms, bool heavy_epilogue,
+                  const bsg_gemm_opts* opts) {
   if (opts && (opts->tile_n == 128 || opts->tile_n == 256)) return opts->tile_n;
+  if (opts && (opts->tile_n == 192 || opts->tile_n == 224) && fmt == bsg::kMXFP8) return opts->tile_n;
   if (n <= 128) return 128;
-  // prefer 256-wide tiles unless that leaves SMs idle
-  return (m_tiles_total * cdiv(n, 256) >= num_sms) ? 256 : 128;
+  if (fmt != bsg::kMXFP8 || !heavy_epilogue) return (m_tiles_total * cdiv(n, 256) >= num_sms) ? 256 : 128;
+  // MXFP8 with an epilogue about as long as a tile's MMAs (tanh clamp, E4M3 D re-quantised
+  // both ways): 192- or 224-wide tiles keep two accumulators in TMEM, so the epilogue of one tile
+  // overlaps the MMAs of the next.  Pick the width with the least padded work per SM (waves of
+  // tiles times the tile width), ties to the wider tile.
+  int best = 224;
+  int64_t best_cost = -1;
+  for (int bn : {224, 192}) {
+    const int64_t tiles = m_tiles_total * cdiv(n, bn);
+    const int64_t cost = cdiv(tiles, num_sms) * bn;
+    if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
+  }
+  return best;
 }
 
 // CTA pairs (256 x 256 tiles) when asked for, or when the problem still gives every pair a tile.
@@ -213,7 +226,7 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
 
   const bool pairs = use_pairs(l * cdiv(m, 256) * cdiv(n, 256), m, n, info.num_sms, opts);
   const int64_t m_tiles = pairs ? cdiv(m, 256) : cdiv(m, 128);
-  const int bn = pairs ? 256 : choose_tile_n(n, m_tiles * l, info.num_sms, opts);
+  const int bn = pairs ? 256 : choose_tile_n(fmt, n, m_tiles * l, info.num_sms, false, opts);
   const int64_t n_tiles = cdiv(n, bn);
   const int64_t tiles = l * m_tiles * n_tiles;
   const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
@@ -323,7 +336,7 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
 
   const bool pairs = use_pairs((valid_m / 256) * cdiv(n, 256), valid_m, n, info.num_sms, opts);
   const int64_t m_tiles = pairs ? valid_m / 256 : valid_m / 128;
-  const int bn = pairs ? 256 : choose_tile_n(n, m_tiles, info.num_sms, opts);
+  const int bn = pairs ? 256 : choose_tile_n(fmt, n, m_tiles, info.num_sms, fp8_d || tanh_clamp_scale > 0.0f, opts);
   const int64_t n_tiles = cdiv(n, bn);
   const int64_t tiles = m_tiles * n_tiles;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;

@@ -2,23 +2,24 @@
 //
 // One CTA per SM walks a static list of 128 x BN output tiles (dense: batch-major, then
 // groups of 16 M-tiles swept along N; grouped: M-tile-major over the experts' padded row
-// ranges).  Six warps:
+// ranges).  Fourteen warps:
 //   warp 0     TMA producer: per 128-byte K slice, A (128 rows) and B (BN rows) tiles with
 //              128-byte swizzle via cp.async.bulk.tensor, and the scale-factor atoms via
 //              cp.async.bulk, into a STAGES-deep shared-memory ring (full/empty mbarriers);
 //   warp 1     TMEM owner and MMA issuer: one thread issues the stage's four block-scaled
 //              tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for MXFP8, kind::mxf4nvf4 scale_vec::4X
 //              for NVFP4) into an fp32 accumulator in TMEM, then tcgen05.commit frees the stage;
-//   warps 2-5  epilogue: each warp owns one 32-lane quadrant of TMEM (= 32 rows of the
-//              tile), reads 32-column chunks with tcgen05.ld and applies the dense (C + amax)
+//   warps 2-9  epilogue: two warps per 32-lane quadrant of TMEM (= 32 rows of the tile), each
+//              taking alternate 32-column chunks, read with tcgen05.ld, and applying the dense (C + amax)
 //              or grouped (alpha, C, sReLU / tanh clamp, D, per-expert amax or MXFP8 row and
 //              column re-quantisation) epilogue;
-//   warps 6-9  scale-factor stagers: each warp writes its 32-lane quadrant of the stage's
+//   warps 10-13 scale-factor stagers: each warp writes its 32-lane quadrant of the stage's
 //              scale factors from shared memory into TMEM with tcgen05.st, in the layout a
 //              tcgen05.cp 32x128b.warpx4 of each atom would produce.  tcgen05.cp runs in the
 //              tensor pipe, serialised with the MMAs (about 40 cycles per 2 KB atom copy, i.e.
 //              up to twelve copies per four MMAs for NVFP4); the stores run beside it.
-// ACC accumulator buffers let the epilogue of one tile overlap the MMAs of the next.
+// Tiles are 128 x BN with BN in {128, 192, 224, 256}; below 256 two accumulator buffers (ACC)
+// let the epilogue of one tile overlap the MMAs of the next.
 // Every wait is bounded: a wait longer than kWaitLimitNs records a device error, the CTA
 // drains its own in-flight copies and MMAs, frees TMEM and exits.
 #pragma once
@@ -33,7 +34,7 @@
 
 namespace bsg {
 
-constexpr int kThreadsGemm = 320;  // producer, MMA issuer, four epilogue and four scale-factor warps
+constexpr int kThreadsGemm = 448;  // producer, MMA issuer, eight epilogue and four scale-factor warps
 constexpr int kTileM = 128;
 constexpr int kTileKBytes = 128;  // one 128-byte swizzle row of K per stage
 
@@ -43,26 +44,40 @@ struct GemmTraits {
   static constexpr int kMmaK = FMT == kMXFP8 ? 32 : 64;  // elements per tcgen05.mma (32 bytes)
   static constexpr int kMmasPerStage = 4;
   static constexpr int kAtomsPerStage = FMT == kMXFP8 ? 1 : 4;  // SF atoms (128 rows x 4 blocks) along K
-  static constexpr int kBRowGroups = BN / 128;
+  static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
+  static_assert(BN % 128 == 0 || FMT == kMXFP8, "NVFP4 tiles are 128 or 256 wide");
+  // A tile of B rows starting at a multiple of BN: aligned to the 128-row scale-factor atoms
+  // when BN is a multiple of 128, else it may start inside an atom and touch three of them.
+  static constexpr bool kSfbAligned = BN % 128 == 0;
+  static constexpr int kBRowGroups = kSfbAligned ? BN / 128 : 3;  // SFB atom groups loaded per stage
+  static constexpr int kBBlocks = BN / 32;                         // 32-row blocks of the tile
   static constexpr int kABytes = kTileM * kTileKBytes;
   static constexpr int kBBytes = BN * kTileKBytes;
   static constexpr int kSfaBytes = kAtomsPerStage * 512;
   static constexpr int kSfbBytes = kBRowGroups * kAtomsPerStage * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kStages = (BN == 256) ? 4 : (FMT == kMXFP8 ? 6 : 5);
   static constexpr int kAcc = (BN == 256) ? 1 : 2;
   static constexpr int kSfaCols = kAtomsPerStage * 4;
-  static constexpr int kSfbCols = kBRowGroups * kAtomsPerStage * 4;
+  // SFB columns per MMA: column n / 32 of a unit holds the scales of tile rows n (TMEM lane n % 32
+  // of every quadrant), padded to whole four-column groups
+  static constexpr int kSfbColsPerMma = ((kBBlocks + 3) / 4) * 4;
+  static constexpr int kSfbCols = kSfbColsPerMma * kAtomsPerStage;
   static constexpr int kSfStride = ((kSfaCols + kSfbCols + 15) / 16) * 16;
   static constexpr int kSfBase = kAcc * BN;
-  static constexpr int kTmemUsed = kSfBase + kStages * kSfStride;
-  static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
-                                   : kTmemUsed <= 256 ? 256 : 512;
-  static_assert(kTmemUsed <= 512, "TMEM budget");
   // barrier / scalar area after the stages
   static constexpr int kBarBytes = 1024;
   static constexpr int kOffsetsBytes = 4096;  // padded_offsets of up to 1024 experts (grouped)
   static constexpr int kAmaxBytes = 4096;     // per-expert amax staging (grouped bf16 D)
+  // as many stages as shared memory and the TMEM scale-factor slots allow, at most six
+  static constexpr int kStagesSmem = (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes) / kStageBytes;
+  static constexpr int kStagesTmem = (512 - kSfBase) / kSfStride;
+  static constexpr int kStages = kStagesSmem < kStagesTmem ? (kStagesSmem < 6 ? kStagesSmem : 6)
+                                                           : (kStagesTmem < 6 ? kStagesTmem : 6);
+  static_assert(kStages >= 3, "pipeline depth");
+  static constexpr int kTmemUsed = kSfBase + kStages * kSfStride;
+  static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                   : kTmemUsed <= 256 ? 256 : 512;
+  static_assert(kTmemUsed <= 512, "TMEM budget");
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarBytes +
                                     kOffsetsBytes + kAmaxBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -165,12 +180,12 @@ __device__ __forceinline__ void warp_colmax_scatter(float (&v)[32], int lane) {
 // col_base .. col_base + BN - 1 (clipped at N).  `l` is the batch (dense) or expert (grouped).
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int row, int col_base, uint32_t tmem_acc,
-                                              int lane, float alpha_g, float prob_r, float nc, float& run_max) {
+                                              int lane, float alpha_g, float prob_r, float nc, float& run_max,
+                                              int c_first, int c_step) {
   const bool row_ok = row < p.m;
   const float s_clamp = p.clamp_s;
-  uint32_t sfd_row_word = 0;
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = c_first; c < BN / 32; c += c_step) {
     const int col0 = col_base + c * 32;
     if (col0 >= p.n) break;  // warp-uniform
     uint32_t r[32];
@@ -254,13 +269,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
         uint8_t* drow = reinterpret_cast<uint8_t*>(p.d) + rc;
         store16(drow, q[0], q[1], q[2], q[3]);
         store16(drow + 16, q[4], q[5], q[6], q[7]);
+        // one byte per block: a tile need not start on a four-block word of the SF layout; the
+        // row's last block also zeroes the padding blocks of its word
         const int nb = col0 >> 5;
-        sfd_row_word |= code_r << (8 * (nb & 3));
-        if ((nb & 3) == 3 || col0 + 32 >= p.n || c == BN / 32 - 1) {
-          const uint64_t off = sf_offset(row, nb & ~3, 0, (p.m + 127) / 128, p.sfd_row_kt);
-          *reinterpret_cast<uint32_t*>(p.sfd_row + off) = sfd_row_word;
-          sfd_row_word = 0;
-        }
+        const int nb_end = col0 + 32 >= p.n ? (nb | 3) : nb;
+        for (int b = nb; b <= nb_end; ++b)
+          p.sfd_row[sf_offset(row, b, 0, (p.m + 127) / 128, p.sfd_row_kt)] = static_cast<uint8_t>(b == nb ? code_r : 0u);
         // column MXFP8: the warp's 32 lanes are 32 consecutive rows (one block per column)
         float cm[32];
 #pragma unroll
@@ -304,39 +318,57 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uin
     if (FMT == kMXFP8) {
       tc_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t, sfb_t, accumulate);
     } else {
-      tc_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4, sfb_t + j * T::kBRowGroups * 4,
+      tc_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4, sfb_t + j * T::kSfbColsPerMma,
                       accumulate);
     }
   }
 }
 
 // One stager warp's share of a stage's scale factors: lane i of quadrant q (TMEM lanes 32q + i)
-// receives row i of every 512-byte atom (16 bytes: the scales of rows i, 32 + i, 64 + i and
+// receives row i of every 512-byte SFA atom (16 bytes: the scales of rows i, 32 + i, 64 + i and
 // 96 + i of the 128-row group, four K blocks each) as four consecutive 32-bit columns, i.e. what
-// tcgen05.cp 32x128b.warpx4 of the atom writes into every quadrant.  SFA atoms go to columns
-// sfa_t + 4a, SFB atom a of row group g to sfb_t + 4 (a * groups + g).
+// tcgen05.cp 32x128b.warpx4 of the atom writes into every quadrant; SFA atom a goes to columns
+// sfa_t + 4a.  For B, column sfb_t + kSfbColsPerMma * a + c holds, in lane i of every quadrant,
+// the scales of tile row 32c + i: for tiles aligned to the atoms these are again whole atom rows
+// (atom g of the unit fills columns 4g .. 4g + 3), otherwise single 32-bit words gathered from the
+// (up to three) atoms the tile's rows fall in.  b_blk0 is the 32-row block index of the tile's
+// first row within the first atom group loaded.
 template <class T>
 __device__ __forceinline__ void stage_scale_factors(const uint8_t* sfa_s, const uint8_t* sfb_s, uint32_t sfa_t,
-                                                    uint32_t sfb_t, int lane) {
-  constexpr int A = T::kAtomsPerStage, G = T::kBRowGroups;
+                                                    uint32_t sfb_t, int lane, int b_blk0) {
+  constexpr int A = T::kAtomsPerStage, G = T::kBRowGroups, C = T::kSfbColsPerMma;
   uint32_t ra[4 * A];
 #pragma unroll
   for (int a = 0; a < A; ++a) {
     const uint4 v = *reinterpret_cast<const uint4*>(sfa_s + a * 512 + lane * 16);
     ra[4 * a] = v.x; ra[4 * a + 1] = v.y; ra[4 * a + 2] = v.z; ra[4 * a + 3] = v.w;
   }
-  uint32_t rb[4 * A * G];
+  uint32_t rb[C * A];
+  if constexpr (T::kSfbAligned) {
 #pragma unroll
-  for (int a = 0; a < A; ++a) {
+    for (int a = 0; a < A; ++a) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const uint4 v = *reinterpret_cast<const uint4*>(sfb_s + (g * A + a) * 512 + lane * 16);
-      const int c = 4 * (a * G + g);
-      rb[c] = v.x; rb[c + 1] = v.y; rb[c + 2] = v.z; rb[c + 3] = v.w;
+      for (int g = 0; g < G; ++g) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sfb_s + (g * A + a) * 512 + lane * 16);
+        const int c = C * a + 4 * g;
+        rb[c] = v.x; rb[c + 1] = v.y; rb[c + 2] = v.z; rb[c + 3] = v.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int a = 0; a < A; ++a) {
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        const int blk = b_blk0 + c;  // 32-row block within the loaded atom groups
+        rb[C * a + c] = c < T::kBBlocks
+                            ? *reinterpret_cast<const uint32_t*>(sfb_s + ((blk >> 2) * A + a) * 512 + lane * 16 +
+                                                                 (blk & 3) * 4)
+                            : 0u;
+      }
     }
   }
   tmem_st_32x32b<4 * A>(sfa_t, ra);
-  tmem_st_32x32b<4 * A * G>(sfb_t, rb);
+  tmem_st_32x32b<C * A>(sfb_t, rb);
 }
 
 template <int FMT, int BN, int EPI>
@@ -377,7 +409,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(&tmem_full[a], 1);
-      mbar_init(&tmem_empty[a], 4);
+      mbar_init(&tmem_empty[a], 8);
     }
     mbar_init(drain, 1);
     for (int s = 0; s < S; ++s) mbar_init(&sf_ready[s], 4);
@@ -440,7 +472,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
 #pragma unroll
           for (int i = 0; i < T::kBRowGroups; ++i) {
             // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
-            const int rb = min(tc.nt * T::kBRowGroups + i, p.sfb_mt - 1);
+            const int rb = min((tc.nt * BN) / 128 + i, p.sfb_mt - 1);
             const uint8_t* sfb_src =
                 p.sfb + ((static_cast<uint64_t>(tc.l) * p.sfb_mt + rb) * p.sf_kt +
                          static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
@@ -516,20 +548,22 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         __syncwarp();
       }
     }
-  } else if (warp >= 6) {
-    // ------------------------------------------------------------ scale-factor stagers 6..9
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ scale-factor stagers 10..13
     // A stage's TMEM scale columns are free once its smem stage has been refilled: the refill
     // waited for the commit of the MMAs that read them.
     const uint32_t quad_lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; !bad && ok && t < p.num_tiles; t += gridDim.x) {
+      const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
+      const int b_blk0 = ((tc.nt * BN) >> 5) & 3;  // the tile's first 32-row block within its first atom
       for (int kt = 0; kt < p.k_tiles; ++kt) {
         ok &= wait_bounded(&full[stage], phase, abort_flag, p.err);
         tc_fence_after();
         const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
         stage_scale_factors<T>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t, sfa_t + T::kSfaCols,
-                               lane);
+                               lane, b_blk0);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -538,8 +572,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue warps 2..5
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    // ------------------------------------------------------------ epilogue warps 2..9
+    const int quad = warp & 3;          // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;   // two warps per quadrant take alternate 32-column chunks
     float run_max = 0.0f;       // dense amax, or grouped per-expert segment max
     int run_expert = -1;
     uint32_t acc = 0, acc_phase = 0;
@@ -564,7 +599,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         }
       }
       epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN,
-                             lane, alpha_g, prob_r, nc, run_max);
+                             lane, alpha_g, prob_r, nc, run_max, half, 2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);

@@ -61,6 +61,8 @@ def run_dense(fmt, m, n, k, l, c_kind, tile_n=0, seed=1, boost=False, spread=Fal
     ("mxfp8", 384, 520, 1024, 1, "f32", 128),
     ("mxfp8", 128, 128, 160, 1, "f32", 128),    # K tail: one 32-wide MMA in the last stage
     ("mxfp8", 1, 8, 32, 1, "f32", 128),         # minimal
+    ("mxfp8", 384, 1000, 512, 1, "bf16", 224),  # tiles starting inside a 128-row scale atom
+    ("mxfp8", 256, 640, 256, 2, "f32", 192),
     ("nvfp4", 256, 256, 512, 1, "bf16", 256),
     ("nvfp4", 300, 264, 320, 2, "f32", 128),    # K tail: one MMA in the last stage
     ("nvfp4", 130, 136, 96, 1, "f32", 0),       # K = 96: half of the second MMA is zero fill

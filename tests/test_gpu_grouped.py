@@ -96,6 +96,8 @@ EDGE = [0, 300, 0, 0, 1, 256, 0]  # empty experts first, in a run and last; one 
     ([200, 200, 200, 200], 512, 384, 128),
     ([512], 384, 256, 256),   # single expert
     ([1, 2, 3, 700, 4], 256, 1024, 256),
+    (EDGE, 704, 512, 224),    # tiles starting inside a 128-row scale atom
+    ([200, 200, 200, 200], 600, 384, 192),
 ])
 def test_grouped_bf16_d(lib, counts, n, k, tile_n):
     run_grouped(counts, n, k, "bf16", None, "bf16", tile_n=tile_n)
@@ -112,7 +114,7 @@ def test_grouped_tanh_clamp(lib, approx):
     run_grouped([300, 500, 0, 220], 256, 512, "bf16", 32.0, "bf16", a_scale=700.0, tanh_approx=approx)
 
 
-@pytest.mark.parametrize("nc,tile_n", [(1.0, 256), (1.0, 128), (0.75, 256)])
+@pytest.mark.parametrize("nc,tile_n", [(1.0, 256), (1.0, 128), (0.75, 256), (1.0, 224), (0.75, 192)])
 def test_grouped_fp8_d(lib, nc, tile_n):
     run_grouped(EDGE, 384, 512, "e4m3", None, "bf16", nc=nc, tile_n=tile_n)
 
