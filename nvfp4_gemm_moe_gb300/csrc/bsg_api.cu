@@ -117,19 +117,11 @@ int choose_tile_n(int fmt, int64_t n, int64_t m_tiles_total, int num_sms, bool h
   if (opts && (opts->tile_n == 128 || opts->tile_n == 256)) return opts->tile_n;
   if (opts && (opts->tile_n == 192 || opts->tile_n == 224) && fmt == bsg::kMXFP8) return opts->tile_n;
   if (n <= 128) return 128;
-  if (fmt != bsg::kMXFP8 || !heavy_epilogue) return (m_tiles_total * cdiv(n, 256) >= num_sms) ? 256 : 128;
-  // MXFP8 with an epilogue about as long as a tile's MMAs (tanh clamp, E4M3 D re-quantised
-  // both ways): 192- or 224-wide tiles keep two accumulators in TMEM, so the epilogue of one tile
-  // overlaps the MMAs of the next.  Pick the width with the least padded work per SM (waves of
-  // tiles times the tile width), ties to the wider tile.
-  int best = 224;
-  int64_t best_cost = -1;
-  for (int bn : {224, 192}) {
-    const int64_t tiles = m_tiles_total * cdiv(n, bn);
-    const int64_t cost = cdiv(tiles, num_sms) * bn;
-    if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
-  }
-  return best;
+  // E4M3 D (row and column re-quantisation, three outputs per element) makes the epilogue about
+  // as long as a tile's MMAs: 224-wide tiles keep two accumulators in TMEM so it overlaps the
+  // next tile's MMAs.  Lighter epilogues run faster on 256-wide tiles (fewer, larger MMAs).
+  if (fmt == bsg::kMXFP8 && heavy_epilogue) return 224;
+  return (m_tiles_total * cdiv(n, 256) >= num_sms) ? 256 : 128;
 }
 
 // CTA pairs (256 x 256 tiles) when asked for, or when the problem still gives every pair a tile.
@@ -336,7 +328,7 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
 
   const bool pairs = use_pairs((valid_m / 256) * cdiv(n, 256), valid_m, n, info.num_sms, opts);
   const int64_t m_tiles = pairs ? valid_m / 256 : valid_m / 128;
-  const int bn = pairs ? 256 : choose_tile_n(fmt, n, m_tiles, info.num_sms, fp8_d || tanh_clamp_scale > 0.0f, opts);
+  const int bn = pairs ? 256 : choose_tile_n(fmt, n, m_tiles, info.num_sms, fp8_d, opts);
   const int64_t n_tiles = cdiv(n, bn);
   const int64_t tiles = m_tiles * n_tiles;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;

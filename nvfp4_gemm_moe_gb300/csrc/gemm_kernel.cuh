@@ -142,11 +142,13 @@ __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
   atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
 }
 
-// sReLU with optional tanh soft clamp: s * min(tanh(relu(c) / s), 1) (or relu(c)), squared, times prob.
-__device__ __forceinline__ float srelu_clamp(float c, float prob, float s, int tanh_approx) {
+// sReLU with optional tanh soft clamp: s * min(tanh(relu(c) / s), 1) (or relu(c)), squared, times
+// prob.  relu(c) / s is taken as relu(c) * (1/s): within an ulp of the quotient (exact for a
+// power-of-two s), far inside the output tolerances.
+__device__ __forceinline__ float srelu_clamp(float c, float prob, float s, float inv_s, int tanh_approx) {
   float r = fmaxf(c, 0.0f);
   if (s > 0.0f) {
-    const float u = __fdiv_rn(r, s);
+    const float u = r * inv_s;
     float t;
     if (tanh_approx) {
       asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(u));
@@ -179,11 +181,14 @@ __device__ __forceinline__ void warp_colmax_scatter(float (&v)[32], int lane) {
 // quadrant, first accumulator column) and writes the outputs of row `row`, columns
 // col_base .. col_base + BN - 1 (clipped at N).  `l` is the batch (dense) or expert (grouped).
 template <int BN, int EPI>
+// s_inv: 32 floats of shared memory owned by this warp (E4M3 D only: the column scales'
+// reciprocals are exchanged through it).
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int row, int col_base, uint32_t tmem_acc,
                                               int lane, float alpha_g, float prob_r, float nc, float& run_max,
-                                              int c_first, int c_step) {
+                                              int c_first, int c_step, float* s_inv) {
   const bool row_ok = row < p.m;
   const float s_clamp = p.clamp_s;
+  const float inv_s = s_clamp > 0.0f ? 1.0f / s_clamp : 0.0f;
 #pragma unroll 1
   for (int c = c_first; c < BN / 32; c += c_step) {
     const int col0 = col_base + c * 32;
@@ -222,7 +227,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
       for (int j = 0; j < 32; ++j) {
         const float cv = alpha_g * __uint_as_float(r[j]);
         r[j] = __float_as_uint(cv);
-        d[j] = srelu_clamp(cv, prob_r, s_clamp, p.tanh_approx);
+        d[j] = srelu_clamp(cv, prob_r, s_clamp, inv_s, p.tanh_approx);
       }
       // a chunk may run past N (N % 8 == 0 for 16-bit outputs, % 4 for fp32): 16-byte granules
       if (p.c_kind == kOutBF16) {
@@ -251,19 +256,21 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
             store16(dst + j, pack_bf16x2(d[j], d[j + 1]), pack_bf16x2(d[j + 2], d[j + 3]),
                     pack_bf16x2(d[j + 4], d[j + 5]), pack_bf16x2(d[j + 6], d[j + 7]));
       } else {
+        // D * norm_const once (rounding is monotonic, so the block maxima of the products are
+        // norm_const times the block maxima of D, rounded); scaling by 2^-e is exact
+#pragma unroll
+        for (int j = 0; j < 32; ++j) d[j] = __fmul_rn(d[j], nc);
         // row MXFP8: this thread's 32 columns form one block
         float bmax = 0.0f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, fabsf(d[j]));
-        const uint32_t code_r = e8m0_ceil_code(nc * bmax);
+        const uint32_t code_r = e8m0_ceil_code(bmax);
         const float inv_r = e8m0_inv_scale(code_r);
         uint32_t q[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j], nc), inv_r),
-                                         __fmul_rn(__fmul_rn(d[4 * j + 1], nc), inv_r));
-          const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j + 2], nc), inv_r),
-                                         __fmul_rn(__fmul_rn(d[4 * j + 3], nc), inv_r));
+          const uint32_t lo = cvt_e4m3x2(__fmul_rn(d[4 * j], inv_r), __fmul_rn(d[4 * j + 1], inv_r));
+          const uint32_t hi = cvt_e4m3x2(__fmul_rn(d[4 * j + 2], inv_r), __fmul_rn(d[4 * j + 3], inv_r));
           q[j] = lo | (hi << 16);
         }
         uint8_t* drow = reinterpret_cast<uint8_t*>(p.d) + rc;
@@ -280,22 +287,21 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
 #pragma unroll
         for (int j = 0; j < 32; ++j) cm[j] = fabsf(d[j]);
         warp_colmax_scatter(cm, lane);
-        const uint32_t code_c = e8m0_ceil_code(nc * cm[0]);
-        const float inv_c = e8m0_inv_scale(code_c);
+        const uint32_t code_c = e8m0_ceil_code(cm[0]);
         const int mblk = row >> 5;  // same for the whole warp
         p.sfd_col[sf_offset(col0 + lane, mblk, 0, p.sfd_col_mt, p.sfd_col_kt)] = static_cast<uint8_t>(code_c);
+        // every lane needs the 32 column reciprocals: one shared-memory round trip (broadcast
+        // reads) instead of 32 shuffles
+        s_inv[lane] = e8m0_inv_scale(code_c);
+        __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float i0 = __shfl_sync(0xffffffffu, inv_c, 4 * j);
-          const float i1 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 1);
-          const float i2 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 2);
-          const float i3 = __shfl_sync(0xffffffffu, inv_c, 4 * j + 3);
-          const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j], nc), i0),
-                                         __fmul_rn(__fmul_rn(d[4 * j + 1], nc), i1));
-          const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(d[4 * j + 2], nc), i2),
-                                         __fmul_rn(__fmul_rn(d[4 * j + 3], nc), i3));
+          const float4 iv = reinterpret_cast<const float4*>(s_inv)[j];
+          const uint32_t lo = cvt_e4m3x2(__fmul_rn(d[4 * j], iv.x), __fmul_rn(d[4 * j + 1], iv.y));
+          const uint32_t hi = cvt_e4m3x2(__fmul_rn(d[4 * j + 2], iv.z), __fmul_rn(d[4 * j + 3], iv.w));
           q[j] = lo | (hi << 16);
         }
+        __syncwarp();  // the next chunk overwrites s_inv
         uint8_t* dcol = reinterpret_cast<uint8_t*>(p.d_col) + rc;
         store16(dcol, q[0], q[1], q[2], q[3]);
         store16(dcol + 16, q[4], q[5], q[6], q[7]);
@@ -599,7 +605,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         }
       }
       epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN,
-                             lane, alpha_g, prob_r, nc, run_max, half, 2);
+                             lane, alpha_g, prob_r, nc, run_max, half, 2, s_amax + (warp - 2) * 32);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);

@@ -282,7 +282,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
         }
       }
       epilogue_tile<256, EPI>(p, tc.l, row, tc.nt * 256, tmem_base + (static_cast<uint32_t>(quad * 32) << 16), lane,
-                              alpha_g, prob_r, nc, run_max, 0, 1);
+                              alpha_g, prob_r, nc, run_max, 0, 1, s_amax + (warp - 2) * 32);
       tc_fence_before();
       __syncwarp();
       // the arrival publishes no memory the even CTA reads, so it needs no release
