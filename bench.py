@@ -236,14 +236,10 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     # ---------------- max over ranks
-    times = torch.tensor([elapsed_ms, e2e_ms, statistics.mean(gemm_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_ms, gemm_mean_ms = times.tolist()
+    elapsed_ms, e2e_ms, gemm_mean_ms = max_over_ranks([elapsed_ms, e2e_ms, statistics.mean(gemm_ms)], world, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    value = replica_throughput(flops * args.steps, elapsed_ms, world)
+    e2e_value = replica_throughput(flops, e2e_ms, world)
 
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"] * NOMINAL_RATIO[fmt]
@@ -265,6 +261,22 @@ def run_ours(args, rank, world, local_rank):
         "gemm_ms": round(gemm_mean_ms, 4),
     }
     return line
+
+
+def max_over_ranks(times_ms, world, device="cpu"):
+    """Each time maximised over the ranks (every rank gets the result); identity for one rank."""
+    import torch
+    if world <= 1:
+        return [float(t) for t in times_ms]
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_throughput(flops_per_rank, elapsed_ms, world):
+    """TFLOP/s of the whole job: every rank ran the same work in at most elapsed_ms."""
+    return world * flops_per_rank / (elapsed_ms * 1e-3) / 1e12
 
 
 def _traffic(workload):
