@@ -176,13 +176,52 @@ __device__ __forceinline__ void warp_colmax_scatter(float (&v)[32], int lane) {
   }
 }
 
+// Dense epilogue with bf16 C that gives the accumulator back early: this warp's chunks
+// (c_first, c_first + 2, ...) are read from TMEM, folded into the running |max| and packed to
+// bf16 in registers; then `release` (the accumulator-empty arrival) runs, and only then are the
+// packed rows stored, overlapping the next tile's MMAs.
+template <int BN, class Release>
+__device__ __forceinline__ void epilogue_dense_bf16_early(const GemmParams& p, int l, int row, int col_base,
+                                                          uint32_t tmem_acc, int c_first, float& run_max,
+                                                          Release release) {
+  constexpr int kChunks = (BN / 32 + 1) / 2;  // this warp's chunks (alternate 32-column chunks)
+  uint32_t pk[kChunks][16];
+#pragma unroll
+  for (int ci = 0; ci < kChunks; ++ci) {
+    const int c = c_first + 2 * ci;
+    if (c < BN / 32 && col_base + c * 32 < p.n) {  // warp-uniform
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tmem_acc + c * 32, r);
+      tmem_ld_wait(r);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(__uint_as_float(r[j])));
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pk[ci][j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    }
+  }
+  release();
+  if (row >= p.m) return;
+  __nv_bfloat16* rowp = reinterpret_cast<__nv_bfloat16*>(p.c) + (static_cast<uint64_t>(l) * p.m + row) *
+                                                                     static_cast<uint64_t>(p.n);
+#pragma unroll
+  for (int ci = 0; ci < kChunks; ++ci) {
+    const int c = c_first + 2 * ci;
+    const int col0 = col_base + c * 32;
+    if (c < BN / 32 && col0 < p.n) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8)
+        if (col0 + j < p.n) store16(rowp + col0 + j, pk[ci][j / 2], pk[ci][j / 2 + 1], pk[ci][j / 2 + 2], pk[ci][j / 2 + 3]);
+    }
+  }
+}
+
 // Epilogue of one tile for the rows of one warp: reads the fp32 accumulator chunk by chunk
 // (32 columns of this thread's row per tcgen05.ld) from `tmem_acc` (this warp's lane
 // quadrant, first accumulator column) and writes the outputs of row `row`, columns
 // col_base .. col_base + BN - 1 (clipped at N).  `l` is the batch (dense) or expert (grouped).
-template <int BN, int EPI>
 // s_inv: 32 floats of shared memory owned by this warp (E4M3 D only: the column scales'
 // reciprocals are exchanged through it).
+template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int row, int col_base, uint32_t tmem_acc,
                                               int lane, float alpha_g, float prob_r, float nc, float& run_max,
                                               int c_first, int c_step, float* s_inv) {
@@ -604,11 +643,19 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           run_max = 0.0f;
         }
       }
-      epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN,
-                             lane, alpha_g, prob_r, nc, run_max, half, 2, s_amax + (warp - 2) * 32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      const uint32_t tmem_acc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      };
+      if (EPI == kEpiDense && p.c_kind == kOutBF16) {
+        epilogue_dense_bf16_early<BN>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release);
+      } else {
+        epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
+                               s_amax + (warp - 2) * 32);
+        release();
+      }
       if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
     }
     // fold this warp's running maximum into shared memory
