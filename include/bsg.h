@@ -94,8 +94,9 @@ typedef struct bsg_gemm_opts {
   int tanh_approx;       /* grouped only: 1 = tanh.approx.f32 in the soft clamp, 0 = tanhf */
   int validate_offsets;  /* grouped only: 1 = copy padded_offsets to the host and check them
                             before launching (synchronises the stream) */
-  int cta_pair;          /* 0 = automatic, 1 = one CTA per 128 x tile_n tile, 2 = CTA pairs on
-                            256 x 256 tiles (tile_n is then 256) */
+  int cta_pair;          /* 0 = automatic (CTA pairs when tile_n is 0, the epilogue is not E4M3 D
+                            and there are at least #SMs/2 256 x 256 tiles), 1 = one CTA per
+                            128 x tile_n tile, 2 = CTA pairs on 256 x 256 tiles */
   int reserved[3];
 } bsg_gemm_opts;
 

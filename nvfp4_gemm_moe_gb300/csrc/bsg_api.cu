@@ -80,19 +80,6 @@ bool make_operand_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Scale-factor buffer viewed as rows of one 512-byte atom (128 x u32), loaded `atoms` rows at a time.
-bool make_sf_map(CUtensorMap* m, const void* base, uint64_t total_atoms, uint32_t atoms) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {128, total_atoms};
-  const cuuint64_t strides[1] = {512};
-  const cuuint32_t box[2] = {128, atoms};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -125,14 +112,15 @@ int choose_tile_n(int fmt, int64_t n, int64_t m_tiles_total, int num_sms, bool h
 }
 
 // CTA pairs (256 x 256 tiles) when asked for, or when the problem still gives every pair a tile.
-bool use_pairs(int64_t tiles256, int64_t m, int64_t n, int num_sms, const bsg_gemm_opts* opts) {
+bool use_pairs(int64_t tiles256, int64_t m, int64_t n, int num_sms, bool heavy_epilogue, const bsg_gemm_opts* opts) {
   if (opts && opts->cta_pair == 1) return false;
   if (opts && opts->cta_pair == 2) return true;
-  // The one-CTA kernel stages scale factors into TMEM beside the tensor pipe; the pair kernel
-  // still copies them through it and is slower on every shape measured, so it is used only
-  // on request.
-  (void)tiles256; (void)m; (void)n; (void)num_sms;
-  return false;
+  if (opts && opts->tile_n != 0) return false;
+  // CTA pairs halve the B tile each SM loads per K slice; the TMA feed is the limit of the
+  // one-CTA kernel once its epilogue is overlapped.  They need enough 256 x 256 tiles to fill
+  // the GPU, and their single accumulator exposes heavy epilogues (E4M3 D), which run better
+  // on the one-CTA kernel's double-buffered 224-wide tiles.
+  return !heavy_epilogue && m >= 256 && n > 128 && tiles256 >= num_sms / 2;
 }
 
 int max_pairs(int64_t tiles, int num_sms, const bsg_gemm_opts* opts) {
@@ -216,7 +204,7 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   st = current_device(nullptr, &info);
   if (st != BSG_OK) return st;
 
-  const bool pairs = use_pairs(l * cdiv(m, 256) * cdiv(n, 256), m, n, info.num_sms, opts);
+  const bool pairs = use_pairs(l * cdiv(m, 256) * cdiv(n, 256), m, n, info.num_sms, false, opts);
   const int64_t m_tiles = pairs ? cdiv(m, 256) : cdiv(m, 128);
   const int bn = pairs ? 256 : choose_tile_n(fmt, n, m_tiles * l, info.num_sms, false, opts);
   const int64_t n_tiles = cdiv(n, bn);
@@ -224,15 +212,11 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
 
-  CUtensorMap ta, tb, tsfa, tsfb;
+  CUtensorMap ta, tb;
   if (!make_operand_map(&ta, a, row_bytes, m, l, 128) ||
       !make_operand_map(&tb, b, row_bytes, n, l, pairs ? 128 : bn))
     return BSG_ERR_CUDA;
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
-  const uint32_t atoms_per_stage = fmt == bsg::kMXFP8 ? 1 : 4;
-  if (pairs && (!make_sf_map(&tsfa, sfa, l * cdiv(m, 128) * sf_kt, atoms_per_stage) ||
-                !make_sf_map(&tsfb, sfb, l * cdiv(n, 128) * sf_kt, atoms_per_stage)))
-    return BSG_ERR_CUDA;
 
   GemmParams p;
   memset(&p, 0, sizeof(p));
@@ -258,7 +242,7 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (cudaMemsetAsync(amax, 0, sizeof(float), s) != cudaSuccess) return BSG_ERR_CUDA;
   GemmConfig cfg{fmt, bn, bsg::kEpiDense};
-  cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, tsfa, tsfb, p, max_pairs(tiles, info.num_sms, opts), s)
+  cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
                         : bsg::launch_gemm_dense(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }
@@ -326,7 +310,7 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   }
   if (valid_m == 0) return BSG_OK;
 
-  const bool pairs = use_pairs((valid_m / 256) * cdiv(n, 256), valid_m, n, info.num_sms, opts);
+  const bool pairs = use_pairs((valid_m / 256) * cdiv(n, 256), valid_m, n, info.num_sms, fp8_d, opts);
   const int64_t m_tiles = pairs ? valid_m / 256 : valid_m / 128;
   const int bn = pairs ? 256 : choose_tile_n(fmt, n, m_tiles, info.num_sms, fp8_d, opts);
   const int64_t n_tiles = cdiv(n, bn);
@@ -334,15 +318,11 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
   const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
 
-  CUtensorMap ta, tb, tsfa, tsfb;
+  CUtensorMap ta, tb;
   if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128) ||
       !make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? 128 : bn))
     return BSG_ERR_CUDA;
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
-  const uint32_t atoms_per_stage = fmt == bsg::kMXFP8 ? 1 : 4;
-  if (pairs && (!make_sf_map(&tsfa, sfa, (valid_m / 128) * sf_kt, atoms_per_stage) ||
-                !make_sf_map(&tsfb, sfb, num_experts * cdiv(n, 128) * sf_kt, atoms_per_stage)))
-    return BSG_ERR_CUDA;
 
   GemmParams p;
   memset(&p, 0, sizeof(p));
@@ -378,7 +358,7 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   p.err = static_cast<uint32_t*>(workspace);
 
   GemmConfig cfg{fmt, bn, fp8_d ? bsg::kEpiGroupedFP8 : bsg::kEpiGroupedBF16};
-  cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, tsfa, tsfb, p, max_pairs(tiles, info.num_sms, opts), s)
+  cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
                         : bsg::launch_gemm_grouped(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
   if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;

@@ -1,27 +1,32 @@
 // gemm_pair_kernel.cuh -- the block-scaled GEMM on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles.
 //
-// A cluster of two CTAs on the two SMs of a TPC computes one 256 x 256 output tile: each CTA
-// holds 128 rows of A and 128 rows (one half) of B in its shared memory, and one thread of the
-// even CTA issues tcgen05.mma.cta_group::2 with M = 256, N = 256, so each B tile is fetched from
-// L2 once for 256 rows of A.  Each CTA's TMEM holds the fp32 accumulator of its own 128 rows and
-// the scale factors of all 256 B rows (its tensor core scales every column of its rows).
-//   warp 0     TMA producer in each CTA: its A / B halves and scale-factor atoms.  The loads of
-//              both CTAs complete bytes on the even CTA's stage barrier (cta_group::2 loads); only
-//              the even CTA arrives on that barrier, expecting the bytes of both CTAs, with a
-//              CTA-scope arrive (a cluster-scope release per stage costs about a microsecond);
-//   warp 1     TMEM allocation in both CTAs (collective); in the even CTA one thread copies the
-//              scale factors into both CTAs' TMEM, issues the MMAs, and commits to the stage and
-//              accumulator barriers of both CTAs (multicast);
-//   warps 2-5  epilogue in each CTA on its own rows, then a relaxed arrival on the even CTA's
-//              accumulator-empty barrier.
-// Stages: 6 (MXFP8) or 5 (NVFP4) of 128 bytes of K.  Waits are bounded as in the 1-CTA kernel.
+// A cluster of two CTAs (two SMs) computes one 256 x 256 output tile: each CTA holds 128 rows of
+// A and one 128-row half of B in shared memory, and one thread of the even CTA issues
+// tcgen05.mma.cta_group::2 with M = 256, N = 256, so each SM fetches its own A rows and half of
+// the B tile per K slice instead of all of B.  Each CTA's TMEM holds the fp32 accumulator of its
+// 128 rows and the scale factors of its A rows and of all 256 B rows (its tensor core scales
+// every column of its rows).  Roles in each CTA (448 threads, as in the one-CTA kernel):
+//   warp 0      TMA producer: its A rows and B half with cta_group::2 tensor loads, which
+//               complete bytes on the even CTA's stage barrier (only the even CTA arrives on it,
+//               expecting the A/B bytes of both CTAs and its own scale atoms); its scale atoms
+//               with bulk copies on its own CTA's barrier (the even CTA's stage barrier, or the
+//               odd CTA's own sf_full barrier);
+//   warp 1      TMEM allocation in both CTAs; in the even CTA one thread waits until both CTAs'
+//               scale factors are in TMEM, issues the pair MMAs and commits to the stage barriers
+//               of both CTAs (multicast) and, per tile, to both accumulator barriers;
+//   warps 2-9   epilogue on the CTA's own 128 rows (as in the one-CTA kernel), then an arrival
+//               on the even CTA's accumulator-empty barrier;
+//   warps 10-13 scale-factor stagers: the CTA's atoms from shared memory into its own TMEM with
+//               tcgen05.st, then an arrival on the even CTA's sf_ready barrier.
+// Arrivals of the odd CTA on the even CTA's barriers are relaxed: they publish nothing the even
+// CTA reads through the generic proxy (TMEM stores are complete after tcgen05.wait::st and
+// ordered before the arrival by tcgen05.fence::before_thread_sync), and a cluster-scope release
+// per arrival costs about a microsecond.  Waits are bounded as in the one-CTA kernel.
 #pragma once
 
 #include "gemm_kernel.cuh"
 
 namespace bsg {
-
-constexpr int kThreadsPair = 192;  // producer, MMA issuer, four epilogue warps
 
 template <int FMT>
 struct PairTraits {
@@ -31,15 +36,19 @@ struct PairTraits {
   static constexpr int kMmaK = FMT == kMXFP8 ? 32 : 64;
   static constexpr int kMmasPerStage = 4;
   static constexpr int kAtomsPerStage = FMT == kMXFP8 ? 1 : 4;
-  static constexpr int kSfbGroups = 2;  // scale factors of both 128-row halves of the B tile
+  // the scale-factor layout fields stage_scale_factors reads: all 256 B rows, two atom groups
+  static constexpr bool kSfbAligned = true;
+  static constexpr int kBRowGroups = 2;
+  static constexpr int kBBlocks = 8;
+  static constexpr int kSfbColsPerMma = 8;
   static constexpr int kABytes = 128 * kTileKBytes;
   static constexpr int kBBytes = 128 * kTileKBytes;
   static constexpr int kSfaBytes = kAtomsPerStage * 512;
-  static constexpr int kSfbBytes = kSfbGroups * kAtomsPerStage * 512;
+  static constexpr int kSfbBytes = kBRowGroups * kAtomsPerStage * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStages = FMT == kMXFP8 ? 6 : 5;
   static constexpr int kSfaCols = kAtomsPerStage * 4;
-  static constexpr int kSfbCols = kSfbGroups * kAtomsPerStage * 4;
+  static constexpr int kSfbCols = kSfbColsPerMma * kAtomsPerStage;
   static constexpr int kSfStride = ((kSfaCols + kSfbCols + 15) / 16) * 16;
   static constexpr int kSfBase = kTileN;  // one accumulator of 256 columns
   static constexpr int kTmemCols = 512;
@@ -56,20 +65,11 @@ struct PairTraits {
                                      (static_cast<uint32_t>(kTileMPair >> 4) << 24);
 };
 
-// One stage's scale-factor copies into both CTAs' TMEM and NM pair MMAs (M = 256), issued by one
-// thread of the even CTA (layout as in issue_stage; each CTA holds the scales of all B rows).
+// NM pair MMAs (M = 256) of one stage, issued by one thread of the even CTA; the scale factors
+// are in both CTAs' TMEM at sfa_t / sfb_t (layout as in issue_stage).
 template <int FMT, class T, int NM>
 __device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa_t,
-                                                 uint32_t sfb_t, uint32_t sfa_s, uint32_t sfb_s, uint32_t acc0) {
-  constexpr int kAtoms = FMT == kMXFP8 ? 1 : NM;
-#pragma unroll
-  for (int a = 0; a < kAtoms; ++a) {
-    tc_cp_32x128b_warpx4_pair(sfa_t + a * 4, smem_desc(sfa_s + a * 512, 0, 128, kSwizzleNone));
-#pragma unroll
-    for (int g = 0; g < T::kSfbGroups; ++g)
-      tc_cp_32x128b_warpx4_pair(sfb_t + (a * T::kSfbGroups + g) * 4,
-                                smem_desc(sfb_s + (g * T::kAtomsPerStage + a) * 512, 0, 128, kSwizzleNone));
-  }
+                                                 uint32_t sfb_t, uint32_t acc0) {
 #pragma unroll
   for (int j = 0; j < NM; ++j) {
     const uint32_t accumulate = j > 0 ? 1u : acc0;
@@ -78,15 +78,14 @@ __device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc
                            accumulate);
     } else {
       tc_mma_mxf4nvf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
-                           sfb_t + j * T::kSfbGroups * 4, accumulate);
+                           sfb_t + j * T::kSfbColsPerMma, accumulate);
     }
   }
 }
 
 template <int FMT, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                      const __grid_constant__ GemmParams p) {
   using T = PairTraits<FMT>;
   constexpr int S = T::kStages;
@@ -98,9 +97,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
   uint8_t* s_sfa = s_b + S * T::kBBytes;
   uint8_t* s_sfb = s_sfa + S * T::kSfaBytes;
   uint8_t* s_bar = s_sfb + S * T::kSfbBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_bar);
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_bar);  // even CTA: A/B of both CTAs + its scales
   uint64_t* empty = full + S;
-  uint64_t* tmem_full = empty + S;
+  uint64_t* sf_full = empty + S;                        // odd CTA: its own scale atoms
+  uint64_t* sf_ready = sf_full + S;                     // even CTA: both CTAs' scales in TMEM
+  uint64_t* tmem_full = sf_ready + S;
   uint64_t* tmem_empty = tmem_full + 1;
   uint64_t* drain = tmem_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -116,24 +117,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);  // the even CTA's expect_tx arrival; both CTAs' loads complete bytes on it
+      mbar_init(&full[s], 1);  // the even CTA's expect_tx arrival; both CTAs' A/B loads complete bytes on it
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], 1);
+      mbar_init(&sf_ready[s], 8);  // four stagers in each CTA
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 8);  // four epilogue warps in each CTA (used in the even CTA)
+    mbar_init(tmem_empty, 16);  // eight epilogue warps in each CTA (used in the even CTA)
     mbar_init(drain, 1);
     *abort_flag = 0;
     *bad_flag = 0;
     fence_mbar_init();
   }
   if (EPI != kEpiDense) {
-    for (int i = threadIdx.x; i < 1024; i += kThreadsPair) s_amax[i] = 0.0f;
+    for (int i = threadIdx.x; i < 1024; i += kThreadsGemm) s_amax[i] = 0.0f;
   } else if (threadIdx.x == 0) {
     s_amax[0] = 0.0f;
   }
   __syncthreads();
   if (EPI != kEpiDense) {
-    for (int i = threadIdx.x; i < p.l; i += kThreadsPair) {
+    for (int i = threadIdx.x; i < p.l; i += kThreadsGemm) {
       const int32_t o = p.offsets[i];
       const int32_t prev = i == 0 ? 0 : p.offsets[i - 1];
       s_offs[i] = o;
@@ -147,8 +150,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
-    prefetch_tmap(&tmap_sfa);
-    prefetch_tmap(&tmap_sfb);
   }
   tc_fence_before();
   __syncthreads();
@@ -175,32 +176,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
         const int sfa_group = min(tc.mt * 2 + static_cast<int>(rank), p.sfa_mt - 1);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
-          const uint32_t fbar = full0 + stage * 8;
+          const int k_left = p.k - kt * T::kElemsPerKTile;
+          const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
+          const int atoms = FMT == kMXFP8 ? 1 : n_mma;
+          const uint32_t sf_bytes = static_cast<uint32_t>(atoms * 512 * (1 + T::kBRowGroups));
           // The odd CTA cannot load stage s of the next round before this round's phase has
           // completed (its empty barrier is released after the MMAs that needed that phase), so
-          // its bytes always land in the phase the even CTA's arrival belongs to.
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * T::kStageBytes);
+          // its A/B bytes always land in the phase the even CTA's arrival belongs to.
+          uint64_t* sf_bar = leader ? &full[stage] : &sf_full[stage];
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (T::kABytes + T::kBBytes) + sf_bytes);
+          else mbar_arrive_expect_tx(&sf_full[stage], sf_bytes);
+          const uint32_t fbar = full0 + stage * 8;
           tma_load_3d_pair(s_a + stage * T::kABytes, &tmap_a, fbar, kt * kTileKBytes, a_row, a_batch);
           tma_load_3d_pair(s_b + stage * T::kBBytes, &tmap_b, fbar, kt * kTileKBytes, b_row, tc.l);
-          tma_load_2d_pair(s_sfa + stage * T::kSfaBytes, &tmap_sfa, fbar, 0,
-                           (a_batch * p.sfa_mt + sfa_group) * p.sf_kt + kt * T::kAtomsPerStage);
+          const uint8_t* sfa_src =
+              p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + sfa_group) * p.sf_kt +
+                       static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+          bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, sf_bar);
 #pragma unroll
-          for (int g = 0; g < T::kSfbGroups; ++g) {
+          for (int g = 0; g < T::kBRowGroups; ++g) {
             // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
-            const int grp = min(tc.nt * 2 + g, p.sfb_mt - 1);
-            tma_load_2d_pair(s_sfb + stage * T::kSfbBytes + g * T::kAtomsPerStage * 512, &tmap_sfb, fbar, 0,
-                             (tc.l * p.sfb_mt + grp) * p.sf_kt + kt * T::kAtomsPerStage);
+            const int rb = min(tc.nt * 2 + g, p.sfb_mt - 1);
+            const uint8_t* sfb_src =
+                p.sfb + ((static_cast<uint64_t>(tc.l) * p.sfb_mt + rb) * p.sf_kt +
+                         static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+            bulk_load(s_sfb + stage * T::kSfbBytes + g * T::kAtomsPerStage * 512, sfb_src, atoms * 512, sf_bar);
           }
           ++issued;
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok && leader) {
-        // the even CTA's stage barriers count both CTAs' loads: wait for every stage issued
+      if (!ok) {
+        // drain: every stage barrier this CTA's copies complete on must see them land (the even
+        // CTA's stage barriers count both CTAs' A/B loads)
+        uint64_t* bars = leader ? full : sf_full;
         for (int s = 0; s < S; ++s) {
           if (issued > static_cast<uint64_t>(s)) {
             const uint32_t ph = (s < static_cast<int>(stage)) ? phase : (phase ^ 1u);
-            wait_bounded_plain(&full[s], ph);
+            wait_bounded_plain(&bars[s], ph);
           }
         }
       }
@@ -211,30 +224,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
       uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
-      const uint32_t sfa_base = smem_u32(s_sfa), sfb_base = smem_u32(s_sfb);
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
         if (!wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          // warp-uniform control flow and operands, failures acted on per tile (as in the 1-CTA
-          // kernel)
-          ok &= wait_bounded(&full[stage], phase, abort_flag, p.err);
+          // warp-uniform control flow and operands, failures acted on per tile (as in the
+          // one-CTA kernel); sf_ready implies the stage's A/B data landed (the even CTA's
+          // stagers waited for it)
+          ok &= wait_bounded(&sf_ready[stage], phase, abort_flag, p.err);
           tc_fence_after();
           const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
-          const uint32_t sfa_s = sfa_base + stage * T::kSfaBytes;
-          const uint32_t sfb_s = sfb_base + stage * T::kSfbBytes;
           const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
           const uint32_t acc0 = kt > 0 ? 1u : 0u;
           const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
           if (lane == 0) {
             if (n_mma == T::kMmasPerStage) {
-              issue_stage_pair<FMT, T, T::kMmasPerStage>(tmem_base, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+              issue_stage_pair<FMT, T, T::kMmasPerStage>(tmem_base, adesc, bdesc, sfa_t, sfb_t, acc0);
             } else {
-              if (n_mma == 1) issue_stage_pair<FMT, T, 1>(tmem_base, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
-              if (n_mma == 2) issue_stage_pair<FMT, T, 2>(tmem_base, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
-              if (n_mma == 3) issue_stage_pair<FMT, T, 3>(tmem_base, adesc, bdesc, sfa_t, sfb_t, sfa_s, sfb_s, acc0);
+              if (n_mma == 1) issue_stage_pair<FMT, T, 1>(tmem_base, adesc, bdesc, sfa_t, sfb_t, acc0);
+              if (n_mma == 2) issue_stage_pair<FMT, T, 2>(tmem_base, adesc, bdesc, sfa_t, sfb_t, acc0);
+              if (n_mma == 3) issue_stage_pair<FMT, T, 3>(tmem_base, adesc, bdesc, sfa_t, sfb_t, acc0);
             }
             tc_commit_pair_multicast(&empty[stage], 0x3);
           }
@@ -254,9 +265,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
         __syncwarp();
       }
     }
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ scale-factor stagers (both CTAs)
+    const uint32_t quad_lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ready0 = mapa_shared(smem_u32(&sf_ready[0]), 0);
+    uint64_t* landed = leader ? full : sf_full;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int t = pair_id; !bad && ok && t < p.num_tiles; t += num_pairs) {
+      for (int kt = 0; kt < p.k_tiles; ++kt) {
+        ok &= wait_bounded(&landed[stage], phase, abort_flag, p.err);
+        tc_fence_after();
+        const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
+        stage_scale_factors<T>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t, sfa_t + T::kSfaCols,
+                               lane, 0);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&sf_ready[stage]);
+          else mbar_arrive_cluster_relaxed(ready0 + stage * 8);
+        }
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+    }
   } else {
-    // ------------------------------------------------------------ epilogue warps 2..5 (both CTAs)
+    // ------------------------------------------------------------ epilogue warps 2..9 (both CTAs)
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     float run_max = 0.0f;
     int run_expert = -1;
     uint32_t acc_phase = 0;
@@ -281,12 +317,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
           run_max = 0.0f;
         }
       }
-      epilogue_tile<256, EPI>(p, tc.l, row, tc.nt * 256, tmem_base + (static_cast<uint32_t>(quad * 32) << 16), lane,
-                              alpha_g, prob_r, nc, run_max, 0, 1, s_amax + (warp - 2) * 32);
-      tc_fence_before();
-      __syncwarp();
+      const uint32_t tmem_acc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
       // the arrival publishes no memory the even CTA reads, so it needs no release
-      if (lane == 0) mbar_arrive_cluster_relaxed(empty_leader);
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(empty_leader);
+      };
+      if (EPI == kEpiDense && p.c_kind == kOutBF16) {
+        epilogue_dense_bf16_early<256>(p, tc.l, row, tc.nt * 256, tmem_acc, half, run_max, release);
+      } else {
+        epilogue_tile<256, EPI>(p, tc.l, row, tc.nt * 256, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
+                                s_amax + (warp - 2) * 32);
+        release();
+      }
       acc_phase ^= 1u;
     }
     float v = run_max;
@@ -305,7 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
     if (EPI == kEpiDense) {
       if (threadIdx.x == 0 && s_amax[0] > 0.0f) atomic_max_nonneg(p.amax, s_amax[0]);
     } else if (EPI == kEpiGroupedBF16) {
-      for (int g = threadIdx.x; g < p.l; g += kThreadsPair)
+      for (int g = threadIdx.x; g < p.l; g += kThreadsGemm)
         if (s_amax[g] > 0.0f) atomic_max_nonneg(&p.amax[g], s_amax[g]);
     }
   }
@@ -318,8 +362,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsPair, 1)
 // Launches at most as many CTA pairs as can be resident at once (a cluster must fit in one GPC,
 // so fewer than #SMs / 2 pairs may fit); `max_pairs` is the caller's upper bound.
 template <int FMT, int EPI>
-cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsfa,
-                               const CUtensorMap& tsfb, const GemmParams& p, int max_pairs, cudaStream_t stream) {
+cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int max_pairs,
+                               cudaStream_t stream) {
   using T = PairTraits<FMT>;
   auto kern = gemm_pair_kernel<FMT, EPI>;
   static int resident_pairs[64] = {};  // per device; 0 = not queried yet
@@ -332,7 +376,7 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreadsPair, 1, 1);
+    cfg.blockDim = dim3(kThreadsGemm, 1, 1);
     cfg.dynamicSmemBytes = T::kSmemBytes;
     int clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
@@ -341,7 +385,7 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
   }
   int pairs = max_pairs < resident_pairs[dev] ? max_pairs : resident_pairs[dev];
   if (pairs < 1) pairs = 1;
-  kern<<<2 * pairs, kThreadsPair, T::kSmemBytes, stream>>>(ta, tb, tsfa, tsfb, p);
+  kern<<<2 * pairs, kThreadsGemm, T::kSmemBytes, stream>>>(ta, tb, p);
   return cudaGetLastError();
 }
 

@@ -63,8 +63,7 @@ cudaError_t launch_gemm_grouped(const GemmConfig& cfg, const CUtensorMap& tmap_a
 // Launches the CTA-pair kernel (256 x 256 tiles on clusters of two CTAs) with at most
 // `max_pairs` clusters.
 cudaError_t launch_gemm_pair(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                             const CUtensorMap& tmap_sfa, const CUtensorMap& tmap_sfb, const GemmParams& p,
-                             int max_pairs, cudaStream_t stream);
+                             const GemmParams& p, int max_pairs, cudaStream_t stream);
 
 // Launches the block quantiser.
 cudaError_t launch_quantize(int fmt, const float* x, int64_t batch, int64_t rows, int64_t k, uint8_t* q,
