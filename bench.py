@@ -247,7 +247,7 @@ def run_ours(args, rank, world, local_rank):
     achieved = flops / (gemm_mean_ms * 1e-3) / 1e12
     roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "traffic": _traffic(args.workload),
-            "kernel": "gemm_kernel", "peak_source": f"{peak_src} bf16 burst x {NOMINAL_RATIO[fmt]:g} "
+            "kernel": "GEMM launch (automatic choice: gemm_pair_kernel or gemm_kernel)", "peak_source": f"{peak_src} bf16 burst x {NOMINAL_RATIO[fmt]:g} "
                                                    f"(dense {fmt} / bf16 nominal ratio)"}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
