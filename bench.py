@@ -304,11 +304,24 @@ def _config(wl):
 
 # --------------------------------------------------------------------------- reference arm (CPU oracle)
 
+ORACLE_SAMPLE_FLOPS = 6e11  # float64 GEMM work of one oracle sample (about 10-30 s on the host cores)
+
+
+def oracle_rows(wl, requested=0):
+    """Rows of A in the oracle's timed sample: `requested`, else enough for ORACLE_SAMPLE_FLOPS."""
+    if requested > 0:
+        return int(requested)
+    max_rows = wl.m if isinstance(wl, W.Dense) else wl.valid_m
+    rows = int(ORACLE_SAMPLE_FLOPS / (2.0 * wl.n * wl.k)) // 256 * 256
+    return max(256, min(rows, max_rows))
+
+
 def run_reference(args):
     from oracle import gemm as og, quantize as oq
     wl = W.ALL[args.workload]
     cores = os.cpu_count() or 1
     step_times, sample_flops = [], 0.0
+    args.ref_rows = oracle_rows(wl, args.ref_rows)
 
     def one_step():
         if isinstance(wl, W.Dense):
@@ -373,7 +386,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=W.DENSE_MXFP8_8192.name, choices=sorted(W.ALL))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=2048, help="rows of A in the oracle's timed sample")
+    ap.add_argument("--ref-rows", type=int, default=0,
+                    help="rows of A in the oracle's timed sample (0: sized to about 6e11 float64 flops)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
