@@ -1,6 +1,6 @@
 // quantize.cu -- fp32 -> MXFP8 / NVFP4 block quantiser (memory-bound).
 //
-// A warp takes one row at a time and walks its "units": 128 consecutive fp32 values (512 bytes,
+// MXFP8: a warp takes one row at a time and walks its "units": 128 consecutive fp32 values (512 bytes,
 // one float4 per lane, fully coalesced), kUnroll loads in flight.  For MXFP8 a unit is 4 blocks of 32 (8 lanes per
 // block), for NVFP4 8 blocks of 16 (4 lanes per block).  Block maxima are reduced with
 // warp shuffles, the scale bytes of 4 consecutive blocks are adjacent in the atom layout
@@ -39,18 +39,30 @@ __device__ __forceinline__ uint32_t ue4m3_code_of_amax_over_6(float a) {
   return c;
 }
 
-// E2M1 nibble of RNE_satfinite(x / s) from exact thresholds t[i] = midpoint_i * s: the
+// E2M1 nibble of RNE_satfinite(x / s) from exact thresholds t_i = midpoint_i * s: the
 // magnitude index counts the midpoints below |x|; at a midpoint the even index wins, i.e.
-// midpoints 1, 3, 5 (0.75, 1.75, 3.5) count when equal as well.  The sign bit is the sign
-// of x (a negative value that rounds to zero gives -0), as the E4M3 conversion does.
+// midpoints 1, 3, 5 (0.75, 1.75, 3.5) count when equal as well.  `t` holds thresholds for a
+// strict comparison: t_i itself for i = 0, 2, 4, 6 and the float just below t_i for i = 1, 3, 5
+// (a >= t  <=>  a > prev(t) for positive floats).  Seven independent comparisons summed beat a
+// three-step binary search here (its steps depend on each other).  The sign bit is the sign of
+// x (a negative value that rounds to zero gives -0), as the E4M3 conversion does.
 __device__ __forceinline__ uint32_t e2m1_nibble(float x, const float (&t)[7]) {
   const float a = fabsf(x);
-  uint32_t idx = (a > t[0]) + (a >= t[1]) + (a > t[2]) + (a >= t[3]) + (a > t[4]) + (a >= t[5]) + (a > t[6]);
+  const uint32_t idx = (a > t[0]) + (a > t[1]) + (a > t[2]) + (a > t[3]) + (a > t[4]) + (a > t[5]) + (a > t[6]);
   return idx | ((__float_as_uint(x) >> 28) & 8u);
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restrict__ x, int64_t rows, int k,
+// The seven strict-comparison thresholds of e2m1_nibble for scale s > 0.
+__device__ __forceinline__ void e2m1_thresholds(float s, float (&t)[7]) {
+  const float m[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+#pragma unroll
+  for (int i = 0; i < 7; ++i) {
+    const float v = m[i] * s;  // exact: at most 3 + 4 significant bits
+    t[i] = (i & 1) ? __uint_as_float(__float_as_uint(v) - 1u) : v;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const float* __restrict__ x, int64_t rows, int k,
                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                             int64_t rows_padded, int units_per_row, int64_t total_rows,
                                                             int64_t mt_n, int64_t kt_n) {
@@ -81,45 +93,20 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restr
         const int kk = kc * 128 + lane * 4;
         const bool elem_ok = row_ok && kk < k;
         float a = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
-        if (FMT == kMXFP8) {
-          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-          const uint32_t code = e8m0_ceil_code(a);
-          const float inv = e8m0_inv_scale(code);
-          const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[j].x, inv), __fmul_rn(v[j].y, inv));
-          const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[j].z, inv), __fmul_rn(v[j].w, inv));
-          if (elem_ok) *reinterpret_cast<uint32_t*>(q + row_g * k + kk) = lo | (hi << 16);
-          const uint32_t c1 = __shfl_sync(0xffffffffu, code, 8);
-          const uint32_t c2 = __shfl_sync(0xffffffffu, code, 16);
-          const uint32_t c3 = __shfl_sync(0xffffffffu, code, 24);
-          if (lane == 0) {
-            const uint64_t off = sf_offset(r, kc * 4, l, mt_n, kt_n);
-            *reinterpret_cast<uint32_t*>(sf + off) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
-          }
-        } else {
-          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-          const uint32_t code = ue4m3_code_of_amax_over_6(a);
-          const float s = ue4m3_value(code);
-          const float t[7] = {0.25f * s, 0.75f * s, 1.25f * s, 1.75f * s, 2.5f * s, 3.5f * s, 5.0f * s};
-          uint32_t nib = 0;
-          if (code != 0) {
-            nib = e2m1_nibble(v[j].x, t) | (e2m1_nibble(v[j].y, t) << 4) | (e2m1_nibble(v[j].z, t) << 8) |
-                  (e2m1_nibble(v[j].w, t) << 12);
-          }
-          if (elem_ok) *reinterpret_cast<uint16_t*>(q + (row_g * k + kk) / 2) = static_cast<uint16_t>(nib);
-          // scale bytes: blocks 0-3 from lanes 0, 4, 8, 12 and blocks 4-7 from lanes 16, 20, 24, 28
-          const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 4);
-          const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 8);
-          const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 12);
-          if ((lane & 15) == 0) {
-            const int64_t kb = static_cast<int64_t>(kc) * 8 + (lane >> 2);
-            if ((kb >> 2) < kt_n) {
-              const uint64_t off = sf_offset(r, kb, l, mt_n, kt_n);
-              *reinterpret_cast<uint32_t*>(sf + off) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
-            }
-          }
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+        const uint32_t code = e8m0_ceil_code(a);
+        const float inv = e8m0_inv_scale(code);
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[j].x, inv), __fmul_rn(v[j].y, inv));
+        const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[j].z, inv), __fmul_rn(v[j].w, inv));
+        if (elem_ok) *reinterpret_cast<uint32_t*>(q + row_g * k + kk) = lo | (hi << 16);
+        const uint32_t c1 = __shfl_sync(0xffffffffu, code, 8);
+        const uint32_t c2 = __shfl_sync(0xffffffffu, code, 16);
+        const uint32_t c3 = __shfl_sync(0xffffffffu, code, 24);
+        if (lane == 0) {
+          const uint64_t off = sf_offset(r, kc * 4, l, mt_n, kt_n);
+          *reinterpret_cast<uint32_t*>(sf + off) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
         }
       }
     }
@@ -163,7 +150,8 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const float* _
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
         const uint32_t code = ue4m3_code_of_amax_over_6(a);
         const float s = ue4m3_value(code);
-        const float t[7] = {0.25f * s, 0.75f * s, 1.25f * s, 1.75f * s, 2.5f * s, 3.5f * s, 5.0f * s};
+        float t[7];
+        e2m1_thresholds(s, t);
         uint32_t nib = 0;
         if (code != 0) {
           nib = e2m1_nibble(v0[j].x, t) | (e2m1_nibble(v0[j].y, t) << 4) | (e2m1_nibble(v0[j].z, t) << 8) |
@@ -203,7 +191,7 @@ cudaError_t launch_quantize(int fmt, const float* x, int64_t batch, int64_t rows
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
   if (fmt == kMXFP8) {
-    quantize_kernel<kMXFP8><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+    quantize_mxfp8_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
         x, rows, static_cast<int>(k), q, sf, rows_padded, units_per_row, total_rows, mt_n, kt_n);
   } else {
     quantize_nvfp4_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
