@@ -112,15 +112,29 @@ int choose_tile_n(int fmt, int64_t n, int64_t m_tiles_total, int num_sms, bool h
 }
 
 // CTA pairs (256 x 256 tiles) when asked for, or when the problem still gives every pair a tile.
-bool use_pairs(int64_t tiles256, int64_t m, int64_t n, int num_sms, bool heavy_epilogue, const bsg_gemm_opts* opts) {
-  if (opts && opts->cta_pair == 1) return false;
-  if (opts && opts->cta_pair == 2) return true;
-  if (opts && opts->tile_n != 0) return false;
-  // CTA pairs halve the B tile each SM loads per K slice; the TMA feed is the limit of the
-  // one-CTA kernel once its epilogue is overlapped.  They need enough 256 x 256 tiles to fill
-  // the GPU, and their single accumulator exposes heavy epilogues (E4M3 D), which run better
-  // on the one-CTA kernel's double-buffered 224-wide tiles.
-  return !heavy_epilogue && m >= 256 && n > 128 && tiles256 >= num_sms / 2;
+struct TilePlan {
+  bool pairs;  // CTA-pair kernel (256-row tiles) or one-CTA kernel (128-row tiles)
+  int bn;      // tile width
+};
+
+// Kernel and tile width for a GEMM with `m` rows (per batch), `n` columns and `l` batches.
+// CTA pairs halve the B bytes each SM loads per K slice (the one-CTA kernel's TMA feed is its
+// limit once the epilogue is overlapped); they need enough 256-row tiles to fill the GPU.  E4M3
+// D (row and column re-quantisation) makes the epilogue about as long as a tile's MMAs, so it
+// takes 224-wide tiles with two TMEM accumulators, whose epilogue overlaps the next tile.
+TilePlan plan_tiles(int fmt, int64_t m, int64_t n, int64_t l, int num_sms, bool heavy_epilogue,
+                    const bsg_gemm_opts* opts) {
+  const int cta_pair = opts ? opts->cta_pair : 0;
+  const int tile_n = opts ? opts->tile_n : 0;
+  const bool wide_ok = fmt == bsg::kMXFP8;
+  if (cta_pair == 2) {
+    const bool w224 = wide_ok && (tile_n == 224 || (tile_n == 0 && heavy_epilogue));
+    return {true, w224 ? 224 : 256};
+  }
+  const int64_t tiles256 = l * cdiv(m, 256) * cdiv(n, 256);
+  if (cta_pair == 0 && tile_n == 0 && m >= 256 && n > 128 && tiles256 >= num_sms / 2)
+    return {true, (wide_ok && heavy_epilogue) ? 224 : 256};
+  return {false, choose_tile_n(fmt, n, l * cdiv(m, 128), num_sms, heavy_epilogue, opts)};
 }
 
 int max_pairs(int64_t tiles, int num_sms, const bsg_gemm_opts* opts) {
@@ -204,9 +218,10 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   st = current_device(nullptr, &info);
   if (st != BSG_OK) return st;
 
-  const bool pairs = use_pairs(l * cdiv(m, 256) * cdiv(n, 256), m, n, info.num_sms, false, opts);
+  const TilePlan plan = plan_tiles(fmt, m, n, l, info.num_sms, false, opts);
+  const bool pairs = plan.pairs;
+  const int bn = plan.bn;
   const int64_t m_tiles = pairs ? cdiv(m, 256) : cdiv(m, 128);
-  const int bn = pairs ? 256 : choose_tile_n(fmt, n, m_tiles * l, info.num_sms, false, opts);
   const int64_t n_tiles = cdiv(n, bn);
   const int64_t tiles = l * m_tiles * n_tiles;
   const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
@@ -214,7 +229,7 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
 
   CUtensorMap ta, tb;
   if (!make_operand_map(&ta, a, row_bytes, m, l, 128) ||
-      !make_operand_map(&tb, b, row_bytes, n, l, pairs ? 128 : bn))
+      !make_operand_map(&tb, b, row_bytes, n, l, pairs ? bn / 2 : bn))
     return BSG_ERR_CUDA;
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
 
@@ -310,9 +325,10 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   }
   if (valid_m == 0) return BSG_OK;
 
-  const bool pairs = use_pairs((valid_m / 256) * cdiv(n, 256), valid_m, n, info.num_sms, fp8_d, opts);
+  const TilePlan plan = plan_tiles(fmt, valid_m, n, 1, info.num_sms, fp8_d, opts);
+  const bool pairs = plan.pairs;
+  const int bn = plan.bn;
   const int64_t m_tiles = pairs ? valid_m / 256 : valid_m / 128;
-  const int bn = pairs ? 256 : choose_tile_n(fmt, n, m_tiles, info.num_sms, fp8_d, opts);
   const int64_t n_tiles = cdiv(n, bn);
   const int64_t tiles = m_tiles * n_tiles;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
@@ -320,7 +336,7 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
 
   CUtensorMap ta, tb;
   if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128) ||
-      !make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? 128 : bn))
+      !make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn))
     return BSG_ERR_CUDA;
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
 

@@ -1,10 +1,11 @@
-// gemm_pair_kernel.cuh -- the block-scaled GEMM on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles.
+// gemm_pair_kernel.cuh -- the block-scaled GEMM on CTA pairs (tcgen05 cta_group::2), 256 x BN tiles.
 //
-// A cluster of two CTAs (two SMs) computes one 256 x 256 output tile: each CTA holds 128 rows of
-// A and one 128-row half of B in shared memory, and one thread of the even CTA issues
-// tcgen05.mma.cta_group::2 with M = 256, N = 256, so each SM fetches its own A rows and half of
+// A cluster of two CTAs (two SMs) computes one 256 x BN output tile (BN = 256, or 224 with two
+// TMEM accumulators so that the epilogue overlaps the next tile's MMAs): each CTA holds 128 rows
+// of A and one BN/2-row half of B in shared memory, and one thread of the even CTA issues
+// tcgen05.mma.cta_group::2 with M = 256, N = BN, so each SM fetches its own A rows and half of
 // the B tile per K slice instead of all of B.  Each CTA's TMEM holds the fp32 accumulator of its
-// 128 rows and the scale factors of its A rows and of all 256 B rows (its tensor core scales
+// 128 rows and the scale factors of its A rows and of all BN B rows (its tensor core scales
 // every column of its rows).  Roles in each CTA (448 threads, as in the one-CTA kernel):
 //   warp 0      TMA producer: its A rows and B half with cta_group::2 tensor loads, which
 //               complete bytes on the even CTA's stage barrier (only the even CTA arrives on it,
@@ -28,37 +29,44 @@
 
 namespace bsg {
 
-template <int FMT>
+template <int FMT, int BN>
 struct PairTraits {
+  static_assert(BN == 256 || (BN == 224 && FMT == kMXFP8), "pair tile widths");
   static constexpr int kTileMPair = 256;
-  static constexpr int kTileN = 256;
+  static constexpr int kTileN = BN;
+  static constexpr int kBHalf = BN / 2;  // B rows each CTA holds
   static constexpr int kElemsPerKTile = FMT == kMXFP8 ? 128 : 256;
   static constexpr int kMmaK = FMT == kMXFP8 ? 32 : 64;
   static constexpr int kMmasPerStage = 4;
   static constexpr int kAtomsPerStage = FMT == kMXFP8 ? 1 : 4;
-  // the scale-factor layout fields stage_scale_factors reads: all 256 B rows, two atom groups
-  static constexpr bool kSfbAligned = true;
-  static constexpr int kBRowGroups = 2;
-  static constexpr int kBBlocks = 8;
-  static constexpr int kSfbColsPerMma = 8;
+  // the scale-factor layout fields stage_scale_factors reads: the scales of all BN B rows, from
+  // two atom groups, or three when a 224-wide tile starts inside one
+  static constexpr bool kSfbAligned = BN % 128 == 0;
+  static constexpr int kBRowGroups = kSfbAligned ? BN / 128 : 3;
+  static constexpr int kBBlocks = BN / 32;
+  static constexpr int kSfbColsPerMma = ((kBBlocks + 3) / 4) * 4;
   static constexpr int kABytes = 128 * kTileKBytes;
-  static constexpr int kBBytes = 128 * kTileKBytes;
+  static constexpr int kBBytes = kBHalf * kTileKBytes;
   static constexpr int kSfaBytes = kAtomsPerStage * 512;
   static constexpr int kSfbBytes = kBRowGroups * kAtomsPerStage * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kStages = FMT == kMXFP8 ? 6 : 5;
+  static constexpr int kAcc = BN == 256 ? 1 : 2;  // 224: two accumulators, epilogue overlapped
   static constexpr int kSfaCols = kAtomsPerStage * 4;
   static constexpr int kSfbCols = kSfbColsPerMma * kAtomsPerStage;
   static constexpr int kSfStride = ((kSfaCols + kSfbCols + 15) / 16) * 16;
-  static constexpr int kSfBase = kTileN;  // one accumulator of 256 columns
+  static constexpr int kSfBase = kAcc * BN;
   static constexpr int kTmemCols = 512;
-  static_assert(kSfBase + kStages * kSfStride <= 512, "TMEM budget");
   static constexpr int kBarBytes = 1024;
   static constexpr int kOffsetsBytes = 4096;
   static constexpr int kAmaxBytes = 4096;
+  static constexpr int kStagesSmem = (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes) / kStageBytes;
+  static constexpr int kStagesTmem = (512 - kSfBase) / kSfStride;
+  static constexpr int kStages = kStagesSmem < kStagesTmem ? (kStagesSmem < 6 ? kStagesSmem : 6)
+                                                           : (kStagesTmem < 6 ? kStagesTmem : 6);
+  static_assert(kStages >= 3, "pipeline depth");
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kOffsetsBytes + kAmaxBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // M = 256 across the pair (M >> 4 at bit 24), N = 256 (N >> 3 at bit 17)
+  // M = 256 across the pair (M >> 4 at bit 24), N = BN (N >> 3 at bit 17)
   static constexpr uint32_t kIdesc = (FMT == kMXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))
                                                     : ((1u << 7) | (1u << 10) | (0u << 23))) |
                                      (static_cast<uint32_t>(kTileN >> 3) << 17) |
@@ -83,12 +91,13 @@ __device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc
   }
 }
 
-template <int FMT, int EPI>
+template <int FMT, int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ GemmParams p) {
-  using T = PairTraits<FMT>;
+  using T = PairTraits<FMT, BN>;
   constexpr int S = T::kStages;
+  constexpr int ACC = T::kAcc;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -102,8 +111,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   uint64_t* sf_full = empty + S;                        // odd CTA: its own scale atoms
   uint64_t* sf_ready = sf_full + S;                     // even CTA: both CTAs' scales in TMEM
   uint64_t* tmem_full = sf_ready + S;
-  uint64_t* tmem_empty = tmem_full + 1;
-  uint64_t* drain = tmem_empty + 1;
+  uint64_t* tmem_empty = tmem_full + ACC;
+  uint64_t* drain = tmem_empty + ACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bad_flag = const_cast<int*>(abort_flag) + 1;
@@ -122,8 +131,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       mbar_init(&sf_full[s], 1);
       mbar_init(&sf_ready[s], 8);  // four stagers in each CTA
     }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 16);  // eight epilogue warps in each CTA (used in the even CTA)
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], 16);  // eight epilogue warps in each CTA (used in the even CTA)
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     *bad_flag = 0;
@@ -172,7 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
         const int a_batch = EPI == kEpiDense ? tc.l : 0;
         const int a_row = tc.mt * 256 + static_cast<int>(rank) * 128;
-        const int b_row = tc.nt * 256 + static_cast<int>(rank) * 128;
+        const int b_row = tc.nt * BN + static_cast<int>(rank) * T::kBHalf;
         const int sfa_group = min(tc.mt * 2 + static_cast<int>(rank), p.sfa_mt - 1);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
@@ -196,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
 #pragma unroll
           for (int g = 0; g < T::kBRowGroups; ++g) {
             // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
-            const int rb = min(tc.nt * 2 + g, p.sfb_mt - 1);
+            const int rb = min((tc.nt * BN) / 128 + g, p.sfb_mt - 1);
             const uint8_t* sfb_src =
                 p.sfb + ((static_cast<uint64_t>(tc.l) * p.sfb_mt + rb) * p.sf_kt +
                          static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
@@ -221,12 +232,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (leader && !bad) {
-      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
-        if (!wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+        if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           // warp-uniform control flow and operands, failures acted on per tile (as in the
           // one-CTA kernel); sf_ready implies the stage's A/B data landed (the even CTA's
@@ -241,11 +253,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
           if (lane == 0) {
             if (n_mma == T::kMmasPerStage) {
-              issue_stage_pair<FMT, T, T::kMmasPerStage>(tmem_base, adesc, bdesc, sfa_t, sfb_t, acc0);
+              issue_stage_pair<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
             } else {
-              if (n_mma == 1) issue_stage_pair<FMT, T, 1>(tmem_base, adesc, bdesc, sfa_t, sfb_t, acc0);
-              if (n_mma == 2) issue_stage_pair<FMT, T, 2>(tmem_base, adesc, bdesc, sfa_t, sfb_t, acc0);
-              if (n_mma == 3) issue_stage_pair<FMT, T, 3>(tmem_base, adesc, bdesc, sfa_t, sfb_t, acc0);
+              if (n_mma == 1) issue_stage_pair<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
+              if (n_mma == 2) issue_stage_pair<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
+              if (n_mma == 3) issue_stage_pair<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
             }
             tc_commit_pair_multicast(&empty[stage], 0x3);
           }
@@ -253,9 +265,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        if (lane == 0) tc_commit_pair_multicast(tmem_full, 0x3);
+        if (lane == 0) tc_commit_pair_multicast(&tmem_full[acc], 0x3);
         __syncwarp();
-        acc_phase ^= 1u;
+        if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok) {
         if (lane == 0) {
@@ -273,12 +285,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     for (int t = pair_id; !bad && ok && t < p.num_tiles; t += num_pairs) {
+      const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
+      const int b_blk0 = ((tc.nt * BN) >> 5) & 3;  // the tile's first 32-row block within its first atom
       for (int kt = 0; kt < p.k_tiles; ++kt) {
         ok &= wait_bounded(&landed[stage], phase, abort_flag, p.err);
         tc_fence_after();
         const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
         stage_scale_factors<T>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t, sfa_t + T::kSfaCols,
-                               lane, 0);
+                               lane, b_blk0);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -295,12 +309,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     const int half = (warp - 2) >> 2;
     float run_max = 0.0f;
     int run_expert = -1;
-    uint32_t acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0;
     const float nc = (EPI == kEpiGroupedFP8) ? *p.norm_const : 1.0f;
-    const uint32_t empty_leader = mapa_shared(smem_u32(tmem_empty), 0);
+    const uint32_t empty_leader = mapa_shared(smem_u32(&tmem_empty[0]), 0);
     for (int t = pair_id; !bad && t < p.num_tiles; t += num_pairs) {
       const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
-      if (!wait_bounded(tmem_full, acc_phase, abort_flag, p.err)) break;
+      if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const int row = tc.mt * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
       float alpha_g = 1.0f, prob_r = 0.0f;
@@ -317,21 +331,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           run_max = 0.0f;
         }
       }
-      const uint32_t tmem_acc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+      const uint32_t tmem_acc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       // the arrival publishes no memory the even CTA reads, so it needs no release
       auto release = [&]() {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(empty_leader);
+        if (lane == 0) mbar_arrive_cluster_relaxed(empty_leader + acc * 8);
       };
       if (EPI == kEpiDense && p.c_kind == kOutBF16) {
-        epilogue_dense_bf16_early<256>(p, tc.l, row, tc.nt * 256, tmem_acc, half, run_max, release);
+        epilogue_dense_bf16_early<BN>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release);
       } else {
-        epilogue_tile<256, EPI>(p, tc.l, row, tc.nt * 256, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
-                                s_amax + (warp - 2) * 32);
+        epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
+                               s_amax + (warp - 2) * 32);
         release();
       }
-      acc_phase ^= 1u;
+      if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
     }
     float v = run_max;
     for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -361,11 +375,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
 
 // Launches at most as many CTA pairs as can be resident at once (a cluster must fit in one GPC,
 // so fewer than #SMs / 2 pairs may fit); `max_pairs` is the caller's upper bound.
-template <int FMT, int EPI>
+template <int FMT, int BN, int EPI>
 cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int max_pairs,
                                cudaStream_t stream) {
-  using T = PairTraits<FMT>;
-  auto kern = gemm_pair_kernel<FMT, EPI>;
+  using T = PairTraits<FMT, BN>;
+  auto kern = gemm_pair_kernel<FMT, BN, EPI>;
   static int resident_pairs[64] = {};  // per device; 0 = not queried yet
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -104,6 +104,14 @@ def test_dense_parity_cta_pairs(lib, fmt, m, n, k, l, c_kind):
     run_dense(fmt, m, n, k, l, c_kind, cta_pair=2)
 
 
+@pytest.mark.parametrize("m,n,k,l,c_kind", [
+    (512, 1000, 512, 1, "bf16"),   # 224-wide pair tiles starting inside a 128-row scale atom
+    (300, 448, 384, 2, "f32"),
+])
+def test_dense_parity_cta_pairs_224(lib, m, n, k, l, c_kind):
+    run_dense("mxfp8", m, n, k, l, c_kind, tile_n=224, cta_pair=2)
+
+
 def test_dense_cta_pairs_few_clusters(lib):
     """Two pairs walk many 256 x 256 tiles: stage and accumulator phases wrap around."""
     run_dense("mxfp8", 1024, 1024, 1024, 2, "bf16", cta_pair=2, max_ctas=4, boost=True)

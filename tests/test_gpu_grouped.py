@@ -159,6 +159,11 @@ def test_grouped_cta_pairs(lib, d_dtype, clamp, c_kind, n, nc):
     run_grouped(EDGE, n, 512, d_dtype, clamp, c_kind, nc=nc, cta_pair=2, a_scale=700.0 if clamp else 1.0)
 
 
+@pytest.mark.parametrize("d_dtype,clamp,n", [("e4m3", None, 384), ("e4m3", 32.0, 704), ("bf16", None, 704)])
+def test_grouped_cta_pairs_224(lib, d_dtype, clamp, n):
+    run_grouped(EDGE, n, 512, d_dtype, clamp, "bf16", tile_n=224, cta_pair=2, a_scale=700.0 if clamp else 1.0)
+
+
 def test_grouped_cta_pairs_few_clusters(lib):
     run_grouped([600, 900, 0, 300], 512, 512, "bf16", None, "bf16", cta_pair=2, max_ctas=2)
     run_grouped([600, 900, 0, 300], 512, 512, "e4m3", None, "bf16", cta_pair=2, max_ctas=4)
