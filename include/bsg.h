@@ -141,12 +141,18 @@ bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t 
  *           element or E2M1 packed (k/2 bytes per row).
  * sfa, sfb  device SF buffers for A (rows m) and B (rows n).
  * ab_dtype / sf_dtype / sf_vec_size: (BSG_E4M3, BSG_SF_UE8M0, 32) or (BSG_E2M1, BSG_SF_UE4M3, 16).
- * c         device output (l, m, n), N-major, c_dtype BSG_F32 or BSG_BF16 (RNE from fp32).
+ * c         device output (l, m, n), N-major: c_dtype BSG_F32, BSG_BF16 or BSG_F16 (RNE from
+ *           fp32); with E2M1 operands also BSG_E4M3 or BSG_E2M1 ("GEMM + Amax (SM100)",
+ *           Parameters: FP8 C with FP8 operands is disabled, FP4 C needs FP4 operands), a
+ *           plain RNE_satfinite conversion of the fp32 C without block scales, E2M1 packed two
+ *           per byte with element 2j in the low nibble.
  * amax      device output, one float: the max of |C| taken on the fp32 accumulator
  *           before rounding to c_dtype.  Zeroed by the call on `stream` first.
  * workspace device scratch of bsg_workspace_size() bytes (see bsg_read_device_error).
  * Requirements: m, n, k, l >= 1; k*bytes_per_element % 16 == 0 (k % 16 for E4M3,
- * k % 32 for E2M1); k % sf_vec_size == 0; n*sizeof(c) % 16 == 0.
+ * k % 32 for E2M1); k % sf_vec_size == 0; the bytes of a row of C a multiple of 16
+ * (n % 4, % 8, % 16, % 32 for 4-, 2-, 1-, half-byte elements).  Other C types return
+ * BSG_ERR_UNSUPPORTED.
  */
 bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
                          bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size,
@@ -175,9 +181,9 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
  * alpha           device fp32 (num_experts,).
  * prob            device fp32 (valid_m,).
  * norm_const      device fp32 (1,); required iff d_dtype == BSG_E4M3.
- * c               optional device output (valid_m, n) bf16 or f32 (c_dtype); NULL skips C.
- * d               device output (valid_m, n): d_dtype BSG_BF16 (RNE of the fp32 D) or
- *                 BSG_E4M3 (row-quantised D).
+ * c               optional device output (valid_m, n) f32, bf16 or f16 (c_dtype); NULL skips C.
+ * d               device output (valid_m, n): d_dtype BSG_BF16, BSG_F16 or BSG_F32 (RNE of the
+ *                 fp32 D), or BSG_E4M3 (row-quantised D; E4M3 operands only).
  * d_col           device output (valid_m, n) E4M3 (column-quantised D); required iff
  *                 d_dtype == BSG_E4M3, else must be NULL.
  * sfd_row         device output, SF layout with rows valid_m and K = n (blocks of 32 columns).
@@ -187,9 +193,9 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
  *                 RNE_satfinite_E4M3(D * norm_const / 2^e) ("Grouped GEMM + dSwiGLU (SM100)",
  *                 Step 3, with the scale rounded up to a power of two).
  * amax            device fp32 (num_experts,): max |D| over each expert's rows (0 for an
- *                 empty expert); required iff d_dtype == BSG_BF16.  Zeroed by the call.
+ *                 empty expert); required iff d_dtype is not BSG_E4M3.  Zeroed by the call.
  * Requirements: valid_m % 256 == 0, 1 <= num_experts <= 1024, sf as for bsg_gemm_amax,
- * n % 32 == 0 for E4M3 D, n*sizeof(d) % 16 == 0.
+ * n % 32 == 0 for E4M3 D, the bytes of a row of C and of D a multiple of 16.
  */
 bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
                                   bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size,

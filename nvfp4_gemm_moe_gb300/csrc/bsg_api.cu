@@ -99,6 +99,22 @@ bsg_status operand_format(bsg_dtype ab, bsg_sf_dtype sf, int v, int* fmt) {
 
 bool fits_int32(int64_t v) { return v >= 0 && v < (int64_t(1) << 31); }
 
+int out_kind(bsg_dtype t) {
+  switch (t) {
+    case BSG_F32: return bsg::kOutF32;
+    case BSG_BF16: return bsg::kOutBF16;
+    case BSG_F16: return bsg::kOutF16;
+    case BSG_E4M3: return bsg::kOutE4M3;
+    case BSG_E2M1: return bsg::kOutE2M1;
+    default: return bsg::kOutNone;
+  }
+}
+
+// Bits per element of an output kind.
+int64_t out_bits(int kind) {
+  return kind == bsg::kOutF32 ? 32 : (kind == bsg::kOutBF16 || kind == bsg::kOutF16) ? 16 : kind == bsg::kOutE4M3 ? 8 : 4;
+}
+
 int choose_tile_n(int fmt, int64_t n, int64_t m_tiles_total, int num_sms, bool heavy_epilogue,
                   const bsg_gemm_opts* opts) {
   if (opts && (opts->tile_n == 128 || opts->tile_n == 256)) return opts->tile_n;
@@ -207,10 +223,13 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   if (m < 1 || n < 1 || k < 1 || l < 1) return BSG_ERR_INVALID_ARG;
   if (!fits_int32(m) || !fits_int32(n) || !fits_int32(k) || !fits_int32(l)) return BSG_ERR_INVALID_ARG;
   if (k % sf_vec_size != 0) return BSG_ERR_INVALID_ARG;
-  if (c_dtype != BSG_F32 && c_dtype != BSG_BF16) return BSG_ERR_UNSUPPORTED;
+  // C: f32, bf16 or f16; with FP4 operands also plain E4M3 or packed E2M1 (the pages disable FP8
+  // C with FP8 operands and allow FP4 C only with FP4 operands)
+  const int c_kind = out_kind(c_dtype);
+  if (c_kind == bsg::kOutNone) return BSG_ERR_UNSUPPORTED;
+  if ((c_kind == bsg::kOutE4M3 || c_kind == bsg::kOutE2M1) && fmt != bsg::kNVFP4) return BSG_ERR_UNSUPPORTED;
   const int64_t row_bytes = fmt == bsg::kMXFP8 ? k : k / 2;
-  const int64_t c_size = c_dtype == BSG_F32 ? 4 : 2;
-  if (row_bytes % 16 != 0 || (n * c_size) % 16 != 0) return BSG_ERR_ALIGNMENT;
+  if (row_bytes % 16 != 0 || (n * out_bits(c_kind)) % 128 != 0) return BSG_ERR_ALIGNMENT;
   if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(c) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || (reinterpret_cast<uintptr_t>(amax) & 3u) != 0)
     return BSG_ERR_ALIGNMENT;
@@ -249,7 +268,7 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   p.sfb_mt = static_cast<int>(cdiv(n, 128));
   p.sf_kt = static_cast<int>(sf_kt);
   p.c = c;
-  p.c_kind = c_dtype == BSG_F32 ? bsg::kOutF32 : bsg::kOutBF16;
+  p.c_kind = c_kind;
   p.amax = amax;
   p.err = static_cast<uint32_t*>(workspace);
 
@@ -280,7 +299,8 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   if (!fits_int32(valid_m) || !fits_int32(n) || !fits_int32(k)) return BSG_ERR_INVALID_ARG;
   if (k % sf_vec_size != 0) return BSG_ERR_INVALID_ARG;
   const bool fp8_d = d_dtype == BSG_E4M3;
-  if (d_dtype != BSG_BF16 && !fp8_d) return BSG_ERR_UNSUPPORTED;
+  const int d_kind = fp8_d ? bsg::kOutE4M3 : out_kind(d_dtype);
+  if (!fp8_d && d_kind != bsg::kOutBF16 && d_kind != bsg::kOutF16 && d_kind != bsg::kOutF32) return BSG_ERR_UNSUPPORTED;
   if (fp8_d) {
     if (fmt != bsg::kMXFP8) return BSG_ERR_UNSUPPORTED;
     if (!d_col || !sfd_row || !sfd_col || !norm_const) return BSG_ERR_INVALID_ARG;
@@ -288,12 +308,12 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   } else {
     if (!amax || d_col || sfd_row || sfd_col) return BSG_ERR_INVALID_ARG;
   }
-  if (c && c_dtype != BSG_BF16 && c_dtype != BSG_F32) return BSG_ERR_UNSUPPORTED;
+  const int c_kind = c ? out_kind(c_dtype) : bsg::kOutNone;
+  if (c && c_kind != bsg::kOutBF16 && c_kind != bsg::kOutF16 && c_kind != bsg::kOutF32) return BSG_ERR_UNSUPPORTED;
   if (!(tanh_clamp_scale == tanh_clamp_scale)) return BSG_ERR_INVALID_ARG;  // NaN
   const int64_t row_bytes = fmt == bsg::kMXFP8 ? k : k / 2;
-  const int64_t d_size = fp8_d ? 1 : 2;
-  const int64_t c_size = c_dtype == BSG_F32 ? 4 : 2;
-  if (row_bytes % 16 != 0 || (n * d_size) % 16 != 0 || (c && (n * c_size) % 16 != 0)) return BSG_ERR_ALIGNMENT;
+  if (row_bytes % 16 != 0 || (n * out_bits(d_kind)) % 128 != 0 || (c && (n * out_bits(c_kind)) % 128 != 0))
+    return BSG_ERR_ALIGNMENT;
   if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d) ||
       (c && !aligned16(c)) || (d_col && !aligned16(d_col)) || (sfd_row && !aligned16(sfd_row)) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || (reinterpret_cast<uintptr_t>(padded_offsets) & 3u))
@@ -356,7 +376,8 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   p.sfb_mt = static_cast<int>(cdiv(n, 128));
   p.sf_kt = static_cast<int>(sf_kt);
   p.c = c;
-  p.c_kind = !c ? bsg::kOutNone : (c_dtype == BSG_F32 ? bsg::kOutF32 : bsg::kOutBF16);
+  p.c_kind = c_kind;
+  p.d_kind = d_kind;
   p.amax = amax;
   p.offsets = padded_offsets;
   p.alpha = alpha;

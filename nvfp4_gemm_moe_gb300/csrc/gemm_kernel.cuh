@@ -26,6 +26,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -138,6 +139,51 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Stores the 32 fp32 values v of one row chunk as `kind` at element `off` of `base` (row-major,
+// N columns, chunk starting at column col0), in 16-byte granules; a granule is written when its
+// first column is below N (N is a multiple of the granule width for every kind the host allows).
+__device__ __forceinline__ void store_row32(void* base, uint64_t off, int kind, const float (&v)[32], int col0, int n) {
+  if (kind == kOutF32) {
+    float* dst = reinterpret_cast<float*>(base) + off;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      if (col0 + j < n)
+        store16(dst + j, __float_as_uint(v[j]), __float_as_uint(v[j + 1]), __float_as_uint(v[j + 2]),
+                __float_as_uint(v[j + 3]));
+  } else if (kind == kOutBF16 || kind == kOutF16) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(base) + off;
+    const bool bf = kind == kOutBF16;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8)
+      if (col0 + j < n)
+        store16(dst + j, bf ? pack_bf16x2(v[j], v[j + 1]) : pack_f16x2(v[j], v[j + 1]),
+                bf ? pack_bf16x2(v[j + 2], v[j + 3]) : pack_f16x2(v[j + 2], v[j + 3]),
+                bf ? pack_bf16x2(v[j + 4], v[j + 5]) : pack_f16x2(v[j + 4], v[j + 5]),
+                bf ? pack_bf16x2(v[j + 6], v[j + 7]) : pack_f16x2(v[j + 6], v[j + 7]));
+  } else if (kind == kOutE4M3) {
+    uint8_t* dst = reinterpret_cast<uint8_t*>(base) + off;
+    uint32_t q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      q[j] = cvt_e4m3x2(v[4 * j], v[4 * j + 1]) | (static_cast<uint32_t>(cvt_e4m3x2(v[4 * j + 2], v[4 * j + 3])) << 16);
+    if (col0 < n) store16(dst, q[0], q[1], q[2], q[3]);
+    if (col0 + 16 < n) store16(dst + 16, q[4], q[5], q[6], q[7]);
+  } else if (kind == kOutE2M1) {
+    uint8_t* dst = reinterpret_cast<uint8_t*>(base) + off / 2;
+    uint32_t q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      q[j] = cvt_e2m1x2(v[8 * j], v[8 * j + 1]) | (cvt_e2m1x2(v[8 * j + 2], v[8 * j + 3]) << 8) |
+             (cvt_e2m1x2(v[8 * j + 4], v[8 * j + 5]) << 16) | (cvt_e2m1x2(v[8 * j + 6], v[8 * j + 7]) << 24);
+    if (col0 < n) store16(dst, q[0], q[1], q[2], q[3]);
+  }
+}
+
 __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
   atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
 }
@@ -239,25 +285,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
 #pragma unroll
       for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(__uint_as_float(r[j])));
       if (row_ok) {
-        if (p.c_kind == kOutF32) {
-          float* dst = reinterpret_cast<float*>(p.c) +
-                       (static_cast<uint64_t>(l) * p.m + row) * static_cast<uint64_t>(p.n) + col0;
+        float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            if (col0 + j < p.n) store16(dst + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
-        } else {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.c) +
-                               (static_cast<uint64_t>(l) * p.m + row) * static_cast<uint64_t>(p.n) + col0;
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            if (col0 + j < p.n) {
-              store16(dst + j, pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                      pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
-                      pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
-                      pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
-            }
-          }
-        }
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        store_row32(p.c, (static_cast<uint64_t>(l) * p.m + row) * static_cast<uint64_t>(p.n) + col0, p.c_kind, v,
+                    col0, p.n);
       }
     } else {
       float d[32];
@@ -268,32 +300,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
         r[j] = __float_as_uint(cv);
         d[j] = srelu_clamp(cv, prob_r, s_clamp, inv_s, p.tanh_approx);
       }
-      // a chunk may run past N (N % 8 == 0 for 16-bit outputs, % 4 for fp32): 16-byte granules
-      if (p.c_kind == kOutBF16) {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.c) + rc;
+      // a chunk may run past N: 16-byte granules (N % 8 == 0 for 16-bit outputs, % 4 for fp32)
+      if (p.c_kind != kOutNone) {
+        float cvals[32];
 #pragma unroll
-        for (int j = 0; j < 32; j += 8)
-          if (col0 + j < p.n)
-            store16(dst + j, pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                    pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
-                    pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
-                    pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
-      } else if (p.c_kind == kOutF32) {
-        float* dst = reinterpret_cast<float*>(p.c) + rc;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          if (col0 + j < p.n) store16(dst + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
+        for (int j = 0; j < 32; ++j) cvals[j] = __uint_as_float(r[j]);
+        store_row32(p.c, rc, p.c_kind, cvals, col0, p.n);
       }
       if (EPI == kEpiGroupedBF16) {
         // columns past N hold zeros (zero-filled B rows), so they cannot raise the maximum
 #pragma unroll
         for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(d[j]));
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.d) + rc;
-#pragma unroll
-        for (int j = 0; j < 32; j += 8)
-          if (col0 + j < p.n)
-            store16(dst + j, pack_bf16x2(d[j], d[j + 1]), pack_bf16x2(d[j + 2], d[j + 3]),
-                    pack_bf16x2(d[j + 4], d[j + 5]), pack_bf16x2(d[j + 6], d[j + 7]));
+        store_row32(p.d, rc, p.d_kind, d, col0, p.n);
       } else {
         // D * norm_const once (rounding is monotonic, so the block maxima of the products are
         // norm_const times the block maxima of D, rounded); scaling by 2^-e is exact

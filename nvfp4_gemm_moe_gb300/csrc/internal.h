@@ -8,7 +8,10 @@
 namespace bsg {
 
 enum Fmt : int { kMXFP8 = 0, kNVFP4 = 1 };
-enum OutKind : int { kOutNone = 0, kOutF32 = 1, kOutBF16 = 2, kOutE4M3 = 3 };
+// Element types of the C / D outputs.  E4M3 and E2M1 here are plain conversions (round to
+// nearest even, saturating), without block scales; E2M1 packs two values per byte, element 2j
+// in the low nibble.
+enum OutKind : int { kOutNone = 0, kOutF32 = 1, kOutBF16 = 2, kOutE4M3 = 3, kOutF16 = 4, kOutE2M1 = 5 };
 enum EpiKind : int { kEpiDense = 0, kEpiGroupedBF16 = 1, kEpiGroupedFP8 = 2 };
 
 // Everything a GEMM kernel needs besides the two tensor maps.
@@ -32,6 +35,7 @@ struct GemmParams {
   const int32_t* offsets;
   const float* alpha;
   const float* prob;
+  int d_kind;            // OutKind of D for the bf16 / f16 / f32 grouped epilogue
   float clamp_s;         // <= 0: no tanh clamp
   int tanh_approx;
   const float* norm_const;

@@ -7,7 +7,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (BF16, E4M3, F32, FORMATS, bsg_gemm_amax, bsg_grouped_gemm_srelu, bsg_quantize_mx, bsg_sf_bytes,
+from . import (BF16, E2M1, E4M3, F16, F32, FORMATS, bsg_gemm_amax, bsg_grouped_gemm_srelu, bsg_quantize_mx, bsg_sf_bytes,
                bsg_workspace_size)
 
 
@@ -30,17 +30,33 @@ def quantize(x: torch.Tensor, fmt: str, q=None, sf=None, stream=None):
     return q, sf
 
 
+# C / D element types: torch dtypes, or "e4m3" / "e2m1" for plain FP8 / packed FP4 outputs (uint8 tensors)
+_OUT_KINDS = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16, "e4m3": E4M3, "e2m1": E2M1,
+              "f32": F32, "bf16": BF16, "f16": F16}
+_TORCH_OUT = {F32: torch.float32, BF16: torch.bfloat16, F16: torch.float16}
+
+
+def _out_tensor(kind, rows, n, lead, dev):
+    shape = (lead, rows, n) if lead is not None else (rows, n)
+    if kind in _TORCH_OUT:
+        return torch.empty(shape, dtype=_TORCH_OUT[kind], device=dev)
+    cols = n if kind == E4M3 else n // 2
+    return torch.empty(shape[:-1] + (cols,), dtype=torch.uint8, device=dev)
+
+
 def gemm_amax(a, b, sfa, sfb, fmt: str, m: int, n: int, k: int, l: int, c_dtype=torch.bfloat16, c=None,
               amax=None, workspace=None, stream=None, **opts):
+    """C (l, m, n) of c_dtype (torch.float32 / bfloat16 / float16, or "e4m3" / "e2m1" with NVFP4
+    operands, returned as uint8) and the fp32 amax."""
     ab, sfd, v = FORMATS[fmt]
     dev = a.device
+    ck = _OUT_KINDS[c_dtype] if c is None or c.dtype == torch.uint8 else _OUT_KINDS[c.dtype]
     if c is None:
-        c = torch.empty((l, m, n), dtype=c_dtype, device=dev)
+        c = _out_tensor(ck, m, n, l, dev)
     if amax is None:
         amax = torch.empty(1, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = new_workspace(dev)
-    ck = F32 if c.dtype == torch.float32 else BF16
     bsg_gemm_amax(a, b, sfa, sfb, ab, sfd, v, m, n, k, l, c, ck, amax, workspace, stream=stream, **opts)
     return c, amax
 
@@ -48,7 +64,8 @@ def gemm_amax(a, b, sfa, sfb, fmt: str, m: int, n: int, k: int, l: int, c_dtype=
 def grouped_gemm_srelu(a, b, sfa, sfb, fmt: str, padded_offsets, alpha, prob, n: int, k: int,
                        tanh_clamp_scale=None, d_dtype="bf16", c_dtype=torch.bfloat16, norm_const=None,
                        outputs=None, workspace=None, stream=None, **opts):
-    """Returns a dict of the outputs (c, d, amax or d, d_col, sfd_row, sfd_col)."""
+    """Returns a dict of the outputs (c, d, amax or d, d_col, sfd_row, sfd_col); d_dtype is
+    "bf16", "f16", "f32" or "e4m3", c_dtype a torch float dtype or None."""
     ab, sfd, v = FORMATS[fmt]
     dev = a.device
     valid_m = a.shape[0] if a.dim() == 2 else a.shape[1]
@@ -56,10 +73,10 @@ def grouped_gemm_srelu(a, b, sfa, sfb, fmt: str, padded_offsets, alpha, prob, n:
     out = dict(outputs or {})
     if "c" not in out:
         out["c"] = None if c_dtype is None else torch.empty((valid_m, n), dtype=c_dtype, device=dev)
-    if d_dtype == "bf16":
-        out.setdefault("d", torch.empty((valid_m, n), dtype=torch.bfloat16, device=dev))
+    if d_dtype in ("bf16", "f16", "f32"):
+        dk = _OUT_KINDS[d_dtype]
+        out.setdefault("d", _out_tensor(dk, valid_m, n, None, dev))
         out.setdefault("amax", torch.empty(num_experts, dtype=torch.float32, device=dev))
-        dk = BF16
     else:
         out.setdefault("d", torch.empty((valid_m, n), dtype=torch.uint8, device=dev))
         out.setdefault("d_col", torch.empty((valid_m, n), dtype=torch.uint8, device=dev))
@@ -71,7 +88,7 @@ def grouped_gemm_srelu(a, b, sfa, sfb, fmt: str, padded_offsets, alpha, prob, n:
     if workspace is None:
         workspace = new_workspace(dev)
     c = out["c"]
-    ck = BF16 if c is None or c.dtype == torch.bfloat16 else F32
+    ck = BF16 if c is None else _OUT_KINDS[c.dtype]
     bsg_grouped_gemm_srelu(a, b, sfa, sfb, ab, sfd, v, valid_m, n, k, num_experts, padded_offsets, alpha, prob,
                            tanh_clamp_scale, norm_const, c, ck, out["d"], out.get("d_col"), dk, out.get("sfd_row"),
                            out.get("sfd_col"), out.get("amax"), workspace, stream=stream, **opts)

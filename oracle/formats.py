@@ -136,3 +136,22 @@ def bf16_ulp(x) -> np.ndarray:
     a = np.abs(np.asarray(x, dtype=np.float64))
     _, ex = np.frexp(np.where(a > 0, a, 2.0 ** -126))
     return np.exp2(ex.astype(np.float64) - 8.0)
+
+
+def f16_round(x) -> np.ndarray:
+    """Round float64 values to IEEE half precision (RNE, saturating to +-inf beyond 65504 as
+    the conversion does) and return them as float64; numpy's conversion is the library step."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+def f16_ulp(x) -> np.ndarray:
+    """Spacing of half-precision numbers at |x| (11 significant bits; 2^-24 in the subnormal range)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    _, ex = np.frexp(np.where(a > 0, a, 2.0 ** -14))
+    return np.maximum(np.exp2(ex.astype(np.float64) - 11.0), 2.0 ** -24)
+
+
+def encode_e2m1(x) -> np.ndarray:
+    """E2M1 nibble of RNE_satfinite(x) for float64 x (a plain conversion, scale 1)."""
+    return encode_e2m1_scaled(x, 1.0)
+

@@ -36,6 +36,57 @@ def check_c(c_gpu, ref, abs_sum, kind: str, scale=1.0, what="C"):
                              f"gpu={c_gpu.ravel()[i]} ref={ref.ravel()[i]} tol={np.broadcast_to(tol, ref.shape).ravel()[i]}")
 
 
+def check_c_float(c_gpu, ref, abs_sum, kind: str, scale=1.0, what="C"):
+    """fp32 / bf16 / f16 C: the accumulation bound plus one unit in the last place of the output."""
+    c_gpu = np.asarray(c_gpu, dtype=np.float64)
+    tol = TOL_C * np.abs(scale) * abs_sum
+    if kind == "bf16":
+        tol = tol + formats.bf16_ulp(ref)
+    elif kind == "f16":
+        tol = tol + formats.f16_ulp(ref)
+    err = np.abs(c_gpu - ref)
+    bad = ~(err <= tol)
+    if bad.any():
+        i = np.flatnonzero(bad.ravel())[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first "
+                             f"gpu={c_gpu.ravel()[i]} ref={ref.ravel()[i]} tol={np.broadcast_to(tol, ref.shape).ravel()[i]}")
+
+
+def _e2m1_rank(nib):
+    n = np.asarray(nib).astype(np.int64)
+    return np.where(n & 8, -(n & 7), n & 7)
+
+
+def check_codes_plain(codes_gpu, ref, tol, kind: str, what="C"):
+    """Plain (unscaled) E4M3 / E2M1 conversions of C: codes equal to the oracle's RNE_satfinite
+    of the exact value, except a neighbouring code where the exact value lies within `tol` of
+    the rounding midpoint between the two."""
+    ref = np.asarray(ref, dtype=np.float64)
+    if kind == "e4m3":
+        want = formats.encode_e4m3(ref)
+        got = np.asarray(codes_gpu, dtype=np.uint8)
+        rank_g, rank_w = _rank(got), _rank(want)
+        dec = formats.decode_e4m3
+    else:
+        want = formats.encode_e2m1(ref)
+        g = np.asarray(codes_gpu, dtype=np.uint8)
+        got = np.empty(g.shape[:-1] + (g.shape[-1] * 2,), dtype=np.uint8)
+        got[..., 0::2] = g & 0xF
+        got[..., 1::2] = g >> 4
+        rank_g, rank_w = _e2m1_rank(got), _e2m1_rank(want)
+        dec = formats.decode_e2m1
+    # +0 and -0 are the same value (the sign of a tiny C may differ within the C bound)
+    mism = (want != got) & ~((dec(want) == 0) & (dec(got) == 0))
+    if mism.any():
+        vg, vw = dec(got[mism]), dec(want[mism])
+        adjacent = np.abs(rank_g[mism] - rank_w[mism]) == 1
+        near = np.abs(ref[mism] - (vg + vw) / 2.0) <= np.broadcast_to(tol, ref.shape)[mism] + 1e-12
+        if not np.all(adjacent & near):
+            k = np.flatnonzero(~(adjacent & near))[:5]
+            raise AssertionError(f"{what}: {(~(adjacent & near)).sum()} codes differ away from a rounding "
+                                 f"midpoint; ref={ref[mism][k]} gpu={vg[k]} want={vw[k]}")
+
+
 def check_amax(amax_gpu, ref, what="amax"):
     amax_gpu = np.asarray(amax_gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -59,6 +110,22 @@ def check_d_bf16(d_gpu, d_ref, c_ref, prob, c_tol, what="D"):
         i = np.flatnonzero(bad.ravel())[:5]
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first gpu={d_gpu.ravel()[i]} "
                              f"ref={d_ref.ravel()[i]} tol={tol.ravel()[i]}")
+
+
+def check_d_float(d_gpu, d_ref, c_ref, prob, c_tol, kind: str, what="D"):
+    """bf16 / f16 / f32 D: one unit in the last place of the output type (none for f32) plus
+    the C bound carried through d(r^2) = 2r dr and fp32 epilogue rounding."""
+    if kind == "bf16":
+        return check_d_bf16(d_gpu, d_ref, c_ref, prob, c_tol, what)
+    d_gpu = np.asarray(d_gpu, dtype=np.float64)
+    ulp = formats.f16_ulp(d_ref) if kind == "f16" else 0.0
+    tol = ulp + d_tolerance(c_ref, prob, c_tol) + 2.0 ** -20 * np.abs(d_ref)
+    err = np.abs(d_gpu - d_ref)
+    bad = ~(err <= tol)
+    if bad.any():
+        i = np.flatnonzero(bad.ravel())[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first gpu={d_gpu.ravel()[i]} "
+                             f"ref={d_ref.ravel()[i]} tol={np.broadcast_to(tol, d_ref.shape).ravel()[i]}")
 
 
 def _rank(codes):

@@ -82,7 +82,11 @@ def test_dense_validation():
     assert _dense(m=0) == INVALID
     assert _dense(k=48) == INVALID
     assert _dense(k=16 * 33) == INVALID                # not a multiple of 32
-    assert _dense(ck=bsg.F16) == UNSUPPORTED
+    assert _dense(ck=bsg.E5M2) == UNSUPPORTED
+    assert _dense(ck=bsg.E4M3) == UNSUPPORTED         # FP8 C with FP8 operands is disabled
+    assert _dense(ck=bsg.E2M1) == UNSUPPORTED         # FP4 C needs FP4 operands
+    assert _dense(ck=bsg.F16, n=4) == ALIGN           # 8 bytes per row of C
+    assert _dense(ab=bsg.E2M1, sf=bsg.SF_UE4M3, v=16, ck=bsg.E2M1, n=16) == ALIGN  # 8 bytes per row
     assert _dense(n=4) == ALIGN                         # 4 bf16 = 8 bytes per row of C
     assert _dense(c=P + 8) == ALIGN
     assert _dense(ws=P + 16) == ALIGN                   # workspace is 256-byte aligned
@@ -112,8 +116,11 @@ def test_grouped_validation():
     assert _grouped(dcol=P) == INVALID                   # D_col only with E4M3 D
     assert _grouped(dk=bsg.E4M3) == INVALID              # E4M3 D needs d_col, SFD and norm_const
     assert _grouped(dk=bsg.E4M3, dcol=P, sfr=P, sfc=P, nc=P, amax=None, n=48) == INVALID  # n % 32
-    assert _grouped(dk=bsg.F32) == UNSUPPORTED
-    assert _grouped(ck=bsg.F16) == UNSUPPORTED
+    assert _grouped(dk=bsg.E5M2) == UNSUPPORTED
+    assert _grouped(ck=bsg.E4M3) == UNSUPPORTED
+    assert _grouped(dk=bsg.F32, n=2) == ALIGN             # 8 bytes per row of D
+    assert _grouped(dk=bsg.E4M3, dcol=P, sfr=P, sfc=P, nc=P, amax=None, ab=bsg.E2M1, sf=bsg.SF_UE4M3,
+                    v=16) == UNSUPPORTED                  # E4M3 D only with E4M3 operands
     assert _grouped(s=float("nan")) == INVALID
     assert _grouped(ws=None) == WORKSPACE
     assert _grouped(offs=P + 2) == ALIGN

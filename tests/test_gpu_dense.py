@@ -10,7 +10,7 @@ import torch
 
 import workloads as W
 from oracle import gemm as og, quantize as oq
-from parity import check_amax, check_c
+from parity import TOL_C, check_amax, check_c, check_c_float, check_codes_plain
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def run_dense(fmt, m, n, k, l, c_kind, tile_n=0, seed=1, boost=False, spread=Fal
     a, b = _operands(seed, fmt, m, n, k, l, boost, spread)
     qa, sfa = torch_ops.quantize(torch.from_numpy(a).cuda(), fmt)
     qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), fmt)
-    c_dtype = torch.float32 if c_kind == "f32" else torch.bfloat16
+    c_dtype = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "e4m3": "e4m3", "e2m1": "e2m1"}[c_kind]
     ws = torch_ops.new_workspace()
     c, amax = torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, m, n, k, l, c_dtype=c_dtype, workspace=ws,
                                   tile_n=tile_n, max_ctas=max_ctas, cta_pair=cta_pair)
@@ -48,7 +48,10 @@ def run_dense(fmt, m, n, k, l, c_kind, tile_n=0, seed=1, boost=False, spread=Fal
     assert np.array_equal(sfa.cpu().numpy(), sfa_ref) and np.array_equal(sfb.cpu().numpy(), sfb_ref)
     ref, amax_ref = og.dense_gemm_amax(qa_ref, qb_ref, sfa_ref, sfb_ref, fmt, m, n, k, l)
     s = og.dense_abs_sum(qa_ref, qb_ref, sfa_ref, sfb_ref, fmt, m, n, k, l)
-    check_c(c.float().cpu().numpy(), ref, s, c_kind)
+    if c_kind in ("e4m3", "e2m1"):
+        check_codes_plain(c.cpu().numpy(), ref, TOL_C * s, c_kind)
+    else:
+        check_c_float(c.float().cpu().numpy(), ref, s, c_kind)
     check_amax(amax.cpu().numpy()[0], amax_ref)
     return c, amax
 
@@ -110,6 +113,30 @@ def test_dense_parity_cta_pairs(lib, fmt, m, n, k, l, c_kind):
 ])
 def test_dense_parity_cta_pairs_224(lib, m, n, k, l, c_kind):
     run_dense("mxfp8", m, n, k, l, c_kind, tile_n=224, cta_pair=2)
+
+
+@pytest.mark.parametrize("fmt,m,n,k,l,c_kind,cta_pair", [
+    ("mxfp8", 300, 264, 384, 2, "f16", 1),
+    ("mxfp8", 512, 512, 512, 1, "f16", 2),
+    ("nvfp4", 300, 264, 320, 2, "f16", 1),
+    ("nvfp4", 256, 256, 512, 1, "e4m3", 1),   # plain FP8 C with FP4 operands
+    ("nvfp4", 512, 512, 512, 1, "e4m3", 2),
+    ("nvfp4", 256, 320, 512, 1, "e2m1", 1),   # packed FP4 C
+    ("nvfp4", 512, 512, 1024, 2, "e2m1", 2),
+])
+def test_dense_c_types(lib, fmt, m, n, k, l, c_kind, cta_pair):
+    run_dense(fmt, m, n, k, l, c_kind, cta_pair=cta_pair)
+
+
+def test_dense_c_type_rejections(lib):
+    import nvfp4_gemm_moe_gb300 as bsg
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    q = torch.zeros((1, 256, 256), dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(bsg.bsg_sf_bytes(1, 256, 256, 32), dtype=torch.uint8, device="cuda")
+    for ck in ("e4m3", "e2m1"):  # FP8 C with FP8 operands is disabled; FP4 C needs FP4 operands
+        with pytest.raises(bsg.BsgError) as ei:
+            torch_ops.gemm_amax(q, q, sf, sf, "mxfp8", 256, 256, 256, 1, c_dtype=ck)
+        assert ei.value.status == 2  # BSG_ERR_UNSUPPORTED
 
 
 def test_dense_cta_pairs_few_clusters(lib):

@@ -5,7 +5,7 @@ import torch
 
 import workloads as W
 from oracle import formats, gemm as og, quantize as oq, sf_layout
-from parity import check_amax, check_c, check_d_bf16, check_e4m3_blocks, d_tolerance, TOL_C
+from parity import check_amax, check_c, check_c_float, check_d_bf16, check_d_float, check_e4m3_blocks, d_tolerance, TOL_C
 
 pytestmark = pytest.mark.gpu
 
@@ -20,31 +20,31 @@ def _case(counts, n, k, seed=3, a_scale=1.0):
 
 
 def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0, tile_n=0, seed=3, a_scale=1.0,
-                tanh_approx=False, max_ctas=0, cta_pair=0):
+                tanh_approx=False, max_ctas=0, cta_pair=0, fmt="mxfp8"):
     from nvfp4_gemm_moe_gb300 import torch_ops
     import nvfp4_gemm_moe_gb300 as bsg
     wl, offs, a, b, alpha, prob = _case(counts, n, k, seed, a_scale)
     vm = int(offs[-1])
-    qa, sfa = torch_ops.quantize(torch.from_numpy(a).cuda(), "mxfp8")
-    qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), "mxfp8")
+    qa, sfa = torch_ops.quantize(torch.from_numpy(a).cuda(), fmt)
+    qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), fmt)
     ws = torch_ops.new_workspace()
-    c_dtype = {"bf16": torch.bfloat16, "f32": torch.float32, None: None}[c_kind]
+    c_dtype = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16, None: None}[c_kind]
     out = torch_ops.grouped_gemm_srelu(
-        qa[0], qb, sfa, sfb, "mxfp8", torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
+        qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
         torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=clamp, d_dtype=d_dtype, c_dtype=c_dtype,
         norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
         tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair)
     torch.cuda.synchronize()
     assert bsg.bsg_read_device_error(ws) == 0
-    qa_ref, sfa_ref = oq.quantize(a, "mxfp8")
-    qb_ref, sfb_ref = oq.quantize(b, "mxfp8")
+    qa_ref, sfa_ref = oq.quantize(a, fmt)
+    qb_ref, sfb_ref = oq.quantize(b, fmt)
     assert np.array_equal(qa.cpu().numpy(), qa_ref) and np.array_equal(qb.cpu().numpy(), qb_ref)
     assert np.array_equal(sfa.cpu().numpy(), sfa_ref) and np.array_equal(sfb.cpu().numpy(), sfb_ref)
-    ref = og.grouped_srelu(qa_ref[0], qb_ref, sfa_ref, sfb_ref, "mxfp8", offs, alpha, prob, k, n,
+    ref = og.grouped_srelu(qa_ref[0], qb_ref, sfa_ref, sfb_ref, fmt, offs, alpha, prob, k, n,
                            tanh_clamp_scale=clamp, d_fp8=(d_dtype == "e4m3"), norm_const=nc)
     # sum_k |Ahat||Bhat| per element for the tolerance, with each row's expert
-    ahat = np.abs(oq.dequantize(qa_ref, sfa_ref, "mxfp8", vm, k, 1)[0])
-    bhat = np.abs(oq.dequantize(qb_ref, sfb_ref, "mxfp8", n, k, len(counts)))
+    ahat = np.abs(oq.dequantize(qa_ref, sfa_ref, fmt, vm, k, 1)[0])
+    bhat = np.abs(oq.dequantize(qb_ref, sfb_ref, fmt, n, k, len(counts)))
     g_of = og.expert_of_rows(offs, vm)
     s = np.zeros((vm, n))
     for g in range(len(counts)):
@@ -53,18 +53,18 @@ def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0,
             s[rows] = float(alpha[g]) * (ahat[rows] @ bhat[g].T)
     c_tol = TOL_C * s
     if c_kind is not None:
-        check_c(out["c"].float().cpu().numpy(), ref["c"], s, c_kind)
+        check_c_float(out["c"].float().cpu().numpy(), ref["c"], s, c_kind)
     d_tol = d_tolerance(ref["c"], prob, c_tol) + 2.0 ** -20 * ref["d"]
     if tanh_approx and clamp is not None:
         # the approximate tanh (max abs error 7.7e-6 on the pages' sweep) through d(c^2) = 2c dc
         d_tol = d_tol + np.asarray(prob, np.float64)[:, None] * 2 * clamp * clamp * 7.7e-6
-    if d_dtype == "bf16":
+    if d_dtype in ("bf16", "f16", "f32"):
         d_gpu = out["d"].float().cpu().numpy()
         if tanh_approx and clamp is not None:
             err = np.abs(d_gpu - ref["d"])
             assert np.all(err <= formats.bf16_ulp(ref["d"]) + d_tol)
         else:
-            check_d_bf16(d_gpu, ref["d"], ref["c"], prob, c_tol)
+            check_d_float(d_gpu, ref["d"], ref["c"], prob, c_tol, d_dtype)
         amax = out["amax"].cpu().numpy()
         assert np.all(amax[ref["amax"] == 0] == 0)
         nz = ref["amax"] > 0
@@ -101,6 +101,31 @@ EDGE = [0, 300, 0, 0, 1, 256, 0]  # empty experts first, in a run and last; one 
 ])
 def test_grouped_bf16_d(lib, counts, n, k, tile_n):
     run_grouped(counts, n, k, "bf16", None, "bf16", tile_n=tile_n)
+
+
+@pytest.mark.parametrize("counts,n,k,tile_n,cta_pair", [
+    (EDGE, 256, 256, 0, 0),
+    (EDGE, 264, 512, 256, 1),     # ragged N tile
+    ([200, 200, 200, 200], 512, 384, 128, 1),
+    ([1, 2, 3, 700, 4], 512, 1024, 0, 2),
+])
+def test_grouped_nvfp4_bf16_d(lib, counts, n, k, tile_n, cta_pair):
+    run_grouped(counts, n, k, "bf16", None, "bf16", tile_n=tile_n, cta_pair=cta_pair, fmt="nvfp4")
+
+
+def test_grouped_nvfp4_tanh_clamp(lib):
+    run_grouped([300, 500, 0, 220], 256, 512, "bf16", 32.0, "f32", a_scale=700.0, fmt="nvfp4")
+
+
+@pytest.mark.parametrize("fmt,d_dtype,c_kind,clamp,cta_pair", [
+    ("mxfp8", "f16", "f16", None, 1),
+    ("mxfp8", "f32", "f32", 32.0, 2),
+    ("nvfp4", "f16", None, None, 2),
+    ("nvfp4", "f32", "f16", 32.0, 1),
+])
+def test_grouped_d_types(lib, fmt, d_dtype, c_kind, clamp, cta_pair):
+    run_grouped([300, 500, 0, 220], 256, 512, d_dtype, clamp, c_kind, cta_pair=cta_pair, fmt=fmt,
+                a_scale=700.0 if clamp else 1.0)
 
 
 def test_grouped_bf16_c_f32_and_no_c(lib):

@@ -119,6 +119,24 @@ def test_bf16_round_matches_torch():
     assert np.array_equal(formats.bf16_round(x), ref)
 
 
+def test_f16_round_and_ulp():
+    # values fixed by the binary16 format: 11 significant bits, ties to even, max 65504
+    x = np.array([1.0, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 2049.0, 2051.0, 65504.0, 2.0 ** -24, 2.0 ** -26])
+    want = np.array([1.0, 1.0, 1.0 + 2.0 ** -9, 2048.0, 2052.0, 65504.0, 2.0 ** -24, 0.0])
+    assert np.array_equal(formats.f16_round(x), want)
+    assert np.array_equal(formats.f16_ulp(np.array([1.0, 1.5, 2.0, 2.0 ** -20])),
+                          np.array([2.0 ** -10, 2.0 ** -10, 2.0 ** -9, 2.0 ** -24]))
+
+
+def test_e2m1_plain_conversion():
+    # the E2M1 grid and its midpoints: ties go to the even code, beyond 6 saturates
+    x = np.array([0.2, 0.25, 0.3, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 5.1, 100.0, -0.75, -0.1])
+    mag = np.array([0, 0, 1, 2, 2, 4, 4, 6, 6, 7, 7, 2, 0])
+    got = formats.encode_e2m1(x)
+    assert np.array_equal(got & 7, mag)
+    assert np.array_equal(got >> 3, (x < 0).astype(np.uint8))
+
+
 def test_golden_worked_block_mxfp8():
     from oracle import quantize
     g = json.load(open(os.path.join(GOLDEN, "mxfp8_block_worked.json")))
