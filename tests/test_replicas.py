@@ -30,7 +30,7 @@ def _rank_main(rank, world, port, out):
 
 def test_max_over_ranks_two_gloo_ranks():
     world, port = 2, _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
     want = [11.0, 3.0, 3.0]
