@@ -12,7 +12,8 @@
  *                           optional tanh soft clamp, per-expert amax or FP8 D with
  *                           row/column MXFP8 scale factors
  *                           ("Grouped GEMM + sReLU (SM100)", Overview, Equations,
- *                           Tanh soft clamp).
+ *                           Tanh soft clamp); bsg_grouped_gemm_srelu_discrete takes
+ *                           the experts' weights as separate allocations.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -207,6 +208,36 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
                                   uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
                                   const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
                                   void* stream);
+
+/*
+ * bsg_grouped_gemm_srelu_discrete -- bsg_grouped_gemm_srelu with per-expert weight allocations
+ * ("Grouped GEMM + sReLU (SM100)", Shapes: B and SFB given as per-expert tensors addressed by
+ * pointer arrays; API usage, discrete input B and SFB pointers).
+ *
+ * Arguments and results are those of bsg_grouped_gemm_srelu except:
+ * b_ptrs     device int64 (num_experts,): b_ptrs[g] is the device address of expert g's codes,
+ *            (n, k) K-major, C-contiguous, 16-byte aligned.
+ * sfb_ptrs   device int64 (num_experts,): sfb_ptrs[g] is the device address of expert g's SF
+ *            buffer for a (1, n, k) operand (bsg_sf_bytes(1, n, k, v) bytes), 16-byte aligned.
+ * workspace  at least bsg_grouped_discrete_workspace_size(num_experts) bytes, 64-byte aligned:
+ *            besides the error word it holds one TMA descriptor per expert.
+ * The call copies b_ptrs and sfb_ptrs to the host and synchronises `stream` once before it
+ * enqueues the kernel (it builds the experts' tensor maps on the host), so it cannot be
+ * captured into a CUDA graph.  A null or misaligned pointer entry returns
+ * BSG_ERR_INVALID_ARG / BSG_ERR_ALIGNMENT before anything is launched.  The weight buffers
+ * must stay allocated until the kernel has completed.
+ */
+size_t bsg_grouped_discrete_workspace_size(int64_t num_experts);
+bsg_status bsg_grouped_gemm_srelu_discrete(const void* a, const int64_t* b_ptrs, const uint8_t* sfa,
+                                           const int64_t* sfb_ptrs, bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype,
+                                           int sf_vec_size, int64_t valid_m, int64_t n, int64_t k,
+                                           int64_t num_experts, const int32_t* padded_offsets,
+                                           const float* alpha, const float* prob, float tanh_clamp_scale,
+                                           const float* norm_const, void* c, bsg_dtype c_dtype,
+                                           void* d, void* d_col, bsg_dtype d_dtype,
+                                           uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
+                                           const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
+                                           void* stream);
 
 /*
  * bsg_gemm_amax_noalloc -- bsg_gemm_amax for callers that cannot provide device memory.

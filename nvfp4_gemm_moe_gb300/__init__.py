@@ -60,6 +60,10 @@ def _load():
     lib.bsg_grouped_gemm_srelu.restype = I
     lib.bsg_grouped_gemm_srelu.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, P, P, F, P, P, I, P, P, I,
                                            P, P, P, ctypes.POINTER(bsg_gemm_opts), P, SZ, P]
+    lib.bsg_grouped_discrete_workspace_size.restype = SZ
+    lib.bsg_grouped_discrete_workspace_size.argtypes = [I64]
+    lib.bsg_grouped_gemm_srelu_discrete.restype = I
+    lib.bsg_grouped_gemm_srelu_discrete.argtypes = lib.bsg_grouped_gemm_srelu.argtypes
     lib.bsg_gemm_amax_noalloc.restype = I
     lib.bsg_gemm_amax_noalloc.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, I, P,
                                           ctypes.POINTER(bsg_gemm_opts), P]
@@ -148,6 +152,25 @@ def bsg_grouped_gemm_srelu(a, b, sfa, sfb, ab_dtype, sf_dtype, sf_vec_size, vali
                                        _ptr(norm_const), _ptr(c), c_dtype, _ptr(d), _ptr(d_col), d_dtype,
                                        _ptr(sfd_row), _ptr(sfd_col), _ptr(amax), ctypes.byref(o), _ptr(workspace),
                                        ws_bytes, _stream(stream)), "bsg_grouped_gemm_srelu")
+
+
+def bsg_grouped_discrete_workspace_size(num_experts: int) -> int:
+    return int(_lib.bsg_grouped_discrete_workspace_size(num_experts))
+
+
+def bsg_grouped_gemm_srelu_discrete(a, b_ptrs, sfa, sfb_ptrs, ab_dtype, sf_dtype, sf_vec_size, valid_m, n, k,
+                                    num_experts, padded_offsets, alpha, prob, tanh_clamp_scale, norm_const, c, c_dtype,
+                                    d, d_col, d_dtype, sfd_row, sfd_col, amax, workspace, workspace_bytes=None,
+                                    stream=None, **opts):
+    """b_ptrs / sfb_ptrs: device int64 arrays of the experts' B and SFB addresses."""
+    ws_bytes = bsg_grouped_discrete_workspace_size(num_experts) if workspace_bytes is None else workspace_bytes
+    o = _opts(**opts)
+    s = 0.0 if tanh_clamp_scale is None else float(tanh_clamp_scale)
+    _check(_lib.bsg_grouped_gemm_srelu_discrete(
+        _ptr(a), _ptr(b_ptrs), _ptr(sfa), _ptr(sfb_ptrs), ab_dtype, sf_dtype, sf_vec_size, valid_m, n, k,
+        num_experts, _ptr(padded_offsets), _ptr(alpha), _ptr(prob), s, _ptr(norm_const), _ptr(c), c_dtype, _ptr(d),
+        _ptr(d_col), d_dtype, _ptr(sfd_row), _ptr(sfd_col), _ptr(amax), ctypes.byref(o), _ptr(workspace), ws_bytes,
+        _stream(stream)), "bsg_grouped_gemm_srelu_discrete")
 
 
 def bsg_read_device_error(workspace, stream=None) -> int:

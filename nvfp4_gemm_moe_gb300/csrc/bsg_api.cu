@@ -281,19 +281,27 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }
 
-bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
-                                  bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size, int64_t valid_m,
-                                  int64_t n, int64_t k, int64_t num_experts, const int32_t* padded_offsets,
-                                  const float* alpha, const float* prob, float tanh_clamp_scale,
-                                  const float* norm_const, void* c, bsg_dtype c_dtype, void* d, void* d_col,
-                                  bsg_dtype d_dtype, uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
-                                  const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
-                                  void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The grouped GEMM for contiguous B / SFB (b, sfb) or per-expert pointer arrays (b_ptrs, sfb_ptrs,
+// device int64 (num_experts,)); exactly one of the two forms is given.
+bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, const uint8_t* sfa, const uint8_t* sfb,
+                        const int64_t* sfb_ptrs, bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size,
+                        int64_t valid_m, int64_t n, int64_t k, int64_t num_experts, const int32_t* padded_offsets,
+                        const float* alpha, const float* prob, float tanh_clamp_scale, const float* norm_const,
+                        void* c, bsg_dtype c_dtype, void* d, void* d_col, bsg_dtype d_dtype, uint8_t* sfd_row,
+                        uint8_t* sfd_col, float* amax, const bsg_gemm_opts* opts, void* workspace,
+                        size_t workspace_bytes, void* stream) {
   int fmt = 0;
   bsg_status st = operand_format(ab_dtype, sf_dtype, sf_vec_size, &fmt);
   if (st != BSG_OK) return st;
-  if (!a || !b || !sfa || !sfb || !padded_offsets || !alpha || !prob || !d) return BSG_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
+  const bool discrete = b_ptrs != nullptr;
+  if (!a || !sfa || !padded_offsets || !alpha || !prob || !d) return BSG_ERR_INVALID_ARG;
+  if (discrete ? (b || sfb || !sfb_ptrs) : (!b || !sfb || sfb_ptrs)) return BSG_ERR_INVALID_ARG;
+  const size_t ws_need = discrete ? bsg_grouped_discrete_workspace_size(num_experts) : kWorkspaceBytes;
+  if (!workspace || workspace_bytes < ws_need) return BSG_ERR_WORKSPACE;
   if (valid_m < 0 || valid_m % 256 != 0 || n < 1 || k < 1 || num_experts < 1 || num_experts > 1024)
     return BSG_ERR_INVALID_ARG;
   if (!fits_int32(valid_m) || !fits_int32(n) || !fits_int32(k)) return BSG_ERR_INVALID_ARG;
@@ -314,7 +322,8 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   const int64_t row_bytes = fmt == bsg::kMXFP8 ? k : k / 2;
   if (row_bytes % 16 != 0 || (n * out_bits(d_kind)) % 128 != 0 || (c && (n * out_bits(c_kind)) % 128 != 0))
     return BSG_ERR_ALIGNMENT;
-  if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d) ||
+  if (!aligned16(a) || (b && !aligned16(b)) || !aligned16(sfa) || (sfb && !aligned16(sfb)) || !aligned16(d) ||
+      (reinterpret_cast<uintptr_t>(b_ptrs) & 7u) || (reinterpret_cast<uintptr_t>(sfb_ptrs) & 7u) ||
       (c && !aligned16(c)) || (d_col && !aligned16(d_col)) || (sfd_row && !aligned16(sfd_row)) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || (reinterpret_cast<uintptr_t>(padded_offsets) & 3u))
     return BSG_ERR_ALIGNMENT;
@@ -337,6 +346,21 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
     if (prev != valid_m) return BSG_ERR_BAD_OFFSETS;
   }
 
+  // per-expert weights: the experts' addresses, copied to the host and checked before anything is enqueued
+  std::vector<int64_t> hb, hs;
+  if (discrete) {
+    hb.resize(static_cast<size_t>(num_experts));
+    hs.resize(static_cast<size_t>(num_experts));
+    if (cudaMemcpyAsync(hb.data(), b_ptrs, hb.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(hs.data(), sfb_ptrs, hs.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return BSG_ERR_CUDA;
+    for (size_t g = 0; g < hb.size(); ++g) {
+      if (!hb[g] || !hs[g]) return BSG_ERR_INVALID_ARG;
+      if ((hb[g] & 15) || (hs[g] & 15)) return BSG_ERR_ALIGNMENT;
+    }
+  }
+
   if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (!fp8_d && cudaMemsetAsync(amax, 0, sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (fp8_d && n % 128 != 0) {
@@ -355,9 +379,25 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
 
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128) ||
-      !make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn))
-    return BSG_ERR_CUDA;
+  if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128)) return BSG_ERR_CUDA;
+  const CUtensorMap* b_maps = nullptr;
+  if (!discrete) {
+    if (!make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn)) return BSG_ERR_CUDA;
+  } else {
+    // One tensor map per expert, encoded here and stored in the workspace after the error word;
+    // the kernel reads them from global memory (after a tensormap-proxy acquire fence).
+    std::vector<CUtensorMap> maps(static_cast<size_t>(num_experts));
+    for (size_t g = 0; g < maps.size(); ++g) {
+      if (!make_operand_map(&maps[g], reinterpret_cast<const void*>(hb[g]), row_bytes, n, 1, pairs ? bn / 2 : bn))
+        return BSG_ERR_CUDA;
+    }
+    uint8_t* dst = static_cast<uint8_t*>(workspace) + kWorkspaceBytes;
+    if (cudaMemcpyAsync(dst, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return BSG_ERR_CUDA;
+    b_maps = reinterpret_cast<const CUtensorMap*>(dst);
+    tb = maps[0];  // unused by the kernel in this form
+  }
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
 
   GemmParams p;
@@ -372,6 +412,8 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
   p.num_tiles = static_cast<int>(tiles);
   p.sfa = sfa;
   p.sfb = sfb;
+  p.b_maps = b_maps;
+  p.sfb_ptrs = sfb_ptrs;
   p.sfa_mt = static_cast<int>(valid_m / 128);
   p.sfb_mt = static_cast<int>(cdiv(n, 128));
   p.sf_kt = static_cast<int>(sf_kt);
@@ -399,6 +441,44 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
                         : bsg::launch_gemm_grouped(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
   if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
+                                  bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size, int64_t valid_m,
+                                  int64_t n, int64_t k, int64_t num_experts, const int32_t* padded_offsets,
+                                  const float* alpha, const float* prob, float tanh_clamp_scale,
+                                  const float* norm_const, void* c, bsg_dtype c_dtype, void* d, void* d_col,
+                                  bsg_dtype d_dtype, uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
+                                  const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (!b || !sfb) return BSG_ERR_INVALID_ARG;
+  return grouped_impl(a, b, nullptr, sfa, sfb, nullptr, ab_dtype, sf_dtype, sf_vec_size, valid_m, n, k, num_experts,
+                      padded_offsets, alpha, prob, tanh_clamp_scale, norm_const, c, c_dtype, d, d_col, d_dtype,
+                      sfd_row, sfd_col, amax, opts, workspace, workspace_bytes, stream);
+}
+
+size_t bsg_grouped_discrete_workspace_size(int64_t num_experts) {
+  if (num_experts < 1) return kWorkspaceBytes;
+  return kWorkspaceBytes + static_cast<size_t>(num_experts) * sizeof(CUtensorMap);
+}
+
+bsg_status bsg_grouped_gemm_srelu_discrete(const void* a, const int64_t* b_ptrs, const uint8_t* sfa,
+                                           const int64_t* sfb_ptrs, bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype,
+                                           int sf_vec_size, int64_t valid_m, int64_t n, int64_t k,
+                                           int64_t num_experts, const int32_t* padded_offsets, const float* alpha,
+                                           const float* prob, float tanh_clamp_scale, const float* norm_const,
+                                           void* c, bsg_dtype c_dtype, void* d, void* d_col, bsg_dtype d_dtype,
+                                           uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
+                                           const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+  if (!b_ptrs || !sfb_ptrs) return BSG_ERR_INVALID_ARG;
+  return grouped_impl(a, nullptr, b_ptrs, sfa, nullptr, sfb_ptrs, ab_dtype, sf_dtype, sf_vec_size, valid_m, n, k,
+                      num_experts, padded_offsets, alpha, prob, tanh_clamp_scale, norm_const, c, c_dtype, d, d_col,
+                      d_dtype, sfd_row, sfd_col, amax, opts, workspace, workspace_bytes, stream);
 }
 
 bsg_status bsg_read_device_error(const void* workspace, void* stream, uint32_t* error_bits) {

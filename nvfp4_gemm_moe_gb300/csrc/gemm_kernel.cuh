@@ -516,9 +516,17 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       uint32_t stage = 0, phase = 0;
       uint64_t issued = 0;
       bool ok = true;
+      int fenced_l = -1;  // expert whose global tensor map this thread has acquired
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
         const int a_batch = EPI == kEpiDense ? tc.l : 0;
+        // per-expert weights: the expert's own tensor map and scale array, else batch tc.l of one
+        const CUtensorMap* bmap = p.b_maps ? p.b_maps + tc.l : &tmap_b;
+        if (p.b_maps && tc.l != fenced_l) { tmap_acquire(bmap); fenced_l = tc.l; }
+        const int b_batch = p.b_maps ? 0 : tc.l;
+        const uint8_t* sfb_base =
+            p.sfb_ptrs ? reinterpret_cast<const uint8_t*>(p.sfb_ptrs[tc.l])
+                       : p.sfb + static_cast<uint64_t>(tc.l) * p.sfb_mt * p.sf_kt * 512;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           const int k_left = p.k - kt * T::kElemsPerKTile;
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           const uint32_t sf_bytes = static_cast<uint32_t>(atoms * 512 * (1 + T::kBRowGroups));
           mbar_arrive_expect_tx(&full[stage], T::kABytes + T::kBBytes + sf_bytes);
           tma_load_3d(s_a + stage * T::kABytes, &tmap_a, &full[stage], kt * kTileKBytes, tc.mt * kTileM, a_batch);
-          tma_load_3d(s_b + stage * T::kBBytes, &tmap_b, &full[stage], kt * kTileKBytes, tc.nt * BN, tc.l);
+          tma_load_3d(s_b + stage * T::kBBytes, bmap, &full[stage], kt * kTileKBytes, tc.nt * BN, b_batch);
           const uint8_t* sfa_src =
               p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + tc.mt) * p.sf_kt +
                        static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
@@ -537,8 +545,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
             const int rb = min((tc.nt * BN) / 128 + i, p.sfb_mt - 1);
             const uint8_t* sfb_src =
-                p.sfb + ((static_cast<uint64_t>(tc.l) * p.sfb_mt + rb) * p.sf_kt +
-                         static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+                sfb_base + (static_cast<uint64_t>(rb) * p.sf_kt + static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
             bulk_load(s_sfb + stage * T::kSfbBytes + i * T::kAtomsPerStage * 512, sfb_src, atoms * 512,
                       &full[stage]);
           }

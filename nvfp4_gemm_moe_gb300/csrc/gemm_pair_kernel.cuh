@@ -178,6 +178,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       uint32_t stage = 0, phase = 0;
       uint64_t issued = 0;
       bool ok = true;
+      int fenced_l = -1;  // expert whose global tensor map this thread has acquired
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
         const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
@@ -185,6 +186,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         const int a_row = tc.mt * 256 + static_cast<int>(rank) * 128;
         const int b_row = tc.nt * BN + static_cast<int>(rank) * T::kBHalf;
         const int sfa_group = min(tc.mt * 2 + static_cast<int>(rank), p.sfa_mt - 1);
+        // per-expert weights: the expert's own tensor map and scale array, else batch tc.l of one
+        const CUtensorMap* bmap = p.b_maps ? p.b_maps + tc.l : &tmap_b;
+        if (p.b_maps && tc.l != fenced_l) { tmap_acquire(bmap); fenced_l = tc.l; }
+        const int b_batch = p.b_maps ? 0 : tc.l;
+        const uint8_t* sfb_base =
+            p.sfb_ptrs ? reinterpret_cast<const uint8_t*>(p.sfb_ptrs[tc.l])
+                       : p.sfb + static_cast<uint64_t>(tc.l) * p.sfb_mt * p.sf_kt * 512;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           const int k_left = p.k - kt * T::kElemsPerKTile;
@@ -199,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           else mbar_arrive_expect_tx(&sf_full[stage], sf_bytes);
           const uint32_t fbar = full0 + stage * 8;
           tma_load_3d_pair(s_a + stage * T::kABytes, &tmap_a, fbar, kt * kTileKBytes, a_row, a_batch);
-          tma_load_3d_pair(s_b + stage * T::kBBytes, &tmap_b, fbar, kt * kTileKBytes, b_row, tc.l);
+          tma_load_3d_pair(s_b + stage * T::kBBytes, bmap, fbar, kt * kTileKBytes, b_row, b_batch);
           const uint8_t* sfa_src =
               p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + sfa_group) * p.sf_kt +
                        static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
@@ -209,8 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
             // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
             const int rb = min((tc.nt * BN) / 128 + g, p.sfb_mt - 1);
             const uint8_t* sfb_src =
-                p.sfb + ((static_cast<uint64_t>(tc.l) * p.sfb_mt + rb) * p.sf_kt +
-                         static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+                sfb_base + (static_cast<uint64_t>(rb) * p.sf_kt + static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
             bulk_load(s_sfb + stage * T::kSfbBytes + g * T::kAtomsPerStage * 512, sfb_src, atoms * 512, sf_bar);
           }
           ++issued;

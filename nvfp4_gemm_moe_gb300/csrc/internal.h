@@ -25,6 +25,8 @@ struct GemmParams {
   // scale factors
   const uint8_t* sfa;
   const uint8_t* sfb;
+  const CUtensorMap* b_maps;   // grouped with per-expert weights: one B tensor map per expert (global)
+  const int64_t* sfb_ptrs;     // grouped with per-expert weights: one SFB pointer per expert
   int sfa_mt, sfb_mt;    // ceil(m/128), ceil(n/128)
   int sf_kt;             // ceil(K / (4 v)) atoms along K
   // dense epilogue

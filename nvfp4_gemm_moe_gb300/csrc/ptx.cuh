@@ -54,6 +54,13 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
 
+// Makes a tensor map that sits in global memory (written before the launch) visible to the
+// tensor-map proxy of the calling thread before its first TMA use.
+__device__ __forceinline__ void tmap_acquire(const CUtensorMap* tm) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.sys [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(tm))
+               : "memory");
+}
+
 // 3-D tiled load global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, uint64_t* bar, int c0, int c1,
                                             int c2) {

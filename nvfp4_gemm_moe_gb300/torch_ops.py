@@ -7,7 +7,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (BF16, E2M1, E4M3, F16, F32, FORMATS, bsg_gemm_amax, bsg_grouped_gemm_srelu, bsg_quantize_mx, bsg_sf_bytes,
+from . import (BF16, E2M1, E4M3, F16, F32, FORMATS, bsg_gemm_amax, bsg_grouped_discrete_workspace_size,
+               bsg_grouped_gemm_srelu, bsg_grouped_gemm_srelu_discrete, bsg_quantize_mx, bsg_sf_bytes,
                bsg_workspace_size)
 
 
@@ -61,15 +62,7 @@ def gemm_amax(a, b, sfa, sfb, fmt: str, m: int, n: int, k: int, l: int, c_dtype=
     return c, amax
 
 
-def grouped_gemm_srelu(a, b, sfa, sfb, fmt: str, padded_offsets, alpha, prob, n: int, k: int,
-                       tanh_clamp_scale=None, d_dtype="bf16", c_dtype=torch.bfloat16, norm_const=None,
-                       outputs=None, workspace=None, stream=None, **opts):
-    """Returns a dict of the outputs (c, d, amax or d, d_col, sfd_row, sfd_col); d_dtype is
-    "bf16", "f16", "f32" or "e4m3", c_dtype a torch float dtype or None."""
-    ab, sfd, v = FORMATS[fmt]
-    dev = a.device
-    valid_m = a.shape[0] if a.dim() == 2 else a.shape[1]
-    num_experts = padded_offsets.numel()
+def _grouped_outputs(valid_m, n, num_experts, d_dtype, c_dtype, norm_const, outputs, dev):
     out = dict(outputs or {})
     if "c" not in out:
         out["c"] = None if c_dtype is None else torch.empty((valid_m, n), dtype=c_dtype, device=dev)
@@ -85,11 +78,51 @@ def grouped_gemm_srelu(a, b, sfa, sfb, fmt: str, padded_offsets, alpha, prob, n:
         if norm_const is None:
             norm_const = torch.ones(1, dtype=torch.float32, device=dev)
         dk = E4M3
-    if workspace is None:
-        workspace = new_workspace(dev)
     c = out["c"]
     ck = BF16 if c is None else _OUT_KINDS[c.dtype]
+    return out, dk, ck, norm_const
+
+
+def grouped_gemm_srelu(a, b, sfa, sfb, fmt: str, padded_offsets, alpha, prob, n: int, k: int,
+                       tanh_clamp_scale=None, d_dtype="bf16", c_dtype=torch.bfloat16, norm_const=None,
+                       outputs=None, workspace=None, stream=None, **opts):
+    """Returns a dict of the outputs (c, d, amax or d, d_col, sfd_row, sfd_col); d_dtype is
+    "bf16", "f16", "f32" or "e4m3", c_dtype a torch float dtype or None."""
+    ab, sfd, v = FORMATS[fmt]
+    dev = a.device
+    valid_m = a.shape[0] if a.dim() == 2 else a.shape[1]
+    num_experts = padded_offsets.numel()
+    out, dk, ck, norm_const = _grouped_outputs(valid_m, n, num_experts, d_dtype, c_dtype, norm_const, outputs, dev)
+    if workspace is None:
+        workspace = new_workspace(dev)
     bsg_grouped_gemm_srelu(a, b, sfa, sfb, ab, sfd, v, valid_m, n, k, num_experts, padded_offsets, alpha, prob,
-                           tanh_clamp_scale, norm_const, c, ck, out["d"], out.get("d_col"), dk, out.get("sfd_row"),
-                           out.get("sfd_col"), out.get("amax"), workspace, stream=stream, **opts)
+                           tanh_clamp_scale, norm_const, out["c"], ck, out["d"], out.get("d_col"), dk,
+                           out.get("sfd_row"), out.get("sfd_col"), out.get("amax"), workspace, stream=stream, **opts)
+    return out
+
+
+def _pointer_array(ptrs, dev):
+    if isinstance(ptrs, torch.Tensor):
+        return ptrs
+    return torch.tensor([t.data_ptr() for t in ptrs], dtype=torch.int64, device=dev)
+
+
+def grouped_gemm_srelu_discrete(a, b_ptrs, sfa, sfb_ptrs, fmt: str, padded_offsets, alpha, prob, n: int, k: int,
+                                tanh_clamp_scale=None, d_dtype="bf16", c_dtype=torch.bfloat16, norm_const=None,
+                                outputs=None, workspace=None, stream=None, **opts):
+    """grouped_gemm_srelu with per-expert weights: b_ptrs / sfb_ptrs are lists of the experts'
+    code tensors (n, k) / SF buffers, or device int64 tensors of their addresses. The call
+    synchronises the stream once (the experts' TMA descriptors are built on the host)."""
+    ab, sfd, v = FORMATS[fmt]
+    dev = a.device
+    valid_m = a.shape[0] if a.dim() == 2 else a.shape[1]
+    num_experts = padded_offsets.numel()
+    bp, sp = _pointer_array(b_ptrs, dev), _pointer_array(sfb_ptrs, dev)
+    out, dk, ck, norm_const = _grouped_outputs(valid_m, n, num_experts, d_dtype, c_dtype, norm_const, outputs, dev)
+    if workspace is None:
+        workspace = torch.zeros(bsg_grouped_discrete_workspace_size(num_experts), dtype=torch.uint8, device=dev)
+    bsg_grouped_gemm_srelu_discrete(a, bp, sfa, sp, ab, sfd, v, valid_m, n, k, num_experts, padded_offsets, alpha,
+                                    prob, tanh_clamp_scale, norm_const, out["c"], ck, out["d"], out.get("d_col"), dk,
+                                    out.get("sfd_row"), out.get("sfd_col"), out.get("amax"), workspace,
+                                    stream=stream, **opts)
     return out

@@ -128,6 +128,28 @@ def test_grouped_validation():
     assert st in (OK, ARCH, CUDA)
 
 
+def _discrete(**kw):
+    a = dict(a=P, bp=P, sfa=P, sp=P, L=2, ws=P, wsb=256 + 2 * 128, d=P)
+    a.update(kw)
+    return bsg.raw_status("bsg_grouped_gemm_srelu_discrete", a["a"], a["bp"], a["sfa"], a["sp"], bsg.E4M3,
+                          bsg.SF_UE8M0, 32, 512, 256, 256, a["L"], P, P, P, ctypes.c_float(0.0), None, P, bsg.BF16,
+                          a["d"], None, bsg.BF16, None, None, P, _opts(), a["ws"], a["wsb"], None)
+
+
+def test_discrete_validation():
+    # the error word plus one 128-byte TMA descriptor per expert
+    assert bsg.bsg_grouped_discrete_workspace_size(1) == 256 + 128
+    assert bsg.bsg_grouped_discrete_workspace_size(32) == 256 + 32 * 128
+    assert _discrete(bp=None) == INVALID
+    assert _discrete(sp=None) == INVALID
+    assert _discrete(wsb=256) == WORKSPACE                # too small for the descriptors
+    assert _discrete(bp=P + 4) == ALIGN                    # int64 array
+    assert _discrete(ws=P + 64) == ALIGN
+    assert _discrete(L=0) == INVALID
+    st = _discrete()
+    assert st in (OK, ARCH, CUDA)
+
+
 def test_noalloc_validation():
     def call(**kw):
         a = dict(a=P, c=P, amax=P, n=256)

@@ -20,7 +20,7 @@ def _case(counts, n, k, seed=3, a_scale=1.0):
 
 
 def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0, tile_n=0, seed=3, a_scale=1.0,
-                tanh_approx=False, max_ctas=0, cta_pair=0, fmt="mxfp8"):
+                tanh_approx=False, max_ctas=0, cta_pair=0, fmt="mxfp8", discrete=False):
     from nvfp4_gemm_moe_gb300 import torch_ops
     import nvfp4_gemm_moe_gb300 as bsg
     wl, offs, a, b, alpha, prob = _case(counts, n, k, seed, a_scale)
@@ -29,11 +29,23 @@ def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0,
     qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), fmt)
     ws = torch_ops.new_workspace()
     c_dtype = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16, None: None}[c_kind]
-    out = torch_ops.grouped_gemm_srelu(
-        qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
-        torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=clamp, d_dtype=d_dtype, c_dtype=c_dtype,
-        norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
-        tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair)
+    if discrete:
+        # each expert's codes and scales in an allocation of its own, allocated in reverse order
+        per_sf = sfb.numel() // len(counts)
+        b_list = [qb[g].clone() for g in reversed(range(len(counts)))][::-1]
+        sfb_list = [sfb[g * per_sf:(g + 1) * per_sf].clone() for g in reversed(range(len(counts)))][::-1]
+        ws = torch.zeros(bsg.bsg_grouped_discrete_workspace_size(len(counts)), dtype=torch.uint8, device="cuda")
+        out = torch_ops.grouped_gemm_srelu_discrete(
+            qa[0], b_list, sfa, sfb_list, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
+            torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=clamp, d_dtype=d_dtype, c_dtype=c_dtype,
+            norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
+            tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair)
+    else:
+        out = torch_ops.grouped_gemm_srelu(
+            qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
+            torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=clamp, d_dtype=d_dtype, c_dtype=c_dtype,
+            norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
+            tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair)
     torch.cuda.synchronize()
     assert bsg.bsg_read_device_error(ws) == 0
     qa_ref, sfa_ref = oq.quantize(a, fmt)
@@ -192,3 +204,54 @@ def test_grouped_cta_pairs_224(lib, d_dtype, clamp, n):
 def test_grouped_cta_pairs_few_clusters(lib):
     run_grouped([600, 900, 0, 300], 512, 512, "bf16", None, "bf16", cta_pair=2, max_ctas=2)
     run_grouped([600, 900, 0, 300], 512, 512, "e4m3", None, "bf16", cta_pair=2, max_ctas=4)
+
+
+@pytest.mark.parametrize("fmt,d_dtype,clamp,n,tile_n,cta_pair", [
+    ("mxfp8", "bf16", None, 264, 256, 1),    # ragged N, one-CTA tiles
+    ("mxfp8", "bf16", 32.0, 512, 0, 2),      # CTA pairs
+    ("mxfp8", "e4m3", None, 384, 224, 2),    # FP8 D on 224-wide pair tiles
+    ("mxfp8", "e4m3", None, 384, 128, 1),
+    ("nvfp4", "bf16", None, 512, 0, 2),
+    ("nvfp4", "f16", None, 264, 128, 1),
+])
+def test_grouped_discrete_weights(lib, fmt, d_dtype, clamp, n, tile_n, cta_pair):
+    """Per-expert weight allocations addressed by pointer arrays give the contiguous form's result."""
+    run_grouped(EDGE, n, 512, d_dtype, clamp, "bf16", tile_n=tile_n, cta_pair=cta_pair, fmt=fmt,
+                a_scale=700.0 if clamp else 1.0, discrete=True)
+
+
+def test_grouped_discrete_host_validation(lib):
+    """Null or misaligned pointer entries and a short workspace are rejected before any launch."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    k, n, vm = 256, 256, 512
+    qa = torch.zeros((vm, k), dtype=torch.uint8, device="cuda")
+    bs = [torch.zeros((n, k), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    sfa = torch.zeros(bsg.bsg_sf_bytes(1, vm, k, 32), dtype=torch.uint8, device="cuda")
+    sfbs = [torch.zeros(bsg.bsg_sf_bytes(1, n, k, 32), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    offs = torch.tensor([256, 512], dtype=torch.int32, device="cuda")
+    ones = torch.ones(2, device="cuda")
+    prob = torch.ones(vm, device="cuda")
+    good_b = torch.tensor([t.data_ptr() for t in bs], dtype=torch.int64, device="cuda")
+    good_s = torch.tensor([t.data_ptr() for t in sfbs], dtype=torch.int64, device="cuda")
+    cases = [
+        (torch.tensor([bs[0].data_ptr(), 0], dtype=torch.int64, device="cuda"), good_s, None, 1),
+        (good_b, torch.tensor([0, sfbs[1].data_ptr()], dtype=torch.int64, device="cuda"), None, 1),
+        (torch.tensor([bs[0].data_ptr() + 8, bs[1].data_ptr()], dtype=torch.int64, device="cuda"), good_s, None, 3),
+        (good_b, torch.tensor([sfbs[0].data_ptr(), sfbs[1].data_ptr() + 4], dtype=torch.int64, device="cuda"),
+         None, 3),
+        (good_b, good_s, bsg.bsg_workspace_size(), 8),
+    ]
+    for bp, sp, ws_bytes, status in cases:
+        ws = torch.zeros(bsg.bsg_grouped_discrete_workspace_size(2), dtype=torch.uint8, device="cuda")
+        out = {"d": torch.empty((vm, n), dtype=torch.bfloat16, device="cuda"),
+               "amax": torch.empty(2, device="cuda"), "c": None}
+        with pytest.raises(bsg.BsgError) as ei:
+            bsg.bsg_grouped_gemm_srelu_discrete(qa, bp, sfa, sp, bsg.E4M3, bsg.SF_UE8M0, 32, vm, n, k, 2, offs, ones,
+                                                prob, None, None, None, bsg.BF16, out["d"], None, bsg.BF16, None,
+                                                None, out["amax"], ws, workspace_bytes=ws_bytes)
+        assert ei.value.status == status, (status, ei.value.status)
+    # the good pointers run and give zeros
+    out = torch_ops.grouped_gemm_srelu_discrete(qa, good_b, sfa, good_s, "mxfp8", offs, ones, prob, n, k)
+    torch.cuda.synchronize()
+    assert float(out["d"].float().abs().max()) == 0.0
