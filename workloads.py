@@ -29,7 +29,7 @@ import numpy as np
 CHUNK = 1 << 20
 
 # stream ids: one per tensor kind so tensors never share random numbers
-S_A, S_B, S_ALPHA, S_PROB, S_ROUTE = 1, 2, 3, 4, 5
+S_A, S_B, S_ALPHA, S_PROB, S_ROUTE, S_C, S_BETA = 1, 2, 3, 4, 5, 6, 7
 
 PAD = 256  # expert row ranges are padded to multiples of 256 rows
 
@@ -243,6 +243,31 @@ class Grouped:
         return uniform_f32(self.seed, S_PROB, self.valid_m, 0.0, 1.0)
 
 
+@dataclasses.dataclass(frozen=True)
+class GroupedDswiglu(Grouped):
+    """Grouped GEMM + dSwiGLU backward workload: the grouped operands plus the stored forward
+    intermediate C (valid_m, 2N) and the per-expert scale beta of C."""
+    c_dtype: str = "bf16"   # element type C is stored in
+
+    def c_rows(self, rows: np.ndarray | None = None) -> np.ndarray:
+        """fp32 C (valid_m, 2N) as 3 N(0,1) on routed rows (gates reach the sigmoid's tails),
+        zero on padding rows (the forward pass left them zero)."""
+        two_n, vm = 2 * self.n, self.valid_m
+        mask = self.routed_mask()
+        if rows is None:
+            x = normal_f32(self.seed, S_C, 0, vm * two_n).reshape(vm, two_n)
+            x *= np.float32(3.0)
+            x[~mask] = 0.0
+        else:
+            x = normal_f32_rows(self.seed, S_C, rows, two_n)
+            x *= np.float32(3.0)
+            x[~mask[np.asarray(rows)]] = 0.0
+        return x
+
+    def beta(self) -> np.ndarray:
+        return uniform_f32(self.seed, S_BETA, self.experts, 0.5, 2.0)
+
+
 # The five named workloads.  The first is small enough for the oracle to finish
 # in seconds; the second is the large batched dense one throughput is quoted on.
 DENSE_MXFP8_256 = Dense("dense_mxfp8_m256_n256_k256_l1", 256, 256, 256, 1, "mxfp8", "f32")
@@ -256,5 +281,11 @@ GROUPED_SRELU_E32_CLAMP = dataclasses.replace(GROUPED_SRELU_E32, name=GROUPED_SR
                                               tanh_clamp=32.0)
 GROUPED_FP8D_E128 = Grouped("grouped_mxfp8_fp8d_e128_k4096_n4096", 128, 4096, 4096, 65536, "zipf1.2", "e4m3")
 
+# the backward of the E32 expert layer: dSwiGLU over the same routing, ref N = 2048 (C and D 4096 wide)
+GROUPED_DSWIGLU_E32 = GroupedDswiglu("grouped_mxfp8_dswiglu_e32_k7168_n2048", 32, 7168, 2048, 32768, "uniform",
+                                     "bf16")
+GROUPED_DSWIGLU_E32_FP8D = dataclasses.replace(GROUPED_DSWIGLU_E32, name="grouped_mxfp8_dswiglu_fp8d_e32_k7168_n2048",
+                                               d_dtype="e4m3")
+
 ALL = {w.name: w for w in (DENSE_MXFP8_256, DENSE_MXFP8_8192, DENSE_MXFP8_8192_L1, DENSE_NVFP4_16384, GROUPED_SRELU_E32,
-                           GROUPED_SRELU_E32_CLAMP, GROUPED_FP8D_E128)}
+                           GROUPED_SRELU_E32_CLAMP, GROUPED_FP8D_E128, GROUPED_DSWIGLU_E32, GROUPED_DSWIGLU_E32_FP8D)}
