@@ -13,7 +13,9 @@
  *                           row/column MXFP8 scale factors
  *                           ("Grouped GEMM + sReLU (SM100)", Overview, Equations,
  *                           Tanh soft clamp); bsg_grouped_gemm_srelu_discrete takes
- *                           the experts' weights as separate allocations.
+ *                           the experts' weights as separate allocations;
+ *   bsg_grouped_gemm_dswiglu grouped MoE block-scaled GEMM + dSwiGLU backward epilogue
+ *                           ("Grouped GEMM + dSwiGLU (SM100)", Equations).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -208,6 +210,50 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
                                   uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
                                   const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
                                   void* stream);
+
+/*
+ * bsg_grouped_gemm_dswiglu -- grouped MoE block-scaled GEMM + dSwiGLU backward epilogue
+ * ("Grouped GEMM + dSwiGLU (SM100)", Shapes, Equations Steps 1-3).  Rows
+ * [padded_offsets[g-1], padded_offsets[g]) belong to expert g.  C is the stored forward
+ * intermediate (valid_m, 2N): 32-column blocks alternating input, gate, input, gate, ...; ref
+ * column n (block j = n / 32, i = n % 32) pairs with C columns 64 j + i (input) and 64 j + 32 + i
+ * (gate).  With x = beta[g] * input, gt = beta[g] * gate, s = 1 / (1 + exp(-gt)):
+ *     ref[m, n]          = alpha[g] * sum_k Ahat[m, k] * Bhat[n, k, g]
+ *     D[m, 64 j + i]      = ab      = ref * prob[m] * gt * s
+ *     D[m, 64 j + 32 + i] = dswiglu = ref * prob[m] * x * s * (1 + gt * (1 - s))
+ *     dprob[m]           += sum_n gt * s * x * ref
+ * evaluated in fp32 from the fp32 accumulator (the sigmoid from the fast exponential and
+ * division, within a few ulp).  The page's Step 1 prints alpha_g squared while its diagram and
+ * the grouped sReLU page scale by alpha_g once: alpha is applied once here (pass the squares for
+ * the other reading).
+ *
+ * a, b, sfa, sfb  as for bsg_grouped_gemm_srelu (b: (num_experts, n, k)).
+ * alpha, beta     device fp32 (num_experts,).
+ * prob            device fp32 (valid_m,).
+ * c               device input (valid_m, 2n), c_dtype BSG_BF16, BSG_F16, BSG_F32 or BSG_E4M3
+ *                 (plain E4M3 values; beta carries any scale).
+ * d_row           device output (valid_m, 2n): d_dtype BSG_BF16 / BSG_F16 / BSG_F32 (RNE of the
+ *                 fp32 values), or BSG_E4M3 (row-quantised, MXFP8 operands only).
+ * d_col           E4M3 D only: device output (valid_m, 2n), column-quantised; else NULL.
+ * sfd_row, sfd_col E4M3 D only: SF layout with rows valid_m and K = 2n (sfd_row), rows 2n and
+ *                 K = valid_m (sfd_col); scales and codes as for bsg_grouped_gemm_srelu.
+ * norm_const      device fp32 (1,); required iff d_dtype == BSG_E4M3.
+ * dprob           device fp32 (valid_m,): the call ADDS each row's sum (atomic adds in an
+ *                 unspecified order); zero it first for the plain gradient.
+ * amax            device fp32 (num_experts, 2): [g][0] = max |ab|, [g][1] = max |dswiglu| over
+ *                 expert g's rows (0 for an empty expert); required iff d_dtype is not E4M3.
+ *                 Zeroed by the call.
+ * Requirements: valid_m % 256 == 0, n % 32 == 0, 1 <= num_experts <= 512, k a multiple of the
+ * scale block, operand rows a multiple of 16 bytes.  opts->tile_n may be 128, 224 (MXFP8) or 256.
+ */
+bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
+                                    bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size,
+                                    int64_t valid_m, int64_t n, int64_t k, int64_t num_experts,
+                                    const int32_t* padded_offsets, const float* alpha, const float* beta,
+                                    const float* prob, const void* c, bsg_dtype c_dtype, const float* norm_const,
+                                    void* d_row, void* d_col, bsg_dtype d_dtype, uint8_t* sfd_row,
+                                    uint8_t* sfd_col, float* dprob, float* amax, const bsg_gemm_opts* opts,
+                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * bsg_grouped_gemm_srelu_discrete -- bsg_grouped_gemm_srelu with per-expert weight allocations

@@ -64,6 +64,9 @@ def _load():
     lib.bsg_grouped_discrete_workspace_size.argtypes = [I64]
     lib.bsg_grouped_gemm_srelu_discrete.restype = I
     lib.bsg_grouped_gemm_srelu_discrete.argtypes = lib.bsg_grouped_gemm_srelu.argtypes
+    lib.bsg_grouped_gemm_dswiglu.restype = I
+    lib.bsg_grouped_gemm_dswiglu.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, P, P, P, P, I, P, P, P, I,
+                                             P, P, P, P, ctypes.POINTER(bsg_gemm_opts), P, SZ, P]
     lib.bsg_gemm_amax_noalloc.restype = I
     lib.bsg_gemm_amax_noalloc.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, I, P,
                                           ctypes.POINTER(bsg_gemm_opts), P]
@@ -171,6 +174,18 @@ def bsg_grouped_gemm_srelu_discrete(a, b_ptrs, sfa, sfb_ptrs, ab_dtype, sf_dtype
         num_experts, _ptr(padded_offsets), _ptr(alpha), _ptr(prob), s, _ptr(norm_const), _ptr(c), c_dtype, _ptr(d),
         _ptr(d_col), d_dtype, _ptr(sfd_row), _ptr(sfd_col), _ptr(amax), ctypes.byref(o), _ptr(workspace), ws_bytes,
         _stream(stream)), "bsg_grouped_gemm_srelu_discrete")
+
+
+def bsg_grouped_gemm_dswiglu(a, b, sfa, sfb, ab_dtype, sf_dtype, sf_vec_size, valid_m, n, k, num_experts,
+                             padded_offsets, alpha, beta, prob, c, c_dtype, norm_const, d_row, d_col, d_dtype,
+                             sfd_row, sfd_col, dprob, amax, workspace, workspace_bytes=None, stream=None, **opts):
+    ws_bytes = bsg_workspace_size() if workspace_bytes is None else workspace_bytes
+    o = _opts(**opts)
+    _check(_lib.bsg_grouped_gemm_dswiglu(
+        _ptr(a), _ptr(b), _ptr(sfa), _ptr(sfb), ab_dtype, sf_dtype, sf_vec_size, valid_m, n, k, num_experts,
+        _ptr(padded_offsets), _ptr(alpha), _ptr(beta), _ptr(prob), _ptr(c), c_dtype, _ptr(norm_const), _ptr(d_row),
+        _ptr(d_col), d_dtype, _ptr(sfd_row), _ptr(sfd_col), _ptr(dprob), _ptr(amax), ctypes.byref(o),
+        _ptr(workspace), ws_bytes, _stream(stream)), "bsg_grouped_gemm_dswiglu")
 
 
 def bsg_read_device_error(workspace, stream=None) -> int:

@@ -481,6 +481,132 @@ bsg_status bsg_grouped_gemm_srelu_discrete(const void* a, const int64_t* b_ptrs,
                       d_dtype, sfd_row, sfd_col, amax, opts, workspace, workspace_bytes, stream);
 }
 
+bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
+                                    bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size, int64_t valid_m,
+                                    int64_t n, int64_t k, int64_t num_experts, const int32_t* padded_offsets,
+                                    const float* alpha, const float* beta, const float* prob, const void* c,
+                                    bsg_dtype c_dtype, const float* norm_const, void* d_row, void* d_col,
+                                    bsg_dtype d_dtype, uint8_t* sfd_row, uint8_t* sfd_col, float* dprob,
+                                    float* amax, const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  int fmt = 0;
+  bsg_status st = operand_format(ab_dtype, sf_dtype, sf_vec_size, &fmt);
+  if (st != BSG_OK) return st;
+  if (!a || !b || !sfa || !sfb || !padded_offsets || !alpha || !beta || !prob || !c || !d_row || !dprob)
+    return BSG_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
+  // N a multiple of 32: C and D are 32-column input / gate (ab / dswiglu) blocks; 2 * num_experts
+  // amax values are staged in the kernel's shared memory
+  if (valid_m < 0 || valid_m % 256 != 0 || n < 32 || n % 32 != 0 || k < 1 || num_experts < 1 ||
+      num_experts > 512)
+    return BSG_ERR_INVALID_ARG;
+  if (!fits_int32(valid_m) || !fits_int32(2 * n) || !fits_int32(k)) return BSG_ERR_INVALID_ARG;
+  if (k % sf_vec_size != 0) return BSG_ERR_INVALID_ARG;
+  const bool fp8_d = d_dtype == BSG_E4M3;
+  const int d_kind = out_kind(d_dtype);
+  if (!fp8_d && d_kind != bsg::kOutBF16 && d_kind != bsg::kOutF16 && d_kind != bsg::kOutF32) return BSG_ERR_UNSUPPORTED;
+  if (fp8_d) {
+    if (fmt != bsg::kMXFP8) return BSG_ERR_UNSUPPORTED;
+    if (!d_col || !sfd_row || !sfd_col || !norm_const) return BSG_ERR_INVALID_ARG;
+  } else {
+    if (!amax || d_col || sfd_row || sfd_col) return BSG_ERR_INVALID_ARG;
+  }
+  const int c_kind = out_kind(c_dtype);
+  if (c_kind != bsg::kOutBF16 && c_kind != bsg::kOutF16 && c_kind != bsg::kOutF32 && c_kind != bsg::kOutE4M3)
+    return BSG_ERR_UNSUPPORTED;
+  const int64_t row_bytes = fmt == bsg::kMXFP8 ? k : k / 2;
+  if (row_bytes % 16 != 0 || (2 * n * out_bits(d_kind)) % 128 != 0 || (2 * n * out_bits(c_kind)) % 128 != 0)
+    return BSG_ERR_ALIGNMENT;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(c) || !aligned16(d_row) ||
+      (d_col && !aligned16(d_col)) || (sfd_row && !aligned16(sfd_row)) || (sfd_col && !aligned16(sfd_col)) ||
+      (reinterpret_cast<uintptr_t>(dprob) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      (reinterpret_cast<uintptr_t>(padded_offsets) & 3u))
+    return BSG_ERR_ALIGNMENT;
+  DeviceInfo info;
+  st = current_device(nullptr, &info);
+  if (st != BSG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (opts && opts->validate_offsets) {
+    std::vector<int32_t> h(static_cast<size_t>(num_experts));
+    if (cudaMemcpyAsync(h.data(), padded_offsets, h.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return BSG_ERR_CUDA;
+    int32_t prev = 0;
+    for (size_t i = 0; i < h.size(); ++i) {
+      if (h[i] % 256 != 0 || h[i] < prev || h[i] > valid_m) return BSG_ERR_BAD_OFFSETS;
+      prev = h[i];
+    }
+    if (prev != valid_m) return BSG_ERR_BAD_OFFSETS;
+  }
+
+  const int64_t n_d = 2 * n;
+  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
+  if (!fp8_d && cudaMemsetAsync(amax, 0, 2 * sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
+  if (fp8_d && n_d % 128 != 0) {
+    // SFD_col rows 2N .. ceil(2N/128)*128 are padding the kernel never touches
+    if (cudaMemsetAsync(sfd_col, 0, bsg_sf_bytes(1, n_d, valid_m, 32), s) != cudaSuccess) return BSG_ERR_CUDA;
+  }
+  if (valid_m == 0) return BSG_OK;
+
+  const TilePlan plan = plan_tiles(fmt, valid_m, n, 1, info.num_sms, true, opts);
+  const bool pairs = plan.pairs;
+  const int bn = plan.bn;
+  const int64_t m_tiles = pairs ? valid_m / 256 : valid_m / 128;
+  const int64_t n_tiles = cdiv(n, bn);
+  const int64_t tiles = m_tiles * n_tiles;
+  if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
+  const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
+
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128) ||
+      !make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn))
+    return BSG_ERR_CUDA;
+  const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
+
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.m = static_cast<int>(valid_m);
+  p.n = static_cast<int>(n);
+  p.k = static_cast<int>(k);
+  p.l = static_cast<int>(num_experts);
+  p.m_tiles = static_cast<int>(m_tiles);
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.k_tiles = static_cast<int>(cdiv(k, elems_per_ktile));
+  p.num_tiles = static_cast<int>(tiles);
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.sfa_mt = static_cast<int>(valid_m / 128);
+  p.sfb_mt = static_cast<int>(cdiv(n, 128));
+  p.sf_kt = static_cast<int>(sf_kt);
+  p.c_kind = bsg::kOutNone;
+  p.d_kind = d_kind;
+  p.amax = fp8_d ? nullptr : amax;
+  p.offsets = padded_offsets;
+  p.alpha = alpha;
+  p.prob = prob;
+  p.norm_const = norm_const;
+  p.d = d_row;
+  p.d_col = d_col;
+  p.sfd_row = sfd_row;
+  p.sfd_col = sfd_col;
+  p.sfd_row_kt = static_cast<int>(cdiv(n_d, 128));
+  p.sfd_col_mt = static_cast<int>(cdiv(n_d, 128));
+  p.sfd_col_kt = static_cast<int>(cdiv(valid_m, 128));
+  p.c_in = c;
+  p.c_in_kind = c_kind;
+  p.beta = beta;
+  p.dprob = dprob;
+  p.err = static_cast<uint32_t*>(workspace);
+
+  GemmConfig cfg{fmt, bn, fp8_d ? bsg::kEpiDswigluFP8 : bsg::kEpiDswigluF};
+  cudaError_t e = pairs ? bsg::launch_gemm_pair_dswiglu(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
+                        : bsg::launch_gemm_dswiglu(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
+  if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+}
+
 bsg_status bsg_read_device_error(const void* workspace, void* stream, uint32_t* error_bits) {
   if (!workspace || !error_bits) return BSG_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -261,6 +261,189 @@ __device__ __forceinline__ void epilogue_dense_bf16_early(const GemmParams& p, i
   }
 }
 
+// Row- and column-quantised E4M3 store of one 32-column block of D: row `row`, D columns
+// dcol0 .. dcol0 + 31 of a row-major D that is n_d wide (n_d a multiple of 32), values already
+// multiplied by norm_const.  D_row takes one E8M0 scale per row and block (this thread's 32
+// values), D_col one per column and 32-row block (the warp's 32 lanes are 32 consecutive rows).
+// s_inv: 32 floats of shared memory owned by this warp.
+__device__ __forceinline__ void store_e4m3_block(const GemmParams& p, int row, int dcol0, int n_d, const float (&d)[32],
+                                                 int lane, float* s_inv) {
+  const uint64_t rc = static_cast<uint64_t>(row) * n_d + dcol0;
+  float bmax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, fabsf(d[j]));
+  const uint32_t code_r = e8m0_ceil_code(bmax);
+  const float inv_r = e8m0_inv_scale(code_r);
+  uint32_t q[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t lo = cvt_e4m3x2(__fmul_rn(d[4 * j], inv_r), __fmul_rn(d[4 * j + 1], inv_r));
+    const uint32_t hi = cvt_e4m3x2(__fmul_rn(d[4 * j + 2], inv_r), __fmul_rn(d[4 * j + 3], inv_r));
+    q[j] = lo | (hi << 16);
+  }
+  uint8_t* drow = reinterpret_cast<uint8_t*>(p.d) + rc;
+  store16(drow, q[0], q[1], q[2], q[3]);
+  store16(drow + 16, q[4], q[5], q[6], q[7]);
+  // one byte per block: a tile need not start on a four-block word of the SF layout; the row's
+  // last block also zeroes the padding blocks of its word
+  const int nb = dcol0 >> 5;
+  const int nb_end = dcol0 + 32 >= n_d ? (nb | 3) : nb;
+  for (int b = nb; b <= nb_end; ++b)
+    p.sfd_row[sf_offset(row, b, 0, (p.m + 127) / 128, p.sfd_row_kt)] = static_cast<uint8_t>(b == nb ? code_r : 0u);
+  float cm[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) cm[j] = fabsf(d[j]);
+  warp_colmax_scatter(cm, lane);
+  const uint32_t code_c = e8m0_ceil_code(cm[0]);
+  const int mblk = row >> 5;  // same for the whole warp
+  p.sfd_col[sf_offset(dcol0 + lane, mblk, 0, p.sfd_col_mt, p.sfd_col_kt)] = static_cast<uint8_t>(code_c);
+  // every lane needs the 32 column reciprocals: one shared-memory round trip (broadcast reads)
+  // instead of 32 shuffles
+  s_inv[lane] = e8m0_inv_scale(code_c);
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 iv = reinterpret_cast<const float4*>(s_inv)[j];
+    const uint32_t lo = cvt_e4m3x2(__fmul_rn(d[4 * j], iv.x), __fmul_rn(d[4 * j + 1], iv.y));
+    const uint32_t hi = cvt_e4m3x2(__fmul_rn(d[4 * j + 2], iv.z), __fmul_rn(d[4 * j + 3], iv.w));
+    q[j] = lo | (hi << 16);
+  }
+  __syncwarp();  // the next block overwrites s_inv
+  uint8_t* dcol = reinterpret_cast<uint8_t*>(p.d_col) + rc;
+  store16(dcol, q[0], q[1], q[2], q[3]);
+  store16(dcol + 16, q[4], q[5], q[6], q[7]);
+}
+
+// Loads 32 consecutive elements of `kind` (f32, bf16, f16 or E4M3) at element `off` of `base`
+// as fp32, with streaming loads (the dSwiGLU input C is read once).  `off` is a multiple of 32.
+__device__ __forceinline__ void load_row32(const void* base, uint64_t off, int kind, float (&v)[32]) {
+  if (kind == kOutF32) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 q = __ldcs(src + j);
+      v[4 * j] = q.x;
+      v[4 * j + 1] = q.y;
+      v[4 * j + 2] = q.z;
+      v[4 * j + 3] = q.w;
+    }
+  } else if (kind == kOutE4M3) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(base) + off);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint4 q = __ldcs(src + j);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w[i] & 0xffffu));
+        const float2 hi = e4m3x2_to_float2(static_cast<uint16_t>(w[i] >> 16));
+        v[16 * j + 4 * i] = lo.x;
+        v[16 * j + 4 * i + 1] = lo.y;
+        v[16 * j + 4 * i + 2] = hi.x;
+        v[16 * j + 4 * i + 3] = hi.y;
+      }
+    }
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off);
+    const bool bf = kind == kOutBF16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 q = __ldcs(src + j);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (bf) {
+          v[8 * j + 2 * i] = __uint_as_float(w[i] << 16);
+          v[8 * j + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        } else {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+          v[8 * j + 2 * i] = f.x;
+          v[8 * j + 2 * i + 1] = f.y;
+        }
+      }
+    }
+  }
+}
+
+// dSwiGLU backward epilogue of one tile for the rows of one warp ("Grouped GEMM + dSwiGLU
+// (SM100)", Step 2).  Accumulator chunk c (ref columns n0 .. n0 + 31, n0 = col_base + 32 c)
+// pairs with the input block at C columns 2 n0 .. 2 n0 + 31 and the gate block right after it;
+// with x = beta_g * input, g = beta_g * gate, s = sigmoid(g) and ref = alpha_g * acc:
+//   ab = ref * prob * g * s,   dswiglu = ref * prob * x * s * (1 + g (1 - s)),
+// stored at the same two D blocks; sum(g * s * x * ref) over the warp's chunks is added to
+// dprob[row].  Float D folds |ab| and |dswiglu| into max_ab / max_dsw; E4M3 D quantises each
+// block by rows and by columns.  N is a multiple of 32, so a chunk is wholly in or out.
+template <int BN, bool kFP8>
+__device__ __forceinline__ void epilogue_tile_dswiglu(const GemmParams& p, int row, int col_base, uint32_t tmem_acc,
+                                                      int lane, float alpha_g, float beta_g, float prob_r, float nc,
+                                                      float& max_ab, float& max_dsw, int c_first, int c_step,
+                                                      float* s_inv) {
+  const int n_d = 2 * p.n;
+  float dprob_part = 0.0f;
+#pragma unroll 1
+  for (int c = c_first; c < BN / 32; c += c_step) {
+    const int col0 = col_base + c * 32;
+    if (col0 >= p.n) break;  // warp-uniform
+    const uint64_t off = static_cast<uint64_t>(row) * n_d + 2 * col0;  // input block; gate at off + 32
+    float x[32], g[32];
+    load_row32(p.c_in, off, p.c_in_kind, x);
+    load_row32(p.c_in, off + 32, p.c_in_kind, g);
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tmem_acc + c * 32, r);
+    tmem_ld_wait(r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float ref = alpha_g * __uint_as_float(r[j]);
+      const float xv = beta_g * x[j];
+      const float gv = beta_g * g[j];
+      // sigmoid from the fast exponential and division: a few ulp, and 0 / 1 at the tails
+      const float sig = __fdividef(1.0f, 1.0f + __expf(-gv));
+      const float sw = gv * sig;
+      dprob_part = fmaf(sw * xv, ref, dprob_part);
+      const float rp = ref * prob_r;
+      x[j] = rp * sw;                                        // ab
+      g[j] = rp * xv * sig * fmaf(gv, 1.0f - sig, 1.0f);     // dswiglu
+    }
+    if (!kFP8) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        max_ab = fmaxf(max_ab, fabsf(x[j]));
+        max_dsw = fmaxf(max_dsw, fabsf(g[j]));
+      }
+      store_row32(p.d, off, p.d_kind, x, 2 * col0, n_d);
+      store_row32(p.d, off + 32, p.d_kind, g, 2 * col0 + 32, n_d);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        x[j] = __fmul_rn(x[j], nc);
+        g[j] = __fmul_rn(g[j], nc);
+      }
+      store_e4m3_block(p, row, 2 * col0, n_d, x, lane, s_inv);
+      store_e4m3_block(p, row, 2 * col0 + 32, n_d, g, lane, s_inv);
+    }
+  }
+  if (dprob_part != 0.0f) atomicAdd(&p.dprob[row], dprob_part);
+}
+
+// Folds one warp's running maxima of expert g into shared memory: the per-expert amax of the
+// grouped sReLU float D, or the (|ab|, |dswiglu|) pair of the dSwiGLU float D.
+template <int EPI>
+__device__ __forceinline__ void fold_expert_max(float* s_amax, int g, float m1, float m2, int lane) {
+  if (EPI != kEpiGroupedBF16 && EPI != kEpiDswigluF) return;
+  for (int o = 16; o >= 1; o >>= 1) {
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+  }
+  if (lane == 0) {
+    if (EPI == kEpiGroupedBF16) {
+      atomic_max_nonneg(&s_amax[g], m1);
+    } else {
+      atomic_max_nonneg(&s_amax[2 * g], m1);
+      atomic_max_nonneg(&s_amax[2 * g + 1], m2);
+    }
+  }
+}
+
 // Epilogue of one tile for the rows of one warp: reads the fp32 accumulator chunk by chunk
 // (32 columns of this thread's row per tcgen05.ld) from `tmem_acc` (this warp's lane
 // quadrant, first accumulator column) and writes the outputs of row `row`, columns
@@ -317,51 +500,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
         // norm_const times the block maxima of D, rounded); scaling by 2^-e is exact
 #pragma unroll
         for (int j = 0; j < 32; ++j) d[j] = __fmul_rn(d[j], nc);
-        // row MXFP8: this thread's 32 columns form one block
-        float bmax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, fabsf(d[j]));
-        const uint32_t code_r = e8m0_ceil_code(bmax);
-        const float inv_r = e8m0_inv_scale(code_r);
-        uint32_t q[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t lo = cvt_e4m3x2(__fmul_rn(d[4 * j], inv_r), __fmul_rn(d[4 * j + 1], inv_r));
-          const uint32_t hi = cvt_e4m3x2(__fmul_rn(d[4 * j + 2], inv_r), __fmul_rn(d[4 * j + 3], inv_r));
-          q[j] = lo | (hi << 16);
-        }
-        uint8_t* drow = reinterpret_cast<uint8_t*>(p.d) + rc;
-        store16(drow, q[0], q[1], q[2], q[3]);
-        store16(drow + 16, q[4], q[5], q[6], q[7]);
-        // one byte per block: a tile need not start on a four-block word of the SF layout; the
-        // row's last block also zeroes the padding blocks of its word
-        const int nb = col0 >> 5;
-        const int nb_end = col0 + 32 >= p.n ? (nb | 3) : nb;
-        for (int b = nb; b <= nb_end; ++b)
-          p.sfd_row[sf_offset(row, b, 0, (p.m + 127) / 128, p.sfd_row_kt)] = static_cast<uint8_t>(b == nb ? code_r : 0u);
-        // column MXFP8: the warp's 32 lanes are 32 consecutive rows (one block per column)
-        float cm[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) cm[j] = fabsf(d[j]);
-        warp_colmax_scatter(cm, lane);
-        const uint32_t code_c = e8m0_ceil_code(cm[0]);
-        const int mblk = row >> 5;  // same for the whole warp
-        p.sfd_col[sf_offset(col0 + lane, mblk, 0, p.sfd_col_mt, p.sfd_col_kt)] = static_cast<uint8_t>(code_c);
-        // every lane needs the 32 column reciprocals: one shared-memory round trip (broadcast
-        // reads) instead of 32 shuffles
-        s_inv[lane] = e8m0_inv_scale(code_c);
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 iv = reinterpret_cast<const float4*>(s_inv)[j];
-          const uint32_t lo = cvt_e4m3x2(__fmul_rn(d[4 * j], iv.x), __fmul_rn(d[4 * j + 1], iv.y));
-          const uint32_t hi = cvt_e4m3x2(__fmul_rn(d[4 * j + 2], iv.z), __fmul_rn(d[4 * j + 3], iv.w));
-          q[j] = lo | (hi << 16);
-        }
-        __syncwarp();  // the next chunk overwrites s_inv
-        uint8_t* dcol = reinterpret_cast<uint8_t*>(p.d_col) + rc;
-        store16(dcol, q[0], q[1], q[2], q[3]);
-        store16(dcol + 16, q[4], q[5], q[6], q[7]);
+        store_e4m3_block(p, row, col0, p.n, d, lane, s_inv);
       }
     }
   }
@@ -645,10 +784,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     // ------------------------------------------------------------ epilogue warps 2..9
     const int quad = warp & 3;          // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2;   // two warps per quadrant take alternate 32-column chunks
-    float run_max = 0.0f;       // dense amax, or grouped per-expert segment max
+    float run_max = 0.0f;       // dense amax, or grouped per-expert segment max (dSwiGLU: of |ab|)
+    float run_max2 = 0.0f;      // dSwiGLU: per-expert segment max of |dswiglu|
     int run_expert = -1;
     uint32_t acc = 0, acc_phase = 0;
-    const float nc = (EPI == kEpiGroupedFP8) ? *p.norm_const : 1.0f;
+    const float nc = epi_has_fp8_d(EPI) ? *p.norm_const : 1.0f;
     for (int t = blockIdx.x; !bad && t < p.num_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
       if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
@@ -659,13 +799,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         alpha_g = p.alpha[tc.l];
         prob_r = p.prob[row];
         if (tc.l != run_expert) {
-          if (run_expert >= 0) {
-            float v = run_max;
-            for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0 && EPI == kEpiGroupedBF16) atomic_max_nonneg(&s_amax[run_expert], v);
-          }
+          if (run_expert >= 0) fold_expert_max<EPI>(s_amax, run_expert, run_max, run_max2, lane);
           run_expert = tc.l;
           run_max = 0.0f;
+          run_max2 = 0.0f;
         }
       }
       const uint32_t tmem_acc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
@@ -674,7 +811,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tmem_empty[acc]);
       };
-      if (EPI == kEpiDense && p.c_kind == kOutBF16) {
+      if constexpr (epi_is_dswiglu(EPI)) {
+        epilogue_tile_dswiglu<BN, EPI == kEpiDswigluFP8>(p, row, tc.nt * BN, tmem_acc, lane, alpha_g, p.beta[tc.l],
+                                                         prob_r, nc, run_max, run_max2, half, 2,
+                                                         s_amax + (warp - 2) * 32);
+        release();
+      } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
         epilogue_dense_bf16_early<BN>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
@@ -683,12 +825,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       }
       if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
     }
-    // fold this warp's running maximum into shared memory
-    float v = run_max;
-    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (lane == 0) {
-      if (EPI == kEpiDense) atomic_max_nonneg(&s_amax[0], v);
-      else if (EPI == kEpiGroupedBF16 && run_expert >= 0) atomic_max_nonneg(&s_amax[run_expert], v);
+    // fold this warp's running maxima into shared memory
+    if (EPI == kEpiDense) {
+      float v = run_max;
+      for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+      if (lane == 0) atomic_max_nonneg(&s_amax[0], v);
+    } else if (run_expert >= 0) {
+      fold_expert_max<EPI>(s_amax, run_expert, run_max, run_max2, lane);
     }
   }
 
@@ -702,6 +845,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     } else if (EPI == kEpiGroupedBF16) {
       for (int g = threadIdx.x; g < p.l; g += kThreadsGemm)
         if (s_amax[g] > 0.0f) atomic_max_nonneg(&p.amax[g], s_amax[g]);
+    } else if (EPI == kEpiDswigluF) {
+      // (|ab|, |dswiglu|) per expert: 2 * num_experts <= 1024 values
+      for (int i = threadIdx.x; i < 2 * p.l; i += kThreadsGemm)
+        if (s_amax[i] > 0.0f) atomic_max_nonneg(&p.amax[i], s_amax[i]);
     }
   }
   if (warp == 1) {

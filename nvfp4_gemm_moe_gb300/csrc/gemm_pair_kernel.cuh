@@ -314,10 +314,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     // ------------------------------------------------------------ epilogue warps 2..9 (both CTAs)
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
-    float run_max = 0.0f;
+    float run_max = 0.0f, run_max2 = 0.0f;
     int run_expert = -1;
     uint32_t acc = 0, acc_phase = 0;
-    const float nc = (EPI == kEpiGroupedFP8) ? *p.norm_const : 1.0f;
+    const float nc = epi_has_fp8_d(EPI) ? *p.norm_const : 1.0f;
     const uint32_t empty_leader = mapa_shared(smem_u32(&tmem_empty[0]), 0);
     for (int t = pair_id; !bad && t < p.num_tiles; t += num_pairs) {
       const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
@@ -329,13 +329,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         alpha_g = p.alpha[tc.l];
         prob_r = p.prob[row];
         if (tc.l != run_expert) {
-          if (run_expert >= 0) {
-            float v = run_max;
-            for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0 && EPI == kEpiGroupedBF16) atomic_max_nonneg(&s_amax[run_expert], v);
-          }
+          if (run_expert >= 0) fold_expert_max<EPI>(s_amax, run_expert, run_max, run_max2, lane);
           run_expert = tc.l;
           run_max = 0.0f;
+          run_max2 = 0.0f;
         }
       }
       const uint32_t tmem_acc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
@@ -345,7 +342,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(empty_leader + acc * 8);
       };
-      if (EPI == kEpiDense && p.c_kind == kOutBF16) {
+      if constexpr (epi_is_dswiglu(EPI)) {
+        epilogue_tile_dswiglu<BN, EPI == kEpiDswigluFP8>(p, row, tc.nt * BN, tmem_acc, lane, alpha_g, p.beta[tc.l],
+                                                         prob_r, nc, run_max, run_max2, half, 2,
+                                                         s_amax + (warp - 2) * 32);
+        release();
+      } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
         epilogue_dense_bf16_early<BN>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
@@ -354,11 +356,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       }
       if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
     }
-    float v = run_max;
-    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (lane == 0) {
-      if (EPI == kEpiDense) atomic_max_nonneg(&s_amax[0], v);
-      else if (EPI == kEpiGroupedBF16 && run_expert >= 0) atomic_max_nonneg(&s_amax[run_expert], v);
+    // fold this warp's running maxima into shared memory
+    if (EPI == kEpiDense) {
+      float v = run_max;
+      for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+      if (lane == 0) atomic_max_nonneg(&s_amax[0], v);
+    } else if (run_expert >= 0) {
+      fold_expert_max<EPI>(s_amax, run_expert, run_max, run_max2, lane);
     }
   }
 
@@ -372,6 +376,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     } else if (EPI == kEpiGroupedBF16) {
       for (int g = threadIdx.x; g < p.l; g += kThreadsGemm)
         if (s_amax[g] > 0.0f) atomic_max_nonneg(&p.amax[g], s_amax[g]);
+    } else if (EPI == kEpiDswigluF) {
+      // (|ab|, |dswiglu|) per expert: 2 * num_experts <= 1024 values
+      for (int i = threadIdx.x; i < 2 * p.l; i += kThreadsGemm)
+        if (s_amax[i] > 0.0f) atomic_max_nonneg(&p.amax[i], s_amax[i]);
     }
   }
   if (warp == 1) {

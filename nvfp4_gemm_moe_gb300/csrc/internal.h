@@ -12,7 +12,15 @@ enum Fmt : int { kMXFP8 = 0, kNVFP4 = 1 };
 // nearest even, saturating), without block scales; E2M1 packs two values per byte, element 2j
 // in the low nibble.
 enum OutKind : int { kOutNone = 0, kOutF32 = 1, kOutBF16 = 2, kOutE4M3 = 3, kOutF16 = 4, kOutE2M1 = 5 };
-enum EpiKind : int { kEpiDense = 0, kEpiGroupedBF16 = 1, kEpiGroupedFP8 = 2 };
+enum EpiKind : int {
+  kEpiDense = 0,        // C + global amax
+  kEpiGroupedBF16 = 1,  // grouped sReLU, float D (bf16 / f16 / f32) + per-expert amax
+  kEpiGroupedFP8 = 2,   // grouped sReLU, E4M3 D with row and column scale factors
+  kEpiDswigluF = 3,     // grouped dSwiGLU backward, float D + per-expert (|ab|, |dswiglu|) amax
+  kEpiDswigluFP8 = 4    // grouped dSwiGLU backward, E4M3 D with row and column scale factors
+};
+__host__ __device__ constexpr bool epi_is_dswiglu(int epi) { return epi == kEpiDswigluF || epi == kEpiDswigluFP8; }
+__host__ __device__ constexpr bool epi_has_fp8_d(int epi) { return epi == kEpiGroupedFP8 || epi == kEpiDswigluFP8; }
 
 // Everything a GEMM kernel needs besides the two tensor maps.
 struct GemmParams {
@@ -48,6 +56,11 @@ struct GemmParams {
   int sfd_row_kt;        // ceil(n / 128): atoms along N of SFD_row
   int sfd_col_mt;        // ceil(n / 128): 128-row groups of SFD_col
   int sfd_col_kt;        // ceil(valid_m / 128): atoms along M of SFD_col
+  // dSwiGLU backward: C is an input of 2N columns (32-column input / gate blocks), D is 2N wide
+  const void* c_in;
+  int c_in_kind;         // OutKind of C (f32 / bf16 / f16 / E4M3 values)
+  const float* beta;     // per-expert scale of C
+  float* dprob;          // (valid_m,) accumulated with atomic adds
   // device error word (workspace)
   uint32_t* err;
 };
@@ -70,6 +83,12 @@ cudaError_t launch_gemm_grouped(const GemmConfig& cfg, const CUtensorMap& tmap_a
 // `max_pairs` clusters.
 cudaError_t launch_gemm_pair(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                              const GemmParams& p, int max_pairs, cudaStream_t stream);
+
+// The dSwiGLU backward epilogue kernels (one-CTA and CTA-pair tiles).
+cudaError_t launch_gemm_dswiglu(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                                const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_pair_dswiglu(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                                     const GemmParams& p, int max_pairs, cudaStream_t stream);
 
 // Launches the block quantiser.
 cudaError_t launch_quantize(int fmt, const float* x, int64_t batch, int64_t rows, int64_t k, uint8_t* q,

@@ -324,6 +324,16 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Two E4M3 codes (byte 0 = first element) to two fp32 values (exact).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t codes) {
+  float2 r;
+  asm("{\n\t.reg .b32 h;\n\t.reg .b16 l, u;\n\tcvt.rn.f16x2.e4m3x2 h, %2;\n\tmov.b32 {l, u}, h;\n\t"
+      "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "h"(codes));
+  return r;
+}
+
 // Two fp32 -> packed E2M1 nibbles (round to nearest even, saturate to +-6); `lo` in bits 0-3.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
   uint32_t r;

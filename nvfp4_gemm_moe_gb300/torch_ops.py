@@ -8,8 +8,8 @@ from __future__ import annotations
 import torch
 
 from . import (BF16, E2M1, E4M3, F16, F32, FORMATS, bsg_gemm_amax, bsg_grouped_discrete_workspace_size,
-               bsg_grouped_gemm_srelu, bsg_grouped_gemm_srelu_discrete, bsg_quantize_mx, bsg_sf_bytes,
-               bsg_workspace_size)
+               bsg_grouped_gemm_dswiglu, bsg_grouped_gemm_srelu, bsg_grouped_gemm_srelu_discrete, bsg_quantize_mx,
+               bsg_sf_bytes, bsg_workspace_size)
 
 
 def new_workspace(device="cuda") -> torch.Tensor:
@@ -125,4 +125,38 @@ def grouped_gemm_srelu_discrete(a, b_ptrs, sfa, sfb_ptrs, fmt: str, padded_offse
                                     prob, tanh_clamp_scale, norm_const, out["c"], ck, out["d"], out.get("d_col"), dk,
                                     out.get("sfd_row"), out.get("sfd_col"), out.get("amax"), workspace,
                                     stream=stream, **opts)
+    return out
+
+
+def grouped_gemm_dswiglu(a, b, sfa, sfb, fmt: str, padded_offsets, alpha, beta, prob, c, n: int, k: int,
+                         c_dtype=None, d_dtype="bf16", norm_const=None, outputs=None, workspace=None, stream=None,
+                         **opts):
+    """dSwiGLU backward over the grouped GEMM.  ``c`` (valid_m, 2n) is the stored forward
+    intermediate (a bf16 / f16 / f32 tensor, or uint8 E4M3 codes with c_dtype="e4m3").  Returns a
+    dict: d_row, dprob (fresh zeros unless given: the call adds into it) and amax (L, 2) for
+    d_dtype "bf16" / "f16" / "f32", or d_row, d_col, sfd_row, sfd_col and dprob for "e4m3"."""
+    ab, sfd, v = FORMATS[fmt]
+    dev = a.device
+    valid_m = a.shape[0] if a.dim() == 2 else a.shape[1]
+    num_experts = padded_offsets.numel()
+    ck = _OUT_KINDS[c_dtype] if c_dtype is not None else _OUT_KINDS[c.dtype]
+    out = dict(outputs or {})
+    out.setdefault("dprob", torch.zeros(valid_m, dtype=torch.float32, device=dev))
+    if d_dtype in ("bf16", "f16", "f32"):
+        dk = _OUT_KINDS[d_dtype]
+        out.setdefault("d_row", _out_tensor(dk, valid_m, 2 * n, None, dev))
+        out.setdefault("amax", torch.empty((num_experts, 2), dtype=torch.float32, device=dev))
+    else:
+        dk = E4M3
+        out.setdefault("d_row", torch.empty((valid_m, 2 * n), dtype=torch.uint8, device=dev))
+        out.setdefault("d_col", torch.empty((valid_m, 2 * n), dtype=torch.uint8, device=dev))
+        out.setdefault("sfd_row", torch.empty(bsg_sf_bytes(1, valid_m, 2 * n, 32), dtype=torch.uint8, device=dev))
+        out.setdefault("sfd_col", torch.empty(bsg_sf_bytes(1, 2 * n, valid_m, 32), dtype=torch.uint8, device=dev))
+        if norm_const is None:
+            norm_const = torch.ones(1, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(dev)
+    bsg_grouped_gemm_dswiglu(a, b, sfa, sfb, ab, sfd, v, valid_m, n, k, num_experts, padded_offsets, alpha, beta,
+                             prob, c, ck, norm_const, out["d_row"], out.get("d_col"), dk, out.get("sfd_row"),
+                             out.get("sfd_col"), out["dprob"], out.get("amax"), workspace, stream=stream, **opts)
     return out

@@ -9,6 +9,11 @@ The acceptance rules (derived from the arithmetic; the reasoning is in the desig
 * bf16 D:  |D - ref| <= 1 bf16 ulp(ref) + prob * 2|C_ref| * tolC + 2^-20 |ref|, i.e. the
            one-ulp rule plus the C tolerance carried through d(r^2) = 2r dr (the clamp's
            derivative is smaller) and fp32 epilogue rounding;
+* dSwiGLU D (ab, dswiglu): the ref bound carried through the (linear in ref) epilogue, plus
+           the fp32 epilogue: a relative 2^-20 (1 + |gate|) for the fast exponential (its error
+           grows with the argument) and division, applied to each factor so the cancellation in
+           1 + gate (1 - sigmoid) is covered; then one ulp of the output type;
+* dprob:   the carried ref bound plus fp32 summation over the kernel's partial sums;
 * E4M3 D / D_col: codes equal, except a neighbouring code where the oracle's pre-quantised
            value lies within max(1e-5 relative, carried C tolerance) of the rounding boundary;
            a block scale may differ by one code where the oracle's block amax lies that close to
@@ -185,3 +190,44 @@ def check_e4m3_blocks(codes_gpu, sf_gpu, d_ref, d_tol, nc: float, axis: int, wha
         if not np.all(err <= bound * (1 + 1e-9)):
             raise AssertionError(f"{what}: values of re-scaled blocks outside half an E4M3 ulp")
     return int(diff_sf.sum()), int(mism.sum())
+
+
+def dswiglu_tolerances(ref_out, ref_tol, prob):
+    """Absolute bounds (float64, (valid_m, N) each) on the fp32 ab and dswiglu values, from the
+    oracle's exact x, gate and ref and the ref bound ``ref_tol``."""
+    p = np.asarray(prob, np.float64).reshape(-1, 1)
+    x, g, ref = ref_out["x"], ref_out["gate"], ref_out["ref"]
+    sig = 1.0 / (1.0 + np.exp(-np.clip(g, -700, 700)))
+    sw = g * sig
+    h = 1.0 + g * (1.0 - sig)
+    eps = 2.0 ** -20 * (1.0 + np.abs(g))
+    tol_ab = p * np.abs(sw) * ref_tol + eps * np.abs(ref_out["ab"]) + 1e-30
+    base = np.abs(ref * p * x * sig)
+    tol_dsw = p * np.abs(x * sig * h) * ref_tol + base * eps * (1.0 + np.abs(h) + np.abs(g)) + 1e-30
+    return tol_ab, tol_dsw
+
+
+def check_float_out(got, ref, tol, kind: str, what="D"):
+    """bf16 / f16 / f32 output: |got - ref| <= one ulp of the output type (none for f32) + tol."""
+    got = np.asarray(got, dtype=np.float64)
+    ulp = formats.bf16_ulp(ref) if kind == "bf16" else formats.f16_ulp(ref) if kind == "f16" else 0.0
+    err = np.abs(got - ref)
+    bad = ~(err <= ulp + tol)
+    if bad.any():
+        i = np.flatnonzero(bad.ravel())[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first gpu={got.ravel()[i]} "
+                             f"ref={np.asarray(ref).ravel()[i]} tol={np.broadcast_to(tol, np.shape(ref)).ravel()[i]}")
+
+
+def dprob_tolerance(ref_out, ref_tol, terms_per_partial: int, partials: int):
+    """Bound on the fp32 dprob: the carried ref bound, the epilogue's relative error and the
+    rounding of a sum of ``terms_per_partial`` terms per partial and ``partials`` partial sums
+    added in any order."""
+    x, g, ref = ref_out["x"], ref_out["gate"], ref_out["ref"]
+    sig = 1.0 / (1.0 + np.exp(-np.clip(g, -700, 700)))
+    sw = g * sig
+    terms = np.abs(sw * x * ref)
+    eps = 2.0 ** -20 * (1.0 + np.abs(g))
+    depth = terms_per_partial + partials + 4
+    return (np.sum(np.abs(sw * x) * ref_tol, axis=1) + np.sum(eps * terms, axis=1) +
+            depth * 2.0 ** -23 * np.sum(terms, axis=1) + 1e-30)

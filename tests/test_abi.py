@@ -150,6 +150,36 @@ def test_discrete_validation():
     assert st in (OK, ARCH, CUDA)
 
 
+def _dsw(**kw):
+    a = dict(a=P, b=P, sfa=P, sfb=P, ab=bsg.E4M3, sf=bsg.SF_UE8M0, v=32, vm=512, n=256, k=256, L=2, offs=P,
+             alpha=P, beta=P, prob=P, c=P, ck=bsg.BF16, nc=None, d=P, dcol=None, dk=bsg.BF16, sfr=None, sfc=None,
+             dprob=P, amax=P, ws=P, wsb=256)
+    a.update(kw)
+    return bsg.raw_status("bsg_grouped_gemm_dswiglu", a["a"], a["b"], a["sfa"], a["sfb"], a["ab"], a["sf"], a["v"],
+                          a["vm"], a["n"], a["k"], a["L"], a["offs"], a["alpha"], a["beta"], a["prob"], a["c"],
+                          a["ck"], a["nc"], a["d"], a["dcol"], a["dk"], a["sfr"], a["sfc"], a["dprob"], a["amax"],
+                          _opts(), a["ws"], a["wsb"], None)
+
+
+def test_dswiglu_validation():
+    assert _dsw(c=None) == INVALID                       # the forward intermediate is an input
+    assert _dsw(beta=None) == INVALID and _dsw(dprob=None) == INVALID
+    assert _dsw(n=48) == INVALID                         # 32-column input / gate blocks
+    assert _dsw(L=513) == INVALID                        # 2 * L amax values in shared memory
+    assert _dsw(amax=None) == INVALID                    # float D needs the (L, 2) amax
+    assert _dsw(dk=bsg.E4M3) == INVALID                  # E4M3 D needs d_col, SFD and norm_const
+    assert _dsw(dk=bsg.E4M3, dcol=P, sfr=P, sfc=P, nc=P, ab=bsg.E2M1, sf=bsg.SF_UE4M3, v=16) == UNSUPPORTED
+    assert _dsw(ck=bsg.E2M1) == UNSUPPORTED
+    assert _dsw(dk=bsg.E5M2) == UNSUPPORTED
+    assert _dsw(dprob=P + 2) == ALIGN
+    assert _dsw(c=P + 8) == ALIGN
+    assert _dsw(wsb=16) == WORKSPACE
+    st = _dsw()
+    assert st in (OK, ARCH, CUDA)
+    st = _dsw(dk=bsg.E4M3, dcol=P, sfr=P, sfc=P, nc=P, amax=None, ck=bsg.E4M3)
+    assert st in (OK, ARCH, CUDA)
+
+
 def test_noalloc_validation():
     def call(**kw):
         a = dict(a=P, c=P, amax=P, n=256)
