@@ -118,6 +118,7 @@ def run_ours(args, rank, world, local_rank):
     wl = W.ALL[args.workload]
     stream = torch.cuda.current_stream()
     is_dense = isinstance(wl, W.Dense)
+    is_dsw = isinstance(wl, W.GroupedDswiglu)
     fmt = wl.fmt
     flops = wl.flops
 
@@ -149,11 +150,23 @@ def run_ours(args, rank, world, local_rank):
         alpha = torch.from_numpy(wl.alpha()).to(dev)
         prob = torch.from_numpy(wl.prob()).to(dev)
         nc = torch.ones(1, dtype=torch.float32, device=dev)
-        outs = {"c": torch.empty((wl.valid_m, wl.n), dtype=torch.bfloat16, device=dev)}
+        if is_dsw:
+            # the stored forward intermediate (valid_m, 2N) in bf16 and the per-expert scale of it
+            c_pin = torch.from_numpy(wl.c_rows()).to(torch.bfloat16).pin_memory()
+            c_in = c_pin.to(dev)
+            beta = torch.from_numpy(wl.beta()).to(dev)
+            outs = {"dprob": torch.zeros(wl.valid_m, dtype=torch.float32, device=dev)}
+        else:
+            outs = {"c": torch.empty((wl.valid_m, wl.n), dtype=torch.bfloat16, device=dev)}
 
     def gemm():
         if is_dense:
             torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, wl.m, wl.n, wl.k, wl.l, c=c, amax=amax, workspace=ws)
+        elif is_dsw:
+            outs["dprob"].zero_()  # the call adds each row's sum into dprob
+            outs.update(torch_ops.grouped_gemm_dswiglu(qa[0], qb, sfa, sfb, fmt, offs, alpha, beta, prob, c_in, wl.n,
+                                                       wl.k, d_dtype=wl.d_dtype, norm_const=nc, outputs=outs,
+                                                       workspace=ws))
         else:
             # the first call allocates D, amax / D_col, SFD_row, SFD_col; later calls reuse them
             outs.update(torch_ops.grouped_gemm_srelu(qa[0], qb, sfa, sfb, fmt, offs, alpha, prob, wl.n, wl.k,
@@ -203,34 +216,26 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------- end to end through the C ABI from pinned host buffers
     e2e_steps = max(3, min(args.steps, 20))
-    c_out = c if is_dense else outs["c"]
-    c_host = torch.empty(c_out.shape, dtype=c_out.dtype, pin_memory=True)
-    amax_t = amax if is_dense else None
-    res_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
-    h2d = a_pin.numel() * 4 + b_pin.numel() * 4
-    d2h = c_out.numel() * c_out.element_size() + 4
-    if not is_dense:
-        if wl.d_dtype == "bf16":
-            d_out = outs["d"]
-        else:
-            d_out = outs["d"]
-        d_host = torch.empty(d_out.shape, dtype=d_out.dtype, pin_memory=True)
-        d2h += d_out.numel() * d_out.element_size()
+    inputs = [(a_d, a_pin), (b_d, b_pin)] + ([(c_in, c_pin)] if is_dsw else [])
+    if is_dense:
+        results = [c, amax]
+    elif is_dsw:
+        results = [outs["d_row"], outs["dprob"]] + ([outs["amax"]] if "amax" in outs else [outs["sfd_row"]])
+    else:
+        results = [outs["c"], outs["d"]] + ([outs["amax"][:1]] if "amax" in outs else [])
+    hosts = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
+    h2d = sum(p.numel() * p.element_size() for _, p in inputs)
+    d2h = sum(r.numel() * r.element_size() for r in results)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(e2e_steps):
-        a_d.copy_(a_pin, non_blocking=True)
-        b_d.copy_(b_pin, non_blocking=True)
+        for dst, src in inputs:
+            dst.copy_(src, non_blocking=True)
         step()
-        c_host.copy_(c_out, non_blocking=True)
-        if is_dense:
-            res_host.copy_(amax_t, non_blocking=True)
-        else:
-            d_host.copy_(d_out, non_blocking=True)
-            res_host.copy_(outs["amax"][:1] if "amax" in outs else outs["sfd_row"][:4].view(torch.float32),
-                           non_blocking=True)
+        for h, r in zip(hosts, results):
+            h.copy_(r, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -296,6 +301,11 @@ def _config(wl):
                 "c_dtype": wl.c_dtype, "flops_per_step": wl.flops,
                 "l2": "no flush: fp32 inputs of 2 x %.2f GB exceed L2" % (wl.l * wl.m * wl.k * 4 / 1e9),
                 "step": "quantise A + quantise B + GEMM/amax"}
+    if isinstance(wl, W.GroupedDswiglu):
+        return {"workload": wl.name, "format": wl.fmt, "experts": wl.experts, "n": wl.n, "k": wl.k,
+                "valid_m": wl.valid_m, "routed_rows": wl.routed_rows, "c_dtype": wl.c_dtype, "d_dtype": wl.d_dtype,
+                "flops_per_step": wl.flops, "l2": "no flush: fp32 inputs exceed L2",
+                "step": "quantise A + quantise B + grouped GEMM/dSwiGLU backward (C read, D and dprob written)"}
     return {"workload": wl.name, "format": wl.fmt, "experts": wl.experts, "n": wl.n, "k": wl.k,
             "valid_m": wl.valid_m, "routed_rows": wl.routed_rows, "d_dtype": wl.d_dtype, "tanh_clamp": wl.tanh_clamp,
             "flops_per_step": wl.flops, "l2": "no flush: fp32 inputs exceed L2",
@@ -317,7 +327,7 @@ def oracle_rows(wl, requested=0):
 
 
 def run_reference(args):
-    from oracle import gemm as og, quantize as oq
+    from oracle import dswiglu as od, gemm as og, quantize as oq
     wl = W.ALL[args.workload]
     cores = os.cpu_count() or 1
     step_times, sample_flops = [], 0.0
@@ -340,6 +350,11 @@ def run_reference(args):
         qa, sfa = oq.quantize(a, wl.fmt)
         qb, sfb = oq.quantize(b, wl.fmt)
         o = np.array([len(rows)], np.int32)
+        if isinstance(wl, W.GroupedDswiglu):
+            c_vals = wl.c_rows(rows)  # fp32 draws; the GPU arm stores them as bf16
+            od.grouped_dswiglu(qa[0], qb, sfa, sfb, wl.fmt, o, wl.alpha()[:1], wl.beta()[:1], wl.prob()[:len(rows)],
+                               c_vals, wl.k, wl.n, d_fp8=(wl.d_dtype == "e4m3"))
+            return 2.0 * len(rows) * wl.n * wl.k
         og.grouped_srelu(qa[0], qb, sfa, sfb, wl.fmt, o, wl.alpha()[:1], wl.prob()[:len(rows)], wl.k, wl.n,
                          tanh_clamp_scale=wl.tanh_clamp, d_fp8=(wl.d_dtype == "e4m3"))
         del g, offs

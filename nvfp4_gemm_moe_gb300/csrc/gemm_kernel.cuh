@@ -38,8 +38,9 @@ namespace bsg {
 constexpr int kThreadsGemm = 448;  // producer, MMA issuer, eight epilogue and four scale-factor warps
 constexpr int kTileM = 128;
 constexpr int kTileKBytes = 128;  // one 128-byte swizzle row of K per stage
+constexpr int kXposeBlockBytes = 32 * 64;  // a warp's 32 rows x 64 bytes transpose block
 
-template <int FMT, int BN>
+template <int FMT, int BN, int EPI = kEpiDense>
 struct GemmTraits {
   static constexpr int kElemsPerKTile = FMT == kMXFP8 ? 128 : 256;
   static constexpr int kMmaK = FMT == kMXFP8 ? 32 : 64;  // elements per tcgen05.mma (32 bytes)
@@ -69,8 +70,11 @@ struct GemmTraits {
   static constexpr int kBarBytes = 1024;
   static constexpr int kOffsetsBytes = 4096;  // padded_offsets of up to 1024 experts (grouped)
   static constexpr int kAmaxBytes = 4096;     // per-expert amax staging (grouped bf16 D)
+  // grouped epilogues: one 32-row x 64-byte transpose block per epilogue warp
+  static constexpr int kXposeBytes = EPI == kEpiDense ? 0 : 8 * kXposeBlockBytes;
   // as many stages as shared memory and the TMEM scale-factor slots allow, at most six
-  static constexpr int kStagesSmem = (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes) / kStageBytes;
+  static constexpr int kStagesSmem =
+      (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
   static constexpr int kStagesTmem = (512 - kSfBase) / kSfStride;
   static constexpr int kStages = kStagesSmem < kStagesTmem ? (kStagesSmem < 6 ? kStagesSmem : 6)
                                                            : (kStagesTmem < 6 ? kStagesTmem : 6);
@@ -80,7 +84,7 @@ struct GemmTraits {
                                    : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM budget");
   static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarBytes +
-                                    kOffsetsBytes + kAmaxBytes;
+                                    kOffsetsBytes + kAmaxBytes + kXposeBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 
   // Instruction descriptor: A/B formats (bits 7-12), K-major A and B, N >> 3 (bits 17-22),
@@ -184,6 +188,111 @@ __device__ __forceinline__ void store_row32(void* base, uint64_t off, int kind, 
   }
 }
 
+// Byte offset of 16-byte unit `unit` (0..3) of row `row` (0..31) in a warp's 32 x 64-byte
+// transpose block.  The unit index is XORed with (row / 2) % 4, so that eight threads writing
+// unit u of eight consecutive rows, and eight threads reading the four units of two consecutive
+// rows, each touch eight distinct 16-byte bank groups (no bank conflicts either way).
+__device__ __forceinline__ uint32_t xpose_off(int row, int unit) {
+  return static_cast<uint32_t>(row * 64 + ((unit ^ ((row >> 1) & 3)) << 4));
+}
+
+// Stores 64 bytes per row for the warp's 32 rows row0 .. row0 + 31 (this thread's row holds the
+// four 16-byte units u): row r goes to base + (row0 + r) * pitch + col_byte.  The rows pass
+// through the warp's transpose block, so each global store instruction writes 8 rows x 64
+// contiguous bytes (whole sectors) instead of 32 rows x 16 bytes.  Units at or past byte
+// `limit_byte` of a row are not written.
+__device__ __forceinline__ void store_rows64(uint8_t* s_blk, void* base, uint64_t pitch, int row0, int col_byte,
+                                             int limit_byte, const uint4 (&u)[4], int lane) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(s_blk + xpose_off(lane, j)) = u[j];
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2), j = lane & 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(s_blk + xpose_off(r, j));
+    if (col_byte + j * 16 < limit_byte)
+      *reinterpret_cast<uint4*>(static_cast<char*>(base) + static_cast<uint64_t>(row0 + r) * pitch + col_byte +
+                                j * 16) = v;
+  }
+  __syncwarp();
+}
+
+// As store_rows64 for 32 bytes per row (two 16-byte units, E4M3 blocks): the unit index is
+// XORed with (row / 4) % 2, and each global store instruction writes 16 rows x 32 bytes.
+__device__ __forceinline__ uint32_t xpose32_off(int row, int unit) {
+  return static_cast<uint32_t>(row * 32 + ((unit ^ ((row >> 2) & 1)) << 4));
+}
+
+__device__ __forceinline__ void store_rows32(uint8_t* s_blk, void* base, uint64_t pitch, int row0, int col_byte,
+                                             const uint4& u0, const uint4& u1, int lane) {
+  *reinterpret_cast<uint4*>(s_blk + xpose32_off(lane, 0)) = u0;
+  *reinterpret_cast<uint4*>(s_blk + xpose32_off(lane, 1)) = u1;
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int r = it * 16 + (lane >> 1), j = lane & 1;
+    const uint4 v = *reinterpret_cast<const uint4*>(s_blk + xpose32_off(r, j));
+    *reinterpret_cast<uint4*>(static_cast<char*>(base) + static_cast<uint64_t>(row0 + r) * pitch + col_byte + j * 16) = v;
+  }
+  __syncwarp();
+}
+
+// The inverse, in two steps: fetch_rows64 loads 64 bytes per row of the warp's 32 rows
+// (streaming loads, whole sectors per instruction) into v; xpose_rows64 passes them through the
+// transpose block and returns this thread's row as four 16-byte units.  Several fetches may be
+// in flight before their transposes.
+__device__ __forceinline__ void fetch_rows64(const void* base, uint64_t pitch, int row0, int col_byte, uint4 (&v)[4],
+                                             int lane) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2), j = lane & 3;
+    v[it] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const char*>(base) +
+                                                  static_cast<uint64_t>(row0 + r) * pitch + col_byte + j * 16));
+  }
+}
+
+__device__ __forceinline__ void xpose_rows64(uint8_t* s_blk, const uint4 (&v)[4], uint4 (&u)[4], int lane) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 8 + (lane >> 2), j = lane & 3;
+    *reinterpret_cast<uint4*>(s_blk + xpose_off(r, j)) = v[it];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) u[j] = *reinterpret_cast<const uint4*>(s_blk + xpose_off(lane, j));
+  __syncwarp();
+}
+
+// Stores this thread's 32 fp32 values v (one row chunk) as f32 / bf16 / f16 at element column
+// col0 of the warp's rows row0 .. row0 + 31 of a row-major array of `ld` elements per row and
+// `n` valid columns, through the transpose block (see store_rows64).
+__device__ __forceinline__ void store_block_coalesced(uint8_t* s_blk, void* base, int kind, int ld, int n, int row0,
+                                                      int col0, const float (&v)[32], int lane) {
+  if (kind == kOutF32) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint4 u[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        u[j] = make_uint4(__float_as_uint(v[16 * h + 4 * j]), __float_as_uint(v[16 * h + 4 * j + 1]),
+                          __float_as_uint(v[16 * h + 4 * j + 2]), __float_as_uint(v[16 * h + 4 * j + 3]));
+      store_rows64(s_blk, base, static_cast<uint64_t>(ld) * 4, row0, (col0 + 16 * h) * 4, n * 4, u, lane);
+    }
+  } else {
+    const bool bf = kind == kOutBF16;
+    uint4 u[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float* w = v + 8 * j;
+      u[j] = bf ? make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                             pack_bf16x2(w[6], w[7]))
+                : make_uint4(pack_f16x2(w[0], w[1]), pack_f16x2(w[2], w[3]), pack_f16x2(w[4], w[5]),
+                             pack_f16x2(w[6], w[7]));
+    }
+    store_rows64(s_blk, base, static_cast<uint64_t>(ld) * 2, row0, col0 * 2, n * 2, u, lane);
+  }
+}
+
 __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
   atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
 }
@@ -265,10 +374,11 @@ __device__ __forceinline__ void epilogue_dense_bf16_early(const GemmParams& p, i
 // dcol0 .. dcol0 + 31 of a row-major D that is n_d wide (n_d a multiple of 32), values already
 // multiplied by norm_const.  D_row takes one E8M0 scale per row and block (this thread's 32
 // values), D_col one per column and 32-row block (the warp's 32 lanes are 32 consecutive rows).
-// s_inv: 32 floats of shared memory owned by this warp.
+// s_inv: 32 floats of shared memory owned by this warp; s_blk: the warp's transpose block (the
+// code rows are stored coalesced through it).
 __device__ __forceinline__ void store_e4m3_block(const GemmParams& p, int row, int dcol0, int n_d, const float (&d)[32],
-                                                 int lane, float* s_inv) {
-  const uint64_t rc = static_cast<uint64_t>(row) * n_d + dcol0;
+                                                 int lane, float* s_inv, uint8_t* s_blk) {
+  const int row0 = row - lane;
   float bmax = 0.0f;
 #pragma unroll
   for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, fabsf(d[j]));
@@ -281,9 +391,8 @@ __device__ __forceinline__ void store_e4m3_block(const GemmParams& p, int row, i
     const uint32_t hi = cvt_e4m3x2(__fmul_rn(d[4 * j + 2], inv_r), __fmul_rn(d[4 * j + 3], inv_r));
     q[j] = lo | (hi << 16);
   }
-  uint8_t* drow = reinterpret_cast<uint8_t*>(p.d) + rc;
-  store16(drow, q[0], q[1], q[2], q[3]);
-  store16(drow + 16, q[4], q[5], q[6], q[7]);
+  store_rows32(s_blk, p.d, static_cast<uint64_t>(n_d), row0, dcol0, make_uint4(q[0], q[1], q[2], q[3]),
+               make_uint4(q[4], q[5], q[6], q[7]), lane);
   // one byte per block: a tile need not start on a four-block word of the SF layout; the row's
   // last block also zeroes the padding blocks of its word
   const int nb = dcol0 >> 5;
@@ -309,30 +418,24 @@ __device__ __forceinline__ void store_e4m3_block(const GemmParams& p, int row, i
     q[j] = lo | (hi << 16);
   }
   __syncwarp();  // the next block overwrites s_inv
-  uint8_t* dcol = reinterpret_cast<uint8_t*>(p.d_col) + rc;
-  store16(dcol, q[0], q[1], q[2], q[3]);
-  store16(dcol + 16, q[4], q[5], q[6], q[7]);
+  store_rows32(s_blk, p.d_col, static_cast<uint64_t>(n_d), row0, dcol0, make_uint4(q[0], q[1], q[2], q[3]),
+               make_uint4(q[4], q[5], q[6], q[7]), lane);
 }
 
-// Loads 32 consecutive elements of `kind` (f32, bf16, f16 or E4M3) at element `off` of `base`
-// as fp32, with streaming loads (the dSwiGLU input C is read once).  `off` is a multiple of 32.
-__device__ __forceinline__ void load_row32(const void* base, uint64_t off, int kind, float (&v)[32]) {
+// Decodes 16-byte units of `kind` (bf16, f16, f32 or E4M3 values) into fp32 v[first ..].
+__device__ __forceinline__ void decode_units(int kind, const uint4 (&u)[4], float* v) {
   if (kind == kOutF32) {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 q = __ldcs(src + j);
-      v[4 * j] = q.x;
-      v[4 * j + 1] = q.y;
-      v[4 * j + 2] = q.z;
-      v[4 * j + 3] = q.w;
+    for (int j = 0; j < 4; ++j) {
+      v[4 * j] = __uint_as_float(u[j].x);
+      v[4 * j + 1] = __uint_as_float(u[j].y);
+      v[4 * j + 2] = __uint_as_float(u[j].z);
+      v[4 * j + 3] = __uint_as_float(u[j].w);
     }
   } else if (kind == kOutE4M3) {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(base) + off);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const uint4 q = __ldcs(src + j);
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w[i] & 0xffffu));
@@ -344,12 +447,10 @@ __device__ __forceinline__ void load_row32(const void* base, uint64_t off, int k
       }
     }
   } else {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off);
     const bool bf = kind == kOutBF16;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint4 q = __ldcs(src + j);
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+      const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (bf) {
@@ -365,6 +466,64 @@ __device__ __forceinline__ void load_row32(const void* base, uint64_t off, int k
   }
 }
 
+// Loads the input block x and the gate block g (32 values each, this thread's row) of ref
+// columns col0 .. col0 + 31 from C (valid_m, 2N) for the warp's rows row0 .. row0 + 31: the
+// 64 * element-size contiguous bytes of each row in 64-byte pieces, fetched coalesced and
+// transposed through the warp's block (see fetch_rows64 / xpose_rows64).
+__device__ __forceinline__ void load_dswiglu_c(uint8_t* s_blk, const GemmParams& p, int row0, int col0,
+                                               float (&x)[32], float (&g)[32], int lane) {
+  const int kind = p.c_in_kind;
+  uint4 v0[4], v1[4], u[4];
+  if (kind == kOutE4M3) {  // one piece: 32 input codes then 32 gate codes
+    fetch_rows64(p.c_in, static_cast<uint64_t>(2 * p.n), row0, 2 * col0, v0, lane);
+    xpose_rows64(s_blk, v0, u, lane);
+    float t[64];
+    decode_units(kind, u, t);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      x[j] = t[j];
+      g[j] = t[32 + j];
+    }
+  } else if (kind == kOutF32) {  // four pieces of 16 values: x low, x high, g low, g high
+    const uint64_t pitch = static_cast<uint64_t>(2 * p.n) * 4;
+    const int b0 = 2 * col0 * 4;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float* dst = h == 0 ? x : g;
+      fetch_rows64(p.c_in, pitch, row0, b0 + 128 * h, v0, lane);
+      fetch_rows64(p.c_in, pitch, row0, b0 + 128 * h + 64, v1, lane);
+      xpose_rows64(s_blk, v0, u, lane);
+      decode_units(kind, u, dst);
+      xpose_rows64(s_blk, v1, u, lane);
+      decode_units(kind, u, dst + 16);
+    }
+  } else {  // 16-bit: two pieces, the input block and the gate block
+    const uint64_t pitch = static_cast<uint64_t>(2 * p.n) * 2;
+    fetch_rows64(p.c_in, pitch, row0, 4 * col0, v0, lane);
+    fetch_rows64(p.c_in, pitch, row0, 4 * col0 + 64, v1, lane);
+    xpose_rows64(s_blk, v0, u, lane);
+    decode_units(kind, u, x);
+    xpose_rows64(s_blk, v1, u, lane);
+    decode_units(kind, u, g);
+  }
+}
+
+// Prefetches into L2 the C lines the warp's chunks of a dSwiGLU tile will read (row `row`,
+// ref columns col_base + 32 c for c = c_first, c_first + c_step, ...): issued before the wait for
+// the tile's accumulator, so C streams in while the tile's MMAs run.
+template <int BN>
+__device__ __forceinline__ void prefetch_dswiglu_c(const GemmParams& p, int row, int col_base, int c_first,
+                                                   int c_step) {
+  const int es = p.c_in_kind == kOutF32 ? 4 : p.c_in_kind == kOutE4M3 ? 1 : 2;
+  const char* base = static_cast<const char*>(p.c_in) + static_cast<uint64_t>(row) * (2 * p.n) * es;
+  for (int c = c_first; c < BN / 32; c += c_step) {
+    const int col0 = col_base + c * 32;
+    if (col0 >= p.n) break;
+    const char* line = base + static_cast<uint64_t>(2 * col0) * es;  // 64 elements: input + gate block
+    for (int b = 0; b < 64 * es; b += 128) prefetch_l2(line + b);
+  }
+}
+
 // dSwiGLU backward epilogue of one tile for the rows of one warp ("Grouped GEMM + dSwiGLU
 // (SM100)", Step 2).  Accumulator chunk c (ref columns n0 .. n0 + 31, n0 = col_base + 32 c)
 // pairs with the input block at C columns 2 n0 .. 2 n0 + 31 and the gate block right after it;
@@ -377,17 +536,16 @@ template <int BN, bool kFP8>
 __device__ __forceinline__ void epilogue_tile_dswiglu(const GemmParams& p, int row, int col_base, uint32_t tmem_acc,
                                                       int lane, float alpha_g, float beta_g, float prob_r, float nc,
                                                       float& max_ab, float& max_dsw, int c_first, int c_step,
-                                                      float* s_inv) {
+                                                      float* s_inv, uint8_t* s_blk) {
   const int n_d = 2 * p.n;
+  const int row0 = row - lane;
   float dprob_part = 0.0f;
 #pragma unroll 1
   for (int c = c_first; c < BN / 32; c += c_step) {
     const int col0 = col_base + c * 32;
     if (col0 >= p.n) break;  // warp-uniform
-    const uint64_t off = static_cast<uint64_t>(row) * n_d + 2 * col0;  // input block; gate at off + 32
     float x[32], g[32];
-    load_row32(p.c_in, off, p.c_in_kind, x);
-    load_row32(p.c_in, off + 32, p.c_in_kind, g);
+    load_dswiglu_c(s_blk, p, row0, col0, x, g, lane);
     uint32_t r[32];
     tmem_ld_32x32b_x32(tmem_acc + c * 32, r);
     tmem_ld_wait(r);
@@ -410,16 +568,16 @@ __device__ __forceinline__ void epilogue_tile_dswiglu(const GemmParams& p, int r
         max_ab = fmaxf(max_ab, fabsf(x[j]));
         max_dsw = fmaxf(max_dsw, fabsf(g[j]));
       }
-      store_row32(p.d, off, p.d_kind, x, 2 * col0, n_d);
-      store_row32(p.d, off + 32, p.d_kind, g, 2 * col0 + 32, n_d);
+      store_block_coalesced(s_blk, p.d, p.d_kind, n_d, n_d, row0, 2 * col0, x, lane);
+      store_block_coalesced(s_blk, p.d, p.d_kind, n_d, n_d, row0, 2 * col0 + 32, g, lane);
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         x[j] = __fmul_rn(x[j], nc);
         g[j] = __fmul_rn(g[j], nc);
       }
-      store_e4m3_block(p, row, 2 * col0, n_d, x, lane, s_inv);
-      store_e4m3_block(p, row, 2 * col0 + 32, n_d, g, lane, s_inv);
+      store_e4m3_block(p, row, 2 * col0, n_d, x, lane, s_inv, s_blk);
+      store_e4m3_block(p, row, 2 * col0 + 32, n_d, g, lane, s_inv, s_blk);
     }
   }
   if (dprob_part != 0.0f) atomicAdd(&p.dprob[row], dprob_part);
@@ -453,7 +611,7 @@ __device__ __forceinline__ void fold_expert_max(float* s_amax, int g, float m1, 
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int row, int col_base, uint32_t tmem_acc,
                                               int lane, float alpha_g, float prob_r, float nc, float& run_max,
-                                              int c_first, int c_step, float* s_inv) {
+                                              int c_first, int c_step, float* s_inv, uint8_t* s_blk) {
   const bool row_ok = row < p.m;
   const float s_clamp = p.clamp_s;
   const float inv_s = s_clamp > 0.0f ? 1.0f / s_clamp : 0.0f;
@@ -476,7 +634,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
       }
     } else {
       float d[32];
-      const uint64_t rc = static_cast<uint64_t>(row) * p.n + col0;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float cv = alpha_g * __uint_as_float(r[j]);
@@ -484,23 +641,24 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
         d[j] = srelu_clamp(cv, prob_r, s_clamp, inv_s, p.tanh_approx);
       }
       // a chunk may run past N: 16-byte granules (N % 8 == 0 for 16-bit outputs, % 4 for fp32)
+      // C and float D pass through the warp's transpose block (coalesced, whole-sector stores)
       if (p.c_kind != kOutNone) {
         float cvals[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) cvals[j] = __uint_as_float(r[j]);
-        store_row32(p.c, rc, p.c_kind, cvals, col0, p.n);
+        store_block_coalesced(s_blk, p.c, p.c_kind, p.n, p.n, row - lane, col0, cvals, lane);
       }
       if (EPI == kEpiGroupedBF16) {
         // columns past N hold zeros (zero-filled B rows), so they cannot raise the maximum
 #pragma unroll
         for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(d[j]));
-        store_row32(p.d, rc, p.d_kind, d, col0, p.n);
+        store_block_coalesced(s_blk, p.d, p.d_kind, p.n, p.n, row - lane, col0, d, lane);
       } else {
         // D * norm_const once (rounding is monotonic, so the block maxima of the products are
         // norm_const times the block maxima of D, rounded); scaling by 2^-e is exact
 #pragma unroll
         for (int j = 0; j < 32; ++j) d[j] = __fmul_rn(d[j], nc);
-        store_e4m3_block(p, row, col0, p.n, d, lane, s_inv);
+        store_e4m3_block(p, row, col0, p.n, d, lane, s_inv, s_blk);
       }
     }
   }
@@ -577,7 +735,7 @@ template <int FMT, int BN, int EPI>
 __global__ void __launch_bounds__(kThreadsGemm, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ GemmParams p) {
-  using T = GemmTraits<FMT, BN>;
+  using T = GemmTraits<FMT, BN, EPI>;
   constexpr int S = T::kStages;
   constexpr int ACC = T::kAcc;
 
@@ -600,6 +758,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   int* bad_flag = const_cast<int*>(abort_flag) + 1;
   int32_t* s_offs = reinterpret_cast<int32_t*>(s_bar + T::kBarBytes);
   float* s_amax = reinterpret_cast<float*>(s_bar + T::kBarBytes + T::kOffsetsBytes);
+  uint8_t* s_xpose = s_bar + T::kBarBytes + T::kOffsetsBytes + T::kAmaxBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -791,9 +950,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     const float nc = epi_has_fp8_d(EPI) ? *p.norm_const : 1.0f;
     for (int t = blockIdx.x; !bad && t < p.num_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
+      const int row = tc.mt * kTileM + quad * 32 + lane;
+      if constexpr (epi_is_dswiglu(EPI)) prefetch_dswiglu_c<BN>(p, row, tc.nt * BN, half, 2);
       if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
-      const int row = tc.mt * kTileM + quad * 32 + lane;
       float alpha_g = 1.0f, prob_r = 0.0f;
       if (EPI != kEpiDense) {
         alpha_g = p.alpha[tc.l];
@@ -814,13 +974,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       if constexpr (epi_is_dswiglu(EPI)) {
         epilogue_tile_dswiglu<BN, EPI == kEpiDswigluFP8>(p, row, tc.nt * BN, tmem_acc, lane, alpha_g, p.beta[tc.l],
                                                          prob_r, nc, run_max, run_max2, half, 2,
-                                                         s_amax + (warp - 2) * 32);
+                                                         s_amax + (warp - 2) * 32,
+                                                         s_xpose + (warp - 2) * kXposeBlockBytes);
         release();
       } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
         epilogue_dense_bf16_early<BN>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
-                               s_amax + (warp - 2) * 32);
+                               s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * kXposeBlockBytes);
         release();
       }
       if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
@@ -860,7 +1021,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
 template <int FMT, int BN, int EPI>
 cudaError_t launch_gemm_t(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const GemmParams& p, int grid,
                           cudaStream_t stream) {
-  using T = GemmTraits<FMT, BN>;
+  using T = GemmTraits<FMT, BN, EPI>;
   auto kern = gemm_kernel<FMT, BN, EPI>;
   static bool attr_set[64] = {};  // per instantiation and device
   int dev = 0;

@@ -29,7 +29,7 @@
 
 namespace bsg {
 
-template <int FMT, int BN>
+template <int FMT, int BN, int EPI = kEpiDense>
 struct PairTraits {
   static_assert(BN == 256 || (BN == 224 && FMT == kMXFP8), "pair tile widths");
   static constexpr int kTileMPair = 256;
@@ -59,12 +59,15 @@ struct PairTraits {
   static constexpr int kBarBytes = 1024;
   static constexpr int kOffsetsBytes = 4096;
   static constexpr int kAmaxBytes = 4096;
-  static constexpr int kStagesSmem = (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes) / kStageBytes;
+  static constexpr int kXposeBytes = EPI == kEpiDense ? 0 : 8 * kXposeBlockBytes;  // grouped epilogues
+  static constexpr int kStagesSmem =
+      (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
   static constexpr int kStagesTmem = (512 - kSfBase) / kSfStride;
   static constexpr int kStages = kStagesSmem < kStagesTmem ? (kStagesSmem < 6 ? kStagesSmem : 6)
                                                            : (kStagesTmem < 6 ? kStagesTmem : 6);
   static_assert(kStages >= 3, "pipeline depth");
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kOffsetsBytes + kAmaxBytes;
+  static constexpr int kSmemBytes =
+      1024 + kStages * kStageBytes + kBarBytes + kOffsetsBytes + kAmaxBytes + kXposeBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // M = 256 across the pair (M >> 4 at bit 24), N = BN (N >> 3 at bit 17)
   static constexpr uint32_t kIdesc = (FMT == kMXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))
@@ -95,7 +98,7 @@ template <int FMT, int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ GemmParams p) {
-  using T = PairTraits<FMT, BN>;
+  using T = PairTraits<FMT, BN, EPI>;
   constexpr int S = T::kStages;
   constexpr int ACC = T::kAcc;
 
@@ -118,6 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   int* bad_flag = const_cast<int*>(abort_flag) + 1;
   int32_t* s_offs = reinterpret_cast<int32_t*>(s_bar + T::kBarBytes);
   float* s_amax = reinterpret_cast<float*>(s_bar + T::kBarBytes + T::kOffsetsBytes);
+  uint8_t* s_xpose = s_bar + T::kBarBytes + T::kOffsetsBytes + T::kAmaxBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -321,9 +325,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     const uint32_t empty_leader = mapa_shared(smem_u32(&tmem_empty[0]), 0);
     for (int t = pair_id; !bad && t < p.num_tiles; t += num_pairs) {
       const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
+      const int row = tc.mt * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
+      if constexpr (epi_is_dswiglu(EPI)) prefetch_dswiglu_c<BN>(p, row, tc.nt * BN, half, 2);
       if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
-      const int row = tc.mt * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
       float alpha_g = 1.0f, prob_r = 0.0f;
       if (EPI != kEpiDense) {
         alpha_g = p.alpha[tc.l];
@@ -345,13 +350,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       if constexpr (epi_is_dswiglu(EPI)) {
         epilogue_tile_dswiglu<BN, EPI == kEpiDswigluFP8>(p, row, tc.nt * BN, tmem_acc, lane, alpha_g, p.beta[tc.l],
                                                          prob_r, nc, run_max, run_max2, half, 2,
-                                                         s_amax + (warp - 2) * 32);
+                                                         s_amax + (warp - 2) * 32,
+                                                         s_xpose + (warp - 2) * kXposeBlockBytes);
         release();
       } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
         epilogue_dense_bf16_early<BN>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
-                               s_amax + (warp - 2) * 32);
+                               s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * kXposeBlockBytes);
         release();
       }
       if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
@@ -393,7 +399,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
 template <int FMT, int BN, int EPI>
 cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int max_pairs,
                                cudaStream_t stream) {
-  using T = PairTraits<FMT, BN>;
+  using T = PairTraits<FMT, BN, EPI>;
   auto kern = gemm_pair_kernel<FMT, BN, EPI>;
   static int resident_pairs[64] = {};  // per device; 0 = not queried yet
   int dev = 0;

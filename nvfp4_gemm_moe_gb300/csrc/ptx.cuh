@@ -54,6 +54,11 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
 
+// Prefetches the 128-byte line holding `ptr` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // Makes a tensor map that sits in global memory (written before the launch) visible to the
 // tensor-map proxy of the calling thread before its first TMA use.
 __device__ __forceinline__ void tmap_acquire(const CUtensorMap* tm) {
