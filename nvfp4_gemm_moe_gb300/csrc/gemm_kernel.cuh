@@ -200,9 +200,9 @@ __device__ __forceinline__ uint32_t xpose_off(int row, int unit) {
 // four 16-byte units u): row r goes to base + (row0 + r) * pitch + col_byte.  The rows pass
 // through the warp's transpose block, so each global store instruction writes 8 rows x 64
 // contiguous bytes (whole sectors) instead of 32 rows x 16 bytes.  Units at or past byte
-// `limit_byte` of a row are not written.
+// `limit_byte` of a row, and rows at or past row_end, are not written.
 __device__ __forceinline__ void store_rows64(uint8_t* s_blk, void* base, uint64_t pitch, int row0, int col_byte,
-                                             int limit_byte, const uint4 (&u)[4], int lane) {
+                                             int limit_byte, const uint4 (&u)[4], int lane, int row_end = 1 << 30) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(s_blk + xpose_off(lane, j)) = u[j];
   __syncwarp();
@@ -210,7 +210,7 @@ __device__ __forceinline__ void store_rows64(uint8_t* s_blk, void* base, uint64_
   for (int it = 0; it < 4; ++it) {
     const int r = it * 8 + (lane >> 2), j = lane & 3;
     const uint4 v = *reinterpret_cast<const uint4*>(s_blk + xpose_off(r, j));
-    if (col_byte + j * 16 < limit_byte)
+    if (col_byte + j * 16 < limit_byte && row0 + r < row_end)
       *reinterpret_cast<uint4*>(static_cast<char*>(base) + static_cast<uint64_t>(row0 + r) * pitch + col_byte +
                                 j * 16) = v;
   }
@@ -334,11 +334,12 @@ __device__ __forceinline__ void warp_colmax_scatter(float (&v)[32], int lane) {
 // Dense epilogue with bf16 C that gives the accumulator back early: this warp's chunks
 // (c_first, c_first + 2, ...) are read from TMEM, folded into the running |max| and packed to
 // bf16 in registers; then `release` (the accumulator-empty arrival) runs, and only then are the
-// packed rows stored, overlapping the next tile's MMAs.
-template <int BN, class Release>
+// packed rows stored, overlapping the next tile's MMAs.  With kXpose the rows are stored
+// through the warp's transpose block s_blk (coalesced, whole sectors), else one row per thread.
+template <int BN, bool kXpose, class Release>
 __device__ __forceinline__ void epilogue_dense_bf16_early(const GemmParams& p, int l, int row, int col_base,
                                                           uint32_t tmem_acc, int c_first, float& run_max,
-                                                          Release release) {
+                                                          Release release, uint8_t* s_blk, int lane) {
   constexpr int kChunks = (BN / 32 + 1) / 2;  // this warp's chunks (alternate 32-column chunks)
   uint32_t pk[kChunks][16];
 #pragma unroll
@@ -355,17 +356,34 @@ __device__ __forceinline__ void epilogue_dense_bf16_early(const GemmParams& p, i
     }
   }
   release();
-  if (row >= p.m) return;
-  __nv_bfloat16* rowp = reinterpret_cast<__nv_bfloat16*>(p.c) + (static_cast<uint64_t>(l) * p.m + row) *
-                                                                     static_cast<uint64_t>(p.n);
+  if constexpr (kXpose) {
+    __nv_bfloat16* batch = reinterpret_cast<__nv_bfloat16*>(p.c) + static_cast<uint64_t>(l) * p.m * p.n;
 #pragma unroll
-  for (int ci = 0; ci < kChunks; ++ci) {
-    const int c = c_first + 2 * ci;
-    const int col0 = col_base + c * 32;
-    if (c < BN / 32 && col0 < p.n) {
+    for (int ci = 0; ci < kChunks; ++ci) {
+      const int c = c_first + 2 * ci;
+      const int col0 = col_base + c * 32;
+      if (c < BN / 32 && col0 < p.n) {  // warp-uniform
+        const uint4 u[4] = {make_uint4(pk[ci][0], pk[ci][1], pk[ci][2], pk[ci][3]),
+                            make_uint4(pk[ci][4], pk[ci][5], pk[ci][6], pk[ci][7]),
+                            make_uint4(pk[ci][8], pk[ci][9], pk[ci][10], pk[ci][11]),
+                            make_uint4(pk[ci][12], pk[ci][13], pk[ci][14], pk[ci][15])};
+        store_rows64(s_blk, batch, static_cast<uint64_t>(p.n) * 2, row - lane, col0 * 2, p.n * 2, u, lane, p.m);
+      }
+    }
+  } else {
+    if (row >= p.m) return;
+    __nv_bfloat16* rowp = reinterpret_cast<__nv_bfloat16*>(p.c) + (static_cast<uint64_t>(l) * p.m + row) *
+                                                                       static_cast<uint64_t>(p.n);
 #pragma unroll
-      for (int j = 0; j < 32; j += 8)
-        if (col0 + j < p.n) store16(rowp + col0 + j, pk[ci][j / 2], pk[ci][j / 2 + 1], pk[ci][j / 2 + 2], pk[ci][j / 2 + 3]);
+    for (int ci = 0; ci < kChunks; ++ci) {
+      const int c = c_first + 2 * ci;
+      const int col0 = col_base + c * 32;
+      if (c < BN / 32 && col0 < p.n) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8)
+          if (col0 + j < p.n)
+            store16(rowp + col0 + j, pk[ci][j / 2], pk[ci][j / 2 + 1], pk[ci][j / 2 + 2], pk[ci][j / 2 + 3]);
+      }
     }
   }
 }
@@ -978,7 +996,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                                                          s_xpose + (warp - 2) * kXposeBlockBytes);
         release();
       } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
-        epilogue_dense_bf16_early<BN>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release);
+        epilogue_dense_bf16_early<BN, false>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release, nullptr,
+                                             lane);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
                                s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * kXposeBlockBytes);

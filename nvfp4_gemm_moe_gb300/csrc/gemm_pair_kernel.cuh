@@ -59,7 +59,7 @@ struct PairTraits {
   static constexpr int kBarBytes = 1024;
   static constexpr int kOffsetsBytes = 4096;
   static constexpr int kAmaxBytes = 4096;
-  static constexpr int kXposeBytes = EPI == kEpiDense ? 0 : 8 * kXposeBlockBytes;  // grouped epilogues
+  static constexpr int kXposeBytes = 8 * kXposeBlockBytes;  // one transpose block per epilogue warp
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
   static constexpr int kStagesTmem = (512 - kSfBase) / kSfStride;
@@ -354,7 +354,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
                                                          s_xpose + (warp - 2) * kXposeBlockBytes);
         release();
       } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
-        epilogue_dense_bf16_early<BN>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release);
+        epilogue_dense_bf16_early<BN, true>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release,
+                                            s_xpose + (warp - 2) * kXposeBlockBytes, lane);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
                                s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * kXposeBlockBytes);
