@@ -11,7 +11,9 @@ Plain, slow, obviously-correct restatements of what the pages define:
                    sReLU (optional tanh clamp), per-expert amax and the row/column
                    MXFP8 re-quantisation of D;
 * ``dswiglu``   -- grouped GEMM + dSwiGLU backward epilogue (32-column
-                   input/gate interleave, dprob, (L, 2) amax, FP8 D).
+                   input/gate interleave, dprob, (L, 2) amax, FP8 D);
+* ``rope``      -- dense MXFP8 projection GEMM + per-head interleaved-in / halves-out
+                   RoPE + dual-direction MXFP8 with plain scale layouts.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 ``--impl reference`` legs of ``bench.py`` may import this package.  It shares no
@@ -24,4 +26,4 @@ against the pages' own implementation because the pages print no outputs: the
 row order inside a 128-row scale-factor atom (``sf_layout``), "parity unpinned"
 in that sense only.
 """
-from . import formats, sf_layout, quantize, gemm, dswiglu  # noqa: F401
+from . import formats, sf_layout, quantize, gemm, dswiglu, rope  # noqa: F401

@@ -30,6 +30,7 @@ CHUNK = 1 << 20
 
 # stream ids: one per tensor kind so tensors never share random numbers
 S_A, S_B, S_ALPHA, S_PROB, S_ROUTE, S_C, S_BETA = 1, 2, 3, 4, 5, 6, 7
+SEQ_LEN_ROPE = 4096  # positions of the RoPE workload restart every 4096 tokens (one sequence)
 
 PAD = 256  # expert row ranges are padded to multiples of 256 rows
 
@@ -268,6 +269,54 @@ class GroupedDswiglu(Grouped):
         return uniform_f32(self.seed, S_BETA, self.experts, 0.5, 2.0)
 
 
+@dataclasses.dataclass(frozen=True)
+class RopeProj:
+    """Dense MXFP8 projection + per-head RoPE + dual-direction MXFP8 workload: x (tokens, q_lora),
+    w (heads * head_dim, q_lora) ([out, in]), rotary tables (tokens, qk_rope)."""
+    name: str
+    tokens: int
+    q_lora: int
+    heads: int
+    head_dim: int
+    qk_rope: int
+    seed: int = 0
+    fmt: str = "mxfp8"
+
+    @property
+    def n(self) -> int:
+        return self.heads * self.head_dim
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.tokens * self.q_lora * self.n
+
+    def x_rows(self, rows: np.ndarray | None = None) -> np.ndarray:
+        """fp32 x (tokens, q_lora) as N(0,1)."""
+        if rows is None:
+            return normal_f32(self.seed, S_A, 0, self.tokens * self.q_lora).reshape(self.tokens, self.q_lora)
+        return normal_f32_rows(self.seed, S_A, rows, self.q_lora)
+
+    def w_rows(self, rows: np.ndarray | None = None) -> np.ndarray:
+        """fp32 w (heads * head_dim, q_lora) as N(0,1)/sqrt(q_lora)."""
+        scale = np.float32(1.0 / math.sqrt(self.q_lora))
+        if rows is None:
+            x = normal_f32(self.seed, S_B, 0, self.n * self.q_lora).reshape(self.n, self.q_lora)
+        else:
+            x = normal_f32_rows(self.seed, S_B, rows, self.q_lora)
+        x *= scale
+        return x
+
+    def tables(self) -> tuple[np.ndarray, np.ndarray]:
+        """fp32 cos, sin (tokens, qk_rope): angle position * 10000^(-2j/qk_rope) for pair j, the
+        same angle in both halves; positions restart every SEQ_LEN_ROPE tokens."""
+        half = self.qk_rope // 2
+        pos = (np.arange(self.tokens) % SEQ_LEN_ROPE).astype(np.float64)
+        inv_freq = 10000.0 ** (-2.0 * np.arange(half) / self.qk_rope)
+        ang = pos[:, None] * inv_freq[None, :]
+        ang = np.concatenate([ang, ang], axis=1)
+        return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
 # The five named workloads.  The first is small enough for the oracle to finish
 # in seconds; the second is the large batched dense one throughput is quoted on.
 DENSE_MXFP8_256 = Dense("dense_mxfp8_m256_n256_k256_l1", 256, 256, 256, 1, "mxfp8", "f32")
@@ -287,5 +336,9 @@ GROUPED_DSWIGLU_E32 = GroupedDswiglu("grouped_mxfp8_dswiglu_e32_k7168_n2048", 32
 GROUPED_DSWIGLU_E32_FP8D = dataclasses.replace(GROUPED_DSWIGLU_E32, name="grouped_mxfp8_dswiglu_fp8d_e32_k7168_n2048",
                                                d_dtype="e4m3")
 
+# the DeepSeek-V3 MLA Q up-projection: 128 heads of 128 + 64 features from a 1536-wide latent
+ROPE_PROJ_T16384 = RopeProj("rope_proj_mxfp8_t16384_q1536_h128_d192", 16384, 1536, 128, 192, 64)
+
 ALL = {w.name: w for w in (DENSE_MXFP8_256, DENSE_MXFP8_8192, DENSE_MXFP8_8192_L1, DENSE_NVFP4_16384, GROUPED_SRELU_E32,
-                           GROUPED_SRELU_E32_CLAMP, GROUPED_FP8D_E128, GROUPED_DSWIGLU_E32, GROUPED_DSWIGLU_E32_FP8D)}
+                           GROUPED_SRELU_E32_CLAMP, GROUPED_FP8D_E128, GROUPED_DSWIGLU_E32, GROUPED_DSWIGLU_E32_FP8D,
+                           ROPE_PROJ_T16384)}
