@@ -15,7 +15,9 @@
  *                           Tanh soft clamp); bsg_grouped_gemm_srelu_discrete takes
  *                           the experts' weights as separate allocations;
  *   bsg_grouped_gemm_dswiglu grouped MoE block-scaled GEMM + dSwiGLU backward epilogue
- *                           ("Grouped GEMM + dSwiGLU (SM100)", Equations).
+ *                           ("Grouped GEMM + dSwiGLU (SM100)", Equations);
+ *   bsg_gemm_rope_mxfp8     MXFP8 projection GEMM + per-head RoPE + row and column MXFP8
+ *                           ("GEMM + RoPE + MXFP8 Projection (SM100)", Equations).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -254,6 +256,39 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
                                     void* d_row, void* d_col, bsg_dtype d_dtype, uint8_t* sfd_row,
                                     uint8_t* sfd_col, float* dprob, float* amax, const bsg_gemm_opts* opts,
                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * bsg_gemm_rope_mxfp8 -- projection GEMM + per-head RoPE + dual-direction MXFP8
+ * ("GEMM + RoPE + MXFP8 Projection (SM100)", Overview, Shapes, Equations; MXFP8 input path).
+ * With N = num_heads * head_dim and P = head_dim - qk_rope:
+ *     Y[t, h, f] = sum_k xhat[t, k] * what[h * head_dim + f, k]              (fp32 accumulator)
+ *     features f >= P of each head are interleaved pairs (a_j, b_j) = (Y[P + 2j], Y[P + 2j + 1])
+ *     rotated into halves: out[P + j] = a_j cos[t, j] - b_j sin[t, j],
+ *                          out[P + R/2 + j] = b_j cos[t, R/2 + j] + a_j sin[t, R/2 + j]  (R = qk_rope)
+ *     (the page's "interleaved-in / halves-out" RoPE; YARN scaling is in the caller's tables);
+ *     out_fp8_row / out_scales_row: MXFP8 of Y in blocks of 32 features of a head,
+ *     out_fp8_col / out_scales_col: MXFP8 of Y in blocks of 32 tokens of a feature; each block's
+ *     E8M0 scale is the smallest 2^e with blockamax <= 448 * 2^e, codes RNE_satfinite(Y / 2^e).
+ *
+ * x               device E4M3 codes (tokens, q_lora), K-major.
+ * w               device E4M3 codes (N, q_lora): the [out, in] weight layout.
+ * x_scale, w_scale device E8M0 block scales along q_lora: scale_layout 0 = the 128x4 atom layout
+ *                 of bsg_quantize_mx (rows tokens / N); 1 = plain row-major (rows, q_lora / 32) (the
+ *                 page's layout; repacked into the workspace on the device).
+ * cos, sin        device bf16 (tokens, qk_rope).
+ * out_fp8_row, out_fp8_col   device E4M3 (tokens, num_heads, head_dim).
+ * out_scales_row  device E8M0 (tokens, num_heads, head_dim / 32), plain row-major.
+ * out_scales_col  device E8M0 (tokens / 32, num_heads, head_dim), plain row-major.
+ * workspace       bsg_workspace_size() bytes for scale_layout 0, bsg_rope_workspace_size(...) for 1.
+ * Requirements: tokens % 128 == 0, q_lora % 32 == 0, head_dim == 192 and qk_rope == 64 (one head
+ * per 128 x 192 tile; other head shapes return BSG_ERR_UNSUPPORTED).
+ */
+size_t bsg_rope_workspace_size(int64_t tokens, int64_t num_heads, int64_t head_dim, int64_t q_lora);
+bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const uint8_t* w, const uint8_t* w_scale,
+                               int scale_layout, const void* cos, const void* sin, int64_t tokens, int64_t q_lora,
+                               int64_t num_heads, int64_t head_dim, int64_t qk_rope, uint8_t* out_fp8_row,
+                               uint8_t* out_scales_row, uint8_t* out_fp8_col, uint8_t* out_scales_col,
+                               const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * bsg_grouped_gemm_srelu_discrete -- bsg_grouped_gemm_srelu with per-expert weight allocations

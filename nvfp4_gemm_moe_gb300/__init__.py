@@ -67,6 +67,11 @@ def _load():
     lib.bsg_grouped_gemm_dswiglu.restype = I
     lib.bsg_grouped_gemm_dswiglu.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, P, P, P, P, I, P, P, P, I,
                                              P, P, P, P, ctypes.POINTER(bsg_gemm_opts), P, SZ, P]
+    lib.bsg_rope_workspace_size.restype = SZ
+    lib.bsg_rope_workspace_size.argtypes = [I64, I64, I64, I64]
+    lib.bsg_gemm_rope_mxfp8.restype = I
+    lib.bsg_gemm_rope_mxfp8.argtypes = [P, P, P, P, I, P, P, I64, I64, I64, I64, I64, P, P, P, P,
+                                        ctypes.POINTER(bsg_gemm_opts), P, SZ, P]
     lib.bsg_gemm_amax_noalloc.restype = I
     lib.bsg_gemm_amax_noalloc.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, I, P,
                                           ctypes.POINTER(bsg_gemm_opts), P]
@@ -186,6 +191,22 @@ def bsg_grouped_gemm_dswiglu(a, b, sfa, sfb, ab_dtype, sf_dtype, sf_vec_size, va
         _ptr(padded_offsets), _ptr(alpha), _ptr(beta), _ptr(prob), _ptr(c), c_dtype, _ptr(norm_const), _ptr(d_row),
         _ptr(d_col), d_dtype, _ptr(sfd_row), _ptr(sfd_col), _ptr(dprob), _ptr(amax), ctypes.byref(o),
         _ptr(workspace), ws_bytes, _stream(stream)), "bsg_grouped_gemm_dswiglu")
+
+
+def bsg_rope_workspace_size(tokens: int, num_heads: int, head_dim: int, q_lora: int) -> int:
+    return int(_lib.bsg_rope_workspace_size(tokens, num_heads, head_dim, q_lora))
+
+
+def bsg_gemm_rope_mxfp8(x, x_scale, w, w_scale, scale_layout, cos, sin, tokens, q_lora, num_heads, head_dim, qk_rope,
+                        out_fp8_row, out_scales_row, out_fp8_col, out_scales_col, workspace, workspace_bytes=None,
+                        stream=None, **opts):
+    ws_bytes = (bsg_rope_workspace_size(tokens, num_heads, head_dim, q_lora) if workspace_bytes is None
+                else workspace_bytes)
+    o = _opts(**opts)
+    _check(_lib.bsg_gemm_rope_mxfp8(_ptr(x), _ptr(x_scale), _ptr(w), _ptr(w_scale), scale_layout, _ptr(cos), _ptr(sin),
+                                    tokens, q_lora, num_heads, head_dim, qk_rope, _ptr(out_fp8_row),
+                                    _ptr(out_scales_row), _ptr(out_fp8_col), _ptr(out_scales_col), ctypes.byref(o),
+                                    _ptr(workspace), ws_bytes, _stream(stream)), "bsg_gemm_rope_mxfp8")
 
 
 def bsg_read_device_error(workspace, stream=None) -> int:

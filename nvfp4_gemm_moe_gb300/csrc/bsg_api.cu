@@ -607,6 +607,94 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }
 
+size_t bsg_rope_workspace_size(int64_t tokens, int64_t num_heads, int64_t head_dim, int64_t q_lora) {
+  if (tokens < 0 || num_heads < 0 || head_dim < 0 || q_lora < 0) return kWorkspaceBytes;
+  return kWorkspaceBytes + bsg_sf_bytes(1, tokens, q_lora, 32) + bsg_sf_bytes(1, num_heads * head_dim, q_lora, 32);
+}
+
+bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const uint8_t* w, const uint8_t* w_scale,
+                               int scale_layout, const void* cos, const void* sin, int64_t tokens, int64_t q_lora,
+                               int64_t num_heads, int64_t head_dim, int64_t qk_rope, uint8_t* out_fp8_row,
+                               uint8_t* out_scales_row, uint8_t* out_fp8_col, uint8_t* out_scales_col,
+                               const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !x_scale || !w || !w_scale || !cos || !sin || !out_fp8_row || !out_scales_row || !out_fp8_col ||
+      !out_scales_col)
+    return BSG_ERR_INVALID_ARG;
+  if (scale_layout != 0 && scale_layout != 1) return BSG_ERR_INVALID_ARG;
+  if (tokens < 128 || tokens % 128 != 0 || q_lora < 32 || q_lora % 32 != 0 || num_heads < 1 || head_dim < 1 ||
+      qk_rope < 1)
+    return BSG_ERR_INVALID_ARG;
+  // the kernel holds one head per 192-wide tile, the last 64 features rotary
+  if (head_dim != 192 || qk_rope != 64) return BSG_ERR_UNSUPPORTED;
+  const int64_t n = num_heads * head_dim;
+  if (!fits_int32(tokens) || !fits_int32(n) || !fits_int32(q_lora) || !fits_int32(tokens * (n / 32)))
+    return BSG_ERR_INVALID_ARG;
+  const size_t ws_need = scale_layout == 1 ? bsg_rope_workspace_size(tokens, num_heads, head_dim, q_lora)
+                                           : kWorkspaceBytes;
+  if (!workspace || workspace_bytes < ws_need) return BSG_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(cos) || !aligned16(sin) || !aligned16(out_fp8_row) ||
+      !aligned16(out_fp8_col) || (scale_layout == 0 && (!aligned16(x_scale) || !aligned16(w_scale))) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return BSG_ERR_ALIGNMENT;
+  DeviceInfo info;
+  bsg_status st = current_device(nullptr, &info);
+  if (st != BSG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
+  const uint8_t* sfa = x_scale;
+  const uint8_t* sfb = w_scale;
+  if (scale_layout == 1) {
+    // plain (rows, q_lora / 32) scales: scattered into the atom layout in the workspace
+    uint8_t* pa = static_cast<uint8_t*>(workspace) + kWorkspaceBytes;
+    uint8_t* pb = pa + bsg_sf_bytes(1, tokens, q_lora, 32);
+    if (bsg::launch_sf_pack(x_scale, tokens, q_lora / 32, pa, s) != cudaSuccess ||
+        bsg::launch_sf_pack(w_scale, n, q_lora / 32, pb, s) != cudaSuccess)
+      return BSG_ERR_CUDA;
+    sfa = pa;
+    sfb = pb;
+  }
+
+  const int bn = 192;
+  const int64_t m_tiles = tokens / 128;
+  const int64_t n_tiles = num_heads;
+  const int64_t tiles = m_tiles * n_tiles;
+  if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, x, q_lora, tokens, 1, 128) || !make_operand_map(&tb, w, q_lora, n, 1, bn))
+    return BSG_ERR_CUDA;
+
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.m = static_cast<int>(tokens);
+  p.n = static_cast<int>(n);
+  p.k = static_cast<int>(q_lora);
+  p.l = 1;
+  p.m_tiles = static_cast<int>(m_tiles);
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.k_tiles = static_cast<int>(cdiv(q_lora, 128));
+  p.num_tiles = static_cast<int>(tiles);
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.sfa_mt = static_cast<int>(m_tiles);
+  p.sfb_mt = static_cast<int>(cdiv(n, 128));
+  p.sf_kt = static_cast<int>(cdiv(q_lora / 32, 4));
+  p.c_kind = bsg::kOutNone;
+  p.d = out_fp8_row;
+  p.d_col = out_fp8_col;
+  p.sfd_row = out_scales_row;
+  p.sfd_col = out_scales_col;
+  p.rope_cos = static_cast<const uint16_t*>(cos);
+  p.rope_sin = static_cast<const uint16_t*>(sin);
+  p.qk_rope = static_cast<int>(qk_rope);
+  p.err = static_cast<uint32_t*>(workspace);
+
+  GemmConfig cfg{bsg::kMXFP8, bn, bsg::kEpiRope};
+  cudaError_t e = bsg::launch_gemm_rope(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
+  if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+}
+
 bsg_status bsg_read_device_error(const void* workspace, void* stream, uint32_t* error_bits) {
   if (!workspace || !error_bits) return BSG_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

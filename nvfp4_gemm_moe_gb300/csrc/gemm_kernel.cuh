@@ -115,7 +115,7 @@ __device__ __forceinline__ int find_expert(const int32_t* offs, int num_experts,
 template <int EPI, int TM = kTileM>
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t, const int32_t* offs) {
   TileCoord tc;
-  if (EPI == kEpiDense) {
+  if (!epi_is_grouped(EPI)) {
     const int per_batch = p.m_tiles * p.n_tiles;
     tc.l = t / per_batch;
     const int idx = t - tc.l * per_batch;
@@ -394,6 +394,9 @@ __device__ __forceinline__ void epilogue_dense_bf16_early(const GemmParams& p, i
 // values), D_col one per column and 32-row block (the warp's 32 lanes are 32 consecutive rows).
 // s_inv: 32 floats of shared memory owned by this warp; s_blk: the warp's transpose block (the
 // code rows are stored coalesced through it).
+// With kPlainScales the scales go to plain row-major arrays instead of the atom layout:
+// sfd_row[row * (n_d / 32) + dcol0 / 32] and sfd_col[(row / 32) * n_d + dcol0 + lane].
+template <bool kPlainScales = false>
 __device__ __forceinline__ void store_e4m3_block(const GemmParams& p, int row, int dcol0, int n_d, const float (&d)[32],
                                                  int lane, float* s_inv, uint8_t* s_blk) {
   const int row0 = row - lane;
@@ -413,17 +416,24 @@ __device__ __forceinline__ void store_e4m3_block(const GemmParams& p, int row, i
                make_uint4(q[4], q[5], q[6], q[7]), lane);
   // one byte per block: a tile need not start on a four-block word of the SF layout; the row's
   // last block also zeroes the padding blocks of its word
-  const int nb = dcol0 >> 5;
-  const int nb_end = dcol0 + 32 >= n_d ? (nb | 3) : nb;
-  for (int b = nb; b <= nb_end; ++b)
-    p.sfd_row[sf_offset(row, b, 0, (p.m + 127) / 128, p.sfd_row_kt)] = static_cast<uint8_t>(b == nb ? code_r : 0u);
+  if constexpr (kPlainScales) {
+    p.sfd_row[static_cast<uint64_t>(row) * (n_d >> 5) + (dcol0 >> 5)] = static_cast<uint8_t>(code_r);
+  } else {
+    const int nb = dcol0 >> 5;
+    const int nb_end = dcol0 + 32 >= n_d ? (nb | 3) : nb;
+    for (int b = nb; b <= nb_end; ++b)
+      p.sfd_row[sf_offset(row, b, 0, (p.m + 127) / 128, p.sfd_row_kt)] = static_cast<uint8_t>(b == nb ? code_r : 0u);
+  }
   float cm[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) cm[j] = fabsf(d[j]);
   warp_colmax_scatter(cm, lane);
   const uint32_t code_c = e8m0_ceil_code(cm[0]);
   const int mblk = row >> 5;  // same for the whole warp
-  p.sfd_col[sf_offset(dcol0 + lane, mblk, 0, p.sfd_col_mt, p.sfd_col_kt)] = static_cast<uint8_t>(code_c);
+  if constexpr (kPlainScales)
+    p.sfd_col[static_cast<uint64_t>(mblk) * n_d + dcol0 + lane] = static_cast<uint8_t>(code_c);
+  else
+    p.sfd_col[sf_offset(dcol0 + lane, mblk, 0, p.sfd_col_mt, p.sfd_col_kt)] = static_cast<uint8_t>(code_c);
   // every lane needs the 32 column reciprocals: one shared-memory round trip (broadcast reads)
   // instead of 32 shuffles
   s_inv[lane] = e8m0_inv_scale(code_c);
@@ -599,6 +609,88 @@ __device__ __forceinline__ void epilogue_tile_dswiglu(const GemmParams& p, int r
     }
   }
   if (dprob_part != 0.0f) atomicAdd(&p.dprob[row], dprob_part);
+}
+
+// bf16 bit pattern to fp32 (exact).
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits) { return __uint_as_float(bits << 16); }
+
+// GEMM + RoPE + MXFP8 epilogue of one tile, 128 tokens x one head of BN = HEAD_DIM features,
+// for the rows (tokens) of one warp ("GEMM + RoPE + MXFP8 Projection (SM100)", Equations).
+// The first BN - 64 features pass unchanged; the last 64 (two accumulator chunks) hold 32
+// interleaved pairs (a_j, b_j) = (y[2j], y[2j+1]) that leave as halves:
+//   out[j] = a_j cos[t, j] - b_j sin[t, j],   out[32 + j] = b_j cos[t, 32 + j] + a_j sin[t, 32 + j].
+// Every 32-feature block is then quantised by rows and by columns (store_e4m3_block with plain
+// scale arrays).  The two warps of a quadrant split the chunks: half 0 takes the first BN/64,
+// half 1 the rest, which include both rotary chunks (their pairs span the two).
+template <int BN>
+__device__ __forceinline__ void epilogue_tile_rope(const GemmParams& p, int row, int head, uint32_t tmem_acc,
+                                                   int lane, int half, float* s_inv, uint8_t* s_blk) {
+  constexpr int kChunks = BN / 32;
+  constexpr int kRope = kChunks - 2;  // first rotary chunk
+  const int c_begin = half == 0 ? 0 : kChunks / 2;
+  const int c_end = half == 0 ? kChunks / 2 : kRope;
+  const int col_head = head * BN;
+#pragma unroll 1
+  for (int c = c_begin; c < c_end; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tmem_acc + c * 32, r);
+    tmem_ld_wait(r);
+    float d[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(r[j]);
+    store_e4m3_block<true>(p, row, col_head + c * 32, p.n, d, lane, s_inv, s_blk);
+  }
+  if (half == 0) return;  // warp-uniform
+  uint32_t r0[32], r1[32];
+  tmem_ld_32x32b_x32(tmem_acc + kRope * 32, r0);
+  tmem_ld_32x32b_x32(tmem_acc + (kRope + 1) * 32, r1);
+  tmem_ld_wait(r0);
+  tmem_ld_wait(r1);
+  const uint16_t* cs = p.rope_cos + static_cast<uint64_t>(row) * p.qk_rope;
+  const uint16_t* sn = p.rope_sin + static_cast<uint64_t>(row) * p.qk_rope;
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    uint32_t(&src)[32] = g == 0 ? r0 : r1;  // pairs j = 16 g .. 16 g + 15
+    // cos / sin of j (first half) and 32 + j (second half): 32 bytes each
+    uint4 c_lo[2], c_hi[2], s_lo[2], s_hi[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      c_lo[i] = __ldg(reinterpret_cast<const uint4*>(cs + 16 * g) + i);
+      c_hi[i] = __ldg(reinterpret_cast<const uint4*>(cs + 32 + 16 * g) + i);
+      s_lo[i] = __ldg(reinterpret_cast<const uint4*>(sn + 16 * g) + i);
+      s_hi[i] = __ldg(reinterpret_cast<const uint4*>(sn + 32 + 16 * g) + i);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const uint4& cl = c_lo[jj >> 3];
+      const uint4& ch = c_hi[jj >> 3];
+      const uint4& sl = s_lo[jj >> 3];
+      const uint4& sh = s_hi[jj >> 3];
+      const int w = (jj >> 1) & 3, hw = jj & 1;  // 32-bit word and 16-bit half within the uint4
+      const uint32_t wc = w == 0 ? cl.x : w == 1 ? cl.y : w == 2 ? cl.z : cl.w;
+      const uint32_t wch = w == 0 ? ch.x : w == 1 ? ch.y : w == 2 ? ch.z : ch.w;
+      const uint32_t ws = w == 0 ? sl.x : w == 1 ? sl.y : w == 2 ? sl.z : sl.w;
+      const uint32_t wsh = w == 0 ? sh.x : w == 1 ? sh.y : w == 2 ? sh.z : sh.w;
+      const float c1 = bf16_bits_to_float(hw ? wc >> 16 : wc & 0xffffu);
+      const float c2 = bf16_bits_to_float(hw ? wch >> 16 : wch & 0xffffu);
+      const float s1 = bf16_bits_to_float(hw ? ws >> 16 : ws & 0xffffu);
+      const float s2 = bf16_bits_to_float(hw ? wsh >> 16 : wsh & 0xffffu);
+      const float a = __uint_as_float(src[2 * jj]);
+      const float b = __uint_as_float(src[2 * jj + 1]);
+      src[2 * jj] = __float_as_uint(fmaf(a, c1, -b * s1));      // out[j]
+      src[2 * jj + 1] = __float_as_uint(fmaf(b, c2, a * s2));   // out[32 + j]
+    }
+  }
+  float lo[32], hi[32];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    lo[j] = __uint_as_float(r0[2 * j]);
+    lo[16 + j] = __uint_as_float(r1[2 * j]);
+    hi[j] = __uint_as_float(r0[2 * j + 1]);
+    hi[16 + j] = __uint_as_float(r1[2 * j + 1]);
+  }
+  store_e4m3_block<true>(p, row, col_head + kRope * 32, p.n, lo, lane, s_inv, s_blk);
+  store_e4m3_block<true>(p, row, col_head + (kRope + 1) * 32, p.n, hi, lane, s_inv, s_blk);
 }
 
 // Folds one warp's running maxima of expert g into shared memory: the per-expert amax of the
@@ -796,13 +888,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     *bad_flag = 0;
     fence_mbar_init();
   }
-  if (EPI != kEpiDense) {
+  if (epi_is_grouped(EPI)) {
     for (int i = threadIdx.x; i < 1024; i += kThreadsGemm) s_amax[i] = 0.0f;
   } else if (threadIdx.x == 0) {
     s_amax[0] = 0.0f;
   }
   __syncthreads();
-  if (EPI != kEpiDense) {
+  if (epi_is_grouped(EPI)) {
     // stage padded_offsets and check: multiples of 256, non-decreasing, last == valid_m
     for (int i = threadIdx.x; i < p.l; i += kThreadsGemm) {
       const int32_t o = p.offsets[i];
@@ -835,7 +927,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       int fenced_l = -1;  // expert whose global tensor map this thread has acquired
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
-        const int a_batch = EPI == kEpiDense ? tc.l : 0;
+        const int a_batch = epi_is_grouped(EPI) ? 0 : tc.l;
         // per-expert weights: the expert's own tensor map and scale array, else batch tc.l of one
         const CUtensorMap* bmap = p.b_maps ? p.b_maps + tc.l : &tmap_b;
         if (p.b_maps && tc.l != fenced_l) { tmap_acquire(bmap); fenced_l = tc.l; }
@@ -973,7 +1065,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
       float alpha_g = 1.0f, prob_r = 0.0f;
-      if (EPI != kEpiDense) {
+      if (epi_is_grouped(EPI)) {
         alpha_g = p.alpha[tc.l];
         prob_r = p.prob[row];
         if (tc.l != run_expert) {
@@ -989,7 +1081,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tmem_empty[acc]);
       };
-      if constexpr (epi_is_dswiglu(EPI)) {
+      if constexpr (EPI == kEpiRope) {
+        epilogue_tile_rope<BN>(p, row, tc.nt, tmem_acc, lane, half, s_amax + (warp - 2) * 32,
+                               s_xpose + (warp - 2) * kXposeBlockBytes);
+        release();
+      } else if constexpr (epi_is_dswiglu(EPI)) {
         epilogue_tile_dswiglu<BN, EPI == kEpiDswigluFP8>(p, row, tc.nt * BN, tmem_acc, lane, alpha_g, p.beta[tc.l],
                                                          prob_r, nc, run_max, run_max2, half, 2,
                                                          s_amax + (warp - 2) * 32,
@@ -1010,7 +1106,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       float v = run_max;
       for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
       if (lane == 0) atomic_max_nonneg(&s_amax[0], v);
-    } else if (run_expert >= 0) {
+    } else if (epi_is_grouped(EPI) && run_expert >= 0) {
       fold_expert_max<EPI>(s_amax, run_expert, run_max, run_max2, lane);
     }
   }

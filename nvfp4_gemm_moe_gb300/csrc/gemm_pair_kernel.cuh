@@ -144,13 +144,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     *bad_flag = 0;
     fence_mbar_init();
   }
-  if (EPI != kEpiDense) {
+  if (epi_is_grouped(EPI)) {
     for (int i = threadIdx.x; i < 1024; i += kThreadsGemm) s_amax[i] = 0.0f;
   } else if (threadIdx.x == 0) {
     s_amax[0] = 0.0f;
   }
   __syncthreads();
-  if (EPI != kEpiDense) {
+  if (epi_is_grouped(EPI)) {
     for (int i = threadIdx.x; i < p.l; i += kThreadsGemm) {
       const int32_t o = p.offsets[i];
       const int32_t prev = i == 0 ? 0 : p.offsets[i - 1];
@@ -186,7 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
         const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
-        const int a_batch = EPI == kEpiDense ? tc.l : 0;
+        const int a_batch = epi_is_grouped(EPI) ? 0 : tc.l;
         const int a_row = tc.mt * 256 + static_cast<int>(rank) * 128;
         const int b_row = tc.nt * BN + static_cast<int>(rank) * T::kBHalf;
         const int sfa_group = min(tc.mt * 2 + static_cast<int>(rank), p.sfa_mt - 1);
@@ -330,7 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
       float alpha_g = 1.0f, prob_r = 0.0f;
-      if (EPI != kEpiDense) {
+      if (epi_is_grouped(EPI)) {
         alpha_g = p.alpha[tc.l];
         prob_r = p.prob[row];
         if (tc.l != run_expert) {
@@ -368,7 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       float v = run_max;
       for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
       if (lane == 0) atomic_max_nonneg(&s_amax[0], v);
-    } else if (run_expert >= 0) {
+    } else if (epi_is_grouped(EPI) && run_expert >= 0) {
       fold_expert_max<EPI>(s_amax, run_expert, run_max, run_max2, lane);
     }
   }

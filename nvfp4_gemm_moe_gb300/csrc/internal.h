@@ -17,8 +17,12 @@ enum EpiKind : int {
   kEpiGroupedBF16 = 1,  // grouped sReLU, float D (bf16 / f16 / f32) + per-expert amax
   kEpiGroupedFP8 = 2,   // grouped sReLU, E4M3 D with row and column scale factors
   kEpiDswigluF = 3,     // grouped dSwiGLU backward, float D + per-expert (|ab|, |dswiglu|) amax
-  kEpiDswigluFP8 = 4    // grouped dSwiGLU backward, E4M3 D with row and column scale factors
+  kEpiDswigluFP8 = 4,   // grouped dSwiGLU backward, E4M3 D with row and column scale factors
+  kEpiRope = 5          // dense projection + per-head RoPE + row / column MXFP8 (plain scale layouts)
 };
+__host__ __device__ constexpr bool epi_is_grouped(int epi) {
+  return epi == kEpiGroupedBF16 || epi == kEpiGroupedFP8 || epi == kEpiDswigluF || epi == kEpiDswigluFP8;
+}
 __host__ __device__ constexpr bool epi_is_dswiglu(int epi) { return epi == kEpiDswigluF || epi == kEpiDswigluFP8; }
 __host__ __device__ constexpr bool epi_has_fp8_d(int epi) { return epi == kEpiGroupedFP8 || epi == kEpiDswigluFP8; }
 
@@ -61,6 +65,11 @@ struct GemmParams {
   int c_in_kind;         // OutKind of C (f32 / bf16 / f16 / E4M3 values)
   const float* beta;     // per-expert scale of C
   float* dprob;          // (valid_m,) accumulated with atomic adds
+  // RoPE projection: bf16 rotary tables (m, qk_rope); d / d_col / sfd_row / sfd_col hold the
+  // row- and column-quantised outputs with plain (row-major) scale arrays
+  const uint16_t* rope_cos;
+  const uint16_t* rope_sin;
+  int qk_rope;
   // device error word (workspace)
   uint32_t* err;
 };
@@ -89,6 +98,14 @@ cudaError_t launch_gemm_dswiglu(const GemmConfig& cfg, const CUtensorMap& tmap_a
                                 const GemmParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_pair_dswiglu(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                                      const GemmParams& p, int max_pairs, cudaStream_t stream);
+
+// The GEMM + RoPE + MXFP8 projection kernel (one-CTA tiles of 128 tokens x one head).
+cudaError_t launch_gemm_rope(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                             const GemmParams& p, int grid, cudaStream_t stream);
+
+// Scatters plain row-major scale bytes (rows, blocks) into the 128x4 atom layout (dst zeroed
+// first, so padding bytes hold the finite scale 0).
+cudaError_t launch_sf_pack(const uint8_t* src, int64_t rows, int64_t blocks, uint8_t* dst, cudaStream_t stream);
 
 // Launches the block quantiser.
 cudaError_t launch_quantize(int fmt, const float* x, int64_t batch, int64_t rows, int64_t k, uint8_t* q,

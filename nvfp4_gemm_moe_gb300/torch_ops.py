@@ -8,8 +8,8 @@ from __future__ import annotations
 import torch
 
 from . import (BF16, E2M1, E4M3, F16, F32, FORMATS, bsg_gemm_amax, bsg_grouped_discrete_workspace_size,
-               bsg_grouped_gemm_dswiglu, bsg_grouped_gemm_srelu, bsg_grouped_gemm_srelu_discrete, bsg_quantize_mx,
-               bsg_sf_bytes, bsg_workspace_size)
+               bsg_gemm_rope_mxfp8, bsg_grouped_gemm_dswiglu, bsg_grouped_gemm_srelu, bsg_grouped_gemm_srelu_discrete,
+               bsg_quantize_mx, bsg_rope_workspace_size, bsg_sf_bytes, bsg_workspace_size)
 
 
 def new_workspace(device="cuda") -> torch.Tensor:
@@ -159,4 +159,28 @@ def grouped_gemm_dswiglu(a, b, sfa, sfb, fmt: str, padded_offsets, alpha, beta, 
     bsg_grouped_gemm_dswiglu(a, b, sfa, sfb, ab, sfd, v, valid_m, n, k, num_experts, padded_offsets, alpha, beta,
                              prob, c, ck, norm_const, out["d_row"], out.get("d_col"), dk, out.get("sfd_row"),
                              out.get("sfd_col"), out["dprob"], out.get("amax"), workspace, stream=stream, **opts)
+    return out
+
+
+def gemm_rope_mxfp8(x, x_scale, w, w_scale, cos, sin, num_heads: int, head_dim: int = 192, qk_rope: int = 64,
+                    scale_layout: str = "atoms", outputs=None, workspace=None, stream=None, **opts):
+    """Projection GEMM + per-head RoPE + row / column MXFP8.  x (tokens, q_lora) and w
+    (num_heads * head_dim, q_lora) are E4M3 codes (uint8); x_scale / w_scale their E8M0 scales,
+    in the atom layout of ``quantize`` (scale_layout="atoms") or plain (rows, q_lora / 32)
+    ("plain"); cos / sin bf16 (tokens, qk_rope).  Returns a dict: out_fp8_row, out_scales_row,
+    out_fp8_col, out_scales_col."""
+    tokens, q_lora = x.shape[-2], x.shape[-1]
+    dev = x.device
+    out = dict(outputs or {})
+    out.setdefault("out_fp8_row", torch.empty((tokens, num_heads, head_dim), dtype=torch.uint8, device=dev))
+    out.setdefault("out_scales_row", torch.empty((tokens, num_heads, head_dim // 32), dtype=torch.uint8, device=dev))
+    out.setdefault("out_fp8_col", torch.empty((tokens, num_heads, head_dim), dtype=torch.uint8, device=dev))
+    out.setdefault("out_scales_col", torch.empty((tokens // 32, num_heads, head_dim), dtype=torch.uint8, device=dev))
+    layout = {"atoms": 0, "plain": 1}[scale_layout]
+    if workspace is None:
+        workspace = torch.zeros(bsg_rope_workspace_size(tokens, num_heads, head_dim, q_lora), dtype=torch.uint8,
+                                device=dev)
+    bsg_gemm_rope_mxfp8(x, x_scale, w, w_scale, layout, cos, sin, tokens, q_lora, num_heads, head_dim, qk_rope,
+                        out["out_fp8_row"], out["out_scales_row"], out["out_fp8_col"], out["out_scales_col"],
+                        workspace, workspace_bytes=workspace.numel(), stream=stream, **opts)
     return out

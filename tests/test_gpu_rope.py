@@ -1,0 +1,111 @@
+"""GPU parity of bsg_gemm_rope_mxfp8 (projection GEMM + per-head RoPE + dual MXFP8) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import formats, quantize as oq, rope as orope, sf_layout
+from parity import TOL_C, check_e4m3_blocks
+
+pytestmark = pytest.mark.gpu
+
+
+def _tolerance(raw, s_abs, cos, sin, head_dim, qk_rope):
+    """Bound on |Y_gpu - Y| per element (tokens, H, D) from the un-rotated projection ``raw`` and
+    s_abs = sum_k |xhat||what|: the accumulation bound 2^-20 s_abs plus fp32 rounding on the
+    no-position features; on the rotary ones that bound carried through the rotation (linear
+    in a and b) plus the rounding of a product and a fused multiply-add."""
+    p, half = head_dim - qk_rope, qk_rope // 2
+    t = TOL_C * s_abs + 2.0 ** -22 * np.abs(raw)
+    a, b = raw[..., p::2], raw[..., p + 1::2]
+    ta, tb = TOL_C * s_abs[..., p::2], TOL_C * s_abs[..., p + 1::2]
+    c1, c2 = np.abs(cos[:, None, :half]), np.abs(cos[:, None, half:])
+    s1, s2 = np.abs(sin[:, None, :half]), np.abs(sin[:, None, half:])
+    t[..., p:p + half] = c1 * ta + s1 * tb + 2.0 ** -22 * (np.abs(a) * c1 + np.abs(b) * s1)
+    t[..., p + half:] = c2 * tb + s2 * ta + 2.0 ** -22 * (np.abs(b) * c2 + np.abs(a) * s2)
+    return t
+
+
+def run_rope(tokens, q_lora, heads, layout="atoms", seed=7):
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    wl = W.RopeProj("t", tokens, q_lora, heads, 192, 64, seed=seed)
+    x, w = wl.x_rows(), wl.w_rows()
+    cos32, sin32 = wl.tables()
+    cos = torch.from_numpy(cos32).to(torch.bfloat16)
+    sin = torch.from_numpy(sin32).to(torch.bfloat16)
+    qx, sx = torch_ops.quantize(torch.from_numpy(x).cuda(), "mxfp8")
+    qw, sw = torch_ops.quantize(torch.from_numpy(w).cuda(), "mxfp8")
+    xc, xs = oq.quantize_logical(x[None], "mxfp8")
+    wc, wsc = oq.quantize_logical(w[None], "mxfp8")
+    assert np.array_equal(qx[0].cpu().numpy(), xc[0]) and np.array_equal(qw[0].cpu().numpy(), wc[0])
+    if layout == "plain":
+        sx_in = torch.from_numpy(np.ascontiguousarray(xs[0])).cuda()
+        sw_in = torch.from_numpy(np.ascontiguousarray(wsc[0])).cuda()
+    else:
+        sx_in, sw_in = sx, sw
+    ws = torch.zeros(bsg.bsg_rope_workspace_size(tokens, heads, 192, q_lora), dtype=torch.uint8, device="cuda")
+    out = torch_ops.gemm_rope_mxfp8(qx[0], sx_in, qw[0], sw_in, cos.cuda(), sin.cuda(), heads, scale_layout=layout,
+                                    workspace=ws)
+    torch.cuda.synchronize()
+    assert bsg.bsg_read_device_error(ws) == 0
+
+    cos64, sin64 = cos.double().numpy(), sin.double().numpy()
+    ref = orope.project(xc[0], xs[0], wc[0], wsc[0], cos64, sin64, heads, 192, 64)
+    xh, wh = orope.dequantize_plain(xc[0], xs[0]), orope.dequantize_plain(wc[0], wsc[0])
+    s_abs = (np.abs(xh) @ np.abs(wh).T).reshape(tokens, heads, 192)
+    tol = _tolerance((xh @ wh.T).reshape(tokens, heads, 192), s_abs, cos64, sin64, 192, 64)
+    n = heads * 192
+    y = ref["y"].reshape(tokens, n)
+    t = tol.reshape(tokens, n)
+    check_e4m3_blocks(out["out_fp8_row"].cpu().numpy().reshape(tokens, n),
+                      out["out_scales_row"].cpu().numpy().reshape(tokens, n // 32), y, t, 1.0, axis=1, what="row")
+    check_e4m3_blocks(out["out_fp8_col"].cpu().numpy().reshape(tokens, n),
+                      out["out_scales_col"].cpu().numpy().reshape(tokens // 32, n).T, y, t, 1.0, axis=0, what="col")
+    return out, ref
+
+
+@pytest.mark.parametrize("tokens,q_lora,heads,layout", [
+    (128, 256, 1, "atoms"),
+    (256, 512, 3, "atoms"),
+    (384, 96, 5, "plain"),     # K below one 128-wide stage
+    (512, 1536, 2, "plain"),
+])
+def test_gemm_rope(lib, tokens, q_lora, heads, layout):
+    run_rope(tokens, q_lora, heads, layout)
+
+
+def test_gemm_rope_identity_tables(lib):
+    """cos = 1, sin = 0: the rotary features are the de-interleaved projection."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    wl = W.RopeProj("t", 128, 128, 2, 192, 64, seed=3)
+    qx, sx = torch_ops.quantize(torch.from_numpy(wl.x_rows()).cuda(), "mxfp8")
+    qw, sw = torch_ops.quantize(torch.from_numpy(wl.w_rows()).cuda(), "mxfp8")
+    ones = torch.ones((128, 64), dtype=torch.bfloat16, device="cuda")
+    zeros = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch_ops.gemm_rope_mxfp8(qx[0], sx, qw[0], sw, ones, zeros, 2)
+    # the same projection with the pair order undone on the host: rotary block codes are a
+    # permutation of the un-rotated ones when the block scale is unchanged
+    out0 = torch_ops.gemm_rope_mxfp8(qx[0], sx, qw[0], sw, ones, zeros, 2)
+    torch.cuda.synchronize()
+    assert torch.equal(out["out_fp8_row"], out0["out_fp8_row"])  # deterministic
+    xc, xs = oq.quantize_logical(wl.x_rows()[None], "mxfp8")
+    wc, wsc = oq.quantize_logical(wl.w_rows()[None], "mxfp8")
+    ref = orope.project(xc[0], xs[0], wc[0], wsc[0], np.ones((128, 64)), np.zeros((128, 64)), 2, 192, 64)
+    y = ref["y"]
+    raw = (orope.dequantize_plain(xc[0], xs[0]) @ orope.dequantize_plain(wc[0], wsc[0]).T).reshape(128, 2, 192)
+    np.testing.assert_array_equal(y[..., 128:160], raw[..., 128::2])
+    np.testing.assert_array_equal(y[..., 160:], raw[..., 129::2])
+
+
+def test_gemm_rope_validation(lib):
+    import nvfp4_gemm_moe_gb300 as bsg
+    P = 0x10000
+    def call(**kw):
+        a = dict(tokens=256, q_lora=256, heads=2, hd=192, rope=64, layout=0, wsb=256)
+        a.update(kw)
+        return bsg.raw_status("bsg_gemm_rope_mxfp8", P, P, P, P, a["layout"], P, P, a["tokens"], a["q_lora"],
+                              a["heads"], a["hd"], a["rope"], P, P, P, P, None, P, a["wsb"], None)
+    assert call(tokens=100) == 1 and call(q_lora=48) == 1 and call(layout=2) == 1
+    assert call(hd=128) == 2 and call(rope=32) == 2
+    assert call(layout=1) == 8  # the plain layout needs room for the repacked scales
