@@ -119,12 +119,15 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     is_dense = isinstance(wl, W.Dense)
     is_dsw = isinstance(wl, W.GroupedDswiglu)
+    is_rope = isinstance(wl, W.RopeProj)
     fmt = wl.fmt
     flops = wl.flops
 
     # ---------------- inputs resident in HBM
     if is_dense:
         a_h, b_h = _dense_inputs(wl)
+    elif is_rope:
+        a_h, b_h = wl.x_rows()[None], wl.w_rows()[None]
     else:
         a_h, b_h = wl.a_rows()[None], wl.b_rows()
     a_pin = torch.from_numpy(a_h).pin_memory()
@@ -145,6 +148,10 @@ def run_ours(args, rank, world, local_rank):
                         device=dev)
         amax = torch.empty(1, dtype=torch.float32, device=dev)
         outs = None
+    elif is_rope:
+        cos_h, sin_h = (torch.from_numpy(t).to(torch.bfloat16).pin_memory() for t in wl.tables())
+        cos_d, sin_d = cos_h.to(dev), sin_h.to(dev)
+        outs = {}
     else:
         offs = torch.from_numpy(wl.padded_offsets()).to(dev)
         alpha = torch.from_numpy(wl.alpha()).to(dev)
@@ -162,6 +169,9 @@ def run_ours(args, rank, world, local_rank):
     def gemm():
         if is_dense:
             torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, wl.m, wl.n, wl.k, wl.l, c=c, amax=amax, workspace=ws)
+        elif is_rope:
+            outs.update(torch_ops.gemm_rope_mxfp8(qa[0], sfa, qb[0], sfb, cos_d, sin_d, wl.heads, wl.head_dim,
+                                                  wl.qk_rope, outputs=outs, workspace=ws))
         elif is_dsw:
             outs["dprob"].zero_()  # the call adds each row's sum into dprob
             outs.update(torch_ops.grouped_gemm_dswiglu(qa[0], qb, sfa, sfb, fmt, offs, alpha, beta, prob, c_in, wl.n,
@@ -216,9 +226,12 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------- end to end through the C ABI from pinned host buffers
     e2e_steps = max(3, min(args.steps, 20))
-    inputs = [(a_d, a_pin), (b_d, b_pin)] + ([(c_in, c_pin)] if is_dsw else [])
+    inputs = [(a_d, a_pin), (b_d, b_pin)] + ([(c_in, c_pin)] if is_dsw else []) + \
+        ([(cos_d, cos_h), (sin_d, sin_h)] if is_rope else [])
     if is_dense:
         results = [c, amax]
+    elif is_rope:
+        results = [outs["out_fp8_row"], outs["out_scales_row"], outs["out_fp8_col"], outs["out_scales_col"]]
     elif is_dsw:
         results = [outs["d_row"], outs["dprob"]] + ([outs["amax"]] if "amax" in outs else [outs["sfd_row"]])
     else:
@@ -296,6 +309,11 @@ def _traffic(workload):
 
 
 def _config(wl):
+    if isinstance(wl, W.RopeProj):
+        return {"workload": wl.name, "format": wl.fmt, "tokens": wl.tokens, "q_lora": wl.q_lora, "heads": wl.heads,
+                "head_dim": wl.head_dim, "qk_rope": wl.qk_rope, "flops_per_step": wl.flops,
+                "l2": "no flush: fp32 inputs of %.2f GB exceed L2" % ((wl.tokens + wl.n) * wl.q_lora * 4 / 1e9),
+                "step": "quantise x + quantise w + projection GEMM/RoPE/row+column MXFP8"}
     if isinstance(wl, W.Dense):
         return {"workload": wl.name, "format": wl.fmt, "m": wl.m, "n": wl.n, "k": wl.k, "l": wl.l,
                 "c_dtype": wl.c_dtype, "flops_per_step": wl.flops,
@@ -321,19 +339,28 @@ def oracle_rows(wl, requested=0):
     """Rows of A in the oracle's timed sample: `requested`, else enough for ORACLE_SAMPLE_FLOPS."""
     if requested > 0:
         return int(requested)
+    if isinstance(wl, W.RopeProj):
+        return max(256, min(int(ORACLE_SAMPLE_FLOPS / (2.0 * wl.n * wl.q_lora)) // 256 * 256, wl.tokens))
     max_rows = wl.m if isinstance(wl, W.Dense) else wl.valid_m
     rows = int(ORACLE_SAMPLE_FLOPS / (2.0 * wl.n * wl.k)) // 256 * 256
     return max(256, min(rows, max_rows))
 
 
 def run_reference(args):
-    from oracle import dswiglu as od, gemm as og, quantize as oq
+    from oracle import dswiglu as od, gemm as og, quantize as oq, rope as orope
     wl = W.ALL[args.workload]
     cores = os.cpu_count() or 1
     step_times, sample_flops = [], 0.0
     args.ref_rows = oracle_rows(wl, args.ref_rows)
 
     def one_step():
+        if isinstance(wl, W.RopeProj):
+            rows = np.arange(args.ref_rows)            # the first tokens, all heads
+            xc, xs = oq.quantize_logical(wl.x_rows(rows)[None], wl.fmt)
+            wc, wsc = oq.quantize_logical(wl.w_rows()[None], wl.fmt)
+            cos, sin = (t[:len(rows)] for t in wl.tables())
+            orope.project(xc[0], xs[0], wc[0], wsc[0], cos, sin, wl.heads, wl.head_dim, wl.qk_rope)
+            return 2.0 * len(rows) * wl.n * wl.q_lora
         if isinstance(wl, W.Dense):
             rows = np.arange(args.ref_rows)           # first rows of batch 0 of A
             a = wl.a_rows(rows)[None]

@@ -68,10 +68,13 @@ struct GemmTraits {
   static constexpr int kSfBase = kAcc * BN;
   // barrier / scalar area after the stages
   static constexpr int kBarBytes = 1024;
-  static constexpr int kOffsetsBytes = 4096;  // padded_offsets of up to 1024 experts (grouped)
-  static constexpr int kAmaxBytes = 4096;     // per-expert amax staging (grouped bf16 D)
-  // grouped epilogues: one 32-row x 64-byte transpose block per epilogue warp
-  static constexpr int kXposeBytes = EPI == kEpiDense ? 0 : 8 * kXposeBlockBytes;
+  // padded_offsets of up to 1024 experts (grouped only)
+  static constexpr int kOffsetsBytes = epi_is_grouped(EPI) ? 4096 : 0;
+  // per-expert amax staging (grouped), the dense amax, or the warps' 32-float scale exchange
+  static constexpr int kAmaxBytes = epi_is_grouped(EPI) ? 4096 : 1024;
+  // one transpose block per epilogue warp: 32 rows x 64 bytes (grouped), 32 x 32 bytes (RoPE)
+  static constexpr int kXposeBlock = EPI == kEpiRope ? 1024 : kXposeBlockBytes;
+  static constexpr int kXposeBytes = EPI == kEpiDense ? 0 : 8 * kXposeBlock;
   // as many stages as shared memory and the TMEM scale-factor slots allow, at most six
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
@@ -1083,20 +1086,20 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       };
       if constexpr (EPI == kEpiRope) {
         epilogue_tile_rope<BN>(p, row, tc.nt, tmem_acc, lane, half, s_amax + (warp - 2) * 32,
-                               s_xpose + (warp - 2) * kXposeBlockBytes);
+                               s_xpose + (warp - 2) * T::kXposeBlock);
         release();
       } else if constexpr (epi_is_dswiglu(EPI)) {
         epilogue_tile_dswiglu<BN, EPI == kEpiDswigluFP8>(p, row, tc.nt * BN, tmem_acc, lane, alpha_g, p.beta[tc.l],
                                                          prob_r, nc, run_max, run_max2, half, 2,
                                                          s_amax + (warp - 2) * 32,
-                                                         s_xpose + (warp - 2) * kXposeBlockBytes);
+                                                         s_xpose + (warp - 2) * T::kXposeBlock);
         release();
       } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
         epilogue_dense_bf16_early<BN, false>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release, nullptr,
                                              lane);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
-                               s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * kXposeBlockBytes);
+                               s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * T::kXposeBlock);
         release();
       }
       if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }

@@ -59,7 +59,8 @@ struct PairTraits {
   static constexpr int kBarBytes = 1024;
   static constexpr int kOffsetsBytes = 4096;
   static constexpr int kAmaxBytes = 4096;
-  static constexpr int kXposeBytes = 8 * kXposeBlockBytes;  // one transpose block per epilogue warp
+  static constexpr int kXposeBlock = kXposeBlockBytes;
+  static constexpr int kXposeBytes = 8 * kXposeBlock;  // one transpose block per epilogue warp
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
   static constexpr int kStagesTmem = (512 - kSfBase) / kSfStride;
@@ -351,14 +352,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         epilogue_tile_dswiglu<BN, EPI == kEpiDswigluFP8>(p, row, tc.nt * BN, tmem_acc, lane, alpha_g, p.beta[tc.l],
                                                          prob_r, nc, run_max, run_max2, half, 2,
                                                          s_amax + (warp - 2) * 32,
-                                                         s_xpose + (warp - 2) * kXposeBlockBytes);
+                                                         s_xpose + (warp - 2) * T::kXposeBlock);
         release();
       } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
         epilogue_dense_bf16_early<BN, true>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release,
-                                            s_xpose + (warp - 2) * kXposeBlockBytes, lane);
+                                            s_xpose + (warp - 2) * T::kXposeBlock, lane);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
-                               s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * kXposeBlockBytes);
+                               s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * T::kXposeBlock);
         release();
       }
       if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }

@@ -163,3 +163,47 @@ def test_grouped_full_size_sampled(lib, wl):
                 d_max = float(out["d"][begin:end].float().abs().max().cpu())
                 assert abs(amax[g] - d_max) <= float(formats.bf16_ulp(np.array([amax[g]]))[0]), (g, amax[g], d_max)
             begin = end
+
+
+def test_rope_full_size_sampled(lib):
+    """The 16384-token DeepSeek-V3 Q up-projection: 32-token blocks x single heads recomputed by
+    the oracle (row and column scales of a block depend only on its own 32 tokens / features)."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    from oracle import rope as orope
+    from test_gpu_rope import _tolerance
+    wl = W.ROPE_PROJ_T16384
+    x = torch.from_numpy(wl.x_rows()).cuda()
+    w = torch.from_numpy(wl.w_rows()).cuda()
+    qx, sx = torch_ops.quantize(x, "mxfp8")
+    qw, sw = torch_ops.quantize(w, "mxfp8")
+    del x, w
+    cos32, sin32 = wl.tables()
+    cos = torch.from_numpy(cos32).to(torch.bfloat16)
+    sin = torch.from_numpy(sin32).to(torch.bfloat16)
+    ws = torch_ops.new_workspace()
+    out = torch_ops.gemm_rope_mxfp8(qx[0], sx, qw[0], sw, cos.cuda(), sin.cuda(), wl.heads, wl.head_dim, wl.qk_rope,
+                                    workspace=ws)
+    torch.cuda.synchronize()
+    assert bsg.bsg_read_device_error(ws) == 0
+    d = wl.head_dim
+    for t0 in (0, 8192, wl.tokens - 32):
+        rows = np.arange(t0, t0 + 32)
+        xc, xs = oq.quantize_logical(wl.x_rows(rows)[None], "mxfp8")
+        assert np.array_equal(qx[0][t0:t0 + 32].cpu().numpy(), xc[0])
+        for h in (0, 77, wl.heads - 1):
+            wrows = np.arange(h * d, (h + 1) * d)
+            wc, wsc = oq.quantize_logical(wl.w_rows(wrows)[None], "mxfp8")
+            c64 = cos[t0:t0 + 32].double().numpy()
+            s64 = sin[t0:t0 + 32].double().numpy()
+            ref = orope.project(xc[0], xs[0], wc[0], wsc[0], c64, s64, 1, d, wl.qk_rope)
+            xh, wh = orope.dequantize_plain(xc[0], xs[0]), orope.dequantize_plain(wc[0], wsc[0])
+            tol = _tolerance((xh @ wh.T).reshape(32, 1, d), (np.abs(xh) @ np.abs(wh).T).reshape(32, 1, d), c64, s64,
+                             d, wl.qk_rope).reshape(32, d)
+            y = ref["y"].reshape(32, d)
+            check_e4m3_blocks(out["out_fp8_row"][t0:t0 + 32, h].cpu().numpy(),
+                              out["out_scales_row"][t0:t0 + 32, h].cpu().numpy(), y, tol, 1.0, axis=1,
+                              what=f"row[t{t0}, h{h}]")
+            check_e4m3_blocks(out["out_fp8_col"][t0:t0 + 32, h].cpu().numpy(),
+                              out["out_scales_col"][t0 // 32, h].cpu().numpy()[:, None], y, tol, 1.0, axis=0,
+                              what=f"col[t{t0}, h{h}]")
