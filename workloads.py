@@ -330,6 +330,9 @@ GROUPED_SRELU_E32_CLAMP = dataclasses.replace(GROUPED_SRELU_E32, name=GROUPED_SR
                                               tanh_clamp=32.0)
 GROUPED_FP8D_E128 = Grouped("grouped_mxfp8_fp8d_e128_k4096_n4096", 128, 4096, 4096, 65536, "zipf1.2", "e4m3")
 
+# the E4M3-D kernel on 32 experts (same K, N, routing skew): the case its ncu capture runs on,
+# a few GB on the device instead of the 128-expert workload's twelve
+GROUPED_FP8D_E32 = Grouped("grouped_mxfp8_fp8d_e32_k4096_n4096", 32, 4096, 4096, 16384, "zipf1.2", "e4m3")
 # the backward of the E32 expert layer: dSwiGLU over the same routing, ref N = 2048 (C and D 4096 wide)
 GROUPED_DSWIGLU_E32 = GroupedDswiglu("grouped_mxfp8_dswiglu_e32_k7168_n2048", 32, 7168, 2048, 32768, "uniform",
                                      "bf16")
@@ -340,5 +343,5 @@ GROUPED_DSWIGLU_E32_FP8D = dataclasses.replace(GROUPED_DSWIGLU_E32, name="groupe
 ROPE_PROJ_T16384 = RopeProj("rope_proj_mxfp8_t16384_q1536_h128_d192", 16384, 1536, 128, 192, 64)
 
 ALL = {w.name: w for w in (DENSE_MXFP8_256, DENSE_MXFP8_8192, DENSE_MXFP8_8192_L1, DENSE_NVFP4_16384, GROUPED_SRELU_E32,
-                           GROUPED_SRELU_E32_CLAMP, GROUPED_FP8D_E128, GROUPED_DSWIGLU_E32, GROUPED_DSWIGLU_E32_FP8D,
-                           ROPE_PROJ_T16384)}
+                           GROUPED_SRELU_E32_CLAMP, GROUPED_FP8D_E128, GROUPED_FP8D_E32, GROUPED_DSWIGLU_E32,
+                           GROUPED_DSWIGLU_E32_FP8D, ROPE_PROJ_T16384)}
