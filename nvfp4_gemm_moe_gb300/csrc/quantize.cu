@@ -150,13 +150,41 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const float* _
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
         const uint32_t code = ue4m3_code_of_amax_over_6(a);
         const float s = ue4m3_value(code);
-        float t[7];
-        e2m1_thresholds(s, t);
-        uint32_t nib = 0;
-        if (code != 0) {
-          nib = e2m1_nibble(v0[j].x, t) | (e2m1_nibble(v0[j].y, t) << 4) | (e2m1_nibble(v0[j].z, t) << 8) |
-                (e2m1_nibble(v0[j].w, t) << 12) | (e2m1_nibble(v1[j].x, t) << 16) | (e2m1_nibble(v1[j].y, t) << 20) |
-                (e2m1_nibble(v1[j].z, t) << 24) | (e2m1_nibble(v1[j].w, t) << 28);
+        // Fast path: y = x * RN(1/s) rounded once more, converted by the hardware's RNE
+        // E2M1 conversion.  y is within a relative 2^-23 of the exact x / s, so the two round
+        // alike unless a midpoint of E2M1 lies between them or one of them is a midpoint, and
+        // then y is within a few ulps of that midpoint.  Every midpoint (0.25, 0.75, ..., 5) has
+        // a float pattern whose low 21 mantissa bits are zero, so a y with |y| >= 0.2 whose
+        // pattern lies within 16 of a multiple of 2^21 sends the whole unit to the exact
+        // threshold path below (about 1e-5 of random values).  The sign bit of x is or-ed in,
+        // so a negative value that rounds to zero gives -0 as on the exact path; s = 0 gives +0.
+        const float inv = code != 0 ? __frcp_rn(s) : 0.0f;
+        const float y[8] = {v0[j].x * inv, v0[j].y * inv, v0[j].z * inv, v0[j].w * inv,
+                            v1[j].x * inv, v1[j].y * inv, v1[j].z * inv, v1[j].w * inv};
+        bool near = false;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t b = __float_as_uint(y[e]) & 0x7FFFFFFFu;
+          near |= b >= 0x3E4CCCCDu /* 0.2f */ && ((b + 16u) & 0x1FFFFFu) < 32u;
+        }
+        uint32_t nib;
+        if (!__any_sync(0xffffffffu, near)) {
+          nib = cvt_e2m1x2(y[0], y[1]) | (cvt_e2m1x2(y[2], y[3]) << 8) | (cvt_e2m1x2(y[4], y[5]) << 16) |
+                (cvt_e2m1x2(y[6], y[7]) << 24);
+          const float xs[8] = {v0[j].x, v0[j].y, v0[j].z, v0[j].w, v1[j].x, v1[j].y, v1[j].z, v1[j].w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) nib |= (__float_as_uint(xs[e]) >> 31) << (4 * e + 3);
+          if (code == 0) nib = 0;
+        } else {
+          float t[7];
+          e2m1_thresholds(s, t);
+          nib = 0;
+          if (code != 0) {
+            nib = e2m1_nibble(v0[j].x, t) | (e2m1_nibble(v0[j].y, t) << 4) | (e2m1_nibble(v0[j].z, t) << 8) |
+                  (e2m1_nibble(v0[j].w, t) << 12) | (e2m1_nibble(v1[j].x, t) << 16) |
+                  (e2m1_nibble(v1[j].y, t) << 20) | (e2m1_nibble(v1[j].z, t) << 24) |
+                  (e2m1_nibble(v1[j].w, t) << 28);
+          }
         }
         if (row_ok && kk < k) *reinterpret_cast<uint32_t*>(q + (row_g * k + kk) / 2) = nib;
         // block b of the unit is held by lanes 2b and 2b + 1; scale word w (blocks 4w..4w+3)

@@ -92,3 +92,30 @@ def test_quantize_workload_rows_bit_exact(lib):
     q, sf = _run(lib, x, "mxfp8")
     q_ref, sf_ref = oq.quantize(x, "mxfp8")
     assert np.array_equal(sf, sf_ref) and np.array_equal(q.reshape(q_ref.shape), q_ref)
+
+
+def test_quantize_nvfp4_near_midpoints(lib):
+    """Values 1 to 80 ulps on either side of every E2M1 midpoint, under many block scales: the
+    hardware-conversion fast path and its exact fallback must both agree with the oracle."""
+    rng = np.random.default_rng(17)
+    rows, k = 256, 512
+    mids = np.asarray(formats.E2M1_MIDS, dtype=np.float32)
+    n = rows * k
+    m = mids[rng.integers(0, len(mids), n)]
+    # even rows stay 40+ ulps of x (20+ of x / s) away, so their units take the fast path; odd
+    # rows come within 1 ulp
+    lo = np.where((np.arange(n) // k) % 2 == 0, 40, 1)
+    ulps = (rng.integers(lo, 81) * rng.choice([-1, 1], n)).astype(np.int32)
+    scale_codes = rng.integers(0x10, 0x70, rows * k // 16)  # UE4M3 scales 2^-5 .. 2^6 with mantissas
+    s = np.repeat(formats.decode_ue4m3(scale_codes), 16).astype(np.float32)
+    base = (m * s).astype(np.float32)  # exact: 3 + 4 significant bits
+    x = (base.view(np.int32) + ulps).view(np.float32)
+    x = np.where(rng.random(n) < 0.5, -x, x).astype(np.float32)
+    # each block's amax (40 ulps above 6 s, so off the E2M1 grid) pins its scale to s
+    pin = ((6.0 * s[::16]).astype(np.float32).view(np.int32) + 40).view(np.float32)
+    x[::16] = np.copysign(pin, x[::16])
+    x = x.reshape(1, rows, k)
+    q, sf = _run(lib, x, "nvfp4")
+    q_ref, sf_ref = oq.quantize(x, "nvfp4")
+    assert np.array_equal(sf, sf_ref)
+    assert np.array_equal(q.reshape(q_ref.shape), q_ref), f"{(q.reshape(q_ref.shape) != q_ref).sum()} code bytes differ"
