@@ -629,6 +629,13 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
   const int64_t n = num_heads * head_dim;
   if (!fits_int32(tokens) || !fits_int32(n) || !fits_int32(q_lora) || !fits_int32(tokens * (n / 32)))
     return BSG_ERR_INVALID_ARG;
+  // One head per 128 x 192 tile (two accumulators: the dual E4M3 epilogue overlaps the next
+  // tile's MMAs), or with opts->cta_pair == 2 CTA pairs on 256 x 256 tiles spanning heads (a
+  // head's rotary chunk pair never straddles a 256-column tile); the pair tiles' single
+  // accumulator exposes that epilogue and measured slower at the DeepSeek-V3 shapes
+  const int cta_pair = opts ? opts->cta_pair : 0;
+  const bool pair_ok = tokens % 256 == 0 && n % 256 == 0;
+  if (cta_pair == 2 && !pair_ok) return BSG_ERR_INVALID_ARG;
   const size_t ws_need = scale_layout == 1 ? bsg_rope_workspace_size(tokens, num_heads, head_dim, q_lora)
                                            : kWorkspaceBytes;
   if (!workspace || workspace_bytes < ws_need) return BSG_ERR_WORKSPACE;
@@ -655,13 +662,14 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
     sfb = pb;
   }
 
-  const int bn = 192;
-  const int64_t m_tiles = tokens / 128;
-  const int64_t n_tiles = num_heads;
+  const bool pairs = pair_ok && cta_pair == 2;
+  const int bn = pairs ? 256 : 192;
+  const int64_t m_tiles = pairs ? tokens / 256 : tokens / 128;
+  const int64_t n_tiles = n / bn;
   const int64_t tiles = m_tiles * n_tiles;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, x, q_lora, tokens, 1, 128) || !make_operand_map(&tb, w, q_lora, n, 1, bn))
+  if (!make_operand_map(&ta, x, q_lora, tokens, 1, 128) || !make_operand_map(&tb, w, q_lora, n, 1, pairs ? 128 : bn))
     return BSG_ERR_CUDA;
 
   GemmParams p;
@@ -676,7 +684,7 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
   p.num_tiles = static_cast<int>(tiles);
   p.sfa = sfa;
   p.sfb = sfb;
-  p.sfa_mt = static_cast<int>(m_tiles);
+  p.sfa_mt = static_cast<int>(tokens / 128);
   p.sfb_mt = static_cast<int>(cdiv(n, 128));
   p.sf_kt = static_cast<int>(cdiv(q_lora / 32, 4));
   p.c_kind = bsg::kOutNone;
@@ -690,7 +698,8 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
   p.err = static_cast<uint32_t*>(workspace);
 
   GemmConfig cfg{bsg::kMXFP8, bn, bsg::kEpiRope};
-  cudaError_t e = bsg::launch_gemm_rope(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
+  cudaError_t e = pairs ? bsg::launch_gemm_pair_rope(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
+                        : bsg::launch_gemm_rope(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
   if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }

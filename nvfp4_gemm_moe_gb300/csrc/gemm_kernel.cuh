@@ -617,36 +617,28 @@ __device__ __forceinline__ void epilogue_tile_dswiglu(const GemmParams& p, int r
 // bf16 bit pattern to fp32 (exact).
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits) { return __uint_as_float(bits << 16); }
 
-// GEMM + RoPE + MXFP8 epilogue of one tile, 128 tokens x one head of BN = HEAD_DIM features,
-// for the rows (tokens) of one warp ("GEMM + RoPE + MXFP8 Projection (SM100)", Equations).
-// The first BN - 64 features pass unchanged; the last 64 (two accumulator chunks) hold 32
-// interleaved pairs (a_j, b_j) = (y[2j], y[2j+1]) that leave as halves:
-//   out[j] = a_j cos[t, j] - b_j sin[t, j],   out[32 + j] = b_j cos[t, 32 + j] + a_j sin[t, 32 + j].
-// Every 32-feature block is then quantised by rows and by columns (store_e4m3_block with plain
-// scale arrays).  The two warps of a quadrant split the chunks: half 0 takes the first BN/64,
-// half 1 the rest, which include both rotary chunks (their pairs span the two).
-template <int BN>
-__device__ __forceinline__ void epilogue_tile_rope(const GemmParams& p, int row, int head, uint32_t tmem_acc,
-                                                   int lane, int half, float* s_inv, uint8_t* s_blk) {
-  constexpr int kChunks = BN / 32;
-  constexpr int kRope = kChunks - 2;  // first rotary chunk
-  const int c_begin = half == 0 ? 0 : kChunks / 2;
-  const int c_end = half == 0 ? kChunks / 2 : kRope;
-  const int col_head = head * BN;
-#pragma unroll 1
-  for (int c = c_begin; c < c_end; ++c) {
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(tmem_acc + c * 32, r);
-    tmem_ld_wait(r);
-    float d[32];
+// One 32-feature chunk of the RoPE projection that passes unchanged: read from TMEM at
+// tmem_chunk, quantised by rows and columns at output column dcol0.
+__device__ __forceinline__ void rope_plain_chunk(const GemmParams& p, int row, uint32_t tmem_chunk, int dcol0,
+                                                 int lane, float* s_inv, uint8_t* s_blk) {
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(tmem_chunk, r);
+  tmem_ld_wait(r);
+  float d[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(r[j]);
-    store_e4m3_block<true>(p, row, col_head + c * 32, p.n, d, lane, s_inv, s_blk);
-  }
-  if (half == 0) return;  // warp-uniform
+  for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(r[j]);
+  store_e4m3_block<true>(p, row, dcol0, p.n, d, lane, s_inv, s_blk);
+}
+
+// The two rotary chunks of one head (TMEM tmem_chunk and tmem_chunk + 32, output columns dcol0
+// and dcol0 + 32): 32 interleaved pairs (a_j, b_j) = (y[2j], y[2j+1]) leave as halves,
+//   out[j] = a_j cos[t, j] - b_j sin[t, j],   out[32 + j] = b_j cos[t, 32 + j] + a_j sin[t, 32 + j],
+// then both output blocks are quantised by rows and columns.
+__device__ __forceinline__ void rope_rotary_pair(const GemmParams& p, int row, uint32_t tmem_chunk, int dcol0,
+                                                 int lane, float* s_inv, uint8_t* s_blk) {
   uint32_t r0[32], r1[32];
-  tmem_ld_32x32b_x32(tmem_acc + kRope * 32, r0);
-  tmem_ld_32x32b_x32(tmem_acc + (kRope + 1) * 32, r1);
+  tmem_ld_32x32b_x32(tmem_chunk, r0);
+  tmem_ld_32x32b_x32(tmem_chunk + 32, r1);
   tmem_ld_wait(r0);
   tmem_ld_wait(r1);
   const uint16_t* cs = p.rope_cos + static_cast<uint64_t>(row) * p.qk_rope;
@@ -692,8 +684,44 @@ __device__ __forceinline__ void epilogue_tile_rope(const GemmParams& p, int row,
     hi[j] = __uint_as_float(r0[2 * j + 1]);
     hi[16 + j] = __uint_as_float(r1[2 * j + 1]);
   }
-  store_e4m3_block<true>(p, row, col_head + kRope * 32, p.n, lo, lane, s_inv, s_blk);
-  store_e4m3_block<true>(p, row, col_head + (kRope + 1) * 32, p.n, hi, lane, s_inv, s_blk);
+  store_e4m3_block<true>(p, row, dcol0, p.n, lo, lane, s_inv, s_blk);
+  store_e4m3_block<true>(p, row, dcol0 + 32, p.n, hi, lane, s_inv, s_blk);
+}
+
+// GEMM + RoPE + MXFP8 epilogue of one tile ("GEMM + RoPE + MXFP8 Projection (SM100)",
+// Equations) for the rows (tokens) of one warp: output columns col_base .. col_base + BN - 1
+// of the (tokens, heads x 192) projection.  Global 32-column chunk g is chunk g % 6 of head
+// g / 6; chunks 4 and 5 of a head are rotary (RoPE, rope_rotary_pair), the rest pass unchanged.
+// BN = 192 (one head per tile): half 0 of a quadrant's warps takes chunks 0-2, half 1 chunk 3
+// and the rotary pair.  BN = 256: the tile's chunks go in pairs (0,1), (2,3), (4,5), (6,7), half
+// 0 taking the first and third, half 1 the others; a pair starts at an even global chunk, so
+// it is either two plain chunks or one head's rotary pair (g % 6 == 4), never split.
+template <int BN>
+__device__ __forceinline__ void epilogue_tile_rope(const GemmParams& p, int row, int col_base, uint32_t tmem_acc,
+                                                   int lane, int half, float* s_inv, uint8_t* s_blk) {
+  static_assert(BN == 192 || BN == 256, "RoPE tiles");
+  if constexpr (BN == 192) {
+    // col_base = head * 192: chunks 0-3 plain, 4-5 rotary
+    if (half == 0) {
+#pragma unroll 1
+      for (int c = 0; c < 3; ++c) rope_plain_chunk(p, row, tmem_acc + c * 32, col_base + c * 32, lane, s_inv, s_blk);
+    } else {
+      rope_plain_chunk(p, row, tmem_acc + 3 * 32, col_base + 3 * 32, lane, s_inv, s_blk);
+      rope_rotary_pair(p, row, tmem_acc + 4 * 32, col_base + 4 * 32, lane, s_inv, s_blk);
+    }
+  } else {
+#pragma unroll 1
+    for (int q = half; q < 4; q += 2) {
+      const int c = 2 * q;  // first chunk of the pair within the tile
+      const int g = (col_base >> 5) + c;
+      if (g % 6 == 4) {
+        rope_rotary_pair(p, row, tmem_acc + c * 32, col_base + c * 32, lane, s_inv, s_blk);
+      } else {
+        rope_plain_chunk(p, row, tmem_acc + c * 32, col_base + c * 32, lane, s_inv, s_blk);
+        rope_plain_chunk(p, row, tmem_acc + (c + 1) * 32, col_base + (c + 1) * 32, lane, s_inv, s_blk);
+      }
+    }
+  }
 }
 
 // Folds one warp's running maxima of expert g into shared memory: the per-expert amax of the
@@ -1085,7 +1113,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         if (lane == 0) mbar_arrive(&tmem_empty[acc]);
       };
       if constexpr (EPI == kEpiRope) {
-        epilogue_tile_rope<BN>(p, row, tc.nt, tmem_acc, lane, half, s_amax + (warp - 2) * 32,
+        epilogue_tile_rope<BN>(p, row, tc.nt * BN, tmem_acc, lane, half, s_amax + (warp - 2) * 32,
                                s_xpose + (warp - 2) * T::kXposeBlock);
         release();
       } else if constexpr (epi_is_dswiglu(EPI)) {

@@ -348,7 +348,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(empty_leader + acc * 8);
       };
-      if constexpr (epi_is_dswiglu(EPI)) {
+      if constexpr (EPI == kEpiRope) {
+        epilogue_tile_rope<BN>(p, row, tc.nt * BN, tmem_acc, lane, half, s_amax + (warp - 2) * 32,
+                               s_xpose + (warp - 2) * T::kXposeBlock);
+        release();
+      } else if constexpr (epi_is_dswiglu(EPI)) {
         epilogue_tile_dswiglu<BN, EPI == kEpiDswigluFP8>(p, row, tc.nt * BN, tmem_acc, lane, alpha_g, p.beta[tc.l],
                                                          prob_r, nc, run_max, run_max2, half, 2,
                                                          s_amax + (warp - 2) * 32,

@@ -2,6 +2,7 @@
 // epilogue ("GEMM + RoPE + MXFP8 Projection (SM100)"), and the plain-to-atom scale repack it
 // uses for callers that hold plain row-major E8M0 scales.
 #include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 
 namespace bsg {
 
@@ -9,6 +10,13 @@ cudaError_t launch_gemm_rope(const GemmConfig& cfg, const CUtensorMap& ta, const
                              int grid, cudaStream_t stream) {
   if (cfg.fmt == kMXFP8 && cfg.bn == 192 && cfg.epi == kEpiRope)
     return launch_gemm_t<kMXFP8, 192, kEpiRope>(ta, tb, p, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_pair_rope(const GemmConfig& cfg, const CUtensorMap& ta, const CUtensorMap& tb,
+                                  const GemmParams& p, int max_pairs, cudaStream_t stream) {
+  if (cfg.fmt == kMXFP8 && cfg.bn == 256 && cfg.epi == kEpiRope)
+    return launch_gemm_pair_t<kMXFP8, 256, kEpiRope>(ta, tb, p, max_pairs, stream);
   return cudaErrorInvalidValue;
 }
 

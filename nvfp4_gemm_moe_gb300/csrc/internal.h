@@ -99,9 +99,12 @@ cudaError_t launch_gemm_dswiglu(const GemmConfig& cfg, const CUtensorMap& tmap_a
 cudaError_t launch_gemm_pair_dswiglu(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                                      const GemmParams& p, int max_pairs, cudaStream_t stream);
 
-// The GEMM + RoPE + MXFP8 projection kernel (one-CTA tiles of 128 tokens x one head).
+// The GEMM + RoPE + MXFP8 projection kernels: one-CTA tiles of 128 tokens x one head, or CTA
+// pairs on 256 x 256 tiles spanning heads.
 cudaError_t launch_gemm_rope(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                              const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_pair_rope(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                                  const GemmParams& p, int max_pairs, cudaStream_t stream);
 
 // Scatters plain row-major scale bytes (rows, blocks) into the 128x4 atom layout (dst zeroed
 // first, so padding bytes hold the finite scale 0).

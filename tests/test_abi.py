@@ -1,7 +1,9 @@
 """The C ABI library loads, exports every declared entry point, and validates arguments on the host.
 
 These tests need no GPU: every rejected call returns its status before any CUDA call, and
-the pointers passed are fake values that are never dereferenced.
+the pointers passed are fake values that are never dereferenced.  A call that passes every
+check would enqueue work on those fake pointers, so it runs only where no CUDA device is
+present (it then stops at the device check).
 """
 import ctypes
 import os
@@ -14,6 +16,15 @@ from nvfp4_gemm_moe_gb300 import build as bsg_build
 
 OK, INVALID, UNSUPPORTED, ALIGN, ARCH, CUDA, DEVICE, BAD_OFFS, WORKSPACE = range(9)
 P = 0x10000  # a fake, 16-byte aligned "device pointer" (never dereferenced by a rejected call)
+
+
+def _no_device() -> bool:
+    """True when no CUDA device is visible: only then may a call pass validation with fake pointers."""
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except ImportError:
+        return True
 
 
 def _declared_functions():
@@ -93,8 +104,9 @@ def test_dense_validation():
     assert _dense(ab=bsg.E2M1, sf=bsg.SF_UE4M3, v=16, k=48) == ALIGN  # 24-byte rows
     assert _dense(m=1 << 31) == INVALID
     # a valid call on a machine without a usable sm_103 device stops at the device check
-    st = _dense()
-    assert st in (OK, ARCH, CUDA)
+    if _no_device():
+        st = _dense()
+        assert st in (OK, ARCH, CUDA)
 
 
 def _grouped(**kw):
@@ -124,8 +136,9 @@ def test_grouped_validation():
     assert _grouped(s=float("nan")) == INVALID
     assert _grouped(ws=None) == WORKSPACE
     assert _grouped(offs=P + 2) == ALIGN
-    st = _grouped()
-    assert st in (OK, ARCH, CUDA)
+    if _no_device():
+        st = _grouped()
+        assert st in (OK, ARCH, CUDA)
 
 
 def _discrete(**kw):
@@ -146,8 +159,9 @@ def test_discrete_validation():
     assert _discrete(bp=P + 4) == ALIGN                    # int64 array
     assert _discrete(ws=P + 64) == ALIGN
     assert _discrete(L=0) == INVALID
-    st = _discrete()
-    assert st in (OK, ARCH, CUDA)
+    if _no_device():
+        st = _discrete()
+        assert st in (OK, ARCH, CUDA)
 
 
 def _dsw(**kw):
@@ -174,10 +188,11 @@ def test_dswiglu_validation():
     assert _dsw(dprob=P + 2) == ALIGN
     assert _dsw(c=P + 8) == ALIGN
     assert _dsw(wsb=16) == WORKSPACE
-    st = _dsw()
-    assert st in (OK, ARCH, CUDA)
-    st = _dsw(dk=bsg.E4M3, dcol=P, sfr=P, sfc=P, nc=P, amax=None, ck=bsg.E4M3)
-    assert st in (OK, ARCH, CUDA)
+    if _no_device():
+        st = _dsw()
+        assert st in (OK, ARCH, CUDA)
+        st = _dsw(dk=bsg.E4M3, dcol=P, sfr=P, sfc=P, nc=P, amax=None, ck=bsg.E4M3)
+        assert st in (OK, ARCH, CUDA)
 
 
 def test_noalloc_validation():

@@ -26,7 +26,7 @@ def _tolerance(raw, s_abs, cos, sin, head_dim, qk_rope):
     return t
 
 
-def run_rope(tokens, q_lora, heads, layout="atoms", seed=7):
+def run_rope(tokens, q_lora, heads, layout="atoms", seed=7, cta_pair=0):
     from nvfp4_gemm_moe_gb300 import torch_ops
     import nvfp4_gemm_moe_gb300 as bsg
     wl = W.RopeProj("t", tokens, q_lora, heads, 192, 64, seed=seed)
@@ -46,7 +46,7 @@ def run_rope(tokens, q_lora, heads, layout="atoms", seed=7):
         sx_in, sw_in = sx, sw
     ws = torch.zeros(bsg.bsg_rope_workspace_size(tokens, heads, 192, q_lora), dtype=torch.uint8, device="cuda")
     out = torch_ops.gemm_rope_mxfp8(qx[0], sx_in, qw[0], sw_in, cos.cuda(), sin.cuda(), heads, scale_layout=layout,
-                                    workspace=ws)
+                                    workspace=ws, cta_pair=cta_pair)
     torch.cuda.synchronize()
     assert bsg.bsg_read_device_error(ws) == 0
 
@@ -75,6 +75,15 @@ def test_gemm_rope(lib, tokens, q_lora, heads, layout):
     run_rope(tokens, q_lora, heads, layout)
 
 
+@pytest.mark.parametrize("tokens,q_lora,heads,layout,cta_pair", [
+    (256, 256, 4, "atoms", 2),    # CTA pairs on 256 x 256 tiles spanning heads
+    (512, 160, 8, "plain", 2),
+    (256, 512, 4, "atoms", 0),    # the same shape on one-CTA 128 x 192 tiles (the default)
+])
+def test_gemm_rope_tile_shapes(lib, tokens, q_lora, heads, layout, cta_pair):
+    run_rope(tokens, q_lora, heads, layout, cta_pair=cta_pair)
+
+
 def test_gemm_rope_identity_tables(lib):
     """cos = 1, sin = 0: the rotary features are the de-interleaved projection."""
     from nvfp4_gemm_moe_gb300 import torch_ops
@@ -99,13 +108,34 @@ def test_gemm_rope_identity_tables(lib):
 
 
 def test_gemm_rope_validation(lib):
+    """Invalid arguments are rejected on the host before anything is enqueued (real buffers, so
+    a call that got through could not touch memory it does not own)."""
+    import ctypes
     import nvfp4_gemm_moe_gb300 as bsg
-    P = 0x10000
-    def call(**kw):
-        a = dict(tokens=256, q_lora=256, heads=2, hd=192, rope=64, layout=0, wsb=256)
+    dev = "cuda"
+    tokens, q_lora, heads = 256, 256, 2
+    n = heads * 192
+    x = torch.zeros((tokens, q_lora), dtype=torch.uint8, device=dev)
+    w = torch.zeros((n, q_lora), dtype=torch.uint8, device=dev)
+    sx = torch.zeros(bsg.bsg_sf_bytes(1, tokens, q_lora, 32), dtype=torch.uint8, device=dev)
+    sw = torch.zeros(bsg.bsg_sf_bytes(1, n, q_lora, 32), dtype=torch.uint8, device=dev)
+    tab = torch.zeros((tokens, 64), dtype=torch.bfloat16, device=dev)
+    o_row = torch.zeros((tokens, heads, 192), dtype=torch.uint8, device=dev)
+    s_row = torch.zeros((tokens, heads, 6), dtype=torch.uint8, device=dev)
+    o_col = torch.zeros((tokens, heads, 192), dtype=torch.uint8, device=dev)
+    s_col = torch.zeros((tokens // 32, heads, 192), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(bsg.bsg_workspace_size(), dtype=torch.uint8, device=dev)
+
+    def call(cta_pair=0, **kw):
+        a = dict(tokens=tokens, q_lora=q_lora, heads=heads, hd=192, rope=64, layout=0, wsb=ws.numel())
         a.update(kw)
-        return bsg.raw_status("bsg_gemm_rope_mxfp8", P, P, P, P, a["layout"], P, P, a["tokens"], a["q_lora"],
-                              a["heads"], a["hd"], a["rope"], P, P, P, P, None, P, a["wsb"], None)
+        o = bsg._opts(cta_pair=cta_pair)
+        return bsg.raw_status("bsg_gemm_rope_mxfp8", x.data_ptr(), sx.data_ptr(), w.data_ptr(), sw.data_ptr(),
+                              a["layout"], tab.data_ptr(), tab.data_ptr(), a["tokens"], a["q_lora"], a["heads"],
+                              a["hd"], a["rope"], o_row.data_ptr(), s_row.data_ptr(), o_col.data_ptr(),
+                              s_col.data_ptr(), ctypes.byref(o), ws.data_ptr(), a["wsb"], None)
     assert call(tokens=100) == 1 and call(q_lora=48) == 1 and call(layout=2) == 1
     assert call(hd=128) == 2 and call(rope=32) == 2
     assert call(layout=1) == 8  # the plain layout needs room for the repacked scales
+    assert call(cta_pair=2, tokens=128) == 1  # CTA pairs need tokens % 256 == 0 and heads * 192 % 256 == 0
+    torch.cuda.synchronize()
