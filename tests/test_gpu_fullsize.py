@@ -207,3 +207,45 @@ def test_rope_full_size_sampled(lib):
             check_e4m3_blocks(out["out_fp8_col"][t0:t0 + 32, h].cpu().numpy(),
                               out["out_scales_col"][t0 // 32, h].cpu().numpy()[:, None], y, tol, 1.0, axis=0,
                               what=f"col[t{t0}, h{h}]")
+
+
+def test_dswiglu_full_size_sampled(lib):
+    """The E32 dSwiGLU backward at full size: 32-row blocks (largest, smallest and last
+    expert) recomputed by the oracle over all 2N columns of D and their dprob rows."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    from oracle import dswiglu as od
+    from parity import check_float_out, dprob_tolerance, dswiglu_tolerances
+    wl = W.GROUPED_DSWIGLU_E32
+    n, k, fmt = wl.n, wl.k, wl.fmt
+    offs, qa, sfa, qb, sfb = _grouped_inputs(wl)
+    vm = int(offs[-1])
+    alpha, beta, prob = wl.alpha(), wl.beta(), wl.prob()
+    c = torch.from_numpy(wl.c_rows()).to(torch.bfloat16)
+    ws = torch_ops.new_workspace()
+    out = torch_ops.grouped_gemm_dswiglu(qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(),
+                                         torch.from_numpy(alpha).cuda(), torch.from_numpy(beta).cuda(),
+                                         torch.from_numpy(prob).cuda(), c.cuda(), n, k, workspace=ws)
+    torch.cuda.synchronize()
+    assert bsg.bsg_read_device_error(ws) == 0
+    ends = np.asarray(offs, dtype=np.int64)
+    begins = np.concatenate([[0], ends[:-1]])
+    sizes = ends - begins
+    nonempty = np.flatnonzero(sizes > 0)
+    for g in sorted({int(nonempty[np.argmax(sizes[nonempty])]), int(nonempty[np.argmin(sizes[nonempty])]),
+                     int(nonempty[-1])}):
+        r0 = int(begins[g])
+        rows = np.arange(r0, r0 + 32)
+        ahat = _check_operand_rows(qa, sfa, rows, vm, wl.a_rows(rows), fmt, k)
+        bhat = _check_operand_rows(qb, sfb, g * n + np.arange(n), n, wl.b_rows(g * n + np.arange(n)), fmt, k)
+        ref = float(alpha[g]) * (ahat @ bhat.T)
+        ref_tol = TOL_C * float(alpha[g]) * (np.abs(ahat) @ np.abs(bhat).T)
+        cv = c[r0:r0 + 32].double().numpy() * float(beta[g])
+        x, gate = od.deinterleave(cv)
+        ab, dsw, dprob = od.epilogue(ref, x, gate, prob[rows])
+        r = {"ref": ref, "x": x, "gate": gate, "ab": ab, "dswiglu": dsw}
+        t_ab, t_dsw = dswiglu_tolerances(r, ref_tol, prob[rows])
+        check_float_out(out["d_row"][r0:r0 + 32].float().cpu().numpy(), od.interleave(ab, dsw),
+                        od.interleave(t_ab, t_dsw), "bf16", what=f"D[e{g}, rows {r0}..]")
+        dp = out["dprob"][r0:r0 + 32].cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(dp - dprob) <= dprob_tolerance(r, ref_tol, 128, 2 * (n // 128) + 2)), (g, dp, dprob)
