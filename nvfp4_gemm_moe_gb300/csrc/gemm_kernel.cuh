@@ -1,18 +1,22 @@
 // gemm_kernel.cuh -- persistent, warp-specialised block-scaled GEMM for sm_103a.
 //
-// One CTA per SM walks a static list of 128 x BN output tiles (dense: batch-major, then
-// groups of 16 M-tiles swept along N; grouped: M-tile-major over the experts' padded row
-// ranges).  Fourteen warps:
+// One CTA per SM walks a static list of 128 x BN output tiles (dense and RoPE projection:
+// batch-major, then groups of 16 M-tiles swept along N; grouped: M-tile-major over the
+// experts' padded row ranges).  Fourteen warps:
 //   warp 0     TMA producer: per 128-byte K slice, A (128 rows) and B (BN rows) tiles with
 //              128-byte swizzle via cp.async.bulk.tensor, and the scale-factor atoms via
-//              cp.async.bulk, into a STAGES-deep shared-memory ring (full/empty mbarriers);
+//              cp.async.bulk, into a STAGES-deep shared-memory ring (full/empty mbarriers); with
+//              per-expert weights, expert g's B tensor map is read from global memory;
 //   warp 1     TMEM owner and MMA issuer: one thread issues the stage's four block-scaled
 //              tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for MXFP8, kind::mxf4nvf4 scale_vec::4X
 //              for NVFP4) into an fp32 accumulator in TMEM, then tcgen05.commit frees the stage;
 //   warps 2-9  epilogue: two warps per 32-lane quadrant of TMEM (= 32 rows of the tile), each
-//              taking alternate 32-column chunks, read with tcgen05.ld, and applying the dense (C + amax)
-//              or grouped (alpha, C, sReLU / tanh clamp, D, per-expert amax or MXFP8 row and
-//              column re-quantisation) epilogue;
+//              taking its share of the 32-column chunks, read with tcgen05.ld, and applying the
+//              dense (C + amax), grouped sReLU (alpha, C, sReLU / tanh clamp, D, per-expert amax
+//              or MXFP8 row and column re-quantisation), grouped dSwiGLU backward (C input,
+//              ab / dswiglu, dprob) or RoPE projection (rotation, row and column MXFP8)
+//              epilogue; rows leave (and the dSwiGLU C rows arrive) through a per-warp shared-
+//              memory transpose block as coalesced whole-sector accesses;
 //   warps 10-13 scale-factor stagers: each warp writes its 32-lane quadrant of the stage's
 //              scale factors from shared memory into TMEM with tcgen05.st, in the layout a
 //              tcgen05.cp 32x128b.warpx4 of each atom would produce.  tcgen05.cp runs in the

@@ -1,7 +1,8 @@
 // gemm_pair_kernel.cuh -- the block-scaled GEMM on CTA pairs (tcgen05 cta_group::2), 256 x BN tiles.
 //
 // A cluster of two CTAs (two SMs) computes one 256 x BN output tile (BN = 256, or 224 with two
-// TMEM accumulators so that the epilogue overlaps the next tile's MMAs): each CTA holds 128 rows
+// TMEM accumulators so that the epilogue overlaps the next tile's MMAs), with any of the
+// one-CTA kernel's epilogues: each CTA holds 128 rows
 // of A and one BN/2-row half of B in shared memory, and one thread of the even CTA issues
 // tcgen05.mma.cta_group::2 with M = 256, N = BN, so each SM fetches its own A rows and half of
 // the B tile per K slice instead of all of B.  Each CTA's TMEM holds the fp32 accumulator of its
