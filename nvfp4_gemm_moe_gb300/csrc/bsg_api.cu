@@ -120,9 +120,10 @@ int choose_tile_n(int fmt, int64_t n, int64_t m_tiles_total, int num_sms, bool h
   if (opts && (opts->tile_n == 128 || opts->tile_n == 256)) return opts->tile_n;
   if (opts && (opts->tile_n == 192 || opts->tile_n == 224) && fmt == bsg::kMXFP8) return opts->tile_n;
   if (n <= 128) return 128;
-  // E4M3 D (row and column re-quantisation, three outputs per element) makes the epilogue about
-  // as long as a tile's MMAs: 224-wide tiles keep two accumulators in TMEM so it overlaps the
-  // next tile's MMAs.  Lighter epilogues run faster on 256-wide tiles (fewer, larger MMAs).
+  // Heavy epilogues (E4M3 D with row and column re-quantisation; the dSwiGLU backward with its
+  // C reads) run about as long as a tile's MMAs: 224-wide tiles keep two accumulators in TMEM so
+  // they overlap the next tile's MMAs.  Lighter epilogues run faster on 256-wide tiles (fewer,
+  // larger MMAs).
   if (fmt == bsg::kMXFP8 && heavy_epilogue) return 224;
   return (m_tiles_total * cdiv(n, 256) >= num_sms) ? 256 : 128;
 }
@@ -135,9 +136,9 @@ struct TilePlan {
 
 // Kernel and tile width for a GEMM with `m` rows (per batch), `n` columns and `l` batches.
 // CTA pairs halve the B bytes each SM loads per K slice (the one-CTA kernel's TMA feed is its
-// limit once the epilogue is overlapped); they need enough 256-row tiles to fill the GPU.  E4M3
-// D (row and column re-quantisation) makes the epilogue about as long as a tile's MMAs, so it
-// takes 224-wide tiles with two TMEM accumulators, whose epilogue overlaps the next tile.
+// limit once the epilogue is overlapped); they need enough 256-row tiles to fill the GPU.  Heavy
+// epilogues (E4M3 D, dSwiGLU) run about as long as a tile's MMAs, so they take 224-wide tiles
+// with two TMEM accumulators, whose epilogue overlaps the next tile.
 TilePlan plan_tiles(int fmt, int64_t m, int64_t n, int64_t l, int num_sms, bool heavy_epilogue,
                     const bsg_gemm_opts* opts) {
   const int cta_pair = opts ? opts->cta_pair : 0;
