@@ -362,14 +362,7 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
     }
   }
 
-  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
-  if (!fp8_d && cudaMemsetAsync(amax, 0, sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
-  if (fp8_d && n % 128 != 0) {
-    // SFD_col rows n .. ceil(n/128)*128 are padding the kernel never touches
-    if (cudaMemsetAsync(sfd_col, 0, bsg_sf_bytes(1, n, valid_m, 32), s) != cudaSuccess) return BSG_ERR_CUDA;
-  }
-  if (valid_m == 0) return BSG_OK;
-
+  // tiles and tensor maps (host only) before anything is enqueued
   const TilePlan plan = plan_tiles(fmt, valid_m, n, 1, info.num_sms, fp8_d, opts);
   const bool pairs = plan.pairs;
   const int bn = plan.bn;
@@ -378,26 +371,38 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   const int64_t tiles = m_tiles * n_tiles;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
   const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
-
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128)) return BSG_ERR_CUDA;
-  const CUtensorMap* b_maps = nullptr;
-  if (!discrete) {
-    if (!make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn)) return BSG_ERR_CUDA;
-  } else {
-    // One tensor map per expert, encoded here and stored in the workspace after the error word;
-    // the kernel reads them from global memory (after a tensormap-proxy acquire fence).
-    std::vector<CUtensorMap> maps(static_cast<size_t>(num_experts));
-    for (size_t g = 0; g < maps.size(); ++g) {
-      if (!make_operand_map(&maps[g], reinterpret_cast<const void*>(hb[g]), row_bytes, n, 1, pairs ? bn / 2 : bn))
-        return BSG_ERR_CUDA;
+  std::vector<CUtensorMap> maps;
+  if (valid_m > 0) {
+    if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128)) return BSG_ERR_CUDA;
+    if (!discrete) {
+      if (!make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn)) return BSG_ERR_CUDA;
+    } else {
+      // one tensor map per expert, stored in the workspace after the error word; the kernel
+      // reads them from global memory (after a tensormap-proxy acquire fence)
+      maps.resize(static_cast<size_t>(num_experts));
+      for (size_t g = 0; g < maps.size(); ++g) {
+        if (!make_operand_map(&maps[g], reinterpret_cast<const void*>(hb[g]), row_bytes, n, 1, pairs ? bn / 2 : bn))
+          return BSG_ERR_CUDA;
+      }
+      tb = maps[0];  // unused by the kernel in this form
     }
+  }
+
+  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
+  if (!fp8_d && cudaMemsetAsync(amax, 0, sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
+  if (fp8_d && n % 128 != 0) {
+    // SFD_col rows n .. ceil(n/128)*128 are padding the kernel never touches
+    if (cudaMemsetAsync(sfd_col, 0, bsg_sf_bytes(1, n, valid_m, 32), s) != cudaSuccess) return BSG_ERR_CUDA;
+  }
+  if (valid_m == 0) return BSG_OK;
+  const CUtensorMap* b_maps = nullptr;
+  if (discrete) {
     uint8_t* dst = static_cast<uint8_t*>(workspace) + kWorkspaceBytes;
     if (cudaMemcpyAsync(dst, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice, s) !=
         cudaSuccess)
       return BSG_ERR_CUDA;
     b_maps = reinterpret_cast<const CUtensorMap*>(dst);
-    tb = maps[0];  // unused by the kernel in this form
   }
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
 
@@ -543,6 +548,21 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
   }
 
   const int64_t n_d = 2 * n;
+  // tiles and tensor maps (host only) before anything is enqueued
+  const TilePlan plan = plan_tiles(fmt, valid_m, n, 1, info.num_sms, true, opts);
+  const bool pairs = plan.pairs;
+  const int bn = plan.bn;
+  if (!pairs && bn == 192) return BSG_ERR_UNSUPPORTED;  // no 192-wide dSwiGLU kernel
+  const int64_t m_tiles = pairs ? valid_m / 256 : valid_m / 128;
+  const int64_t n_tiles = cdiv(n, bn);
+  const int64_t tiles = m_tiles * n_tiles;
+  if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
+  const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
+  CUtensorMap ta, tb;
+  if (valid_m > 0 && (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128) ||
+                      !make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn)))
+    return BSG_ERR_CUDA;
+
   if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (!fp8_d && cudaMemsetAsync(amax, 0, 2 * sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (fp8_d && n_d % 128 != 0) {
@@ -550,20 +570,6 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
     if (cudaMemsetAsync(sfd_col, 0, bsg_sf_bytes(1, n_d, valid_m, 32), s) != cudaSuccess) return BSG_ERR_CUDA;
   }
   if (valid_m == 0) return BSG_OK;
-
-  const TilePlan plan = plan_tiles(fmt, valid_m, n, 1, info.num_sms, true, opts);
-  const bool pairs = plan.pairs;
-  const int bn = plan.bn;
-  const int64_t m_tiles = pairs ? valid_m / 256 : valid_m / 128;
-  const int64_t n_tiles = cdiv(n, bn);
-  const int64_t tiles = m_tiles * n_tiles;
-  if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
-  const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
-
-  CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128) ||
-      !make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn))
-    return BSG_ERR_CUDA;
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
 
   GemmParams p;
