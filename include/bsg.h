@@ -347,6 +347,16 @@ bsg_status bsg_gemm_amax_noalloc(const void* a, const void* b, const uint8_t* sf
                                  void* c, bsg_dtype c_dtype, float* amax,
                                  const bsg_gemm_opts* opts, void* stream);
 
+/*
+ * bsg_selftest_wait_timeout -- failure-detection self-test of the device-side bounded waits.
+ * Launches one warp whose wait on an mbarrier that nothing arrives on runs out after the
+ * library's wait limit (2 s), records BSG_DEVERR_TIMEOUT in `workspace` (bsg_workspace_size()
+ * bytes, 256-byte aligned; cleared first) and returns; the GEMM kernels use the same wait.  No
+ * fault, trap or hang: the context stays usable.  Read the result with bsg_read_device_error;
+ * bit 31 set means the wait completed, which it must not.
+ */
+bsg_status bsg_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream` and returns the device error bits of the last call that
  * used `workspace` in *error_bits; BSG_ERR_DEVICE if any bit is set. */
 bsg_status bsg_read_device_error(const void* workspace, void* stream, uint32_t* error_bits);

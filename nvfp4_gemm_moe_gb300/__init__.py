@@ -72,6 +72,8 @@ def _load():
     lib.bsg_gemm_rope_mxfp8.restype = I
     lib.bsg_gemm_rope_mxfp8.argtypes = [P, P, P, P, I, P, P, I64, I64, I64, I64, I64, P, P, P, P,
                                         ctypes.POINTER(bsg_gemm_opts), P, SZ, P]
+    lib.bsg_selftest_wait_timeout.restype = I
+    lib.bsg_selftest_wait_timeout.argtypes = [P, SZ, P]
     lib.bsg_gemm_amax_noalloc.restype = I
     lib.bsg_gemm_amax_noalloc.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, I, P,
                                           ctypes.POINTER(bsg_gemm_opts), P]
@@ -207,6 +209,12 @@ def bsg_gemm_rope_mxfp8(x, x_scale, w, w_scale, scale_layout, cos, sin, tokens, 
                                     tokens, q_lora, num_heads, head_dim, qk_rope, _ptr(out_fp8_row),
                                     _ptr(out_scales_row), _ptr(out_fp8_col), _ptr(out_scales_col), ctypes.byref(o),
                                     _ptr(workspace), ws_bytes, _stream(stream)), "bsg_gemm_rope_mxfp8")
+
+
+def bsg_selftest_wait_timeout(workspace, workspace_bytes=None, stream=None):
+    """Runs the bounded-wait self-test (about two seconds); read the bits with bsg_read_device_error."""
+    ws_bytes = bsg_workspace_size() if workspace_bytes is None else workspace_bytes
+    _check(_lib.bsg_selftest_wait_timeout(_ptr(workspace), ws_bytes, _stream(stream)), "bsg_selftest_wait_timeout")
 
 
 def bsg_read_device_error(workspace, stream=None) -> int:

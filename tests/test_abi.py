@@ -195,6 +195,14 @@ def test_dswiglu_validation():
         assert st in (OK, ARCH, CUDA)
 
 
+def test_selftest_validation():
+    assert bsg.raw_status("bsg_selftest_wait_timeout", None, 256, None) == WORKSPACE
+    assert bsg.raw_status("bsg_selftest_wait_timeout", P, 16, None) == WORKSPACE
+    assert bsg.raw_status("bsg_selftest_wait_timeout", P + 16, 256, None) == ALIGN
+    if _no_device():
+        assert bsg.raw_status("bsg_selftest_wait_timeout", P, 256, None) in (ARCH, CUDA)
+
+
 def test_noalloc_validation():
     def call(**kw):
         a = dict(a=P, c=P, amax=P, n=256)
