@@ -8,6 +8,8 @@ import numpy as np
 import pytest
 import torch
 
+from guards import Outputs
+
 import workloads as W
 from oracle import gemm as og, quantize as oq
 from parity import TOL_C, check_amax, check_c, check_c_float, check_codes_plain
@@ -35,9 +37,16 @@ def run_dense(fmt, m, n, k, l, c_kind, tile_n=0, seed=1, boost=False, spread=Fal
     qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), fmt)
     c_dtype = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "e4m3": "e4m3", "e2m1": "e2m1"}[c_kind]
     ws = torch_ops.new_workspace()
-    c, amax = torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, m, n, k, l, c_dtype=c_dtype, workspace=ws,
-                                  tile_n=tile_n, max_ctas=max_ctas, cta_pair=cta_pair)
+    g = Outputs()
+    if c_kind in ("e4m3", "e2m1"):
+        c_out = g.codes("c", (l, m, n if c_kind == "e4m3" else n // 2))
+    else:
+        c_out = g.float("c", (l, m, n), c_dtype)
+    amax_out = g.float("amax", (1,), torch.float32)
+    c, amax = torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, m, n, k, l, c_dtype=c_dtype, c=c_out, amax=amax_out,
+                                  workspace=ws, tile_n=tile_n, max_ctas=max_ctas, cta_pair=cta_pair)
     torch.cuda.synchronize()
+    g.check()
     import nvfp4_gemm_moe_gb300 as bsg
     assert bsg.bsg_read_device_error(ws) == 0
     # oracle side

@@ -5,6 +5,7 @@ import torch
 
 import workloads as W
 from oracle import dswiglu as od, formats, quantize as oq, sf_layout
+from guards import Outputs
 from parity import TOL_C, check_e4m3_blocks, check_float_out, dprob_tolerance, dswiglu_tolerances
 
 pytestmark = pytest.mark.gpu
@@ -38,13 +39,24 @@ def run_dswiglu(counts, n, k, d_dtype="bf16", c_kind="bf16", fmt="mxfp8", tile_n
     qa, sfa = torch_ops.quantize(torch.from_numpy(a).cuda(), fmt)
     qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), fmt)
     ws = torch_ops.new_workspace()
+    g = Outputs()
+    outputs = {"dprob": g.zeros("dprob", (vm,))}
+    if d_dtype == "e4m3":
+        outputs.update(d_row=g.codes("d_row", (vm, 2 * n)), d_col=g.codes("d_col", (vm, 2 * n)),
+                       sfd_row=g.scales("sfd_row", bsg.bsg_sf_bytes(1, vm, 2 * n, 32)),
+                       sfd_col=g.scales("sfd_col", bsg.bsg_sf_bytes(1, 2 * n, vm, 32)))
+    else:
+        outputs.update(d_row=g.float("d_row", (vm, 2 * n), {"bf16": torch.bfloat16, "f16": torch.float16,
+                                                            "f32": torch.float32}[d_dtype]),
+                       amax=g.float("amax", (len(counts), 2), torch.float32))
     out = torch_ops.grouped_gemm_dswiglu(
         qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
         torch.from_numpy(beta).cuda(), torch.from_numpy(prob).cuda(), c_dev, n, k,
         c_dtype="e4m3" if c_kind == "e4m3" else None, d_dtype=d_dtype,
         norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
-        cta_pair=cta_pair, max_ctas=max_ctas)
+        cta_pair=cta_pair, max_ctas=max_ctas, outputs=outputs)
     torch.cuda.synchronize()
+    g.check()
     assert bsg.bsg_read_device_error(ws) == 0
 
     qa_ref, sfa_ref = oq.quantize(a, fmt)

@@ -5,6 +5,7 @@ import torch
 
 import workloads as W
 from oracle import formats, gemm as og, quantize as oq, sf_layout
+from guards import Outputs
 from parity import check_amax, check_c, check_c_float, check_d_bf16, check_d_float, check_e4m3_blocks, d_tolerance, TOL_C
 
 pytestmark = pytest.mark.gpu
@@ -29,6 +30,16 @@ def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0,
     qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), fmt)
     ws = torch_ops.new_workspace()
     c_dtype = {"bf16": torch.bfloat16, "f32": torch.float32, "f16": torch.float16, None: None}[c_kind]
+    g = Outputs()
+    outputs = {"c": None if c_dtype is None else g.float("c", (vm, n), c_dtype)}
+    if d_dtype == "e4m3":
+        outputs.update(d=g.codes("d", (vm, n)), d_col=g.codes("d_col", (vm, n)),
+                       sfd_row=g.scales("sfd_row", bsg.bsg_sf_bytes(1, vm, n, 32)),
+                       sfd_col=g.scales("sfd_col", bsg.bsg_sf_bytes(1, n, vm, 32)))
+    else:
+        outputs.update(d=g.float("d", (vm, n), {"bf16": torch.bfloat16, "f16": torch.float16,
+                                                "f32": torch.float32}[d_dtype]),
+                       amax=g.float("amax", (len(counts),), torch.float32))
     if discrete:
         # each expert's codes and scales in an allocation of its own, allocated in reverse order
         per_sf = sfb.numel() // len(counts)
@@ -39,14 +50,15 @@ def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0,
             qa[0], b_list, sfa, sfb_list, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
             torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=clamp, d_dtype=d_dtype, c_dtype=c_dtype,
             norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
-            tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair)
+            tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair, outputs=outputs)
     else:
         out = torch_ops.grouped_gemm_srelu(
             qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
             torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=clamp, d_dtype=d_dtype, c_dtype=c_dtype,
             norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
-            tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair)
+            tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair, outputs=outputs)
     torch.cuda.synchronize()
+    g.check()
     assert bsg.bsg_read_device_error(ws) == 0
     qa_ref, sfa_ref = oq.quantize(a, fmt)
     qb_ref, sfb_ref = oq.quantize(b, fmt)

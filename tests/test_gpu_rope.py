@@ -5,6 +5,7 @@ import torch
 
 import workloads as W
 from oracle import formats, quantize as oq, rope as orope, sf_layout
+from guards import Outputs
 from parity import TOL_C, check_e4m3_blocks
 
 pytestmark = pytest.mark.gpu
@@ -45,9 +46,15 @@ def run_rope(tokens, q_lora, heads, layout="atoms", seed=7, cta_pair=0):
     else:
         sx_in, sw_in = sx, sw
     ws = torch.zeros(bsg.bsg_rope_workspace_size(tokens, heads, 192, q_lora), dtype=torch.uint8, device="cuda")
+    g = Outputs()
+    outputs = {"out_fp8_row": g.codes("row", (tokens, heads, 192)),
+               "out_scales_row": g.scales("scales_row", (tokens, heads, 6)),
+               "out_fp8_col": g.codes("col", (tokens, heads, 192)),
+               "out_scales_col": g.scales("scales_col", (tokens // 32, heads, 192))}
     out = torch_ops.gemm_rope_mxfp8(qx[0], sx_in, qw[0], sw_in, cos.cuda(), sin.cuda(), heads, scale_layout=layout,
-                                    workspace=ws, cta_pair=cta_pair)
+                                    workspace=ws, cta_pair=cta_pair, outputs=outputs)
     torch.cuda.synchronize()
+    g.check()
     assert bsg.bsg_read_device_error(ws) == 0
 
     cos64, sin64 = cos.double().numpy(), sin.double().numpy()
