@@ -7,6 +7,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "bsg.h"
 #include "internal.h"
 
@@ -16,6 +18,15 @@ using bsg::GemmConfig;
 using bsg::GemmParams;
 
 constexpr size_t kWorkspaceBytes = 256;
+
+// One NVTX range per C ABI call, named after the entry point (shown by Nsight tools; without a
+// tool attached the calls return at once).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 struct DeviceInfo {
   bool probed = false;
@@ -196,6 +207,7 @@ const char* bsg_status_string(bsg_status s) {
 
 bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t k, bsg_dtype q_dtype,
                            int sf_vec_size, bsg_sf_dtype sf_dtype, void* q, uint8_t* sf, void* stream) {
+  NvtxRange nvtx_range("bsg_quantize_mx");
   int fmt = 0;
   bsg_status st = operand_format(q_dtype, sf_dtype, sf_vec_size, &fmt);
   if (st != BSG_OK) return st;
@@ -216,6 +228,7 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
                          bsg_sf_dtype sf_dtype, int sf_vec_size, int64_t m, int64_t n, int64_t k, int64_t l,
                          void* c, bsg_dtype c_dtype, float* amax, const bsg_gemm_opts* opts, void* workspace,
                          size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("bsg_gemm_amax");
   int fmt = 0;
   bsg_status st = operand_format(ab_dtype, sf_dtype, sf_vec_size, &fmt);
   if (st != BSG_OK) return st;
@@ -461,6 +474,7 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
                                   bsg_dtype d_dtype, uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
                                   const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
                                   void* stream) {
+  NvtxRange nvtx_range("bsg_grouped_gemm_srelu");
   if (!b || !sfb) return BSG_ERR_INVALID_ARG;
   return grouped_impl(a, b, nullptr, sfa, sfb, nullptr, ab_dtype, sf_dtype, sf_vec_size, valid_m, n, k, num_experts,
                       padded_offsets, alpha, prob, tanh_clamp_scale, norm_const, c, c_dtype, d, d_col, d_dtype,
@@ -481,6 +495,7 @@ bsg_status bsg_grouped_gemm_srelu_discrete(const void* a, const int64_t* b_ptrs,
                                            uint8_t* sfd_row, uint8_t* sfd_col, float* amax,
                                            const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
                                            void* stream) {
+  NvtxRange nvtx_range("bsg_grouped_gemm_srelu_discrete");
   if (!b_ptrs || !sfb_ptrs) return BSG_ERR_INVALID_ARG;
   return grouped_impl(a, nullptr, b_ptrs, sfa, nullptr, sfb_ptrs, ab_dtype, sf_dtype, sf_vec_size, valid_m, n, k,
                       num_experts, padded_offsets, alpha, prob, tanh_clamp_scale, norm_const, c, c_dtype, d, d_col,
@@ -495,6 +510,7 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
                                     bsg_dtype d_dtype, uint8_t* sfd_row, uint8_t* sfd_col, float* dprob,
                                     float* amax, const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes,
                                     void* stream) {
+  NvtxRange nvtx_range("bsg_grouped_gemm_dswiglu");
   int fmt = 0;
   bsg_status st = operand_format(ab_dtype, sf_dtype, sf_vec_size, &fmt);
   if (st != BSG_OK) return st;
@@ -624,6 +640,7 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
                                int64_t num_heads, int64_t head_dim, int64_t qk_rope, uint8_t* out_fp8_row,
                                uint8_t* out_scales_row, uint8_t* out_fp8_col, uint8_t* out_scales_col,
                                const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("bsg_gemm_rope_mxfp8");
   if (!x || !x_scale || !w || !w_scale || !cos || !sin || !out_fp8_row || !out_scales_row || !out_fp8_col ||
       !out_scales_col)
     return BSG_ERR_INVALID_ARG;
