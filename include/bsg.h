@@ -200,7 +200,9 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
  * amax            device fp32 (num_experts,): max |D| over each expert's rows (0 for an
  *                 empty expert); required iff d_dtype is not BSG_E4M3.  Zeroed by the call.
  * Requirements: valid_m % 256 == 0, 1 <= num_experts <= 1024, sf as for bsg_gemm_amax,
- * n % 32 == 0 for E4M3 D, the bytes of a row of C and of D a multiple of 16.
+ * n % 32 == 0 for E4M3 D, the bytes of a row of C and of D a multiple of 16.  With valid_m == 0
+ * only padded_offsets and (float D) amax are used: amax is zeroed, nothing else is touched, and
+ * the other pointers may be null.
  */
 bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
                                   bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size,
@@ -247,6 +249,7 @@ bsg_status bsg_grouped_gemm_srelu(const void* a, const void* b, const uint8_t* s
  *                 Zeroed by the call.
  * Requirements: valid_m % 256 == 0, n % 32 == 0, 1 <= num_experts <= 512, k a multiple of the
  * scale block, operand rows a multiple of 16 bytes.  opts->tile_n may be 128, 224 (MXFP8) or 256.
+ * With valid_m == 0 only padded_offsets and (float D) amax are used, as for the sReLU call.
  */
 bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
                                     bsg_dtype ab_dtype, bsg_sf_dtype sf_dtype, int sf_vec_size,

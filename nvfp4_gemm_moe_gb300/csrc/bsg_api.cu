@@ -312,8 +312,11 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   bsg_status st = operand_format(ab_dtype, sf_dtype, sf_vec_size, &fmt);
   if (st != BSG_OK) return st;
   const bool discrete = b_ptrs != nullptr;
-  if (!a || !sfa || !padded_offsets || !alpha || !prob || !d) return BSG_ERR_INVALID_ARG;
-  if (discrete ? (b || sfb || !sfb_ptrs) : (!b || !sfb || sfb_ptrs)) return BSG_ERR_INVALID_ARG;
+  // with valid_m == 0 nothing is read or written but the per-expert amax: the row-sized and
+  // operand buffers may be null (empty tensors)
+  const bool empty = valid_m == 0;
+  if (!padded_offsets || (!empty && (!a || !sfa || !alpha || !prob || !d))) return BSG_ERR_INVALID_ARG;
+  if (discrete ? (b || sfb || !sfb_ptrs) : (!empty && (!b || !sfb || sfb_ptrs))) return BSG_ERR_INVALID_ARG;
   const size_t ws_need = discrete ? bsg_grouped_discrete_workspace_size(num_experts) : kWorkspaceBytes;
   if (!workspace || workspace_bytes < ws_need) return BSG_ERR_WORKSPACE;
   if (valid_m < 0 || valid_m % 256 != 0 || n < 1 || k < 1 || num_experts < 1 || num_experts > 1024)
@@ -325,7 +328,7 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   if (!fp8_d && d_kind != bsg::kOutBF16 && d_kind != bsg::kOutF16 && d_kind != bsg::kOutF32) return BSG_ERR_UNSUPPORTED;
   if (fp8_d) {
     if (fmt != bsg::kMXFP8) return BSG_ERR_UNSUPPORTED;
-    if (!d_col || !sfd_row || !sfd_col || !norm_const) return BSG_ERR_INVALID_ARG;
+    if (!empty && (!d_col || !sfd_row || !sfd_col || !norm_const)) return BSG_ERR_INVALID_ARG;
     if (n % 32 != 0) return BSG_ERR_INVALID_ARG;
   } else {
     if (!amax || d_col || sfd_row || sfd_col) return BSG_ERR_INVALID_ARG;
@@ -404,11 +407,11 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
 
   if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (!fp8_d && cudaMemsetAsync(amax, 0, sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
-  if (fp8_d && n % 128 != 0) {
+  if (fp8_d && n % 128 != 0 && !empty) {
     // SFD_col rows n .. ceil(n/128)*128 are padding the kernel never touches
     if (cudaMemsetAsync(sfd_col, 0, bsg_sf_bytes(1, n, valid_m, 32), s) != cudaSuccess) return BSG_ERR_CUDA;
   }
-  if (valid_m == 0) return BSG_OK;
+  if (empty) return BSG_OK;
   const CUtensorMap* b_maps = nullptr;
   if (discrete) {
     uint8_t* dst = static_cast<uint8_t*>(workspace) + kWorkspaceBytes;
@@ -514,7 +517,11 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
   int fmt = 0;
   bsg_status st = operand_format(ab_dtype, sf_dtype, sf_vec_size, &fmt);
   if (st != BSG_OK) return st;
-  if (!a || !b || !sfa || !sfb || !padded_offsets || !alpha || !beta || !prob || !c || !d_row || !dprob)
+  // with valid_m == 0 nothing is read or written but the per-expert amax: the row-sized and
+  // operand buffers may be null (empty tensors)
+  const bool empty = valid_m == 0;
+  if (!padded_offsets ||
+      (!empty && (!a || !b || !sfa || !sfb || !alpha || !beta || !prob || !c || !d_row || !dprob)))
     return BSG_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
   // N a multiple of 32: C and D are 32-column input / gate (ab / dswiglu) blocks; 2 * num_experts
@@ -529,7 +536,7 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
   if (!fp8_d && d_kind != bsg::kOutBF16 && d_kind != bsg::kOutF16 && d_kind != bsg::kOutF32) return BSG_ERR_UNSUPPORTED;
   if (fp8_d) {
     if (fmt != bsg::kMXFP8) return BSG_ERR_UNSUPPORTED;
-    if (!d_col || !sfd_row || !sfd_col || !norm_const) return BSG_ERR_INVALID_ARG;
+    if (!empty && (!d_col || !sfd_row || !sfd_col || !norm_const)) return BSG_ERR_INVALID_ARG;
   } else {
     if (!amax || d_col || sfd_row || sfd_col) return BSG_ERR_INVALID_ARG;
   }
@@ -581,11 +588,11 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
 
   if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (!fp8_d && cudaMemsetAsync(amax, 0, 2 * sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
-  if (fp8_d && n_d % 128 != 0) {
+  if (fp8_d && n_d % 128 != 0 && !empty) {
     // SFD_col rows 2N .. ceil(2N/128)*128 are padding the kernel never touches
     if (cudaMemsetAsync(sfd_col, 0, bsg_sf_bytes(1, n_d, valid_m, 32), s) != cudaSuccess) return BSG_ERR_CUDA;
   }
-  if (valid_m == 0) return BSG_OK;
+  if (empty) return BSG_OK;
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
 
   GemmParams p;

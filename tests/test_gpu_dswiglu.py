@@ -179,3 +179,10 @@ def test_dswiglu_bad_offsets_detected_on_device(lib):
     prob = torch.ones(vm, device="cuda")
     torch_ops.grouped_gemm_dswiglu(qa, qb, sfa, sfb, "mxfp8", offs, ones, ones, prob, c, n, k, workspace=ws)
     assert bsg.bsg_read_device_error(ws) == bsg.DEVERR_BAD_OFFSETS
+
+
+def test_dswiglu_max_experts(lib):
+    """512 experts (the dSwiGLU limit: 2 x 512 amax values staged in shared memory)."""
+    counts = [0] * 512
+    counts[0], counts[300], counts[511] = 100, 256, 1
+    run_dswiglu(counts, 128, 256, "bf16", "bf16")

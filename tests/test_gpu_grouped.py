@@ -267,3 +267,31 @@ def test_grouped_discrete_host_validation(lib):
     out = torch_ops.grouped_gemm_srelu_discrete(qa, good_b, sfa, good_s, "mxfp8", offs, ones, prob, n, k)
     torch.cuda.synchronize()
     assert float(out["d"].float().abs().max()) == 0.0
+
+
+def test_grouped_max_experts(lib):
+    """1024 experts (the limit the kernel stages in shared memory), all but three empty."""
+    counts = [0] * 1024
+    counts[0], counts[517], counts[1023] = 40, 300, 256
+    run_grouped(counts, 256, 256, "bf16", None, "bf16")
+
+
+def test_grouped_all_experts_empty(lib):
+    """valid_m = 0: nothing to compute, the per-expert amax is zeroed, no kernel error."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    k, n, num_experts = 256, 256, 4
+    qa = torch.zeros((0, k), dtype=torch.uint8, device="cuda")  # empty: its data pointer may be null
+    qb = torch.zeros((num_experts, n, k), dtype=torch.uint8, device="cuda")
+    sfa = torch.zeros(512, dtype=torch.uint8, device="cuda")
+    sfb = torch.zeros(bsg.bsg_sf_bytes(num_experts, n, k, 32), dtype=torch.uint8, device="cuda")
+    offs = torch.zeros(num_experts, dtype=torch.int32, device="cuda")
+    ws = torch_ops.new_workspace()
+    amax = torch.full((num_experts,), float("nan"), device="cuda")
+    out = torch_ops.grouped_gemm_srelu(qa, qb, sfa, sfb, "mxfp8", offs, torch.ones(num_experts, device="cuda"),
+                                       torch.ones(1, device="cuda"), n, k, workspace=ws,
+                                       outputs={"amax": amax, "c": None,
+                                                "d": torch.zeros((0, n), dtype=torch.bfloat16, device="cuda")})
+    torch.cuda.synchronize()
+    assert bsg.bsg_read_device_error(ws) == 0
+    assert torch.all(out["amax"] == 0)
