@@ -25,11 +25,15 @@
  *   device (or managed memory); the library never allocates, frees or retains
  *   them.  All tensors are caller-owned.
  * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
- *   stream.  Every entry point only enqueues work (memsets and kernel launches)
- *   and returns; results are valid once the stream reaches that point.
+ *   stream.  Every entry point only enqueues work (memsets, copies and kernel
+ *   launches) and returns; results are valid once the stream reaches that point.
+ *   Three calls synchronise `stream` first, as their comments say: a grouped call
+ *   with opts->validate_offsets, bsg_grouped_gemm_srelu_discrete (it reads the
+ *   experts' pointers on the host) and bsg_read_device_error.
  * - Sizes are element counts, not bytes, unless the name says bytes.
  * - Errors: invalid arguments are detected on the host before anything is
  *   enqueued and reported as a bsg_status; nothing is thrown across the ABI.
+ *   Each compute call opens an NVTX range named after itself.
  *   Errors detected on the device (a pipeline wait that exceeded its time limit,
  *   invalid padded_offsets contents) set bits in the caller's workspace; read
  *   them with bsg_read_device_error.
