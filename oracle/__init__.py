@@ -21,7 +21,8 @@ code with the CUDA library and never imports it.
 
 Pinning status: every function is pinned by a ``-m "not gpu"`` test against
 something other than itself (library decoders, closed forms, brute force,
-invariants); see ``tests/test_oracle_*.py``.  One reading remains unpinned
+invariants; the dSwiGLU epilogue against torch autograd through torch's SiLU, the
+RoPE rotation against complex multiplication); see ``tests/test_oracle_*.py``.  One reading remains unpinned
 against the pages' own implementation because the pages print no outputs: the
 row order inside a 128-row scale-factor atom (``sf_layout``), "parity unpinned"
 in that sense only.
