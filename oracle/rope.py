@@ -1,8 +1,9 @@
 """GEMM + per-head RoPE + dual-direction MXFP8 projection (oracle; test infrastructure).
 
-"GEMM + RoPE + MXFP8 Projection (SM100)", Overview, Shapes and Equations, MXFP8 input path:
+"GEMM + RoPE + MXFP8 Projection (SM100)", Overview, Shapes and Equations.  MXFP8 input path:
 x (tokens, K) and w (N, K) = [out, in] are E4M3 codes with E8M0 block scales along K
-(block 32, plain row-major (rows, K/32) arrays), N = NUM_HEADS * HEAD_DIM.
+(block 32, plain row-major (rows, K/32) arrays), N = NUM_HEADS * HEAD_DIM; BF16 input path:
+x and w are bf16 values (``project_bf16``).
 
     Y[t, h, :] = (xhat @ what^T)[t, h * HEAD_DIM : (h + 1) * HEAD_DIM]
     the trailing QK_ROPE features of every head are rotated (RoPE), the leading
@@ -59,12 +60,25 @@ def rope_interleaved_halves(y_rope, cos, sin) -> np.ndarray:
 
 
 def project(x_codes, x_scales, w_codes, w_scales, cos, sin, num_heads: int, head_dim: int, qk_rope: int):
-    """The whole path.  Returns a dict: y (tokens, H, D) float64 after RoPE, out_row / out_col
-    codes (tokens, H, D) uint8, scales_row (tokens, H, D/32), scales_col (tokens/32, H, D)."""
+    """The MXFP8-input path.  Returns a dict: y (tokens, H, D) float64 after RoPE, out_row /
+    out_col codes (tokens, H, D) uint8, scales_row (tokens, H, D/32), scales_col (tokens/32, H, D)."""
     xh = dequantize_plain(x_codes, x_scales)
     wh = dequantize_plain(w_codes, w_scales)
-    tokens = xh.shape[0]
-    y = (xh @ wh.T).reshape(tokens, num_heads, head_dim)
+    return _rotate_and_quantise(xh @ wh.T, cos, sin, num_heads, head_dim, qk_rope)
+
+
+def project_bf16(x_values, w_values, cos, sin, num_heads: int, head_dim: int, qk_rope: int):
+    """The BF16-input path (the page's other input precision): x (tokens, K) and w (N, K) are
+    the bf16 values themselves (given exactly, e.g. as float32 or float64); the rest as
+    ``project``."""
+    xh = np.asarray(x_values, dtype=np.float64)
+    wh = np.asarray(w_values, dtype=np.float64)
+    return _rotate_and_quantise(xh @ wh.T, cos, sin, num_heads, head_dim, qk_rope)
+
+
+def _rotate_and_quantise(y2d, cos, sin, num_heads: int, head_dim: int, qk_rope: int):
+    tokens = y2d.shape[0]
+    y = np.array(y2d, dtype=np.float64).reshape(tokens, num_heads, head_dim)
     p = head_dim - qk_rope
     y[..., p:] = rope_interleaved_halves(y[..., p:], cos, sin)
     flat = y.reshape(tokens, num_heads * head_dim)

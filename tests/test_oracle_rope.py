@@ -97,3 +97,27 @@ def test_scale_layouts_cover_blocks():
     deq = formats.decode_e4m3(out["out_row"]) * np.repeat(formats.decode_e8m0(out["scales_row"]), 32, axis=-1)
     assert np.all(np.abs(deq - y) <= np.abs(y) * 2.0 ** -4 + 2.0 ** -10 * np.repeat(
         formats.decode_e8m0(out["scales_row"]), 32, axis=-1))
+
+
+def test_bf16_path_matches_the_mxfp8_path_on_shared_values():
+    """Inputs whose MXFP8 encoding is exact are also bf16 values: both input paths must give the
+    same projection and outputs."""
+    rng = np.random.default_rng(5)
+    tokens, k, h, d, r = 64, 64, 2, 96, 64
+    grid = formats.decode_e4m3(np.arange(0, 0x7F, dtype=np.uint8))
+    grid = grid[(grid >= 0.125) & (grid <= 8)]
+    x = (rng.choice(grid, (tokens, k)) * rng.choice([-1, 1], (tokens, k))).astype(np.float32)
+    w = (rng.choice(grid, (h * d, k)) * rng.choice([-1, 1], (h * d, k)) / 16).astype(np.float32)
+    # each block's amax (8 and 0.5) fixes its scale (2^-5, 2^-9), under which every value is an
+    # exact E4M3 code
+    x[:, ::32] = 8.0
+    w[:, ::32] = 0.5
+    xc, xs = quantize.quantize_logical(x[None], "mxfp8")
+    wc, wsc = quantize.quantize_logical(w[None], "mxfp8")
+    np.testing.assert_array_equal(rope.dequantize_plain(xc[0], xs[0]), x)
+    np.testing.assert_array_equal(rope.dequantize_plain(wc[0], wsc[0]), w)
+    cos, sin, _ = _tables(tokens, r, rng)
+    a = rope.project(xc[0], xs[0], wc[0], wsc[0], cos, sin, h, d, r)
+    b = rope.project_bf16(x, w, cos, sin, h, d, r)
+    for key in ("y", "out_row", "scales_row", "out_col", "scales_col"):
+        np.testing.assert_array_equal(a[key], b[key])
