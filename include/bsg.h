@@ -300,6 +300,20 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
                                const bsg_gemm_opts* opts, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * bsg_gemm_rope_bf16 -- the BF16-input path of the projection GEMM + RoPE + MXFP8
+ * ("GEMM + RoPE + MXFP8 Projection (SM100)", Overview: the GEMM in bf16).  As
+ * bsg_gemm_rope_mxfp8 with x (tokens, q_lora) and w (num_heads * head_dim, q_lora) bf16 values
+ * (K-major; tcgen05 kind::f16 MMAs, fp32 accumulation) and no scales.  Requirements: q_lora % 8
+ * == 0 (16-byte rows), the rest as bsg_gemm_rope_mxfp8; one-CTA tiles only.  Workspace:
+ * bsg_workspace_size() bytes.
+ */
+bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, const void* sin, int64_t tokens,
+                              int64_t q_lora, int64_t num_heads, int64_t head_dim, int64_t qk_rope,
+                              uint8_t* out_fp8_row, uint8_t* out_scales_row, uint8_t* out_fp8_col,
+                              uint8_t* out_scales_col, const bsg_gemm_opts* opts, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * bsg_grouped_gemm_srelu_discrete -- bsg_grouped_gemm_srelu with per-expert weight allocations
  * ("Grouped GEMM + sReLU (SM100)", Shapes: B and SFB given as per-expert tensors addressed by
  * pointer arrays; API usage, discrete input B and SFB pointers).

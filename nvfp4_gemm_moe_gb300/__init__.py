@@ -72,6 +72,9 @@ def _load():
     lib.bsg_gemm_rope_mxfp8.restype = I
     lib.bsg_gemm_rope_mxfp8.argtypes = [P, P, P, P, I, P, P, I64, I64, I64, I64, I64, P, P, P, P,
                                         ctypes.POINTER(bsg_gemm_opts), P, SZ, P]
+    lib.bsg_gemm_rope_bf16.restype = I
+    lib.bsg_gemm_rope_bf16.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, P, P, P, P,
+                                       ctypes.POINTER(bsg_gemm_opts), P, SZ, P]
     lib.bsg_selftest_wait_timeout.restype = I
     lib.bsg_selftest_wait_timeout.argtypes = [P, SZ, P]
     lib.bsg_gemm_amax_noalloc.restype = I
@@ -209,6 +212,16 @@ def bsg_gemm_rope_mxfp8(x, x_scale, w, w_scale, scale_layout, cos, sin, tokens, 
                                     tokens, q_lora, num_heads, head_dim, qk_rope, _ptr(out_fp8_row),
                                     _ptr(out_scales_row), _ptr(out_fp8_col), _ptr(out_scales_col), ctypes.byref(o),
                                     _ptr(workspace), ws_bytes, _stream(stream)), "bsg_gemm_rope_mxfp8")
+
+
+def bsg_gemm_rope_bf16(x, w, cos, sin, tokens, q_lora, num_heads, head_dim, qk_rope, out_fp8_row, out_scales_row,
+                       out_fp8_col, out_scales_col, workspace, workspace_bytes=None, stream=None, **opts):
+    ws_bytes = bsg_workspace_size() if workspace_bytes is None else workspace_bytes
+    o = _opts(**opts)
+    _check(_lib.bsg_gemm_rope_bf16(_ptr(x), _ptr(w), _ptr(cos), _ptr(sin), tokens, q_lora, num_heads, head_dim,
+                                   qk_rope, _ptr(out_fp8_row), _ptr(out_scales_row), _ptr(out_fp8_col),
+                                   _ptr(out_scales_col), ctypes.byref(o), _ptr(workspace), ws_bytes,
+                                   _stream(stream)), "bsg_gemm_rope_bf16")
 
 
 def bsg_selftest_wait_timeout(workspace, workspace_bytes=None, stream=None):

@@ -735,6 +735,67 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }
 
+bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, const void* sin, int64_t tokens,
+                              int64_t q_lora, int64_t num_heads, int64_t head_dim, int64_t qk_rope,
+                              uint8_t* out_fp8_row, uint8_t* out_scales_row, uint8_t* out_fp8_col,
+                              uint8_t* out_scales_col, const bsg_gemm_opts* opts, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("bsg_gemm_rope_bf16");
+  if (!x || !w || !cos || !sin || !out_fp8_row || !out_scales_row || !out_fp8_col || !out_scales_col)
+    return BSG_ERR_INVALID_ARG;
+  // bf16 rows of q_lora values: a multiple of eight keeps every row 16-byte aligned for TMA
+  if (tokens < 128 || tokens % 128 != 0 || q_lora < 8 || q_lora % 8 != 0 || num_heads < 1 || head_dim < 1 ||
+      qk_rope < 1)
+    return BSG_ERR_INVALID_ARG;
+  if (head_dim != 192 || qk_rope != 64) return BSG_ERR_UNSUPPORTED;
+  if (opts && opts->cta_pair == 2) return BSG_ERR_UNSUPPORTED;  // one-CTA 128 x 192 tiles only
+  const int64_t n = num_heads * head_dim;
+  if (!fits_int32(tokens) || !fits_int32(n) || !fits_int32(q_lora) || !fits_int32(tokens * (n / 32)))
+    return BSG_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
+  const int64_t row_bytes = q_lora * 2;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(cos) || !aligned16(sin) ||
+      !aligned16(out_fp8_row) || !aligned16(out_fp8_col) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return BSG_ERR_ALIGNMENT;
+  DeviceInfo info;
+  bsg_status st = current_device(nullptr, &info);
+  if (st != BSG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int bn = 192;
+  const int64_t m_tiles = tokens / 128;
+  const int64_t tiles = m_tiles * num_heads;
+  if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, x, row_bytes, tokens, 1, 128) || !make_operand_map(&tb, w, row_bytes, n, 1, bn))
+    return BSG_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
+
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.m = static_cast<int>(tokens);
+  p.n = static_cast<int>(n);
+  p.k = static_cast<int>(q_lora);
+  p.l = 1;
+  p.m_tiles = static_cast<int>(m_tiles);
+  p.n_tiles = static_cast<int>(num_heads);
+  p.k_tiles = static_cast<int>(cdiv(q_lora, 64));
+  p.num_tiles = static_cast<int>(tiles);
+  p.c_kind = bsg::kOutNone;
+  p.d = out_fp8_row;
+  p.d_col = out_fp8_col;
+  p.sfd_row = out_scales_row;
+  p.sfd_col = out_scales_col;
+  p.rope_cos = static_cast<const uint16_t*>(cos);
+  p.rope_sin = static_cast<const uint16_t*>(sin);
+  p.qk_rope = static_cast<int>(qk_rope);
+  p.err = static_cast<uint32_t*>(workspace);
+
+  GemmConfig cfg{bsg::kBF16, bn, bsg::kEpiRope};
+  cudaError_t e = bsg::launch_gemm_rope(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
+  if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+}
+
 bsg_status bsg_read_device_error(const void* workspace, void* stream, uint32_t* error_bits) {
   if (!workspace || !error_bits) return BSG_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -46,12 +46,14 @@ constexpr int kXposeBlockBytes = 32 * 64;  // a warp's 32 rows x 64 bytes transp
 
 template <int FMT, int BN, int EPI = kEpiDense>
 struct GemmTraits {
-  static constexpr int kElemsPerKTile = FMT == kMXFP8 ? 128 : 256;
-  static constexpr int kMmaK = FMT == kMXFP8 ? 32 : 64;  // elements per tcgen05.mma (32 bytes)
+  // elements per 128-byte K slice and per tcgen05.mma (32 bytes of K)
+  static constexpr int kElemsPerKTile = FMT == kMXFP8 ? 128 : FMT == kNVFP4 ? 256 : 64;
+  static constexpr int kMmaK = FMT == kMXFP8 ? 32 : FMT == kNVFP4 ? 64 : 16;
   static constexpr int kMmasPerStage = 4;
-  static constexpr int kAtomsPerStage = FMT == kMXFP8 ? 1 : 4;  // SF atoms (128 rows x 4 blocks) along K
+  // SF atoms (128 rows x 4 blocks) along K per stage; bf16 operands carry none
+  static constexpr int kAtomsPerStage = FMT == kMXFP8 ? 1 : FMT == kNVFP4 ? 4 : 0;
   static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
-  static_assert(BN % 128 == 0 || FMT == kMXFP8, "NVFP4 tiles are 128 or 256 wide");
+  static_assert(BN % 128 == 0 || FMT != kNVFP4, "NVFP4 tiles are 128 or 256 wide");
   // A tile of B rows starting at a multiple of BN: aligned to the 128-row scale-factor atoms
   // when BN is a multiple of 128, else it may start inside an atom and touch three of them.
   static constexpr bool kSfbAligned = BN % 128 == 0;
@@ -68,7 +70,7 @@ struct GemmTraits {
   // of every quadrant), padded to whole four-column groups
   static constexpr int kSfbColsPerMma = ((kBBlocks + 3) / 4) * 4;
   static constexpr int kSfbCols = kSfbColsPerMma * kAtomsPerStage;
-  static constexpr int kSfStride = ((kSfaCols + kSfbCols + 15) / 16) * 16;
+  static constexpr int kSfStride = kAtomsPerStage == 0 ? 0 : ((kSfaCols + kSfbCols + 15) / 16) * 16;
   static constexpr int kSfBase = kAcc * BN;
   // barrier / scalar area after the stages
   static constexpr int kBarBytes = 1024;
@@ -82,7 +84,7 @@ struct GemmTraits {
   // as many stages as shared memory and the TMEM scale-factor slots allow, at most six
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
-  static constexpr int kStagesTmem = (512 - kSfBase) / kSfStride;
+  static constexpr int kStagesTmem = kSfStride == 0 ? 6 : (512 - kSfBase) / kSfStride;
   static constexpr int kStages = kStagesSmem < kStagesTmem ? (kStagesSmem < 6 ? kStagesSmem : 6)
                                                            : (kStagesTmem < 6 ? kStagesTmem : 6);
   static_assert(kStages >= 3, "pipeline depth");
@@ -95,9 +97,11 @@ struct GemmTraits {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 
   // Instruction descriptor: A/B formats (bits 7-12), K-major A and B, N >> 3 (bits 17-22),
-  // scale format (bit 23: 1 = UE8M0, 0 = UE4M3), M >> 4 (bits 24-28).
-  static constexpr uint32_t kIdesc = (FMT == kMXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))
-                                                    : ((1u << 7) | (1u << 10) | (0u << 23))) |
+  // scale format (bit 23: 1 = UE8M0, 0 = UE4M3), M >> 4 (bits 24-28).  kind::f16 (bf16): fp32
+  // accumulator (bits 4-5 = 1), A and B both bf16 (1 at bits 7 and 10), no scale field.
+  static constexpr uint32_t kIdesc = (FMT == kMXFP8   ? ((0u << 7) | (0u << 10) | (1u << 23))
+                                      : FMT == kNVFP4 ? ((1u << 7) | (1u << 10) | (0u << 23))
+                                                      : ((1u << 4) | (1u << 7) | (1u << 10))) |
                                      (static_cast<uint32_t>(BN >> 3) << 17) |
                                      (static_cast<uint32_t>(kTileM >> 4) << 24);
 };
@@ -820,7 +824,9 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uin
   for (int j = 0; j < NM; ++j) {
     const uint32_t accumulate = j > 0 ? 1u : acc0;
     // advance the start address by 32 bytes of K per MMA (encoded >> 4)
-    if (FMT == kMXFP8) {
+    if (FMT == kBF16) {
+      tc_mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
+    } else if (FMT == kMXFP8) {
       tc_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t, sfb_t, accumulate);
     } else {
       tc_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4, sfb_t + j * T::kSfbColsPerMma,
@@ -974,23 +980,25 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           const int k_left = p.k - kt * T::kElemsPerKTile;
           const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
-          const int atoms = FMT == kMXFP8 ? 1 : n_mma;
+          const int atoms = FMT == kMXFP8 ? 1 : FMT == kNVFP4 ? n_mma : 0;
           const uint32_t sf_bytes = static_cast<uint32_t>(atoms * 512 * (1 + T::kBRowGroups));
           mbar_arrive_expect_tx(&full[stage], T::kABytes + T::kBBytes + sf_bytes);
           tma_load_3d(s_a + stage * T::kABytes, &tmap_a, &full[stage], kt * kTileKBytes, tc.mt * kTileM, a_batch);
           tma_load_3d(s_b + stage * T::kBBytes, bmap, &full[stage], kt * kTileKBytes, tc.nt * BN, b_batch);
-          const uint8_t* sfa_src =
-              p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + tc.mt) * p.sf_kt +
-                       static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
-          bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, &full[stage]);
+          if constexpr (FMT != kBF16) {
+            const uint8_t* sfa_src =
+                p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + tc.mt) * p.sf_kt +
+                         static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+            bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, &full[stage]);
 #pragma unroll
-          for (int i = 0; i < T::kBRowGroups; ++i) {
-            // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
-            const int rb = min((tc.nt * BN) / 128 + i, p.sfb_mt - 1);
-            const uint8_t* sfb_src =
-                sfb_base + (static_cast<uint64_t>(rb) * p.sf_kt + static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
-            bulk_load(s_sfb + stage * T::kSfbBytes + i * T::kAtomsPerStage * 512, sfb_src, atoms * 512,
-                      &full[stage]);
+            for (int i = 0; i < T::kBRowGroups; ++i) {
+              // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
+              const int rb = min((tc.nt * BN) / 128 + i, p.sfb_mt - 1);
+              const uint8_t* sfb_src = sfb_base + (static_cast<uint64_t>(rb) * p.sf_kt +
+                                                   static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+              bulk_load(s_sfb + stage * T::kSfbBytes + i * T::kAtomsPerStage * 512, sfb_src, atoms * 512,
+                        &full[stage]);
+            }
           }
           ++issued;
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -1025,7 +1033,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           // after a failed wait reads stale shared memory, which is harmless: the results are
           // discarded with the error.
           // the stagers arrive after the stage's data landed and its scale factors are in TMEM
-          ok &= wait_bounded(&sf_ready[stage], phase, abort_flag, p.err);
+          // bf16 stages carry no scale factors: their data landing (full) is all the MMAs need
+          ok &= wait_bounded(FMT == kBF16 ? &full[stage] : &sf_ready[stage], phase, abort_flag, p.err);
           tc_fence_after();
           const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
@@ -1067,7 +1076,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     // waited for the commit of the MMAs that read them.
     const uint32_t quad_lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t stage = 0, phase = 0;
-    bool ok = true;
+    bool ok = FMT != kBF16;  // bf16 operands have no scale factors to stage
     for (int t = blockIdx.x; !bad && ok && t < p.num_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
       const int b_blk0 = ((tc.nt * BN) >> 5) & 3;  // the tile's first 32-row block within its first atom
@@ -1075,8 +1084,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         ok &= wait_bounded(&full[stage], phase, abort_flag, p.err);
         tc_fence_after();
         const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
-        stage_scale_factors<T>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t, sfa_t + T::kSfaCols,
-                               lane, b_blk0);
+        if constexpr (FMT != kBF16)
+          stage_scale_factors<T>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t,
+                                 sfa_t + T::kSfaCols, lane, b_blk0);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();

@@ -10,6 +10,8 @@ cudaError_t launch_gemm_rope(const GemmConfig& cfg, const CUtensorMap& ta, const
                              int grid, cudaStream_t stream) {
   if (cfg.fmt == kMXFP8 && cfg.bn == 192 && cfg.epi == kEpiRope)
     return launch_gemm_t<kMXFP8, 192, kEpiRope>(ta, tb, p, grid, stream);
+  if (cfg.fmt == kBF16 && cfg.bn == 192 && cfg.epi == kEpiRope)
+    return launch_gemm_t<kBF16, 192, kEpiRope>(ta, tb, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

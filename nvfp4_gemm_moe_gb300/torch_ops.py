@@ -8,7 +8,7 @@ from __future__ import annotations
 import torch
 
 from . import (BF16, E2M1, E4M3, F16, F32, FORMATS, bsg_gemm_amax, bsg_grouped_discrete_workspace_size,
-               bsg_gemm_rope_mxfp8, bsg_grouped_gemm_dswiglu, bsg_grouped_gemm_srelu, bsg_grouped_gemm_srelu_discrete,
+               bsg_gemm_rope_bf16, bsg_gemm_rope_mxfp8, bsg_grouped_gemm_dswiglu, bsg_grouped_gemm_srelu, bsg_grouped_gemm_srelu_discrete,
                bsg_quantize_mx, bsg_rope_workspace_size, bsg_sf_bytes, bsg_workspace_size)
 
 
@@ -183,4 +183,25 @@ def gemm_rope_mxfp8(x, x_scale, w, w_scale, cos, sin, num_heads: int, head_dim: 
     bsg_gemm_rope_mxfp8(x, x_scale, w, w_scale, layout, cos, sin, tokens, q_lora, num_heads, head_dim, qk_rope,
                         out["out_fp8_row"], out["out_scales_row"], out["out_fp8_col"], out["out_scales_col"],
                         workspace, workspace_bytes=workspace.numel(), stream=stream, **opts)
+    return out
+
+
+def gemm_rope_bf16(x, w, cos, sin, num_heads: int, head_dim: int = 192, qk_rope: int = 64, outputs=None,
+                   workspace=None, stream=None, **opts):
+    """The BF16-input projection: x (tokens, q_lora) and w (num_heads * head_dim, q_lora) bf16,
+    K-major; the rest (RoPE, dual MXFP8 outputs) as ``gemm_rope_mxfp8``."""
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise TypeError("gemm_rope_bf16 takes bf16 x and w")
+    tokens, q_lora = x.shape[-2], x.shape[-1]
+    dev = x.device
+    out = dict(outputs or {})
+    out.setdefault("out_fp8_row", torch.empty((tokens, num_heads, head_dim), dtype=torch.uint8, device=dev))
+    out.setdefault("out_scales_row", torch.empty((tokens, num_heads, head_dim // 32), dtype=torch.uint8, device=dev))
+    out.setdefault("out_fp8_col", torch.empty((tokens, num_heads, head_dim), dtype=torch.uint8, device=dev))
+    out.setdefault("out_scales_col", torch.empty((tokens // 32, num_heads, head_dim), dtype=torch.uint8, device=dev))
+    if workspace is None:
+        workspace = torch.zeros(bsg_workspace_size(), dtype=torch.uint8, device=dev)
+    bsg_gemm_rope_bf16(x, w, cos, sin, tokens, q_lora, num_heads, head_dim, qk_rope, out["out_fp8_row"],
+                       out["out_scales_row"], out["out_fp8_col"], out["out_scales_col"], workspace,
+                       workspace_bytes=workspace.numel(), stream=stream, **opts)
     return out

@@ -195,6 +195,39 @@ def test_dswiglu_validation():
         assert st in (OK, ARCH, CUDA)
 
 
+def _rope(name="bsg_gemm_rope_mxfp8", cta_pair=0, **kw):
+    a = dict(x=P, w=P, cos=P, sin=P, tokens=256, q=256, h=2, hd=192, r=64, orow=P, srow=P, ocol=P, scol=P,
+             layout=0, ws=P, wsb=256)
+    a.update(kw)
+    o = bsg._opts(cta_pair=cta_pair)
+    tail = (a["tokens"], a["q"], a["h"], a["hd"], a["r"], a["orow"], a["srow"], a["ocol"], a["scol"], ctypes.byref(o),
+            a["ws"], a["wsb"], None)
+    if name == "bsg_gemm_rope_bf16":
+        return bsg.raw_status(name, a["x"], a["w"], a["cos"], a["sin"], *tail)
+    return bsg.raw_status(name, a["x"], P, a["w"], P, a["layout"], a["cos"], a["sin"], *tail)
+
+
+def test_rope_validation():
+    for name in ("bsg_gemm_rope_mxfp8", "bsg_gemm_rope_bf16"):
+        assert _rope(name, x=None) == INVALID and _rope(name, scol=None) == INVALID
+        assert _rope(name, tokens=200) == INVALID and _rope(name, tokens=0) == INVALID
+        assert _rope(name, hd=128) == UNSUPPORTED and _rope(name, r=32) == UNSUPPORTED
+        assert _rope(name, wsb=128) == WORKSPACE and _rope(name, ws=None) == WORKSPACE
+        assert _rope(name, orow=P + 8) == ALIGN and _rope(name, cos=P + 2) == ALIGN
+        assert _rope(name, ws=P + 16) == ALIGN
+    assert _rope(q=48) == INVALID                     # MXFP8: whole 32-value scale blocks
+    assert _rope(layout=2) == INVALID
+    assert _rope(layout=1) == WORKSPACE               # the plain scales are repacked in the workspace
+    assert _rope(cta_pair=2, tokens=128) == INVALID   # pairs need tokens and heads * 192 in 256s
+    bf = "bsg_gemm_rope_bf16"
+    assert _rope(bf, q=12) == INVALID                 # bf16 rows must be 16-byte multiples
+    assert _rope(bf, q=4) == INVALID
+    assert _rope(bf, cta_pair=2) == UNSUPPORTED       # one-CTA tiles only
+    if _no_device():
+        assert _rope() in (OK, ARCH, CUDA)
+        assert _rope(bf, q=72) in (OK, ARCH, CUDA)
+
+
 def test_selftest_validation():
     assert bsg.raw_status("bsg_selftest_wait_timeout", None, 256, None) == WORKSPACE
     assert bsg.raw_status("bsg_selftest_wait_timeout", P, 16, None) == WORKSPACE

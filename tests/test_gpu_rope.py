@@ -1,4 +1,5 @@
-"""GPU parity of bsg_gemm_rope_mxfp8 (projection GEMM + per-head RoPE + dual MXFP8) against the oracle."""
+"""GPU parity of bsg_gemm_rope_mxfp8 and bsg_gemm_rope_bf16 (projection GEMM + per-head RoPE + dual
+MXFP8) against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -146,3 +147,123 @@ def test_gemm_rope_validation(lib):
     assert call(layout=1) == 8  # the plain layout needs room for the repacked scales
     assert call(cta_pair=2, tokens=128) == 1  # CTA pairs need tokens % 256 == 0 and heads * 192 % 256 == 0
     torch.cuda.synchronize()
+
+
+def run_rope_bf16(tokens, q_lora, heads, seed=11):
+    """The BF16-input path: the generator's fp32 values rounded to bf16 are the operands; the
+    oracle takes those exact values."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    wl = W.RopeProj("t", tokens, q_lora, heads, 192, 64, seed=seed)
+    x = torch.from_numpy(wl.x_rows()).to(torch.bfloat16)
+    w = torch.from_numpy(wl.w_rows()).to(torch.bfloat16)
+    cos32, sin32 = wl.tables()
+    cos = torch.from_numpy(cos32).to(torch.bfloat16)
+    sin = torch.from_numpy(sin32).to(torch.bfloat16)
+    ws = torch.zeros(bsg.bsg_workspace_size(), dtype=torch.uint8, device="cuda")
+    g = Outputs()
+    outputs = {"out_fp8_row": g.codes("row", (tokens, heads, 192)),
+               "out_scales_row": g.scales("scales_row", (tokens, heads, 6)),
+               "out_fp8_col": g.codes("col", (tokens, heads, 192)),
+               "out_scales_col": g.scales("scales_col", (tokens // 32, heads, 192))}
+    out = torch_ops.gemm_rope_bf16(x.cuda(), w.cuda(), cos.cuda(), sin.cuda(), heads, workspace=ws, outputs=outputs)
+    torch.cuda.synchronize()
+    g.check()
+    assert bsg.bsg_read_device_error(ws) == 0
+
+    xh, wh = x.double().numpy(), w.double().numpy()
+    cos64, sin64 = cos.double().numpy(), sin.double().numpy()
+    ref = orope.project_bf16(xh, wh, cos64, sin64, heads, 192, 64)
+    # bf16 x bf16 products are exact in fp32, as E4M3 ones are: the same accumulation bound
+    s_abs = (np.abs(xh) @ np.abs(wh).T).reshape(tokens, heads, 192)
+    tol = _tolerance((xh @ wh.T).reshape(tokens, heads, 192), s_abs, cos64, sin64, 192, 64)
+    n = heads * 192
+    y = ref["y"].reshape(tokens, n)
+    t = tol.reshape(tokens, n)
+    check_e4m3_blocks(out["out_fp8_row"].cpu().numpy().reshape(tokens, n),
+                      out["out_scales_row"].cpu().numpy().reshape(tokens, n // 32), y, t, 1.0, axis=1, what="row")
+    check_e4m3_blocks(out["out_fp8_col"].cpu().numpy().reshape(tokens, n),
+                      out["out_scales_col"].cpu().numpy().reshape(tokens // 32, n).T, y, t, 1.0, axis=0, what="col")
+    return out, ref
+
+
+@pytest.mark.parametrize("tokens,q_lora,heads", [
+    (128, 512, 1),
+    (256, 1536, 3),    # the DeepSeek-V3 query down-projection rank
+    (384, 72, 2),      # K tail of 8 values: one MMA with its upper half zero-filled
+    (256, 232, 4),     # a partial last stage of three MMAs
+    (512, 64, 8),      # a single 64-value K stage
+])
+def test_gemm_rope_bf16(lib, tokens, q_lora, heads):
+    run_rope_bf16(tokens, q_lora, heads)
+
+
+def test_gemm_rope_bf16_matches_the_mxfp8_path_on_shared_values(lib):
+    """Operands whose MXFP8 encoding is exact: the bf16 and MXFP8 kernels see the same values and
+    must give identical codes and scales (both accumulate exact products in fp32, in the same
+    K order up to the MMA grouping, so allow the boundary rule of the E4M3 check)."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    tokens, q_lora, heads = 256, 256, 2
+    rng = np.random.default_rng(5)
+    grid = formats.decode_e4m3(np.arange(0, 0x7F, dtype=np.uint8))
+    grid = grid[(grid >= 0.125) & (grid <= 8)]
+    x = (rng.choice(grid, (tokens, q_lora)) * rng.choice([-1, 1], (tokens, q_lora))).astype(np.float32)
+    w = (rng.choice(grid, (heads * 192, q_lora)) * rng.choice([-1, 1], (heads * 192, q_lora)) / 16).astype(np.float32)
+    x[:, ::32] = 8.0
+    w[:, ::32] = 0.5
+    wl = W.RopeProj("t", tokens, q_lora, heads, 192, 64, seed=1)
+    cos32, sin32 = wl.tables()
+    cos = torch.from_numpy(cos32).to(torch.bfloat16).cuda()
+    sin = torch.from_numpy(sin32).to(torch.bfloat16).cuda()
+    qx, sx = torch_ops.quantize(torch.from_numpy(x).cuda(), "mxfp8")
+    qw, sw = torch_ops.quantize(torch.from_numpy(w).cuda(), "mxfp8")
+    a = torch_ops.gemm_rope_mxfp8(qx[0], sx, qw[0], sw, cos, sin, heads)
+    b = torch_ops.gemm_rope_bf16(torch.from_numpy(x).to(torch.bfloat16).cuda(),
+                                 torch.from_numpy(w).to(torch.bfloat16).cuda(), cos, sin, heads)
+    torch.cuda.synchronize()
+    ref = orope.project_bf16(x.astype(np.float64), w.astype(np.float64), cos.double().cpu().numpy(),
+                             sin.double().cpu().numpy(), heads, 192, 64)
+    s_abs = (np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64)).T).reshape(tokens, heads, 192)
+    raw = (x.astype(np.float64) @ w.astype(np.float64).T).reshape(tokens, heads, 192)
+    tol = _tolerance(raw, s_abs, cos.double().cpu().numpy(), sin.double().cpu().numpy(), 192, 64)
+    n = heads * 192
+    for out in (a, b):
+        check_e4m3_blocks(out["out_fp8_row"].cpu().numpy().reshape(tokens, n),
+                          out["out_scales_row"].cpu().numpy().reshape(tokens, n // 32), ref["y"].reshape(tokens, n),
+                          tol.reshape(tokens, n), 1.0, axis=1, what="row")
+    # the scales agree except where a block amax sits on a power-of-two boundary
+    same = (a["out_scales_row"] == b["out_scales_row"]).float().mean().item()
+    assert same > 0.99
+
+
+def test_gemm_rope_bf16_validation(lib):
+    """Invalid arguments are rejected before anything is enqueued (real buffers)."""
+    import ctypes
+    import nvfp4_gemm_moe_gb300 as bsg
+    dev = "cuda"
+    tokens, q_lora, heads = 256, 72, 2
+    x = torch.zeros((tokens, q_lora), dtype=torch.bfloat16, device=dev)
+    w = torch.zeros((heads * 192, q_lora), dtype=torch.bfloat16, device=dev)
+    tab = torch.zeros((tokens, 64), dtype=torch.bfloat16, device=dev)
+    o_row = torch.zeros((tokens, heads, 192), dtype=torch.uint8, device=dev)
+    s_row = torch.zeros((tokens, heads, 6), dtype=torch.uint8, device=dev)
+    o_col = torch.zeros((tokens, heads, 192), dtype=torch.uint8, device=dev)
+    s_col = torch.zeros((tokens // 32, heads, 192), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(bsg.bsg_workspace_size(), dtype=torch.uint8, device=dev)
+
+    def call(cta_pair=0, **kw):
+        a = dict(tokens=tokens, q_lora=q_lora, heads=heads, hd=192, wsb=ws.numel())
+        a.update(kw)
+        o = bsg._opts(cta_pair=cta_pair)
+        return bsg.raw_status("bsg_gemm_rope_bf16", x.data_ptr(), w.data_ptr(), tab.data_ptr(), tab.data_ptr(),
+                              a["tokens"], a["q_lora"], a["heads"], a["hd"], 64, o_row.data_ptr(), s_row.data_ptr(),
+                              o_col.data_ptr(), s_col.data_ptr(), ctypes.byref(o), ws.data_ptr(), a["wsb"], None)
+    assert call(tokens=100) == 1 and call(q_lora=68) == 1
+    assert call(hd=128) == 2 and call(cta_pair=2) == 2
+    assert call(wsb=16) == 8
+    assert call() == 0
+    torch.cuda.synchronize()
+    assert bsg.bsg_read_device_error(ws) == 0
+    with pytest.raises(TypeError):
+        from nvfp4_gemm_moe_gb300 import torch_ops
+        torch_ops.gemm_rope_bf16(x.float(), w, tab, tab, heads)
