@@ -2,7 +2,8 @@
 
 One step = the whole hot path over one batch of synthetic input: quantise A and B
 (fp32 -> MXFP8 / NVFP4 codes + scale factors) and run the block-scaled GEMM with its
-fused epilogue.  Default workload: the batched dense MXFP8 GEMM + amax, L = 4,
+fused epilogue (bf16-operand workloads skip the quantisation: their step is the kernel
+alone).  Default workload: the batched dense MXFP8 GEMM + amax, L = 4,
 M = N = K = 8192, C bf16.  Inputs (2 x 1.07 GB fp32) are larger than L2, so no flush
 is needed between steps.
 
@@ -34,7 +35,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "block-scaled GEMM TFLOPS and % of GB300 FP8/FP4 tensor peak, per config"
 UNIT = "TFLOPS"
-NOMINAL_RATIO = {"mxfp8": 4.5 / 2.25, "nvfp4": 13.5 / 2.25}  # dense fp8 / fp4 vs bf16 tensor peak
+NOMINAL_RATIO = {"mxfp8": 4.5 / 2.25, "nvfp4": 13.5 / 2.25, "bf16": 1.0}  # dense peak vs the bf16 tensor peak
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -130,18 +131,23 @@ def run_ours(args, rank, world, local_rank):
         a_h, b_h = wl.x_rows()[None], wl.w_rows()[None]
     else:
         a_h, b_h = wl.a_rows()[None], wl.b_rows()
-    a_pin = torch.from_numpy(a_h).pin_memory()
-    b_pin = torch.from_numpy(b_h).pin_memory()
+    # bf16 operands are the inputs themselves (the draws rounded to bf16); the others are fp32
+    # inputs that every step quantises
+    host_dtype = torch.bfloat16 if fmt == "bf16" else torch.float32
+    a_pin = torch.from_numpy(a_h).to(host_dtype).pin_memory()
+    b_pin = torch.from_numpy(b_h).to(host_dtype).pin_memory()
+    del a_h, b_h
     a_d = a_pin.to(dev)
     b_d = b_pin.to(dev)
     la, ma, ka = a_d.shape
     lb, nb, _ = b_d.shape
-    v = 32 if fmt == "mxfp8" else 16
-    qcols = ka if fmt == "mxfp8" else ka // 2
-    qa = torch.empty((la, ma, qcols), dtype=torch.uint8, device=dev)
-    qb = torch.empty((lb, nb, qcols), dtype=torch.uint8, device=dev)
-    sfa = torch.empty(bsg.bsg_sf_bytes(la, ma, ka, v), dtype=torch.uint8, device=dev)
-    sfb = torch.empty(bsg.bsg_sf_bytes(lb, nb, ka, v), dtype=torch.uint8, device=dev)
+    if fmt != "bf16":
+        v = 32 if fmt == "mxfp8" else 16
+        qcols = ka if fmt == "mxfp8" else ka // 2
+        qa = torch.empty((la, ma, qcols), dtype=torch.uint8, device=dev)
+        qb = torch.empty((lb, nb, qcols), dtype=torch.uint8, device=dev)
+        sfa = torch.empty(bsg.bsg_sf_bytes(la, ma, ka, v), dtype=torch.uint8, device=dev)
+        sfb = torch.empty(bsg.bsg_sf_bytes(lb, nb, ka, v), dtype=torch.uint8, device=dev)
     ws = torch_ops.new_workspace(dev)
     if is_dense:
         c = torch.empty((wl.l, wl.m, wl.n), dtype=torch.float32 if wl.c_dtype == "f32" else torch.bfloat16,
@@ -176,6 +182,9 @@ def run_ours(args, rank, world, local_rank):
     def gemm():
         if is_dense:
             torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, wl.m, wl.n, wl.k, wl.l, c=c, amax=amax, workspace=ws)
+        elif is_rope and fmt == "bf16":
+            outs.update(torch_ops.gemm_rope_bf16(cur["a"][0], cur["b"][0], cur["cos"], cur["sin"], wl.heads,
+                                                 wl.head_dim, wl.qk_rope, outputs=outs, workspace=ws))
         elif is_rope:
             outs.update(torch_ops.gemm_rope_mxfp8(qa[0], sfa, qb[0], sfb, cur["cos"], cur["sin"], wl.heads, wl.head_dim,
                                                   wl.qk_rope, outputs=outs, workspace=ws))
@@ -191,15 +200,16 @@ def run_ours(args, rank, world, local_rank):
                                                      norm_const=nc, outputs=outs, workspace=ws))
 
     def step(ev0=None, ev1=None):
-        torch_ops.quantize(cur["a"], fmt, q=qa, sf=sfa)
-        torch_ops.quantize(cur["b"], fmt, q=qb, sf=sfb)
+        if fmt != "bf16":
+            torch_ops.quantize(cur["a"], fmt, q=qa, sf=sfa)
+            torch_ops.quantize(cur["b"], fmt, q=qb, sf=sfb)
         if ev0 is not None:
             ev0.record(stream)
         gemm()
         if ev1 is not None:
             ev1.record(stream)
 
-    launches_per_step = 3  # two quantiser kernels + one GEMM kernel
+    launches_per_step = 1 if fmt == "bf16" else 3  # (two quantiser kernels +) one GEMM kernel
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -303,7 +313,7 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3" if fmt == "mxfp8" else "e2m1", "data": "synthetic",
+        "vs_baseline": None, "dtype": {"mxfp8": "e4m3", "nvfp4": "e2m1", "bf16": "bf16"}[fmt], "data": "synthetic",
         "config": _config(wl),
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
@@ -342,6 +352,13 @@ def _traffic(workload):
 
 
 def _config(wl):
+    if isinstance(wl, W.RopeProj) and wl.fmt == "bf16":
+        out_gb = 2 * wl.tokens * wl.n / 1e9
+        return {"workload": wl.name, "format": wl.fmt, "tokens": wl.tokens, "q_lora": wl.q_lora, "heads": wl.heads,
+                "head_dim": wl.head_dim, "qk_rope": wl.qk_rope, "flops_per_step": wl.flops,
+                "l2": "no explicit flush: each step writes %.2f GB of outputs, more than L2, after reading its "
+                      "%.2f GB of bf16 inputs" % (out_gb, (wl.tokens + wl.n) * wl.q_lora * 2 / 1e9),
+                "step": "projection GEMM/RoPE/row+column MXFP8 on bf16 x and w"}
     if isinstance(wl, W.RopeProj):
         return {"workload": wl.name, "format": wl.fmt, "tokens": wl.tokens, "q_lora": wl.q_lora, "heads": wl.heads,
                 "head_dim": wl.head_dim, "qk_rope": wl.qk_rope, "flops_per_step": wl.flops,
@@ -387,6 +404,14 @@ def run_reference(args):
     args.ref_rows = oracle_rows(wl, args.ref_rows)
 
     def one_step():
+        if isinstance(wl, W.RopeProj) and wl.fmt == "bf16":
+            import torch
+            rows = np.arange(args.ref_rows)            # the first tokens, all heads
+            xb = torch.from_numpy(wl.x_rows(rows)).to(torch.bfloat16).double().numpy()
+            wb = torch.from_numpy(wl.w_rows()).to(torch.bfloat16).double().numpy()
+            cos, sin = (torch.from_numpy(t[:len(rows)]).to(torch.bfloat16).double().numpy() for t in wl.tables())
+            orope.project_bf16(xb, wb, cos, sin, wl.heads, wl.head_dim, wl.qk_rope)
+            return 2.0 * len(rows) * wl.n * wl.q_lora
         if isinstance(wl, W.RopeProj):
             rows = np.arange(args.ref_rows)            # the first tokens, all heads
             xc, xs = oq.quantize_logical(wl.x_rows(rows)[None], wl.fmt)
@@ -428,7 +453,9 @@ def run_reference(args):
         step_times.append(time.perf_counter() - t)
     total = sum(step_times)
     value = sample_flops * args.steps / total / 1e12
-    sample = (f"oracle path (quantise, dequantise, float64 GEMM, epilogue) on the first {args.ref_rows} rows of A "
+    steps_txt = ("float64 GEMM on the bf16 values, epilogue" if wl.fmt == "bf16"
+                 else "quantise, dequantise, float64 GEMM, epilogue")
+    sample = (f"oracle path ({steps_txt}) on the first {args.ref_rows} rows of A "
               f"against all {wl.n} rows of B (batch/expert 0) of {wl.name}; numpy/BLAS float64 on {cores} host threads")
     line = {
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,

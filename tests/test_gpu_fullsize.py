@@ -209,6 +209,43 @@ def test_rope_full_size_sampled(lib):
                               what=f"col[t{t0}, h{h}]")
 
 
+def test_rope_bf16_full_size_sampled(lib):
+    """The same projection with bf16 operands: 32-token blocks x single heads recomputed by the
+    oracle from the bf16 values."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    from oracle import rope as orope
+    from test_gpu_rope import _tolerance
+    wl = W.ROPE_PROJ_BF16_T16384
+    x = torch.from_numpy(wl.x_rows()).to(torch.bfloat16)
+    w = torch.from_numpy(wl.w_rows()).to(torch.bfloat16)
+    cos32, sin32 = wl.tables()
+    cos = torch.from_numpy(cos32).to(torch.bfloat16)
+    sin = torch.from_numpy(sin32).to(torch.bfloat16)
+    ws = torch_ops.new_workspace()
+    out = torch_ops.gemm_rope_bf16(x.cuda(), w.cuda(), cos.cuda(), sin.cuda(), wl.heads, wl.head_dim, wl.qk_rope,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    assert bsg.bsg_read_device_error(ws) == 0
+    d = wl.head_dim
+    for t0 in (0, 8192, wl.tokens - 32):
+        xh = x[t0:t0 + 32].double().numpy()
+        for h in (0, 77, wl.heads - 1):
+            wh = w[h * d:(h + 1) * d].double().numpy()
+            c64 = cos[t0:t0 + 32].double().numpy()
+            s64 = sin[t0:t0 + 32].double().numpy()
+            ref = orope.project_bf16(xh, wh, c64, s64, 1, d, wl.qk_rope)
+            tol = _tolerance((xh @ wh.T).reshape(32, 1, d), (np.abs(xh) @ np.abs(wh).T).reshape(32, 1, d), c64, s64,
+                             d, wl.qk_rope).reshape(32, d)
+            y = ref["y"].reshape(32, d)
+            check_e4m3_blocks(out["out_fp8_row"][t0:t0 + 32, h].cpu().numpy(),
+                              out["out_scales_row"][t0:t0 + 32, h].cpu().numpy(), y, tol, 1.0, axis=1,
+                              what=f"row[t{t0}, h{h}]")
+            check_e4m3_blocks(out["out_fp8_col"][t0:t0 + 32, h].cpu().numpy(),
+                              out["out_scales_col"][t0 // 32, h].cpu().numpy()[:, None], y, tol, 1.0, axis=0,
+                              what=f"col[t{t0}, h{h}]")
+
+
 def test_dswiglu_full_size_sampled(lib):
     """The E32 dSwiGLU backward at full size: 32-row blocks (largest, smallest and last
     expert) recomputed by the oracle over all 2N columns of D and their dprob rows."""

@@ -271,8 +271,9 @@ class GroupedDswiglu(Grouped):
 
 @dataclasses.dataclass(frozen=True)
 class RopeProj:
-    """Dense MXFP8 projection + per-head RoPE + dual-direction MXFP8 workload: x (tokens, q_lora),
-    w (heads * head_dim, q_lora) ([out, in]), rotary tables (tokens, qk_rope)."""
+    """Dense projection + per-head RoPE + dual-direction MXFP8 workload: x (tokens, q_lora),
+    w (heads * head_dim, q_lora) ([out, in]), rotary tables (tokens, qk_rope).  fmt "mxfp8": the
+    operands are quantised to MXFP8; fmt "bf16": they are the fp32 draws rounded to bf16."""
     name: str
     tokens: int
     q_lora: int
@@ -341,7 +342,9 @@ GROUPED_DSWIGLU_E32_FP8D = dataclasses.replace(GROUPED_DSWIGLU_E32, name="groupe
 
 # the DeepSeek-V3 MLA Q up-projection: 128 heads of 128 + 64 features from a 1536-wide latent
 ROPE_PROJ_T16384 = RopeProj("rope_proj_mxfp8_t16384_q1536_h128_d192", 16384, 1536, 128, 192, 64)
+# the same projection with bf16 operands
+ROPE_PROJ_BF16_T16384 = RopeProj("rope_proj_bf16_t16384_q1536_h128_d192", 16384, 1536, 128, 192, 64, fmt="bf16")
 
 ALL = {w.name: w for w in (DENSE_MXFP8_256, DENSE_MXFP8_8192, DENSE_MXFP8_8192_L1, DENSE_NVFP4_16384, GROUPED_SRELU_E32,
                            GROUPED_SRELU_E32_CLAMP, GROUPED_FP8D_E128, GROUPED_FP8D_E32, GROUPED_DSWIGLU_E32,
-                           GROUPED_DSWIGLU_E32_FP8D, ROPE_PROJ_T16384)}
+                           GROUPED_DSWIGLU_E32_FP8D, ROPE_PROJ_T16384, ROPE_PROJ_BF16_T16384)}
