@@ -736,17 +736,18 @@ __device__ __forceinline__ void epilogue_tile_rope(const GemmParams& p, int row,
 // grouped sReLU float D, or the (|ab|, |dswiglu|) pair of the dSwiGLU float D.
 template <int EPI>
 __device__ __forceinline__ void fold_expert_max(float* s_amax, int g, float m1, float m2, int lane) {
-  if (EPI != kEpiGroupedBF16 && EPI != kEpiDswigluF) return;
-  for (int o = 16; o >= 1; o >>= 1) {
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-    m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
-  }
-  if (lane == 0) {
-    if (EPI == kEpiGroupedBF16) {
-      atomic_max_nonneg(&s_amax[g], m1);
-    } else {
-      atomic_max_nonneg(&s_amax[2 * g], m1);
-      atomic_max_nonneg(&s_amax[2 * g + 1], m2);
+  if constexpr (EPI == kEpiGroupedBF16 || EPI == kEpiDswigluF) {
+    for (int o = 16; o >= 1; o >>= 1) {
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+    }
+    if (lane == 0) {
+      if (EPI == kEpiGroupedBF16) {
+        atomic_max_nonneg(&s_amax[g], m1);
+      } else {
+        atomic_max_nonneg(&s_amax[2 * g], m1);
+        atomic_max_nonneg(&s_amax[2 * g + 1], m2);
+      }
     }
   }
 }
