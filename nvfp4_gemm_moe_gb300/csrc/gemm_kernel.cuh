@@ -845,7 +845,10 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uin
 // (atom g of the unit fills columns 4g .. 4g + 3), otherwise single 32-bit words gathered from the
 // (up to three) atoms the tile's rows fall in.  b_blk0 is the 32-row block index of the tile's
 // first row within the first atom group loaded.
-template <class T>
+// kWideGather: for unaligned tiles, read whole 16-byte group rows and select words (fewer
+// shared-memory wavefronts; measured faster in the one-CTA kernel, slower in the pair kernel's
+// dSwiGLU variant) rather than single, four-way bank-conflicting words.
+template <class T, bool kWideGather = false>
 __device__ __forceinline__ void stage_scale_factors(const uint8_t* sfa_s, const uint8_t* sfb_s, uint32_t sfa_t,
                                                     uint32_t sfb_t, int lane, int b_blk0) {
   constexpr int A = T::kAtomsPerStage, G = T::kBRowGroups, C = T::kSfbColsPerMma;
@@ -864,6 +867,32 @@ __device__ __forceinline__ void stage_scale_factors(const uint8_t* sfa_s, const 
         const uint4 v = *reinterpret_cast<const uint4*>(sfb_s + (g * A + a) * 512 + lane * 16);
         const int c = C * a + 4 * g;
         rb[c] = v.x; rb[c + 1] = v.y; rb[c + 2] = v.z; rb[c + 3] = v.w;
+      }
+    }
+  } else if constexpr (kWideGather) {
+    // Word w of the loaded groups (group w / 4, word w % 4 of this lane's 16 bytes) holds the
+    // scales of 32-row block w; the tile's block c is word b_blk0 + c.  Each group's 16 bytes
+    // are read whole (conflict-free, unlike four-way conflicting single words) and the words
+    // picked with selects (b_blk0 <= 3, so word b_blk0 + c is one of words c .. c + 3).
+    static_assert(T::kBBlocks + 3 <= 4 * G, "loaded groups cover the tile's blocks");
+#pragma unroll
+    for (int a = 0; a < A; ++a) {
+      uint32_t w[4 * G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sfb_s + (g * A + a) * 512 + lane * 16);
+        w[4 * g] = v.x; w[4 * g + 1] = v.y; w[4 * g + 2] = v.z; w[4 * g + 3] = v.w;
+      }
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        uint32_t x = 0u;
+        if (c < T::kBBlocks) {
+          x = w[c];
+          x = b_blk0 == 1 ? w[c + 1] : x;
+          x = b_blk0 == 2 ? w[c + 2] : x;
+          x = b_blk0 == 3 ? w[c + 3] : x;
+        }
+        rb[C * a + c] = x;
       }
     }
   } else {
@@ -1086,8 +1115,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         tc_fence_after();
         const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
         if constexpr (FMT != kBF16)
-          stage_scale_factors<T>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t,
-                                 sfa_t + T::kSfaCols, lane, b_blk0);
+          stage_scale_factors<T, true>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t,
+                                       sfa_t + T::kSfaCols, lane, b_blk0);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
