@@ -288,9 +288,11 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
  * out_scales_col  device E8M0 (tokens / 32, num_heads, head_dim), plain row-major.
  * workspace       bsg_workspace_size() bytes for scale_layout 0, bsg_rope_workspace_size(...) for 1.
  * Requirements: tokens % 128 == 0, q_lora % 32 == 0, head_dim == 192 and qk_rope == 64 (one head
- * per 128 x 192 tile; other head shapes return BSG_ERR_UNSUPPORTED).  opts->cta_pair == 2 selects
- * CTA pairs on 256 x 256 tiles spanning heads (needs tokens % 256 == 0 and N % 256 == 0, else
- * BSG_ERR_INVALID_ARG).
+ * per CTA tile; other head shapes return BSG_ERR_UNSUPPORTED).  Tiles: opts->cta_pair == 0 takes
+ * CTA pairs on 256 x 192 tiles when tokens % 256 == 0, else one-CTA 128 x 192 tiles; 1 forces the
+ * one-CTA tiles; 2 selects CTA pairs, on 256 x 192 tiles with opts->tile_n == 192 (needs tokens %
+ * 256 == 0), otherwise on 256 x 256 tiles spanning heads (needs tokens % 256 == 0 and N % 256 ==
+ * 0); an ineligible shape returns BSG_ERR_INVALID_ARG.
  */
 size_t bsg_rope_workspace_size(int64_t tokens, int64_t num_heads, int64_t head_dim, int64_t q_lora);
 bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const uint8_t* w, const uint8_t* w_scale,
@@ -304,7 +306,8 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
  * ("GEMM + RoPE + MXFP8 Projection (SM100)", Overview: the GEMM in bf16).  As
  * bsg_gemm_rope_mxfp8 with x (tokens, q_lora) and w (num_heads * head_dim, q_lora) bf16 values
  * (K-major; tcgen05 kind::f16 MMAs, fp32 accumulation) and no scales.  Requirements: q_lora % 8
- * == 0 (16-byte rows), the rest as bsg_gemm_rope_mxfp8; one-CTA tiles only.  Workspace:
+ * == 0 (16-byte rows), the rest as bsg_gemm_rope_mxfp8.  opts->cta_pair == 2 selects CTA pairs on
+ * 256 x 192 tiles (needs tokens % 256 == 0, else BSG_ERR_INVALID_ARG).  Workspace:
  * bsg_workspace_size() bytes.
  */
 bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, const void* sin, int64_t tokens,

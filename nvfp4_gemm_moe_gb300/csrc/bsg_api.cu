@@ -660,12 +660,15 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
   const int64_t n = num_heads * head_dim;
   if (!fits_int32(tokens) || !fits_int32(n) || !fits_int32(q_lora) || !fits_int32(tokens * (n / 32)))
     return BSG_ERR_INVALID_ARG;
-  // One head per 128 x 192 tile (two accumulators: the dual E4M3 epilogue overlaps the next
-  // tile's MMAs), or with opts->cta_pair == 2 CTA pairs on 256 x 256 tiles spanning heads (a
-  // head's rotary chunk pair never straddles a 256-column tile); the pair tiles' single
-  // accumulator exposes that epilogue and measured slower at the DeepSeek-V3 shapes
+  // Tiles: one head per CTA, two accumulators (the dual E4M3 epilogue overlaps the next tile's
+  // MMAs): CTA pairs on 256 x 192 tiles (automatic when tokens % 256 == 0: each SM loads half a
+  // head of w per K slice; measured 8 % faster at the DeepSeek-V3 shapes) or one-CTA 128 x 192
+  // tiles (cta_pair == 1, or tokens % 256 != 0).  cta_pair == 2 with tile_n != 192 selects pairs
+  // on 256 x 256 tiles spanning heads (a head's rotary chunk pair never straddles a 256-column
+  // tile); their single accumulator exposes the epilogue and measured slower.
   const int cta_pair = opts ? opts->cta_pair : 0;
-  const bool pair_ok = tokens % 256 == 0 && n % 256 == 0;
+  const bool pair192 = (cta_pair == 0 && tokens % 256 == 0) || (cta_pair == 2 && opts->tile_n == 192);
+  const bool pair_ok = tokens % 256 == 0 && (pair192 || n % 256 == 0);
   if (cta_pair == 2 && !pair_ok) return BSG_ERR_INVALID_ARG;
   const size_t ws_need = scale_layout == 1 ? bsg_rope_workspace_size(tokens, num_heads, head_dim, q_lora)
                                            : kWorkspaceBytes;
@@ -693,14 +696,16 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
     sfb = pb;
   }
 
-  const bool pairs = pair_ok && cta_pair == 2;
-  const int bn = pairs ? 256 : 192;
+  const bool pairs = pair_ok && (cta_pair == 2 || pair192);
+  const int bn = pairs && !pair192 ? 256 : 192;
   const int64_t m_tiles = pairs ? tokens / 256 : tokens / 128;
   const int64_t n_tiles = n / bn;
   const int64_t tiles = m_tiles * n_tiles;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, x, q_lora, tokens, 1, 128) || !make_operand_map(&tb, w, q_lora, n, 1, pairs ? 128 : bn))
+  // a pair CTA holds half of the tile's B rows
+  if (!make_operand_map(&ta, x, q_lora, tokens, 1, 128) ||
+      !make_operand_map(&tb, w, q_lora, n, 1, pairs ? bn / 2 : bn))
     return BSG_ERR_CUDA;
 
   GemmParams p;
@@ -748,7 +753,10 @@ bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, con
       qk_rope < 1)
     return BSG_ERR_INVALID_ARG;
   if (head_dim != 192 || qk_rope != 64) return BSG_ERR_UNSUPPORTED;
-  if (opts && opts->cta_pair == 2) return BSG_ERR_UNSUPPORTED;  // one-CTA 128 x 192 tiles only
+  // one head per 128 x 192 one-CTA tile, or with opts->cta_pair == 2 per CTA of a 256 x 192 pair
+  // tile (not faster with bf16 operands: there the 192-wide MMAs, not the loads, bound the loop)
+  const bool pairs = opts && opts->cta_pair == 2;
+  if (pairs && tokens % 256 != 0) return BSG_ERR_INVALID_ARG;
   const int64_t n = num_heads * head_dim;
   if (!fits_int32(tokens) || !fits_int32(n) || !fits_int32(q_lora) || !fits_int32(tokens * (n / 32)))
     return BSG_ERR_INVALID_ARG;
@@ -762,11 +770,12 @@ bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, con
   if (st != BSG_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int bn = 192;
-  const int64_t m_tiles = tokens / 128;
+  const int64_t m_tiles = pairs ? tokens / 256 : tokens / 128;
   const int64_t tiles = m_tiles * num_heads;
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, x, row_bytes, tokens, 1, 128) || !make_operand_map(&tb, w, row_bytes, n, 1, bn))
+  if (!make_operand_map(&ta, x, row_bytes, tokens, 1, 128) ||
+      !make_operand_map(&tb, w, row_bytes, n, 1, pairs ? bn / 2 : bn))
     return BSG_ERR_CUDA;
   if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
 
@@ -791,7 +800,8 @@ bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, con
   p.err = static_cast<uint32_t*>(workspace);
 
   GemmConfig cfg{bsg::kBF16, bn, bsg::kEpiRope};
-  cudaError_t e = bsg::launch_gemm_rope(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
+  cudaError_t e = pairs ? bsg::launch_gemm_pair_rope(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
+                        : bsg::launch_gemm_rope(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
   if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }

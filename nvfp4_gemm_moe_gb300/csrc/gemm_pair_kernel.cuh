@@ -1,8 +1,9 @@
 // gemm_pair_kernel.cuh -- the block-scaled GEMM on CTA pairs (tcgen05 cta_group::2), 256 x BN tiles.
 //
-// A cluster of two CTAs (two SMs) computes one 256 x BN output tile (BN = 256, or 224 with two
-// TMEM accumulators so that the epilogue overlaps the next tile's MMAs), with any of the
-// one-CTA kernel's epilogues: each CTA holds 128 rows
+// A cluster of two CTAs (two SMs) computes one 256 x BN output tile (BN = 256, or 224 / 192 with
+// two TMEM accumulators so that the epilogue overlaps the next tile's MMAs; 192 for the RoPE
+// projection, one head per CTA, with MXFP8 or bf16 operands), with any of the one-CTA kernel's
+// epilogues: each CTA holds 128 rows
 // of A and one BN/2-row half of B in shared memory, and one thread of the even CTA issues
 // tcgen05.mma.cta_group::2 with M = 256, N = BN, so each SM fetches its own A rows and half of
 // the B tile per K slice instead of all of B.  Each CTA's TMEM holds the fp32 accumulator of its
@@ -32,14 +33,16 @@ namespace bsg {
 
 template <int FMT, int BN, int EPI = kEpiDense>
 struct PairTraits {
-  static_assert(BN == 256 || (BN == 224 && FMT == kMXFP8), "pair tile widths");
+  static_assert(BN == 256 || (BN == 224 && FMT == kMXFP8) || (BN == 192 && EPI == kEpiRope && FMT != kNVFP4),
+                "pair tile widths");
+  static_assert(FMT != kBF16 || EPI == kEpiRope, "bf16 operands: the RoPE projection only");
   static constexpr int kTileMPair = 256;
   static constexpr int kTileN = BN;
   static constexpr int kBHalf = BN / 2;  // B rows each CTA holds
-  static constexpr int kElemsPerKTile = FMT == kMXFP8 ? 128 : 256;
-  static constexpr int kMmaK = FMT == kMXFP8 ? 32 : 64;
+  static constexpr int kElemsPerKTile = FMT == kMXFP8 ? 128 : FMT == kNVFP4 ? 256 : 64;
+  static constexpr int kMmaK = FMT == kMXFP8 ? 32 : FMT == kNVFP4 ? 64 : 16;
   static constexpr int kMmasPerStage = 4;
-  static constexpr int kAtomsPerStage = FMT == kMXFP8 ? 1 : 4;
+  static constexpr int kAtomsPerStage = FMT == kMXFP8 ? 1 : FMT == kNVFP4 ? 4 : 0;  // bf16: no scales
   // the scale-factor layout fields stage_scale_factors reads: the scales of all BN B rows, from
   // two atom groups, or three when a 224-wide tile starts inside one
   static constexpr bool kSfbAligned = BN % 128 == 0;
@@ -51,10 +54,10 @@ struct PairTraits {
   static constexpr int kSfaBytes = kAtomsPerStage * 512;
   static constexpr int kSfbBytes = kBRowGroups * kAtomsPerStage * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kAcc = BN == 256 ? 1 : 2;  // 224: two accumulators, epilogue overlapped
+  static constexpr int kAcc = BN == 256 ? 1 : 2;  // 224, 192: two accumulators, epilogue overlapped
   static constexpr int kSfaCols = kAtomsPerStage * 4;
   static constexpr int kSfbCols = kSfbColsPerMma * kAtomsPerStage;
-  static constexpr int kSfStride = ((kSfaCols + kSfbCols + 15) / 16) * 16;
+  static constexpr int kSfStride = kAtomsPerStage == 0 ? 0 : ((kSfaCols + kSfbCols + 15) / 16) * 16;
   static constexpr int kSfBase = kAcc * BN;
   static constexpr int kTmemCols = 512;
   static constexpr int kBarBytes = 1024;
@@ -64,7 +67,7 @@ struct PairTraits {
   static constexpr int kXposeBytes = 8 * kXposeBlock;  // one transpose block per epilogue warp
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
-  static constexpr int kStagesTmem = (512 - kSfBase) / kSfStride;
+  static constexpr int kStagesTmem = kSfStride == 0 ? 6 : (512 - kSfBase) / kSfStride;
   static constexpr int kStages = kStagesSmem < kStagesTmem ? (kStagesSmem < 6 ? kStagesSmem : 6)
                                                            : (kStagesTmem < 6 ? kStagesTmem : 6);
   static_assert(kStages >= 3, "pipeline depth");
@@ -72,8 +75,10 @@ struct PairTraits {
       1024 + kStages * kStageBytes + kBarBytes + kOffsetsBytes + kAmaxBytes + kXposeBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // M = 256 across the pair (M >> 4 at bit 24), N = BN (N >> 3 at bit 17)
-  static constexpr uint32_t kIdesc = (FMT == kMXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))
-                                                    : ((1u << 7) | (1u << 10) | (0u << 23))) |
+  // kind::f16 (bf16 A and B): fp32 accumulator at bits 4-5, bf16 = 1 at bits 7 and 10
+  static constexpr uint32_t kIdesc = (FMT == kMXFP8   ? ((0u << 7) | (0u << 10) | (1u << 23))
+                                      : FMT == kNVFP4 ? ((1u << 7) | (1u << 10) | (0u << 23))
+                                                      : ((1u << 4) | (1u << 7) | (1u << 10))) |
                                      (static_cast<uint32_t>(kTileN >> 3) << 17) |
                                      (static_cast<uint32_t>(kTileMPair >> 4) << 24);
 };
@@ -86,7 +91,9 @@ __device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc
 #pragma unroll
   for (int j = 0; j < NM; ++j) {
     const uint32_t accumulate = j > 0 ? 1u : acc0;
-    if (FMT == kMXFP8) {
+    if (FMT == kBF16) {
+      tc_mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
+    } else if (FMT == kMXFP8) {
       tc_mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t, sfb_t,
                            accumulate);
     } else {
@@ -203,7 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
           const int k_left = p.k - kt * T::kElemsPerKTile;
           const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
-          const int atoms = FMT == kMXFP8 ? 1 : n_mma;
+          const int atoms = FMT == kMXFP8 ? 1 : FMT == kNVFP4 ? n_mma : 0;
           const uint32_t sf_bytes = static_cast<uint32_t>(atoms * 512 * (1 + T::kBRowGroups));
           // The odd CTA cannot load stage s of the next round before this round's phase has
           // completed (its empty barrier is released after the MMAs that needed that phase), so
@@ -214,17 +221,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           const uint32_t fbar = full0 + stage * 8;
           tma_load_3d_pair(s_a + stage * T::kABytes, &tmap_a, fbar, kt * kTileKBytes, a_row, a_batch);
           tma_load_3d_pair(s_b + stage * T::kBBytes, bmap, fbar, kt * kTileKBytes, b_row, b_batch);
-          const uint8_t* sfa_src =
-              p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + sfa_group) * p.sf_kt +
-                       static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
-          bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, sf_bar);
+          if constexpr (FMT != kBF16) {
+            const uint8_t* sfa_src =
+                p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + sfa_group) * p.sf_kt +
+                         static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+            bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, sf_bar);
 #pragma unroll
-          for (int g = 0; g < T::kBRowGroups; ++g) {
-            // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
-            const int rb = min((tc.nt * BN) / 128 + g, p.sfb_mt - 1);
-            const uint8_t* sfb_src =
-                sfb_base + (static_cast<uint64_t>(rb) * p.sf_kt + static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
-            bulk_load(s_sfb + stage * T::kSfbBytes + g * T::kAtomsPerStage * 512, sfb_src, atoms * 512, sf_bar);
+            for (int g = 0; g < T::kBRowGroups; ++g) {
+              // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
+              const int rb = min((tc.nt * BN) / 128 + g, p.sfb_mt - 1);
+              const uint8_t* sfb_src = sfb_base + (static_cast<uint64_t>(rb) * p.sf_kt +
+                                                   static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
+              bulk_load(s_sfb + stage * T::kSfbBytes + g * T::kAtomsPerStage * 512, sfb_src, atoms * 512, sf_bar);
+            }
           }
           ++issued;
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -256,7 +265,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           // warp-uniform control flow and operands, failures acted on per tile (as in the
           // one-CTA kernel); sf_ready implies the stage's A/B data landed (the even CTA's
           // stagers waited for it)
-          ok &= wait_bounded(&sf_ready[stage], phase, abort_flag, p.err);
+          // bf16 operands carry no scales: the even CTA's stage barrier (both CTAs' A/B bytes) is
+          // all the MMAs need
+          ok &= wait_bounded(FMT == kBF16 ? &full[stage] : &sf_ready[stage], phase, abort_flag, p.err);
           tc_fence_after();
           const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
@@ -296,7 +307,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     const uint32_t ready0 = mapa_shared(smem_u32(&sf_ready[0]), 0);
     uint64_t* landed = leader ? full : sf_full;
     uint32_t stage = 0, phase = 0;
-    bool ok = true;
+    bool ok = FMT != kBF16;  // bf16 operands have no scale factors to stage
     for (int t = pair_id; !bad && ok && t < p.num_tiles; t += num_pairs) {
       const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
       const int b_blk0 = ((tc.nt * BN) >> 5) & 3;  // the tile's first 32-row block within its first atom
@@ -304,8 +315,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         ok &= wait_bounded(&landed[stage], phase, abort_flag, p.err);
         tc_fence_after();
         const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
-        stage_scale_factors<T>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t, sfa_t + T::kSfaCols,
-                               lane, b_blk0);
+        if constexpr (FMT != kBF16)
+          stage_scale_factors<T>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t,
+                                 sfa_t + T::kSfaCols, lane, b_blk0);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();

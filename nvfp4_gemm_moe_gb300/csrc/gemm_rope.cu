@@ -19,6 +19,10 @@ cudaError_t launch_gemm_pair_rope(const GemmConfig& cfg, const CUtensorMap& ta, 
                                   const GemmParams& p, int max_pairs, cudaStream_t stream) {
   if (cfg.fmt == kMXFP8 && cfg.bn == 256 && cfg.epi == kEpiRope)
     return launch_gemm_pair_t<kMXFP8, 256, kEpiRope>(ta, tb, p, max_pairs, stream);
+  if (cfg.fmt == kMXFP8 && cfg.bn == 192 && cfg.epi == kEpiRope)
+    return launch_gemm_pair_t<kMXFP8, 192, kEpiRope>(ta, tb, p, max_pairs, stream);
+  if (cfg.fmt == kBF16 && cfg.bn == 192 && cfg.epi == kEpiRope)
+    return launch_gemm_pair_t<kBF16, 192, kEpiRope>(ta, tb, p, max_pairs, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -195,11 +195,11 @@ def test_dswiglu_validation():
         assert st in (OK, ARCH, CUDA)
 
 
-def _rope(name="bsg_gemm_rope_mxfp8", cta_pair=0, **kw):
+def _rope(name="bsg_gemm_rope_mxfp8", cta_pair=0, tile_n=0, **kw):
     a = dict(x=P, w=P, cos=P, sin=P, tokens=256, q=256, h=2, hd=192, r=64, orow=P, srow=P, ocol=P, scol=P,
              layout=0, ws=P, wsb=256)
     a.update(kw)
-    o = bsg._opts(cta_pair=cta_pair)
+    o = bsg._opts(cta_pair=cta_pair, tile_n=tile_n)
     tail = (a["tokens"], a["q"], a["h"], a["hd"], a["r"], a["orow"], a["srow"], a["ocol"], a["scol"], ctypes.byref(o),
             a["ws"], a["wsb"], None)
     if name == "bsg_gemm_rope_bf16":
@@ -219,13 +219,16 @@ def test_rope_validation():
     assert _rope(layout=2) == INVALID
     assert _rope(layout=1) == WORKSPACE               # the plain scales are repacked in the workspace
     assert _rope(cta_pair=2, tokens=128) == INVALID   # pairs need tokens and heads * 192 in 256s
+    assert _rope(cta_pair=2, h=3) == INVALID          # 256-wide pair tiles: heads * 192 % 256 != 0
     bf = "bsg_gemm_rope_bf16"
     assert _rope(bf, q=12) == INVALID                 # bf16 rows must be 16-byte multiples
     assert _rope(bf, q=4) == INVALID
-    assert _rope(bf, cta_pair=2) == UNSUPPORTED       # one-CTA tiles only
+    assert _rope(bf, cta_pair=2, tokens=128) == INVALID  # pair tiles need tokens % 256 == 0
     if _no_device():
         assert _rope() in (OK, ARCH, CUDA)
         assert _rope(bf, q=72) in (OK, ARCH, CUDA)
+        assert _rope(cta_pair=2, h=3, tile_n=192) in (OK, ARCH, CUDA)  # 256 x 192 pair tiles
+        assert _rope(bf, cta_pair=2) in (OK, ARCH, CUDA)
 
 
 def test_selftest_validation():

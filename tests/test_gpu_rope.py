@@ -28,7 +28,7 @@ def _tolerance(raw, s_abs, cos, sin, head_dim, qk_rope):
     return t
 
 
-def run_rope(tokens, q_lora, heads, layout="atoms", seed=7, cta_pair=0):
+def run_rope(tokens, q_lora, heads, layout="atoms", seed=7, cta_pair=0, tile_n=0):
     from nvfp4_gemm_moe_gb300 import torch_ops
     import nvfp4_gemm_moe_gb300 as bsg
     wl = W.RopeProj("t", tokens, q_lora, heads, 192, 64, seed=seed)
@@ -53,7 +53,7 @@ def run_rope(tokens, q_lora, heads, layout="atoms", seed=7, cta_pair=0):
                "out_fp8_col": g.codes("col", (tokens, heads, 192)),
                "out_scales_col": g.scales("scales_col", (tokens // 32, heads, 192))}
     out = torch_ops.gemm_rope_mxfp8(qx[0], sx_in, qw[0], sw_in, cos.cuda(), sin.cuda(), heads, scale_layout=layout,
-                                    workspace=ws, cta_pair=cta_pair, outputs=outputs)
+                                    workspace=ws, cta_pair=cta_pair, tile_n=tile_n, outputs=outputs)
     torch.cuda.synchronize()
     g.check()
     assert bsg.bsg_read_device_error(ws) == 0
@@ -83,13 +83,17 @@ def test_gemm_rope(lib, tokens, q_lora, heads, layout):
     run_rope(tokens, q_lora, heads, layout)
 
 
-@pytest.mark.parametrize("tokens,q_lora,heads,layout,cta_pair", [
-    (256, 256, 4, "atoms", 2),    # CTA pairs on 256 x 256 tiles spanning heads
-    (512, 160, 8, "plain", 2),
-    (256, 512, 4, "atoms", 0),    # the same shape on one-CTA 128 x 192 tiles (the default)
+@pytest.mark.parametrize("tokens,q_lora,heads,layout,cta_pair,tile_n", [
+    (256, 256, 4, "atoms", 2, 0),     # CTA pairs on 256 x 256 tiles spanning heads
+    (512, 160, 8, "plain", 2, 0),
+    (256, 512, 4, "atoms", 1, 0),     # the same shape on one-CTA 128 x 192 tiles
+    (256, 512, 4, "atoms", 2, 192),   # CTA pairs on 256 x 192 tiles, one head per CTA (automatic)
+    (384, 256, 2, "atoms", 0, 0),     # automatic with tokens % 256 != 0: one-CTA tiles
+    (512, 160, 3, "plain", 2, 192),   # N = 576: not a multiple of 256, fine for 192-wide pairs
+    (768, 96, 5, "atoms", 2, 192),    # K below one stage
 ])
-def test_gemm_rope_tile_shapes(lib, tokens, q_lora, heads, layout, cta_pair):
-    run_rope(tokens, q_lora, heads, layout, cta_pair=cta_pair)
+def test_gemm_rope_tile_shapes(lib, tokens, q_lora, heads, layout, cta_pair, tile_n):
+    run_rope(tokens, q_lora, heads, layout, cta_pair=cta_pair, tile_n=tile_n)
 
 
 def test_gemm_rope_identity_tables(lib):
@@ -149,7 +153,7 @@ def test_gemm_rope_validation(lib):
     torch.cuda.synchronize()
 
 
-def run_rope_bf16(tokens, q_lora, heads, seed=11):
+def run_rope_bf16(tokens, q_lora, heads, seed=11, cta_pair=0):
     """The BF16-input path: the generator's fp32 values rounded to bf16 are the operands; the
     oracle takes those exact values."""
     from nvfp4_gemm_moe_gb300 import torch_ops
@@ -166,7 +170,8 @@ def run_rope_bf16(tokens, q_lora, heads, seed=11):
                "out_scales_row": g.scales("scales_row", (tokens, heads, 6)),
                "out_fp8_col": g.codes("col", (tokens, heads, 192)),
                "out_scales_col": g.scales("scales_col", (tokens // 32, heads, 192))}
-    out = torch_ops.gemm_rope_bf16(x.cuda(), w.cuda(), cos.cuda(), sin.cuda(), heads, workspace=ws, outputs=outputs)
+    out = torch_ops.gemm_rope_bf16(x.cuda(), w.cuda(), cos.cuda(), sin.cuda(), heads, workspace=ws, outputs=outputs,
+                                   cta_pair=cta_pair)
     torch.cuda.synchronize()
     g.check()
     assert bsg.bsg_read_device_error(ws) == 0
@@ -196,6 +201,17 @@ def run_rope_bf16(tokens, q_lora, heads, seed=11):
 ])
 def test_gemm_rope_bf16(lib, tokens, q_lora, heads):
     run_rope_bf16(tokens, q_lora, heads)
+
+
+@pytest.mark.parametrize("tokens,q_lora,heads,cta_pair", [
+    (256, 1536, 3, 2),   # CTA pairs on 256 x 192 tiles
+    (512, 72, 2, 2),     # K tail of 8 values
+    (256, 232, 5, 2),    # partial last stage
+    (768, 64, 1, 2),     # one head, three pair tiles
+    (256, 512, 2, 1),    # one-CTA tiles requested explicitly
+])
+def test_gemm_rope_bf16_tile_shapes(lib, tokens, q_lora, heads, cta_pair):
+    run_rope_bf16(tokens, q_lora, heads, cta_pair=cta_pair)
 
 
 def test_gemm_rope_bf16_matches_the_mxfp8_path_on_shared_values(lib):
@@ -259,7 +275,7 @@ def test_gemm_rope_bf16_validation(lib):
                               a["tokens"], a["q_lora"], a["heads"], a["hd"], 64, o_row.data_ptr(), s_row.data_ptr(),
                               o_col.data_ptr(), s_col.data_ptr(), ctypes.byref(o), ws.data_ptr(), a["wsb"], None)
     assert call(tokens=100) == 1 and call(q_lora=68) == 1
-    assert call(hd=128) == 2 and call(cta_pair=2) == 2
+    assert call(hd=128) == 2 and call(cta_pair=2, tokens=128) == 1
     assert call(wsb=16) == 8
     assert call() == 0
     torch.cuda.synchronize()
