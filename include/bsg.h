@@ -4,7 +4,7 @@
  * Three operations, each one asynchronous launch sequence on the caller's
  * CUDA stream:
  *
- *   bsg_quantize_mx         fp32 -> MXFP8 / NVFP4 codes + scale factors in the
+ *   bsg_quantize_mx[_bf16]  fp32 (or bf16) -> MXFP8 / NVFP4 codes + scale factors in the
  *                           128x4 scale-factor atom layout (produces the GEMM operands);
  *   bsg_gemm_amax           dense / batched block-scaled GEMM + global amax
  *                           ("GEMM + Amax (SM100)", Overview and Equations);
@@ -139,6 +139,16 @@ size_t bsg_sf_bytes(int64_t batch, int64_t rows, int64_t k, int sf_vec_size);
 bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t k,
                            bsg_dtype q_dtype, int sf_vec_size, bsg_sf_dtype sf_dtype,
                            void* q, uint8_t* sf, void* stream);
+
+/*
+ * bsg_quantize_mx_bf16 -- bsg_quantize_mx on bf16 input: x is device bf16 (batch, rows, k)
+ * row-major, 16-byte aligned.  Each value is taken exactly (bf16 widens to fp32 without
+ * rounding), so the codes and scales equal those bsg_quantize_mx gives for the same values in
+ * fp32; the kernel reads half the bytes.  Arguments, requirements and errors as bsg_quantize_mx.
+ */
+bsg_status bsg_quantize_mx_bf16(const void* x, int64_t batch, int64_t rows, int64_t k,
+                                bsg_dtype q_dtype, int sf_vec_size, bsg_sf_dtype sf_dtype,
+                                void* q, uint8_t* sf, void* stream);
 
 /*
  * bsg_gemm_amax -- dense batched block-scaled GEMM with fused global amax

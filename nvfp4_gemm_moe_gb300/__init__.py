@@ -54,6 +54,8 @@ def _load():
     lib.bsg_status_string.argtypes = [I]
     lib.bsg_quantize_mx.restype = I
     lib.bsg_quantize_mx.argtypes = [P, I64, I64, I64, I, I, I, P, P, P]
+    lib.bsg_quantize_mx_bf16.restype = I
+    lib.bsg_quantize_mx_bf16.argtypes = [P, I64, I64, I64, I, I, I, P, P, P]
     lib.bsg_gemm_amax.restype = I
     lib.bsg_gemm_amax.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, P, I, P,
                                   ctypes.POINTER(bsg_gemm_opts), P, SZ, P]
@@ -133,6 +135,11 @@ def bsg_status_string(status: int) -> str:
 def bsg_quantize_mx(x, batch, rows, k, q_dtype, sf_vec_size, sf_dtype, q, sf, stream=None):
     _check(_lib.bsg_quantize_mx(_ptr(x), batch, rows, k, q_dtype, sf_vec_size, sf_dtype, _ptr(q), _ptr(sf),
                                 _stream(stream)), "bsg_quantize_mx")
+
+
+def bsg_quantize_mx_bf16(x, batch, rows, k, q_dtype, sf_vec_size, sf_dtype, q, sf, stream=None):
+    _check(_lib.bsg_quantize_mx_bf16(_ptr(x), batch, rows, k, q_dtype, sf_vec_size, sf_dtype, _ptr(q), _ptr(sf),
+                                     _stream(stream)), "bsg_quantize_mx_bf16")
 
 
 def bsg_gemm_amax(a, b, sfa, sfb, ab_dtype, sf_dtype, sf_vec_size, m, n, k, l, c, c_dtype, amax, workspace,

@@ -205,9 +205,10 @@ const char* bsg_status_string(bsg_status s) {
   return "BSG_ERR_UNKNOWN";
 }
 
-bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t k, bsg_dtype q_dtype,
-                           int sf_vec_size, bsg_sf_dtype sf_dtype, void* q, uint8_t* sf, void* stream) {
-  NvtxRange nvtx_range("bsg_quantize_mx");
+namespace {
+
+bsg_status quantize_impl(const void* x, bool x_bf16, int64_t batch, int64_t rows, int64_t k, bsg_dtype q_dtype,
+                         int sf_vec_size, bsg_sf_dtype sf_dtype, void* q, uint8_t* sf, void* stream) {
   int fmt = 0;
   bsg_status st = operand_format(q_dtype, sf_dtype, sf_vec_size, &fmt);
   if (st != BSG_OK) return st;
@@ -219,9 +220,23 @@ bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t 
   DeviceInfo info;
   st = current_device(nullptr, &info);
   if (st != BSG_OK) return st;
-  cudaError_t e = bsg::launch_quantize(fmt, x, batch, rows, k, static_cast<uint8_t*>(q), sf, info.num_sms,
+  cudaError_t e = bsg::launch_quantize(fmt, x, x_bf16, batch, rows, k, static_cast<uint8_t*>(q), sf, info.num_sms,
                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+}
+
+}  // namespace
+
+bsg_status bsg_quantize_mx(const float* x, int64_t batch, int64_t rows, int64_t k, bsg_dtype q_dtype,
+                           int sf_vec_size, bsg_sf_dtype sf_dtype, void* q, uint8_t* sf, void* stream) {
+  NvtxRange nvtx_range("bsg_quantize_mx");
+  return quantize_impl(x, false, batch, rows, k, q_dtype, sf_vec_size, sf_dtype, q, sf, stream);
+}
+
+bsg_status bsg_quantize_mx_bf16(const void* x, int64_t batch, int64_t rows, int64_t k, bsg_dtype q_dtype,
+                                int sf_vec_size, bsg_sf_dtype sf_dtype, void* q, uint8_t* sf, void* stream) {
+  NvtxRange nvtx_range("bsg_quantize_mx_bf16");
+  return quantize_impl(x, true, batch, rows, k, q_dtype, sf_vec_size, sf_dtype, q, sf, stream);
 }
 
 bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb, bsg_dtype ab_dtype,

@@ -111,7 +111,8 @@ cudaError_t launch_gemm_pair_rope(const GemmConfig& cfg, const CUtensorMap& tmap
 cudaError_t launch_sf_pack(const uint8_t* src, int64_t rows, int64_t blocks, uint8_t* dst, cudaStream_t stream);
 
 // Launches the block quantiser.
-cudaError_t launch_quantize(int fmt, const float* x, int64_t batch, int64_t rows, int64_t k, uint8_t* q,
+// x: fp32, or bf16 when x_bf16 (widened exactly to fp32 on load).
+cudaError_t launch_quantize(int fmt, const void* x, bool x_bf16, int64_t batch, int64_t rows, int64_t k, uint8_t* q,
                             uint8_t* sf, int num_sms, cudaStream_t stream);
 
 }  // namespace bsg

@@ -1,4 +1,4 @@
-// quantize.cu -- fp32 -> MXFP8 / NVFP4 block quantiser (memory-bound).
+// quantize.cu -- fp32 or bf16 -> MXFP8 / NVFP4 block quantiser (memory-bound).
 //
 // MXFP8: a warp takes one row at a time and walks its "units": 128 consecutive fp32 values (512 bytes,
 // one float4 per lane, fully coalesced), kUnroll loads in flight.  For MXFP8 a unit is 4 blocks of 32 (8 lanes per
@@ -6,6 +6,9 @@
 // warp shuffles, the scale bytes of 4 consecutive blocks are adjacent in the atom layout
 // and leave as one 32-bit store, the codes as one 32-bit (E4M3) or 16-bit (E2M1) store
 // per lane.  Units of the padding rows of the last 128-row atom produce zero scale bytes.
+// bf16 inputs are widened to fp32 on load (exactly), so both input types share the arithmetic;
+// their units are the same element counts at half the bytes (8- or 16-byte loads per lane).
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -62,7 +65,28 @@ __device__ __forceinline__ void e2m1_thresholds(float s, float (&t)[7]) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const float* __restrict__ x, int64_t rows, int k,
+// Four consecutive inputs as fp32 (streaming loads: each input is read once).
+__device__ __forceinline__ float4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));  // element 2i in the low half of word i
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xffff0000u));
+}
+// Eight consecutive inputs as fp32.
+__device__ __forceinline__ void load8(const float* p, float4& a, float4& b) {
+  a = __ldcs(reinterpret_cast<const float4*>(p));
+  b = __ldcs(reinterpret_cast<const float4*>(p + 4));
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float4& a, float4& b) {
+  const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
+  a = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                  __uint_as_float(u.y & 0xffff0000u));
+  b = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u), __uint_as_float(u.w << 16),
+                  __uint_as_float(u.w & 0xffff0000u));
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const TIn* __restrict__ x, int64_t rows, int k,
                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                             int64_t rows_padded, int units_per_row, int64_t total_rows,
                                                             int64_t mt_n, int64_t kt_n) {
@@ -77,14 +101,13 @@ __global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const float* _
     const int64_t r = rg - l * rows_padded;
     const bool row_ok = r < rows;
     const int64_t row_g = l * rows + r;
-    const float* xr = x + row_g * k;
+    const TIn* xr = x + row_g * k;
     for (int kc0 = 0; kc0 < units_per_row; kc0 += kUnroll) {
       float4 v[kUnroll];
 #pragma unroll
       for (int j = 0; j < kUnroll; ++j) {
         const int kk = (kc0 + j) * 128 + lane * 4;
-        v[j] = (row_ok && kc0 + j < units_per_row && kk < k) ? __ldcs(reinterpret_cast<const float4*>(xr + kk))
-                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[j] = (row_ok && kc0 + j < units_per_row && kk < k) ? load4(xr + kk) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < kUnroll; ++j) {
@@ -117,7 +140,8 @@ __global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const float* _
 // float4 loads), so a block of 16 spans two lanes and each lane's eight codes leave as one
 // 32-bit store.  The 16 scale bytes of a unit are four 32-bit words of the atom layout,
 // stored by lanes 0, 8, 16 and 24.
-__global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const float* __restrict__ x, int64_t rows, int k,
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __restrict__ x, int64_t rows, int k,
                                                                   uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                                   int64_t rows_padded, int units_per_row,
                                                                   int64_t total_rows, int64_t mt_n, int64_t kt_n) {
@@ -130,15 +154,19 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const float* _
     const int64_t r = rg - l * rows_padded;
     const bool row_ok = r < rows;
     const int64_t row_g = l * rows + r;
-    const float* xr = x + row_g * k;
+    const TIn* xr = x + row_g * k;
     for (int kc0 = 0; kc0 < units_per_row; kc0 += kU) {
       float4 v0[kU], v1[kU];
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const int kk = (kc0 + j) * 256 + lane * 8;
         const bool ok = row_ok && kc0 + j < units_per_row && kk < k;
-        v0[j] = ok ? __ldcs(reinterpret_cast<const float4*>(xr + kk)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v1[j] = ok ? __ldcs(reinterpret_cast<const float4*>(xr + kk + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok) {
+          load8(xr + kk, v0[j], v1[j]);
+        } else {
+          v0[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          v1[j] = v0[j];
+        }
       }
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
@@ -206,7 +234,7 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const float* _
 
 }  // namespace
 
-cudaError_t launch_quantize(int fmt, const float* x, int64_t batch, int64_t rows, int64_t k, uint8_t* q,
+cudaError_t launch_quantize(int fmt, const void* x, bool x_bf16, int64_t batch, int64_t rows, int64_t k, uint8_t* q,
                             uint8_t* sf, int num_sms, cudaStream_t stream) {
   const int v = fmt == kMXFP8 ? 32 : 16;
   const int64_t mt_n = (rows + 127) / 128;
@@ -218,12 +246,22 @@ cudaError_t launch_quantize(int fmt, const float* x, int64_t batch, int64_t rows
   const int64_t max_blocks = static_cast<int64_t>(num_sms) * 8;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
-  if (fmt == kMXFP8) {
-    quantize_mxfp8_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        x, rows, static_cast<int>(k), q, sf, rows_padded, units_per_row, total_rows, mt_n, kt_n);
+  const unsigned grid = static_cast<unsigned>(blocks);
+  const int units_nvfp4 = static_cast<int>((k + 255) / 256);
+  const float* xf = static_cast<const float*>(x);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (fmt == kMXFP8 && !x_bf16) {
+    quantize_mxfp8_kernel<<<grid, kThreads, 0, stream>>>(xf, rows, static_cast<int>(k), q, sf, rows_padded,
+                                                         units_per_row, total_rows, mt_n, kt_n);
+  } else if (fmt == kMXFP8) {
+    quantize_mxfp8_kernel<<<grid, kThreads, 0, stream>>>(xb, rows, static_cast<int>(k), q, sf, rows_padded,
+                                                         units_per_row, total_rows, mt_n, kt_n);
+  } else if (!x_bf16) {
+    quantize_nvfp4_kernel<<<grid, kThreads, 0, stream>>>(xf, rows, static_cast<int>(k), q, sf, rows_padded,
+                                                         units_nvfp4, total_rows, mt_n, kt_n);
   } else {
-    quantize_nvfp4_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        x, rows, static_cast<int>(k), q, sf, rows_padded, static_cast<int>((k + 255) / 256), total_rows, mt_n, kt_n);
+    quantize_nvfp4_kernel<<<grid, kThreads, 0, stream>>>(xb, rows, static_cast<int>(k), q, sf, rows_padded,
+                                                         units_nvfp4, total_rows, mt_n, kt_n);
   }
   return cudaGetLastError();
 }

@@ -7,9 +7,10 @@ from __future__ import annotations
 
 import torch
 
-from . import (BF16, E2M1, E4M3, F16, F32, FORMATS, bsg_gemm_amax, bsg_grouped_discrete_workspace_size,
-               bsg_gemm_rope_bf16, bsg_gemm_rope_mxfp8, bsg_grouped_gemm_dswiglu, bsg_grouped_gemm_srelu, bsg_grouped_gemm_srelu_discrete,
-               bsg_quantize_mx, bsg_rope_workspace_size, bsg_sf_bytes, bsg_workspace_size)
+from . import (BF16, E2M1, E4M3, F16, F32, FORMATS, bsg_gemm_amax, bsg_gemm_rope_bf16, bsg_gemm_rope_mxfp8,
+               bsg_grouped_discrete_workspace_size, bsg_grouped_gemm_dswiglu, bsg_grouped_gemm_srelu,
+               bsg_grouped_gemm_srelu_discrete, bsg_quantize_mx, bsg_quantize_mx_bf16, bsg_rope_workspace_size,
+               bsg_sf_bytes, bsg_workspace_size)
 
 
 def new_workspace(device="cuda") -> torch.Tensor:
@@ -17,7 +18,7 @@ def new_workspace(device="cuda") -> torch.Tensor:
 
 
 def quantize(x: torch.Tensor, fmt: str, q=None, sf=None, stream=None):
-    """x: fp32 (batch, rows, K) or (rows, K) on the GPU -> (codes uint8, sf uint8 flat)."""
+    """x: fp32 or bf16 (batch, rows, K) or (rows, K) on the GPU -> (codes uint8, sf uint8 flat)."""
     if x.dim() == 2:
         x = x.unsqueeze(0)
     batch, rows, k = x.shape
@@ -27,7 +28,12 @@ def quantize(x: torch.Tensor, fmt: str, q=None, sf=None, stream=None):
         q = torch.empty((batch, rows, q_cols), dtype=torch.uint8, device=x.device)
     if sf is None:
         sf = torch.empty(bsg_sf_bytes(batch, rows, k, v), dtype=torch.uint8, device=x.device)
-    bsg_quantize_mx(x, batch, rows, k, ab, v, sfd, q, sf, stream=stream)
+    if x.dtype == torch.bfloat16:
+        bsg_quantize_mx_bf16(x, batch, rows, k, ab, v, sfd, q, sf, stream=stream)
+    elif x.dtype == torch.float32:
+        bsg_quantize_mx(x, batch, rows, k, ab, v, sfd, q, sf, stream=stream)
+    else:
+        raise TypeError(f"quantize takes fp32 or bf16 input, not {x.dtype}")
     return q, sf
 
 

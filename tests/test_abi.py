@@ -53,11 +53,30 @@ def test_sizes_and_strings():
     assert bsg.bsg_status_string(7) == "BSG_ERR_BAD_OFFSETS"
 
 
-def _quant(**kw):
+def _quant(name="bsg_quantize_mx", **kw):
     a = dict(x=P, batch=1, rows=128, k=256, q=0x1, v=32, sf=0, qp=P, sfp=P, stream=None)
     a.update(kw)
-    return bsg.raw_status("bsg_quantize_mx", a["x"], a["batch"], a["rows"], a["k"], a["q"], a["v"], a["sf"],
+    return bsg.raw_status(name, a["x"], a["batch"], a["rows"], a["k"], a["q"], a["v"], a["sf"],
                           a["qp"], a["sfp"], a["stream"])
+
+
+def test_quantize_bf16_validation():
+    """The bf16-input entry shares the fp32 entry's checks."""
+    E4M3, E2M1 = bsg.E4M3, bsg.E2M1
+
+    def q(**kw):
+        a = dict(q=E4M3, v=32, sf=bsg.SF_UE8M0)
+        a.update(kw)
+        return _quant("bsg_quantize_mx_bf16", **a)
+    assert q(x=None) == INVALID
+    assert q(v=16) == INVALID                         # FP8 needs v = 32
+    assert q(q=bsg.E5M2) == UNSUPPORTED
+    assert q(k=48) == INVALID
+    assert q(x=P + 8) == ALIGN
+    assert q(q=E2M1, v=16, sf=bsg.SF_UE4M3, k=48) == ALIGN
+    if _no_device():
+        assert q() in (ARCH, CUDA)
+        assert q(q=E2M1, v=16, sf=bsg.SF_UE4M3) in (ARCH, CUDA)
 
 
 def test_quantize_validation():

@@ -1,4 +1,5 @@
-"""GPU parity of bsg_quantize_mx against the oracle quantiser: codes and scale bytes bit-exact."""
+"""GPU parity of bsg_quantize_mx (fp32 input) and bsg_quantize_mx_bf16 (bf16 input) against the oracle
+quantiser: codes and scale bytes bit-exact."""
 import numpy as np
 import pytest
 import torch
@@ -119,3 +120,43 @@ def test_quantize_nvfp4_near_midpoints(lib):
     q_ref, sf_ref = oq.quantize(x, "nvfp4")
     assert np.array_equal(sf, sf_ref)
     assert np.array_equal(q.reshape(q_ref.shape), q_ref), f"{(q.reshape(q_ref.shape) != q_ref).sum()} code bytes differ"
+
+
+@pytest.mark.parametrize("fmt,batch,rows,k", [
+    ("mxfp8", 1, 256, 256), ("mxfp8", 2, 130, 160), ("mxfp8", 1, 1, 32), ("mxfp8", 3, 129, 4096),
+    ("nvfp4", 1, 256, 512), ("nvfp4", 2, 130, 96), ("nvfp4", 1, 3, 32), ("nvfp4", 2, 200, 2080),
+])
+def test_quantize_bf16_input_bit_exact(lib, fmt, batch, rows, k):
+    """bf16 input: the codes and scales the oracle gives for the (exactly widened) bf16 values,
+    and the same bytes as the fp32 kernel on those values."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    v = 32 if fmt == "mxfp8" else 16
+    xb = torch.from_numpy(_wide_range(batch * 1000 + rows + k + 7, batch, rows, k, v)).to(torch.bfloat16)
+    q, sf = torch_ops.quantize(xb.cuda(), fmt)
+    q32, sf32 = torch_ops.quantize(xb.float().cuda(), fmt)
+    torch.cuda.synchronize()
+    q, sf = q.cpu().numpy(), sf.cpu().numpy()
+    q_ref, sf_ref = oq.quantize(xb.float().numpy(), fmt)
+    assert np.array_equal(sf, sf_ref), f"{(sf != sf_ref).sum()} scale bytes differ"
+    assert np.array_equal(q.reshape(q_ref.shape), q_ref), f"{(q.reshape(q_ref.shape) != q_ref).sum()} code bytes differ"
+    assert np.array_equal(q, q32.cpu().numpy()) and np.array_equal(sf, sf32.cpu().numpy())
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_quantize_bf16_input_ties(lib, fmt):
+    """Values on rounding midpoints (all representable in bf16: at most five significant bits)."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    x = _ties(fmt, 2, 130, 256)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    assert np.array_equal(xb.float().numpy(), x)
+    q, sf = torch_ops.quantize(xb.cuda(), fmt)
+    torch.cuda.synchronize()
+    q_ref, sf_ref = oq.quantize(x, fmt)
+    assert np.array_equal(sf.cpu().numpy(), sf_ref)
+    assert np.array_equal(q.cpu().numpy().reshape(q_ref.shape), q_ref)
+
+
+def test_quantize_rejects_other_input_types(lib):
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    with pytest.raises(TypeError):
+        torch_ops.quantize(torch.zeros((1, 128, 64), dtype=torch.float16, device="cuda"), "mxfp8")
