@@ -1,7 +1,7 @@
 // quantize.cu -- fp32 or bf16 -> MXFP8 / NVFP4 block quantiser (memory-bound).
 //
 // MXFP8: a warp takes one row at a time and walks its "units": 128 consecutive fp32 values (512 bytes,
-// one float4 per lane, fully coalesced), kUnroll loads in flight.  For MXFP8 a unit is 4 blocks of 32 (8 lanes per
+// one float4 per lane, fully coalesced), 4 KB of loads in flight per warp.  For MXFP8 a unit is 4 blocks of 32 (8 lanes per
 // block), for NVFP4 8 blocks of 16 (4 lanes per block).  Block maxima are reduced with
 // warp shuffles, the scale bytes of 4 consecutive blocks are adjacent in the atom layout
 // and leave as one 32-bit store, the codes as one 32-bit (E4M3) or 16-bit (E2M1) store
@@ -18,7 +18,6 @@
 namespace bsg {
 namespace {
 
-constexpr int kUnroll = 8;  // 512-byte loads in flight per warp
 constexpr int kThreads = 256;
 
 // RNE_UE4M3(a / 6) decided exactly: candidate from an fp32 approximation of the quotient
@@ -65,25 +64,49 @@ __device__ __forceinline__ void e2m1_thresholds(float s, float (&t)[7]) {
   }
 }
 
-// Four consecutive inputs as fp32 (streaming loads: each input is read once).
-__device__ __forceinline__ float4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
-  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));  // element 2i in the low half of word i
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
-                     __uint_as_float(u.y & 0xffff0000u));
+// Raw loads (streaming: each input is read once) and their exact widening to fp32.  A bf16
+// warp keeps twice the units in flight (the same bytes as fp32) in the same registers.
+__device__ __forceinline__ float4 bf16x4_to_float4(uint32_t lo, uint32_t hi) {  // element 2i: low half of word i
+  return make_float4(__uint_as_float(lo << 16), __uint_as_float(lo & 0xffff0000u), __uint_as_float(hi << 16),
+                     __uint_as_float(hi & 0xffff0000u));
 }
-// Eight consecutive inputs as fp32.
-__device__ __forceinline__ void load8(const float* p, float4& a, float4& b) {
-  a = __ldcs(reinterpret_cast<const float4*>(p));
-  b = __ldcs(reinterpret_cast<const float4*>(p + 4));
-}
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float4& a, float4& b) {
-  const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
-  a = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
-                  __uint_as_float(u.y & 0xffff0000u));
-  b = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u), __uint_as_float(u.w << 16),
-                  __uint_as_float(u.w & 0xffff0000u));
-}
+template <typename TIn>
+struct QuantLoads;
+template <>
+struct QuantLoads<float> {
+  static constexpr int kUnitsMx = 8;  // MXFP8 units (128 values) in flight per warp: 4 KB
+  static constexpr int kUnitsNv = 4;  // NVFP4 units (256 values) in flight per warp: 4 KB
+  using Raw4 = float4;
+  struct Raw8 { float4 a, b; };
+  static __device__ __forceinline__ Raw4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+  static __device__ __forceinline__ float4 widen4(const Raw4& r) { return r; }
+  static __device__ __forceinline__ Raw8 load8(const float* p) {
+    return {__ldcs(reinterpret_cast<const float4*>(p)), __ldcs(reinterpret_cast<const float4*>(p + 4))};
+  }
+  static __device__ __forceinline__ void widen8(const Raw8& r, float4& a, float4& b) { a = r.a; b = r.b; }
+  static __device__ __forceinline__ Raw4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+  static __device__ __forceinline__ Raw8 zero8() { return {zero4(), zero4()}; }
+};
+template <>
+struct QuantLoads<__nv_bfloat16> {
+  static constexpr int kUnitsMx = 16;
+  static constexpr int kUnitsNv = 8;
+  using Raw4 = uint2;
+  using Raw8 = uint4;
+  static __device__ __forceinline__ Raw4 load4(const __nv_bfloat16* p) {
+    return __ldcs(reinterpret_cast<const uint2*>(p));
+  }
+  static __device__ __forceinline__ float4 widen4(const Raw4& r) { return bf16x4_to_float4(r.x, r.y); }
+  static __device__ __forceinline__ Raw8 load8(const __nv_bfloat16* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+  }
+  static __device__ __forceinline__ void widen8(const Raw8& r, float4& a, float4& b) {
+    a = bf16x4_to_float4(r.x, r.y);
+    b = bf16x4_to_float4(r.z, r.w);
+  }
+  static __device__ __forceinline__ Raw4 zero4() { return make_uint2(0u, 0u); }
+  static __device__ __forceinline__ Raw8 zero8() { return make_uint4(0u, 0u, 0u, 0u); }
+};
 
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const TIn* __restrict__ x, int64_t rows, int k,
@@ -95,34 +118,37 @@ __global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const TIn* __r
   const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
 
   // one (padded) row per warp iteration: the row's batch and index are computed once, then
-  // the warp walks the row's units kUnroll at a time with kUnroll 512-byte loads in flight
+  // the warp walks the row's units with 4 KB of loads in flight
   for (int64_t rg = warp_id; rg < total_rows; rg += num_warps) {
     const int64_t l = rg / rows_padded;
     const int64_t r = rg - l * rows_padded;
     const bool row_ok = r < rows;
     const int64_t row_g = l * rows + r;
     const TIn* xr = x + row_g * k;
-    for (int kc0 = 0; kc0 < units_per_row; kc0 += kUnroll) {
-      float4 v[kUnroll];
+    using L = QuantLoads<TIn>;
+    constexpr int U = L::kUnitsMx;
+    for (int kc0 = 0; kc0 < units_per_row; kc0 += U) {
+      typename L::Raw4 raw[U];
 #pragma unroll
-      for (int j = 0; j < kUnroll; ++j) {
+      for (int j = 0; j < U; ++j) {
         const int kk = (kc0 + j) * 128 + lane * 4;
-        v[j] = (row_ok && kc0 + j < units_per_row && kk < k) ? load4(xr + kk) : make_float4(0.f, 0.f, 0.f, 0.f);
+        raw[j] = (row_ok && kc0 + j < units_per_row && kk < k) ? L::load4(xr + kk) : L::zero4();
       }
 #pragma unroll
-      for (int j = 0; j < kUnroll; ++j) {
+      for (int j = 0; j < U; ++j) {
         const int kc = kc0 + j;
         if (kc >= units_per_row) break;  // uniform across the warp
         const int kk = kc * 128 + lane * 4;
         const bool elem_ok = row_ok && kk < k;
-        float a = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
+        const float4 vj = L::widen4(raw[j]);
+        float a = fmaxf(fmaxf(fabsf(vj.x), fabsf(vj.y)), fmaxf(fabsf(vj.z), fabsf(vj.w)));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
         const uint32_t code = e8m0_ceil_code(a);
         const float inv = e8m0_inv_scale(code);
-        const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[j].x, inv), __fmul_rn(v[j].y, inv));
-        const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[j].z, inv), __fmul_rn(v[j].w, inv));
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(vj.x, inv), __fmul_rn(vj.y, inv));
+        const uint32_t hi = cvt_e4m3x2(__fmul_rn(vj.z, inv), __fmul_rn(vj.w, inv));
         if (elem_ok) *reinterpret_cast<uint32_t*>(q + row_g * k + kk) = lo | (hi << 16);
         const uint32_t c1 = __shfl_sync(0xffffffffu, code, 8);
         const uint32_t c2 = __shfl_sync(0xffffffffu, code, 16);
@@ -145,7 +171,8 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __r
                                                                   uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                                   int64_t rows_padded, int units_per_row,
                                                                   int64_t total_rows, int64_t mt_n, int64_t kt_n) {
-  constexpr int kU = 4;
+  using L = QuantLoads<TIn>;
+  constexpr int kU = L::kUnitsNv;
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
@@ -156,25 +183,22 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __r
     const int64_t row_g = l * rows + r;
     const TIn* xr = x + row_g * k;
     for (int kc0 = 0; kc0 < units_per_row; kc0 += kU) {
-      float4 v0[kU], v1[kU];
+      typename L::Raw8 raw[kU];
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const int kk = (kc0 + j) * 256 + lane * 8;
         const bool ok = row_ok && kc0 + j < units_per_row && kk < k;
-        if (ok) {
-          load8(xr + kk, v0[j], v1[j]);
-        } else {
-          v0[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          v1[j] = v0[j];
-        }
+        raw[j] = ok ? L::load8(xr + kk) : L::zero8();
       }
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const int kc = kc0 + j;
         if (kc >= units_per_row) break;  // uniform across the warp
         const int kk = kc * 256 + lane * 8;
-        float a = fmaxf(fmaxf(fmaxf(fabsf(v0[j].x), fabsf(v0[j].y)), fmaxf(fabsf(v0[j].z), fabsf(v0[j].w))),
-                        fmaxf(fmaxf(fabsf(v1[j].x), fabsf(v1[j].y)), fmaxf(fabsf(v1[j].z), fabsf(v1[j].w))));
+        float4 a0, a1;  // this lane's eight values
+        L::widen8(raw[j], a0, a1);
+        float a = fmaxf(fmaxf(fmaxf(fabsf(a0.x), fabsf(a0.y)), fmaxf(fabsf(a0.z), fabsf(a0.w))),
+                        fmaxf(fmaxf(fabsf(a1.x), fabsf(a1.y)), fmaxf(fabsf(a1.z), fabsf(a1.w))));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
         const uint32_t code = ue4m3_code_of_amax_over_6(a);
         const float s = ue4m3_value(code);
@@ -187,19 +211,35 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __r
         // threshold path below (about 1e-5 of random values).  The sign bit of x is or-ed in,
         // so a negative value that rounds to zero gives -0 as on the exact path; s = 0 gives +0.
         const float inv = code != 0 ? __frcp_rn(s) : 0.0f;
-        const float y[8] = {v0[j].x * inv, v0[j].y * inv, v0[j].z * inv, v0[j].w * inv,
-                            v1[j].x * inv, v1[j].y * inv, v1[j].z * inv, v1[j].w * inv};
+        float y[8] = {a0.x * inv, a0.y * inv, a0.z * inv, a0.w * inv, a1.x * inv, a1.y * inv, a1.z * inv, a1.w * inv};
+        const float xs[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         bool near = false;
+        if constexpr (sizeof(TIn) == 2) {
+          // bf16 x has 8 significant bits and a value v of at most 3 (every midpoint, every code)
+          // times s at most 7, so x / s is either exactly v or at least 2^-9 (relative) away from
+          // it, while y is within 2^-23 of x / s: a y inside the window is v exactly.  Replacing
+          // it by v lets the RNE conversion decide the exact quotient, ties to even included.
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t b = __float_as_uint(y[e]) & 0x7FFFFFFFu;
-          near |= b >= 0x3E4CCCCDu /* 0.2f */ && ((b + 16u) & 0x1FFFFFu) < 32u;
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t yb = __float_as_uint(y[e]);
+            const uint32_t b = yb & 0x7FFFFFFFu;
+            if (b >= 0x3E4CCCCDu /* 0.2f */ && ((b + 16u) & 0x1FFFFFu) < 32u)
+              y[e] = __uint_as_float(((b + 16u) & ~0x1FFFFFu) | (yb & 0x80000000u));
+          }
+        } else {
+          // When s is a power of two, 1/s and y are exact (y >= 0.2 cannot underflow) and the
+          // RNE conversion already rounds the exact quotient: no guard needed.
+          const bool inv_exact = (__float_as_uint(s) & 0x7FFFFFu) == 0u;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t b = __float_as_uint(y[e]) & 0x7FFFFFFFu;
+            near |= !inv_exact && b >= 0x3E4CCCCDu /* 0.2f */ && ((b + 16u) & 0x1FFFFFu) < 32u;
+          }
         }
         uint32_t nib;
         if (!__any_sync(0xffffffffu, near)) {
           nib = cvt_e2m1x2(y[0], y[1]) | (cvt_e2m1x2(y[2], y[3]) << 8) | (cvt_e2m1x2(y[4], y[5]) << 16) |
                 (cvt_e2m1x2(y[6], y[7]) << 24);
-          const float xs[8] = {v0[j].x, v0[j].y, v0[j].z, v0[j].w, v1[j].x, v1[j].y, v1[j].z, v1[j].w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) nib |= (__float_as_uint(xs[e]) >> 31) << (4 * e + 3);
           if (code == 0) nib = 0;
@@ -208,10 +248,9 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __r
           e2m1_thresholds(s, t);
           nib = 0;
           if (code != 0) {
-            nib = e2m1_nibble(v0[j].x, t) | (e2m1_nibble(v0[j].y, t) << 4) | (e2m1_nibble(v0[j].z, t) << 8) |
-                  (e2m1_nibble(v0[j].w, t) << 12) | (e2m1_nibble(v1[j].x, t) << 16) |
-                  (e2m1_nibble(v1[j].y, t) << 20) | (e2m1_nibble(v1[j].z, t) << 24) |
-                  (e2m1_nibble(v1[j].w, t) << 28);
+            nib = e2m1_nibble(a0.x, t) | (e2m1_nibble(a0.y, t) << 4) | (e2m1_nibble(a0.z, t) << 8) |
+                  (e2m1_nibble(a0.w, t) << 12) | (e2m1_nibble(a1.x, t) << 16) | (e2m1_nibble(a1.y, t) << 20) |
+                  (e2m1_nibble(a1.z, t) << 24) | (e2m1_nibble(a1.w, t) << 28);
           }
         }
         if (row_ok && kk < k) *reinterpret_cast<uint32_t*>(q + (row_g * k + kk) / 2) = nib;

@@ -160,3 +160,34 @@ def test_quantize_rejects_other_input_types(lib):
     from nvfp4_gemm_moe_gb300 import torch_ops
     with pytest.raises(TypeError):
         torch_ops.quantize(torch.zeros((1, 128, 64), dtype=torch.float16, device="cuda"), "mxfp8")
+
+
+def test_quantize_bf16_nvfp4_exact_ties_under_uneven_scales(lib):
+    """NVFP4 from bf16: values exactly on an E2M1 midpoint or code times a block scale that is not
+    a power of two (so x * (1/s) is inexact and lands beside the tie), and their bf16 neighbours
+    one unit away, which must round by value."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    rng = np.random.default_rng(21)
+    scales = np.array([1.125, 1.375, 1.75, 0.625, 2.5, 0.3125, 13.0, 0.0390625])  # UE4M3 values
+    grid = np.array([0.5, 1.0, 1.5, 2.0, 3.0, 4.0])
+    pts = np.concatenate([np.asarray(formats.E2M1_MIDS, dtype=np.float64), grid])
+    rows, k = 256, 512
+    nblk = k // 16
+    s_blk = rng.choice(scales, (rows, nblk))
+    x = rng.choice(pts, (rows, nblk, 16)) * s_blk[..., None]
+    x[..., 0] = 6.0 * s_blk  # the block amax fixes the scale: RNE_UE4M3(amax / 6) = s
+    x *= rng.choice([-1.0, 1.0], x.shape)
+    xb = torch.from_numpy(x.reshape(rows, k).astype(np.float32)).to(torch.bfloat16)
+    assert np.array_equal(xb.double().numpy(), x.reshape(rows, k))  # all exactly representable
+    # a quarter of the non-amax values moved one bf16 unit up or down (no longer ties)
+    bits = xb.view(torch.int16).numpy().copy().reshape(rows, nblk, 16)
+    move = rng.random((rows, nblk, 16)) < 0.25
+    move[..., 0] = False
+    bits = np.where(move, bits + rng.choice(np.array([-1, 1], dtype=np.int16), bits.shape), bits).astype(np.int16)
+    xb = torch.from_numpy(bits.reshape(rows, k)).view(torch.bfloat16)
+    q, sf = torch_ops.quantize(xb.cuda(), "nvfp4")
+    torch.cuda.synchronize()
+    q_ref, sf_ref = oq.quantize(xb.float().numpy()[None], "nvfp4")
+    assert np.array_equal(sf.cpu().numpy(), sf_ref)
+    qg = q.cpu().numpy().reshape(q_ref.shape)
+    assert np.array_equal(qg, q_ref), f"{(qg != q_ref).sum()} code bytes differ"
