@@ -30,6 +30,11 @@
  *   Three calls synchronise `stream` first, as their comments say: a grouped call
  *   with opts->validate_offsets, bsg_grouped_gemm_srelu_discrete (it reads the
  *   experts' pointers on the host) and bsg_read_device_error.
+ * - CUDA graphs: every other compute call enqueues only kernels and memsets on
+ *   `stream`, so it can be captured into a graph and replayed (inputs read, outputs
+ *   written at replay time through the captured pointers).  Make one eager call of
+ *   each kernel configuration first: the first launch of a kernel sets its
+ *   shared-memory limit and, for CTA pairs, queries the resident cluster count.
  * - Sizes are element counts, not bytes, unless the name says bytes.
  * - Errors: invalid arguments are detected on the host before anything is
  *   enqueued and reported as a bsg_status; nothing is thrown across the ABI.
