@@ -12,7 +12,7 @@ from guards import Outputs
 
 import workloads as W
 from oracle import gemm as og, quantize as oq
-from parity import TOL_C, check_amax, check_c, check_c_float, check_codes_plain
+from parity import TOL_C, check_amax, check_c_float, check_codes_plain
 
 pytestmark = pytest.mark.gpu
 

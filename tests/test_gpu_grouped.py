@@ -6,7 +6,7 @@ import torch
 import workloads as W
 from oracle import formats, gemm as og, quantize as oq, sf_layout
 from guards import Outputs
-from parity import check_amax, check_c, check_c_float, check_d_bf16, check_d_float, check_e4m3_blocks, d_tolerance, TOL_C
+from parity import TOL_C, check_amax, check_c_float, check_d_float, check_e4m3_blocks, d_tolerance
 
 pytestmark = pytest.mark.gpu
 

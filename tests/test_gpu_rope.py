@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import workloads as W
-from oracle import formats, quantize as oq, rope as orope, sf_layout
+from oracle import formats, quantize as oq, rope as orope
 from guards import Outputs
 from parity import TOL_C, check_e4m3_blocks
 
