@@ -202,44 +202,39 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __r
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
         const uint32_t code = ue4m3_code_of_amax_over_6(a);
         const float s = ue4m3_value(code);
-        // Fast path: y = x * RN(1/s) rounded once more, converted by the hardware's RNE
-        // E2M1 conversion.  y is within a relative 2^-23 of the exact x / s, so the two round
-        // alike unless a midpoint of E2M1 lies between them or one of them is a midpoint, and
-        // then y is within a few ulps of that midpoint.  Every midpoint (0.25, 0.75, ..., 5) has
-        // a float pattern whose low 21 mantissa bits are zero, so a y with |y| >= 0.2 whose
-        // pattern lies within 16 of a multiple of 2^21 sends the whole unit to the exact
-        // threshold path below (about 1e-5 of random values).  The sign bit of x is or-ed in,
-        // so a negative value that rounds to zero gives -0 as on the exact path; s = 0 gives +0.
+        // Codes from the hardware's RNE conversion, bracketing the exact quotient v = x / s:
+        // y_up = x * RN(RN(1/s) (1 + 2^-20)) and y_dn = x * RN(RN(1/s) (1 - 2^-20)) lie on either
+        // side of v (their rounding errors are below 2^-22 relative), and RNE rounding is
+        // monotonic, so where both convert to the same code so does v.  Where they differ a
+        // midpoint lies between them: fp32 inputs take the exact threshold path (rare); for bf16
+        // inputs v is then exactly that midpoint (x has 8 significant bits, a midpoint times s
+        // at most 7: x / s is a midpoint or at least 2^-9 away from one), and the tie goes to the
+        // even code of the two.  The sign bit of x is or-ed in, so a negative value that rounds
+        // to zero gives -0 as on the exact path; s = 0 gives +0.
         const float inv = code != 0 ? __frcp_rn(s) : 0.0f;
-        float y[8] = {a0.x * inv, a0.y * inv, a0.z * inv, a0.w * inv, a1.x * inv, a1.y * inv, a1.z * inv, a1.w * inv};
+        const float inv_up = inv * (1.0f + 0x1p-20f), inv_dn = inv * (1.0f - 0x1p-20f);
         const float xs[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        uint32_t up = 0, dn = 0;
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          up |= cvt_e2m1x2(xs[e] * inv_up, xs[e + 1] * inv_up) << (4 * e);
+          dn |= cvt_e2m1x2(xs[e] * inv_dn, xs[e + 1] * inv_dn) << (4 * e);
+        }
+        uint32_t nib = up;
         bool near = false;
-        if constexpr (sizeof(TIn) == 2) {
-          // bf16 x has 8 significant bits and a value v of at most 3 (every midpoint, every code)
-          // times s at most 7, so x / s is either exactly v or at least 2^-9 (relative) away from
-          // it, while y is within 2^-23 of x / s: a y inside the window is v exactly.  Replacing
-          // it by v lets the RNE conversion decide the exact quotient, ties to even included.
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t yb = __float_as_uint(y[e]);
-            const uint32_t b = yb & 0x7FFFFFFFu;
-            if (b >= 0x3E4CCCCDu /* 0.2f */ && ((b + 16u) & 0x1FFFFFu) < 32u)
-              y[e] = __uint_as_float(((b + 16u) & ~0x1FFFFFu) | (yb & 0x80000000u));
-          }
-        } else {
-          // When s is a power of two, 1/s and y are exact (y >= 0.2 cannot underflow) and the
-          // RNE conversion already rounds the exact quotient: no guard needed.
-          const bool inv_exact = (__float_as_uint(s) & 0x7FFFFFu) == 0u;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t b = __float_as_uint(y[e]) & 0x7FFFFFFFu;
-            near |= !inv_exact && b >= 0x3E4CCCCDu /* 0.2f */ && ((b + 16u) & 0x1FFFFFu) < 32u;
+        if (up != dn) {
+          if constexpr (sizeof(TIn) == 2) {
+            // nibble k differs -> bit 4k of `differs`; the two codes are neighbours, and the one
+            // whose last bit (bit 4k) is clear is the even one
+            const uint32_t diff = up ^ dn;
+            const uint32_t differs = (diff | (diff >> 1) | (diff >> 2) | (diff >> 3)) & 0x11111111u;
+            const uint32_t take_dn = (differs & up) * 0xFu;  // whole nibbles where dn is even
+            nib = (up & ~take_dn) | (dn & take_dn);
+          } else {
+            near = true;
           }
         }
-        uint32_t nib;
         if (!__any_sync(0xffffffffu, near)) {
-          nib = cvt_e2m1x2(y[0], y[1]) | (cvt_e2m1x2(y[2], y[3]) << 8) | (cvt_e2m1x2(y[4], y[5]) << 16) |
-                (cvt_e2m1x2(y[6], y[7]) << 24);
 #pragma unroll
           for (int e = 0; e < 8; ++e) nib |= (__float_as_uint(xs[e]) >> 31) << (4 * e + 3);
           if (code == 0) nib = 0;
