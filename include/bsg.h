@@ -108,9 +108,12 @@ typedef struct bsg_gemm_opts {
   int tanh_approx;       /* grouped only: 1 = tanh.approx.f32 in the soft clamp, 0 = tanhf */
   int validate_offsets;  /* grouped only: 1 = copy padded_offsets to the host and check them
                             before launching (synchronises the stream) */
-  int cta_pair;          /* 0 = automatic (CTA pairs when tile_n is 0, the epilogue is not E4M3 D
-                            and there are at least #SMs/2 256 x 256 tiles), 1 = one CTA per
-                            128 x tile_n tile, 2 = CTA pairs on 256 x 256 tiles */
+  int cta_pair;          /* 0 = automatic (GEMMs: CTA pairs, widths as for 2, when tile_n is 0,
+                            M >= 256, N > 128 and there are at least #SMs/2 256 x 256 tiles),
+                            1 = one CTA per 128 x tile_n tile,
+                            2 = CTA pairs on 256-row tiles, 256 wide, or 224 wide (MXFP8) with
+                            tile_n == 224 or, when tile_n is 0, an E4M3-D or dSwiGLU epilogue;
+                            the RoPE projections describe their own choices */
   int reserved[3];
 } bsg_gemm_opts;
 
