@@ -28,6 +28,7 @@
 // drains its own in-flight copies and MMAs, frees TMEM and exits.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -1213,14 +1214,16 @@ cudaError_t launch_gemm_t(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, 
                           cudaStream_t stream) {
   using T = GemmTraits<FMT, BN, EPI>;
   auto kern = gemm_kernel<FMT, BN, EPI>;
-  static bool attr_set[64] = {};  // per instantiation and device
+  // per instantiation and device; calls from several host threads may set the (idempotent)
+  // attribute more than once, never read a torn flag
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   kern<<<grid, kThreadsGemm, T::kSmemBytes, stream>>>(tmap_a, tmap_b, p);
   return cudaGetLastError();

@@ -421,12 +421,13 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
                                cudaStream_t stream) {
   using T = PairTraits<FMT, BN, EPI>;
   auto kern = gemm_pair_kernel<FMT, BN, EPI>;
-  static int resident_pairs[64] = {};  // per device; 0 = not queried yet
+  static std::atomic<int> resident_pairs[64];  // per device; 0 = not queried yet
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (resident_pairs[dev] == 0) {
+  int resident = resident_pairs[dev].load(std::memory_order_acquire);
+  if (resident == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -436,9 +437,10 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
     int clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
     if (e != cudaSuccess) return e;
-    resident_pairs[dev] = clusters > 0 ? clusters : 1;
+    resident = clusters > 0 ? clusters : 1;
+    resident_pairs[dev].store(resident, std::memory_order_release);
   }
-  int pairs = max_pairs < resident_pairs[dev] ? max_pairs : resident_pairs[dev];
+  int pairs = max_pairs < resident ? max_pairs : resident;
   if (pairs < 1) pairs = 1;
   kern<<<2 * pairs, kThreadsGemm, T::kSmemBytes, stream>>>(ta, tb, p);
   return cudaGetLastError();
