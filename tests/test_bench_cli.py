@@ -47,3 +47,18 @@ def test_reference_arm_other_ranks_print_nothing():
     out = _run(["--impl", "reference", "--workload", "dense_mxfp8_m256_n256_k256_l1", "--steps", "1",
                 "--warmup", "0", "--ref-rows", "256"], {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert out.strip() == ""
+
+
+def test_every_workload_has_a_config_and_a_bounded_oracle_sample():
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    for name, wl in W.ALL.items():
+        cfg = bench._config(wl)
+        assert cfg["workload"] == name and cfg["flops_per_step"] == wl.flops
+        assert cfg["l2"] and cfg["step"]
+        rows = bench.oracle_rows(wl)
+        limit = wl.tokens if isinstance(wl, W.RopeProj) else (wl.m if isinstance(wl, W.Dense) else wl.valid_m)
+        assert 256 <= rows <= max(256, limit)
+        assert rows % 256 == 0 or rows == limit  # whole 256-row groups, or the whole operand
+        assert bench.oracle_rows(wl, 512) == 512
