@@ -229,3 +229,132 @@ def test_workload_recipes():
     plain = sub[:, kb % 7 != 6]
     assert np.abs(boosted).mean() > 30 * np.abs(plain).mean()
     assert math.isclose(float(np.std(plain)), 1.0, rel_tol=0.05)
+
+
+def _bruteforce_abs_sum(a_codes, b_codes, sfa, sfb, fmt, m, n, k, l):
+    """sum_k |a||sa| |b||sb| by scalar loops over the physical scale bytes (no offset formula, no matmul)."""
+    v = 32 if fmt == "mxfp8" else 16
+    dec = formats.decode_e8m0 if fmt == "mxfp8" else formats.decode_ue4m3
+
+    def scale_of(buf, rows, ll, r, kb):
+        kt_n = -(-(k // v) // 4)
+        mt_n = -(-rows // 128)
+        phys = np.asarray(buf).reshape(l, mt_n, kt_n, 32, 4, 4)
+        return float(dec(phys[ll, r // 128, kb // 4, r % 32, (r % 128) // 32, kb % 4]))
+
+    def value_of(codes, ll, r, kk):
+        if fmt == "mxfp8":
+            return float(formats.decode_e4m3(codes[ll, r, kk]))
+        byte = int(codes[ll, r, kk // 2])
+        return float(formats.decode_e2m1((byte >> 4) if kk % 2 else (byte & 0xF)))
+
+    out = np.zeros((l, m, n))
+    for ll in range(l):
+        for i in range(m):
+            for j in range(n):
+                acc = 0.0
+                for kk in range(k):
+                    x = value_of(a_codes, ll, i, kk) * scale_of(sfa, m, ll, i, kk // v)
+                    y = value_of(b_codes, ll, j, kk) * scale_of(sfb, n, ll, j, kk // v)
+                    acc += abs(x) * abs(y)
+                out[ll, i, j] = acc
+    return out
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_dense_abs_sum_bruteforce_tiny(fmt):
+    """dense_abs_sum (the scale of every C / D tolerance) against scalar loops on a ragged case
+    with mixed signs and a 2^+-8 spread of block magnitudes."""
+    m, n, k, l = 7, 5, 64, 2
+    rng = np.random.default_rng(11)
+    xa = rng.standard_normal((l, m, k)) * np.exp2(rng.integers(-8, 9, (l, m, 1)))
+    xb = rng.standard_normal((l, n, k))
+    a, sfa = quantize.quantize(xa.astype(np.float32), fmt)
+    b, sfb = quantize.quantize(xb.astype(np.float32), fmt)
+    s = gemm.dense_abs_sum(a, b, sfa, sfb, fmt, m, n, k, l)
+    ref = _bruteforce_abs_sum(a, b, sfa, sfb, fmt, m, n, k, l)
+    assert s.shape == (l, m, n)
+    assert np.allclose(s, ref, rtol=1e-13, atol=0)
+    c, _ = gemm.dense_gemm_amax(a, b, sfa, sfb, fmt, m, n, k, l)
+    # the sum of magnitudes bounds |C| and, with mixed signs, is strictly larger somewhere
+    assert np.all(np.abs(c) <= s * (1 + 1e-14)) and np.any(np.abs(c) < 0.9 * s)
+
+
+@pytest.mark.parametrize("fmt,sfa_code,sfb_code,sa,sb", [
+    ("mxfp8", 127 + 4, 127 - 3, 2.0 ** 4, 2.0 ** -3),
+    ("nvfp4", 0x48, 0x28, 4.0, 0.25),  # UE4M3 4.0 and 0.25
+])
+def test_dense_abs_sum_signed_ones_closed_form(fmt, sfa_code, sfb_code, sa, sb):
+    """Codes +-1 with random signs and scales 2^ea, 2^eb: sum_k |Ahat||Bhat| = K 2^(ea+eb) exactly,
+    whatever the signs, while C (the signed sum) is smaller wherever signs disagree."""
+    m, n, k, l = 130, 3, 256, 2
+    rng = np.random.default_rng(12)
+    a, sfa = _ones_operands(fmt, m, k, l, sfa_code)
+    b, sfb = _ones_operands(fmt, n, k, l, sfb_code)
+    if fmt == "mxfp8":
+        a = a | (rng.integers(0, 2, a.shape) << 7).astype(np.uint8)   # sign bit of E4M3
+        b = b | (rng.integers(0, 2, b.shape) << 7).astype(np.uint8)
+    else:
+        # sign bits of both E2M1 nibbles
+        a = a | ((rng.integers(0, 2, a.shape) << 3) | (rng.integers(0, 2, a.shape) << 7)).astype(np.uint8)
+        b = b | ((rng.integers(0, 2, b.shape) << 3) | (rng.integers(0, 2, b.shape) << 7)).astype(np.uint8)
+    s = gemm.dense_abs_sum(a, b, sfa, sfb, fmt, m, n, k, l)
+    assert np.all(s == k * sa * sb)
+    c, _ = gemm.dense_gemm_amax(a, b, sfa, sfb, fmt, m, n, k, l)
+    assert np.all(np.abs(c) < k * sa * sb)
+    # planted mistake: the sum taken without the magnitudes is the signed C, which misses the closed form
+    ahat = quantize.dequantize(a, sfa, fmt, m, k, l)
+    bhat = quantize.dequantize(b, sfb, fmt, n, k, l)
+    no_abs = np.matmul(ahat, np.swapaxes(bhat, -1, -2))
+    assert not np.all(no_abs == k * sa * sb)
+
+
+def _scalar_expert_max(d, padded_offsets):
+    """Per-expert max |D| by a scan of every row (its expert found by a linear search of the ends)."""
+    ends = [int(e) for e in padded_offsets]
+    out = [0.0] * len(ends)
+    for r in range(d.shape[0]):
+        g = next(i for i, e in enumerate(ends) if r < e)
+        for x in d[r]:
+            out[g] = max(out[g], abs(float(x)))
+    return np.array(out)
+
+
+def _amax_case(seed=13):
+    counts = [0, 300, 0, 0, 1, 256, 0]  # empty first, a run of empties, a 1-row expert, empty last
+    pad = (np.asarray(counts) + 255) // 256 * 256
+    offs = np.cumsum(pad).astype(np.int32)
+    vm = int(offs[-1])
+    rng = np.random.default_rng(seed)
+    d = rng.standard_normal((vm, 24)) * np.exp2(rng.integers(-6, 7, (vm, 1)))
+    # in every non-empty expert the largest magnitude is a negative entry
+    begin = 0
+    for end in offs:
+        if end > begin:
+            r = begin + (end - begin) // 3
+            d[r, 5] = -2.0 * np.abs(d[begin:end]).max()
+        begin = end
+    return d, offs
+
+
+def test_per_expert_amax_nonempty_experts():
+    d, offs = _amax_case()
+    got = gemm.per_expert_amax(d, offs)
+    ref = _scalar_expert_max(d, offs)
+    assert np.array_equal(got, ref)
+    assert got[0] == 0 and got[2] == 0 and got[3] == 0 and got[-1] == 0 and np.all(got[[1, 4, 5]] > 0)
+    # equal to the global max |D| over all rows, and to D's own maximum of the expert's rows
+    assert got.max() == np.abs(d).max()
+
+
+def test_per_expert_amax_catches_unadvanced_range():
+    """Planted mistake: a scan whose range start is never advanced (every expert from row 0)
+    disagrees with the scalar reference, so the pin above would catch it."""
+    d, offs = _amax_case(seed=14)
+    ref = _scalar_expert_max(d, offs)
+    wrong = np.zeros(len(offs))
+    for g, end in enumerate(offs):
+        if end > 0:
+            wrong[g] = np.abs(d[0:end]).max()
+    assert not np.array_equal(wrong, ref)
+    assert np.array_equal(gemm.per_expert_amax(d, offs), ref)
