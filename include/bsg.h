@@ -376,11 +376,15 @@ bsg_status bsg_grouped_gemm_srelu_discrete(const void* a, const int64_t* b_ptrs,
  * array of BSG_NOALLOC_SCRATCH_BYTES bytes owned by the library (every GPU that loads the
  * library holds it until the process exits).
  * - The first call on a device looks up that array's address on the current device; make
- *   that first call before any stream capture.
+ *   that first call before any stream capture.  The address is kept with the context it was
+ *   taken in: after a device reset (a new context) the next call looks it up again, so the
+ *   first call after a reset must also come before any stream capture.
  * - All calls on a device share the one array: calls that may overlap on the GPU (other
  *   streams, other threads) race on it.  Each call clears it before its kernel runs.
  * - Returns BSG_ERR_WORKSPACE if the GEMM's scratch (bsg_workspace_size()) is larger than
- *   BSG_NOALLOC_SCRATCH_BYTES.  Device-side errors of these calls are not reported.
+ *   BSG_NOALLOC_SCRATCH_BYTES (the library also checks this when it is compiled).
+ * - Device-side errors of the last call on the current device are read with
+ *   bsg_gemm_amax_noalloc_read_error.
  */
 #define BSG_NOALLOC_SCRATCH_BYTES 256
 bsg_status bsg_gemm_amax_noalloc(const void* a, const void* b, const uint8_t* sfa, const uint8_t* sfb,
@@ -388,6 +392,11 @@ bsg_status bsg_gemm_amax_noalloc(const void* a, const void* b, const uint8_t* sf
                                  int64_t m, int64_t n, int64_t k, int64_t l,
                                  void* c, bsg_dtype c_dtype, float* amax,
                                  const bsg_gemm_opts* opts, void* stream);
+
+/* Synchronises `stream` and returns in *error_bits the device error bits of the last
+ * bsg_gemm_amax_noalloc call on the current device (the error word of the library's static
+ * array); BSG_ERR_DEVICE if any bit is set, BSG_ERR_CUDA if the array cannot be found. */
+bsg_status bsg_gemm_amax_noalloc_read_error(void* stream, uint32_t* error_bits);
 
 /*
  * bsg_selftest_wait_timeout -- failure-detection self-test of the device-side bounded waits.

@@ -84,6 +84,8 @@ def _load():
                                           ctypes.POINTER(bsg_gemm_opts), P]
     lib.bsg_read_device_error.restype = I
     lib.bsg_read_device_error.argtypes = [P, P, U32P]
+    lib.bsg_gemm_amax_noalloc_read_error.restype = I
+    lib.bsg_gemm_amax_noalloc_read_error.argtypes = [P, U32P]
     return lib
 
 
@@ -242,6 +244,15 @@ def bsg_read_device_error(workspace, stream=None) -> int:
     st = _lib.bsg_read_device_error(_ptr(workspace), _stream(stream), ctypes.byref(bits))
     if st not in (OK, 6):
         raise BsgError(st, "bsg_read_device_error")
+    return int(bits.value)
+
+
+def bsg_gemm_amax_noalloc_read_error(stream=None) -> int:
+    """Error bits of the last bsg_gemm_amax_noalloc call on the current device (synchronises)."""
+    bits = ctypes.c_uint32(0)
+    st = _lib.bsg_gemm_amax_noalloc_read_error(_stream(stream), ctypes.byref(bits))
+    if st not in (OK, 6):
+        raise BsgError(st, "bsg_gemm_amax_noalloc_read_error")
     return int(bits.value)
 
 

@@ -16,8 +16,7 @@ namespace {
 
 using bsg::GemmConfig;
 using bsg::GemmParams;
-
-constexpr size_t kWorkspaceBytes = 256;
+using bsg::kWorkspaceBytes;
 
 // One NVTX range per C ABI call, named after the entry point (shown by Nsight tools; without a
 // tool attached the calls return at once).

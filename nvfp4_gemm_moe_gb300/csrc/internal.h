@@ -7,6 +7,10 @@
 
 namespace bsg {
 
+// Bytes of the per-call scratch every GEMM entry point needs (the device error word and the
+// words next to it); bsg_workspace_size() returns it.
+constexpr size_t kWorkspaceBytes = 256;
+
 enum Fmt : int { kMXFP8 = 0, kNVFP4 = 1, kBF16 = 2 };  // kBF16: plain bf16 operands, no scale factors
 // Element types of the C / D outputs.  E4M3 and E2M1 here are plain conversions (round to
 // nearest even, saturating), without block scales; E2M1 packs two values per byte, element 2j

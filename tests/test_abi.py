@@ -266,6 +266,14 @@ def test_noalloc_validation():
                               256, 1, a["c"], bsg.BF16, a["amax"], _opts(), None)
     assert call(a=None) in (INVALID, CUDA)
     assert call(n=4) in (ALIGN, CUDA)
+    # the GEMM's scratch fits the library's static array (also a compile-time check in the library)
+    assert bsg.bsg_workspace_size() <= 256
+    assert "#define BSG_NOALLOC_SCRATCH_BYTES 256" in open(bsg.HEADER).read()
+    assert bsg.raw_status("bsg_gemm_amax_noalloc_read_error", None, None) == INVALID
+    if _no_device():
+        import ctypes as ct
+        bits = ct.c_uint32(7)
+        assert bsg.raw_status("bsg_gemm_amax_noalloc_read_error", None, ct.byref(bits)) == CUDA
 
 
 def test_binding_raises_on_bad_status():
