@@ -322,7 +322,158 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "gemm_ms": round(gemm_mean_ms, 4),
     }
+    if args.per_config and world == 1 and args.workload == W.DENSE_MXFP8_8192.name:
+        line["per_config"] = per_config_records(dev, peaks, peak_src)
     return line
+
+
+# --------------------------------------------------------------------------- per-config GEMM records
+
+# The other workloads the metric is quoted per config on, measured in the default run beside the
+# headline: (label, workload, C present).  The E4M3-D workload is also timed with C = NULL (C is
+# an optional output of the grouped operation).
+PER_CONFIG = (
+    ("1", W.DENSE_MXFP8_256.name, True),
+    ("3", W.DENSE_NVFP4_16384.name, True),
+    ("4", W.GROUPED_SRELU_E32.name, True),
+    ("4'", W.GROUPED_SRELU_E32_CLAMP.name, True),
+    ("5", W.GROUPED_FP8D_E128.name, True),
+    ("5 (C = NULL)", W.GROUPED_FP8D_E128.name, False),
+)
+PER_CONFIG_REGION_S = 0.25  # each config's timed region lasts at least this long (clock samples)
+
+
+def _dense_bytes(wl):
+    """Algorithmic HBM bytes of one dense GEMM launch: codes and scales of A and B once, C once."""
+    per_elem = 1.0 if wl.fmt == "mxfp8" else 0.5
+    ab = wl.l * (wl.m + wl.n) * wl.k * (per_elem + 1.0 / wl.sf_vec)
+    c = wl.l * wl.m * wl.n * (4 if wl.c_dtype == "f32" else 2)
+    return ab + c + 4
+
+
+def per_config_records(dev, peaks, peak_src, entries=PER_CONFIG):
+    """GEMM launch time (CUDA events around back-to-back launches on the current stream, inputs
+    quantised once beforehand), TFLOP/s, fraction of the FP8 / FP4 peak, traffic and clocks for
+    every per-config workload."""
+    import torch
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    stream = torch.cuda.current_stream()
+    recs = []
+    cache = {}
+    for label, name, with_c in entries:
+        wl = W.ALL[name]
+        # the clamp variant and the C = NULL run reuse the operands of the workload before them
+        key = name if isinstance(wl, W.Dense) else (wl.experts, wl.k, wl.n, wl.routed_rows, wl.skew, wl.seed, wl.fmt)
+        if key not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            if isinstance(wl, W.Dense):
+                a, b = wl.a_rows(), wl.b_rows()
+            else:
+                a, b = wl.a_rows()[None], wl.b_rows()
+            a_d = torch.from_numpy(a).to(dev)
+            del a
+            qa, sfa = torch_ops.quantize(a_d, wl.fmt)
+            del a_d
+            b_d = torch.from_numpy(b).to(dev)
+            del b
+            qb, sfb = torch_ops.quantize(b_d, wl.fmt)
+            del b_d
+            cache[key] = (qa, sfa, qb, sfb)
+        qa, sfa, qb, sfb = cache[key]
+        ws = torch_ops.new_workspace(dev)
+        if isinstance(wl, W.Dense):
+            c = torch.empty((wl.l, wl.m, wl.n), dtype=torch.float32 if wl.c_dtype == "f32" else torch.bfloat16,
+                            device=dev)
+            amax = torch.empty(1, dtype=torch.float32, device=dev)
+
+            def call():
+                torch_ops.gemm_amax(qa, qb, sfa, sfb, wl.fmt, wl.m, wl.n, wl.k, wl.l, c=c, amax=amax, workspace=ws)
+        else:
+            offs = torch.from_numpy(wl.padded_offsets()).to(dev)
+            alpha = torch.from_numpy(wl.alpha()).to(dev)
+            prob = torch.from_numpy(wl.prob()).to(dev)
+            nc = torch.ones(1, dtype=torch.float32, device=dev)
+            outs = torch_ops.grouped_gemm_srelu(qa[0], qb, sfa, sfb, wl.fmt, offs, alpha, prob, wl.n, wl.k,
+                                                tanh_clamp_scale=wl.tanh_clamp, d_dtype=wl.d_dtype, norm_const=nc,
+                                                c_dtype=torch.bfloat16 if with_c else None, workspace=ws)
+
+            def call():
+                torch_ops.grouped_gemm_srelu(qa[0], qb, sfa, sfb, wl.fmt, offs, alpha, prob, wl.n, wl.k,
+                                             tanh_clamp_scale=wl.tanh_clamp, d_dtype=wl.d_dtype, norm_const=nc,
+                                             outputs=outs, workspace=ws)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        est = max((time.perf_counter() - t) / 3, 1e-6)
+        calls = int(max(20, min(20000, PER_CONFIG_REGION_S / est)))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks = ClockSampler(dev.index or 0)
+        clocks.start()
+        e0.record(stream)
+        for _ in range(calls):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        import nvfp4_gemm_moe_gb300 as bsg
+        if bsg.bsg_read_device_error(ws):
+            raise RuntimeError(f"device error in the per-config run of {name}")
+        ms = e0.elapsed_time(e1) / calls
+        peak = peaks["bf16_tflops"] * NOMINAL_RATIO[wl.fmt]
+        tf = wl.flops / (ms * 1e-3) / 1e12
+        rec = {"config": label, "workload": name, "format": wl.fmt, "calls": calls, "gemm_ms": round(ms, 5),
+               "tflops": round(tf, 1), "peak": round(peak, 1), "frac": round(tf / peak, 4),
+               "peak_source": f"{peak_src} bf16 burst x {NOMINAL_RATIO[wl.fmt]:g}",
+               "traffic": _traffic(name) if with_c else None, "clocks": clk}
+        if isinstance(wl, W.Dense):
+            gb = _dense_bytes(wl)
+            rec.update(flops=wl.flops, algorithmic_bytes=int(gb), gbs=round(gb / (ms * 1e-3) / 1e9, 1),
+                       l2="inputs and outputs stay in L2 between calls" if gb < 64e6 else
+                       "no flush: C written per call exceeds L2")
+        else:
+            useful = 2.0 * wl.routed_rows * wl.n * wl.k
+            rec.update(flops=wl.flops, valid_m=wl.valid_m, routed_rows=wl.routed_rows,
+                       useful_tflops=round(useful / (ms * 1e-3) / 1e12, 1),
+                       useful_note="2 * routed_rows * N * K (padding rows excluded)",
+                       c=("bf16" if with_c else None), d_dtype=wl.d_dtype, tanh_clamp=wl.tanh_clamp,
+                       l2="no flush: operands and outputs exceed L2")
+        if label == "1":
+            rec.update(_latency_graph(call, stream))
+        recs.append(rec)
+    cache.clear()
+    torch.cuda.empty_cache()
+    return recs
+
+
+def _latency_graph(call, stream, per_graph=100, replays=20):
+    """Per-call device time of a launch-bound call: `per_graph` calls captured into one CUDA graph,
+    replayed `replays` times between CUDA events (no host work between the calls)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        call()  # an eager call on the capture stream first (per-device set-up happens outside capture)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(per_graph):
+                call()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(replays):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (per_graph * replays)
+    return {"us_per_call_graph": round(us, 2), "graph_calls": per_graph * replays}
 
 
 def max_over_ranks(times_ms, world, device="cpu"):
@@ -491,6 +642,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=0,
                     help="rows of A in the oracle's timed sample (0: sized to about 6e11 float64 flops)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the GEMM records of the other configs (measured by default at N = 1)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -39,3 +39,25 @@ def test_bench_line(lib, workload, launches_per_step):
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+
+
+def test_per_config_records(lib):
+    """The per-config GEMM records of the default run, on the small dense workload and a small
+    grouped one: each frac reproduces from its GEMM time, the graph latency of config 1 is there."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    peaks, src = bench.load_peaks()
+    recs = bench.per_config_records(torch.device("cuda", 0), peaks, src,
+                                    entries=(("1", W.DENSE_MXFP8_256.name, True),
+                                             ("5 small", W.GROUPED_FP8D_E32.name, True),
+                                             ("5 small (C = NULL)", W.GROUPED_FP8D_E32.name, False)))
+    assert [r["config"] for r in recs] == ["1", "5 small", "5 small (C = NULL)"]
+    for r in recs:
+        assert r["gemm_ms"] > 0 and r["calls"] >= 20
+        assert abs(r["tflops"] - r["flops"] / (r["gemm_ms"] * 1e-3) / 1e12) <= 0.1 + 1e-3 * r["tflops"]
+        assert abs(r["frac"] - r["tflops"] / r["peak"]) < 1e-3
+        assert "clocks" in r
+    assert recs[0]["gbs"] > 0 and recs[0]["us_per_call_graph"] > 0
+    assert recs[1]["useful_tflops"] < recs[1]["tflops"] and recs[2]["c"] is None
