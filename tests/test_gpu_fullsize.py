@@ -1,13 +1,13 @@
 """GPU parity at the full sizes of the named workloads, launched as bench.py launches them.
 
-The outputs are too large for the oracle to recompute whole, so the checks are
-* sampled outputs the oracle computes one by one: blocks of rows x columns spread over the
-  batches or experts (first, last, ragged and empty ranges included), each checked with the
-  same tolerance rules as the small parity tests;
-* the sampled rows' operand codes and scale bytes, bit-exact against the oracle's quantiser;
-* properties that hold at any size: the global amax equals max |C| of the whole GPU output up
-  to C's own rounding, each expert's amax equals max |D| over that expert's rows, and empty
-  experts give zero.
+* The dense workloads (L = 4 MXFP8 8192^3, NVFP4 16384 x 16384 x 8192) and the grouped ones
+  (32 experts with bf16 D, without and with the tanh clamp; 128 Zipf-routed experts with E4M3 D
+  and its row and column scales) are compared with the oracle element by element: every
+  operand code and scale byte, every element of C and D (D_col, SFD_row, SFD_col), the global
+  amax and each expert's amax.  The oracle runs on row bands and experts in turn (host memory
+  stays bounded) with its quantiser split over host threads (``fullsize``).
+* The RoPE projection and the dSwiGLU backward are checked on sampled blocks the oracle
+  computes one by one, with the same tolerance rules as the small parity tests.
 Inputs are the workloads' seeded recipes; nothing here depends on the CUDA path's values.
 """
 import numpy as np
@@ -16,7 +16,8 @@ import torch
 
 import workloads as W
 from oracle import formats, gemm as og, quantize as oq, sf_layout
-from parity import TOL_C, check_c, check_d_bf16, check_e4m3_blocks, d_tolerance
+import fullsize
+from parity import TOL_C, check_amax, check_c, check_d_bf16, check_e4m3_blocks, d_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -42,8 +43,14 @@ def _check_operand_rows(q_gpu, sf_gpu, flat_rows, rows_per_batch, x_rows, fmt, k
     return deq
 
 
+DENSE_BAND = 2048  # rows of A per oracle band (bounds the host memory of the float64 products)
+
+
 @pytest.mark.parametrize("wl", [W.DENSE_MXFP8_8192, W.DENSE_NVFP4_16384], ids=lambda w: w.name)
-def test_dense_full_size_sampled(lib, wl):
+def test_dense_full_size_elementwise(lib, wl):
+    """Every element of C of the large dense workloads against the oracle ("GEMM + Amax (SM100)",
+    Equations), in bands of rows per batch; every operand code and scale byte bit-exact; the
+    global amax against the oracle's max |C|."""
     from nvfp4_gemm_moe_gb300 import torch_ops
     import nvfp4_gemm_moe_gb300 as bsg
     fmt, m, n, k, l = wl.fmt, wl.m, wl.n, wl.k, wl.l
@@ -57,27 +64,28 @@ def test_dense_full_size_sampled(lib, wl):
     c, amax = torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, m, n, k, l, c_dtype=c_dtype, workspace=ws)
     torch.cuda.synchronize()
     assert bsg.bsg_read_device_error(ws) == 0
+    sfa_h, sfb_h = sfa.cpu().numpy(), sfb.cpu().numpy()
+    qa2, qb2 = qa.reshape(l * m, -1), qb.reshape(l * n, -1)
 
-    rng = np.random.default_rng(11)
-    sampled_max = 0.0
-    for batch in sorted({0, l - 1}):
-        ms = np.unique(np.concatenate([[0, 127, 128, m - 1], rng.choice(m, 8, replace=False)]))
-        ns = np.unique(np.concatenate([[0, 255, 256, n - 1], rng.choice(n, 8, replace=False)]))
-        ra, rb = batch * m + ms, batch * n + ns
-        ahat = _check_operand_rows(qa, sfa, ra, m, wl.a_rows(ra), fmt, k)
-        bhat = _check_operand_rows(qb, sfb, rb, n, wl.b_rows(rb), fmt, k)
-        ref = ahat @ bhat.T
-        s = np.abs(ahat) @ np.abs(bhat).T
-        got = c[batch][torch.as_tensor(ms).cuda()][:, torch.as_tensor(ns).cuda()].float().cpu().numpy()
-        check_c(got, ref, s, wl.c_dtype, what=f"C[batch {batch}]")
-        sampled_max = max(sampled_max, float(np.abs(ref).max()))
-
-    # amax is of the fp32 accumulator; the stored C is that value rounded
-    a_gpu = float(amax.cpu()[0])
-    c_max = float(c.abs().max().float().cpu())
-    ulp = float(formats.bf16_ulp(np.array([a_gpu]))[0]) if wl.c_dtype == "bf16" else 2.0 ** -23 * a_gpu
-    assert abs(a_gpu - c_max) <= ulp, (a_gpu, c_max)
-    assert a_gpu >= sampled_max * (1 - 1e-5)
+    ref_max, checked = 0.0, 0
+    for batch in range(l):
+        bhat = fullsize.checked_operand(wl.b_rows, batch * n, (batch + 1) * n,
+                                        qb2[batch * n:(batch + 1) * n].cpu().numpy(), sfb_h, n, fmt, k, "B")
+        babs_t = np.abs(bhat).T
+        bhat_t = bhat.T
+        for r0 in range(0, m, DENSE_BAND):
+            r1 = min(r0 + DENSE_BAND, m)
+            ahat = fullsize.checked_operand(wl.a_rows, batch * m + r0, batch * m + r1,
+                                            qa2[batch * m + r0:batch * m + r1].cpu().numpy(), sfa_h, m, fmt, k, "A")
+            ref = ahat @ bhat_t
+            s = np.abs(ahat) @ babs_t
+            got = c[batch, r0:r1].float().cpu().numpy()
+            fullsize.run_checks(lambda i, j: check_c(got[i:j], ref[i:j], s[i:j], wl.c_dtype,
+                                                     what=f"C[batch {batch}, rows {r0 + i}..{r0 + j - 1}]"), r1 - r0)
+            ref_max = max(ref_max, float(np.abs(ref).max()))
+            checked += ref.size
+    assert checked == l * m * n
+    check_amax(np.array([float(amax.cpu()[0])]), np.array([ref_max]), what="global amax")
 
 
 def _grouped_inputs(wl):
@@ -92,77 +100,124 @@ def _grouped_inputs(wl):
     return offs, qa, sfa, qb, sfb
 
 
-def _sample_blocks(wl, offs, rng):
-    """32-row x 32-column blocks: in the largest, a small and the last non-empty expert, in a
-    padding range and at the first and last columns."""
-    ends = np.asarray(offs, dtype=np.int64)
-    begins = np.concatenate([[0], ends[:-1]])
-    sizes = ends - begins
-    nonempty = np.flatnonzero(sizes > 0)
-    counts = wl.counts()
-    picks = {int(nonempty[np.argmax(sizes[nonempty])]), int(nonempty[np.argmin(sizes[nonempty])]), int(nonempty[-1])}
-    blocks = []
-    for g in sorted(picks):
-        r_first = int(begins[g])
-        r_pad = int(begins[g] + counts[g]) // 32 * 32  # the block holding the last routed rows / padding
-        for r0 in sorted({r_first, min(r_pad, int(ends[g]) - 32)}):
-            for c0 in sorted({0, wl.n - 32, int(rng.integers(0, wl.n // 32)) * 32}):
-                blocks.append((g, r0, c0))
-    return blocks
+def _bf16_beyond_ulp(d_gpu, d_ref):
+    """Elements whose bf16 D is more than one bf16 ulp from the oracle (inside the tolerance only
+    through the carried C term)."""
+    return int(np.count_nonzero(np.abs(d_gpu - d_ref) > formats.bf16_ulp(d_ref)))
 
 
-@pytest.mark.parametrize("wl", [W.GROUPED_SRELU_E32, W.GROUPED_SRELU_E32_CLAMP, W.GROUPED_FP8D_E128],
-                         ids=lambda w: w.name)
-def test_grouped_full_size_sampled(lib, wl):
+def test_grouped_bf16_full_size_elementwise(lib):
+    """The 32-expert sReLU workload, without and with the tanh clamp (s = 32): every element of C
+    and D of every expert against the oracle ("Grouped GEMM + sReLU (SM100)", Equations and Tanh
+    soft clamp), every operand code and scale byte, and each expert's amax."""
     from nvfp4_gemm_moe_gb300 import torch_ops
     import nvfp4_gemm_moe_gb300 as bsg
+    wl, wl_c = W.GROUPED_SRELU_E32, W.GROUPED_SRELU_E32_CLAMP
+    n, k, fmt = wl.n, wl.k, wl.fmt
+    offs, qa, sfa, qb, sfb = _grouped_inputs(wl)
+    vm = int(offs[-1])
+    alpha, prob = wl.alpha(), wl.prob()
+    ws = torch_ops.new_workspace()
+    args = (qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
+            torch.from_numpy(prob).cuda(), n, k)
+    outs = [torch_ops.grouped_gemm_srelu(*args, tanh_clamp_scale=w.tanh_clamp, d_dtype="bf16", workspace=ws)
+            for w in (wl, wl_c)]
+    torch.cuda.synchronize()
+    assert bsg.bsg_read_device_error(ws) == 0
+    sfa_h, sfb_h = sfa.cpu().numpy(), sfb.cpu().numpy()
+    qa2, qb2 = qa[0], qb.reshape(wl.experts * n, -1)
+    amax_ref = np.zeros((2, wl.experts))
+    beyond = [0, 0]
+    begin = 0
+    for g, end in enumerate(offs):
+        end = int(end)
+        if end == begin:
+            continue
+        bhat = fullsize.checked_operand(wl.b_rows, g * n, (g + 1) * n, qb2[g * n:(g + 1) * n].cpu().numpy(), sfb_h,
+                                        n, fmt, k, f"B[e{g}]")
+        ahat = fullsize.checked_operand(wl.a_rows, begin, end, qa2[begin:end].cpu().numpy(), sfa_h, vm, fmt, k,
+                                        f"A[e{g}]")
+        c_ref = float(alpha[g]) * (ahat @ bhat.T)
+        s = float(alpha[g]) * (np.abs(ahat) @ np.abs(bhat).T)
+        p = prob[begin:end]
+        for i, (w, out) in enumerate(zip((wl, wl_c), outs)):
+            d_ref = og.srelu(c_ref, p, w.tanh_clamp)
+            c_got = out["c"][begin:end].float().cpu().numpy()
+            d_got = out["d"][begin:end].float().cpu().numpy()
+
+            def check(a, b, c_got=c_got, d_got=d_got, d_ref=d_ref):
+                check_c(c_got[a:b], c_ref[a:b], s[a:b], "bf16", what=f"C[e{g}, rows {begin + a}..]")
+                check_d_bf16(d_got[a:b], d_ref[a:b], c_ref[a:b], p[a:b], TOL_C * s[a:b],
+                             what=f"D[{w.name}, e{g}, rows {begin + a}..]")
+                return _bf16_beyond_ulp(d_got[a:b], d_ref[a:b])
+            beyond[i] += sum(fullsize.run_checks(check, end - begin))
+            amax_ref[i, g] = np.abs(d_ref).max()
+        begin = end
+    for i, out in enumerate(outs):
+        got = out["amax"].cpu().numpy().astype(np.float64)
+        empty = amax_ref[i] == 0
+        assert np.all(got[empty] == 0)
+        check_amax(got[~empty], amax_ref[i][~empty], what="per-expert amax")
+    print(f"bf16 D elements beyond one ulp of the oracle (inside the carried C bound): "
+          f"{beyond[0]} (no clamp), {beyond[1]} (tanh clamp) of {vm * n} each")
+
+
+def test_grouped_fp8d_full_size_elementwise(lib):
+    """The 128-expert Zipf-routed workload with E4M3 D: every element of C, D and D_col and every
+    SFD_row / SFD_col byte of every expert against the oracle ("Grouped GEMM + sReLU (SM100)",
+    Equations and Shapes), every operand code and scale byte; the run with C = NULL gives the
+    same D, D_col and scale bytes."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    wl = W.GROUPED_FP8D_E128
     n, k, fmt = wl.n, wl.k, wl.fmt
     offs, qa, sfa, qb, sfb = _grouped_inputs(wl)
     vm = int(offs[-1])
     alpha, prob = wl.alpha(), wl.prob()
     nc = 1.0
     ws = torch_ops.new_workspace()
-    out = torch_ops.grouped_gemm_srelu(
-        qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
-        torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=wl.tanh_clamp, d_dtype=wl.d_dtype,
-        norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws)
+    args = (qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
+            torch.from_numpy(prob).cuda(), n, k)
+    ncd = torch.tensor([nc], dtype=torch.float32, device="cuda")
+    out = torch_ops.grouped_gemm_srelu(*args, d_dtype="e4m3", norm_const=ncd, workspace=ws)
+    out0 = torch_ops.grouped_gemm_srelu(*args, d_dtype="e4m3", norm_const=ncd, c_dtype=None, workspace=ws)
     torch.cuda.synchronize()
     assert bsg.bsg_read_device_error(ws) == 0
-
-    rng = np.random.default_rng(5)
-    for g, r0, c0 in _sample_blocks(wl, offs, rng):
-        rows = np.arange(r0, r0 + 32)
-        cols = np.arange(c0, c0 + 32)
-        ahat = _check_operand_rows(qa, sfa, rows, vm, wl.a_rows(rows), fmt, k)
-        bhat = _check_operand_rows(qb, sfb, g * n + cols, n, wl.b_rows(g * n + cols), fmt, k)
+    for key in ("d", "d_col", "sfd_row", "sfd_col"):
+        assert torch.equal(out[key], out0[key]), key
+    del out0
+    sfa_h, sfb_h = sfa.cpu().numpy(), sfb.cpu().numpy()
+    qa2, qb2 = qa[0], qb.reshape(wl.experts * n, -1)
+    sfd_row_h = out["sfd_row"].cpu().numpy()
+    sf_col = sf_layout.unpack(out["sfd_col"].cpu().numpy(), n, vm // 32)[0]  # (N, valid_m / 32)
+    begin = 0
+    for g, end in enumerate(offs):
+        end = int(end)
+        if end == begin:
+            continue
+        bhat = fullsize.checked_operand(wl.b_rows, g * n, (g + 1) * n, qb2[g * n:(g + 1) * n].cpu().numpy(), sfb_h,
+                                        n, fmt, k, f"B[e{g}]")
+        ahat = fullsize.checked_operand(wl.a_rows, begin, end, qa2[begin:end].cpu().numpy(), sfa_h, vm, fmt, k,
+                                        f"A[e{g}]")
         c_ref = float(alpha[g]) * (ahat @ bhat.T)
         s = float(alpha[g]) * (np.abs(ahat) @ np.abs(bhat).T)
-        c_tol = TOL_C * s
-        d_ref = og.srelu(c_ref, prob[rows], wl.tanh_clamp)
-        rt, ct = torch.as_tensor(rows).cuda(), torch.as_tensor(cols).cuda()
-        check_c(out["c"][rt][:, ct].float().cpu().numpy(), c_ref, s, "bf16", what=f"C[e{g}, {r0}, {c0}]")
-        if wl.d_dtype == "bf16":
-            check_d_bf16(out["d"][rt][:, ct].float().cpu().numpy(), d_ref, c_ref, prob[rows], c_tol,
-                         what=f"D[e{g}, {r0}, {c0}]")
-        else:
-            d_tol = d_tolerance(c_ref, prob[rows], c_tol) + 2.0 ** -20 * d_ref
-            sf_row = sf_layout.unpack_rows(out["sfd_row"].cpu().numpy(), rows, n // 32, vm)[:, c0 // 32:c0 // 32 + 1]
-            sf_col = sf_layout.unpack_rows(out["sfd_col"].cpu().numpy(), cols, vm // 32, n)[:, r0 // 32:r0 // 32 + 1]
-            check_e4m3_blocks(out["d"][rt][:, ct].cpu().numpy(), sf_row, d_ref, d_tol, nc, axis=1, what="D_row")
-            check_e4m3_blocks(out["d_col"][rt][:, ct].cpu().numpy(), sf_col, d_ref, d_tol, nc, axis=0, what="D_col")
+        p = prob[begin:end]
+        d_ref = og.srelu(c_ref, p)
+        d_tol = d_tolerance(c_ref, p, TOL_C * s) + 2.0 ** -20 * d_ref
+        c_got = out["c"][begin:end].float().cpu().numpy()
+        d_got = out["d"][begin:end].cpu().numpy()
+        dc_got = out["d_col"][begin:end].cpu().numpy()
+        sf_row = sf_layout.unpack_rows(sfd_row_h, np.arange(begin, end), n // 32, vm)
 
-    if wl.d_dtype == "bf16":
-        # each expert's amax is max |D| of its rows (fp32, before D's own rounding); empty ones are 0
-        amax = out["amax"].cpu().numpy()
-        begin = 0
-        for g, end in enumerate(offs):
-            end = int(end)
-            if end == begin:
-                assert amax[g] == 0.0
-            else:
-                d_max = float(out["d"][begin:end].float().abs().max().cpu())
-                assert abs(amax[g] - d_max) <= float(formats.bf16_ulp(np.array([amax[g]]))[0]), (g, amax[g], d_max)
-            begin = end
+        def check(a, b):
+            # a, b: 32-row aligned (the chunks are 256 rows), so column blocks lie inside a chunk
+            check_c(c_got[a:b], c_ref[a:b], s[a:b], "bf16", what=f"C[e{g}, rows {begin + a}..]")
+            check_e4m3_blocks(d_got[a:b], sf_row[a:b], d_ref[a:b], d_tol[a:b], nc, axis=1,
+                              what=f"D_row[e{g}, rows {begin + a}..]")
+            check_e4m3_blocks(dc_got[a:b], sf_col[:, (begin + a) // 32:(begin + b) // 32], d_ref[a:b], d_tol[a:b],
+                              nc, axis=0, what=f"D_col[e{g}, rows {begin + a}..]")
+        fullsize.run_checks(check, end - begin)
+        begin = end
 
 
 def test_rope_full_size_sampled(lib):
