@@ -118,8 +118,12 @@ typedef struct bsg_gemm_opts {
 } bsg_gemm_opts;
 
 /* Bytes of scratch the GEMM entry points need in `workspace` (device memory,
- * 256-byte aligned).  The call overwrites it; do not share one workspace between
- * calls that may run concurrently. */
+ * 256-byte aligned).  The calls keep their device error record and the dense amax
+ * reduction there, each tagged with a number unique to the call, so a call never clears
+ * it first (no memset before the kernel).  Zero-fill a new workspace once before reading
+ * errors from it with bsg_read_device_error; do not share one workspace between calls
+ * that may run concurrently.  A CUDA graph replays the tag it captured: the error bits of
+ * a replayed call accumulate over its replays until another call uses the workspace. */
 size_t bsg_workspace_size(void);
 
 /* Bytes of the SF buffer for a (batch, rows, K) operand with block size v. */
@@ -174,7 +178,8 @@ bsg_status bsg_quantize_mx_bf16(const void* x, int64_t batch, int64_t rows, int6
  *           plain RNE_satfinite conversion of the fp32 C without block scales, E2M1 packed two
  *           per byte with element 2j in the low nibble.
  * amax      device output, one float: the max of |C| taken on the fp32 accumulator
- *           before rounding to c_dtype.  Zeroed by the call on `stream` first.
+ *           before rounding to c_dtype.  Written by the kernel itself (the last CTA to finish
+ *           writes the maximum of all CTAs), so the call launches one kernel and nothing else.
  * workspace device scratch of bsg_workspace_size() bytes (see bsg_read_device_error).
  * Requirements: m, n, k, l >= 1; k*bytes_per_element % 16 == 0 (k % 16 for E4M3,
  * k % 32 for E2M1); k % sf_vec_size == 0; the bytes of a row of C a multiple of 16
@@ -380,7 +385,8 @@ bsg_status bsg_grouped_gemm_srelu_discrete(const void* a, const int64_t* b_ptrs,
  *   taken in: after a device reset (a new context) the next call looks it up again, so the
  *   first call after a reset must also come before any stream capture.
  * - All calls on a device share the one array: calls that may overlap on the GPU (other
- *   streams, other threads) race on it.  Each call clears it before its kernel runs.
+ *   streams, other threads) race on it.  Each call tags what it writes there, so what a
+ *   previous call left behind never leaks into the next one.
  * - Returns BSG_ERR_WORKSPACE if the GEMM's scratch (bsg_workspace_size()) is larger than
  *   BSG_NOALLOC_SCRATCH_BYTES (the library also checks this when it is compiled).
  * - Device-side errors of the last call on the current device are read with
@@ -402,7 +408,7 @@ bsg_status bsg_gemm_amax_noalloc_read_error(void* stream, uint32_t* error_bits);
  * bsg_selftest_wait_timeout -- failure-detection self-test of the device-side bounded waits.
  * Launches one warp whose wait on an mbarrier that nothing arrives on runs out after the
  * library's wait limit (2 s), records BSG_DEVERR_TIMEOUT in `workspace` (bsg_workspace_size()
- * bytes, 256-byte aligned; cleared first) and returns; the GEMM kernels use the same wait.  No
+ * bytes, 256-byte aligned) as this call's error and returns; the GEMM kernels use the same wait.  No
  * fault, trap or hang: the context stays usable.  Read the result with bsg_read_device_error;
  * bit 31 set means the wait completed, which it must not.
  */

@@ -4,6 +4,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -35,6 +36,8 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_dev[64];
+
+std::atomic<uint32_t> g_epoch{0};
 
 bsg_status current_device(int* dev_out, DeviceInfo* info_out) {
   int dev = 0;
@@ -180,6 +183,12 @@ int grid_size(int64_t tiles, int num_sms, const bsg_gemm_opts* opts) {
 
 }  // namespace
 
+uint32_t bsg::next_call_epoch() {
+  uint32_t e = 0;
+  while (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
+}
+
 extern "C" {
 
 size_t bsg_workspace_size(void) { return kWorkspaceBytes; }
@@ -299,10 +308,11 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   p.c_kind = c_kind;
   p.amax = amax;
   p.err = static_cast<uint32_t*>(workspace);
+  p.epoch = bsg::next_call_epoch();
 
+  // one launch and nothing else: the kernel tags its error record and amax accumulator in the
+  // workspace with this call's epoch and writes *amax itself
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
-  if (cudaMemsetAsync(amax, 0, sizeof(float), s) != cudaSuccess) return BSG_ERR_CUDA;
   GemmConfig cfg{fmt, bn, bsg::kEpiDense};
   cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
                         : bsg::launch_gemm_dense(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
@@ -419,13 +429,13 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
     }
   }
 
-  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (!fp8_d && cudaMemsetAsync(amax, 0, sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (fp8_d && n % 128 != 0 && !empty) {
     // SFD_col rows n .. ceil(n/128)*128 are padding the kernel never touches
     if (cudaMemsetAsync(sfd_col, 0, bsg_sf_bytes(1, n, valid_m, 32), s) != cudaSuccess) return BSG_ERR_CUDA;
   }
-  if (empty) return BSG_OK;
+  // no kernel runs for an empty call: its error record is cleared instead
+  if (empty) return cudaMemsetAsync(workspace, 0, 16, s) == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
   const CUtensorMap* b_maps = nullptr;
   if (discrete) {
     uint8_t* dst = static_cast<uint8_t*>(workspace) + kWorkspaceBytes;
@@ -471,6 +481,7 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   p.sfd_col_mt = static_cast<int>(cdiv(n, 128));
   p.sfd_col_kt = static_cast<int>(cdiv(valid_m, 128));
   p.err = static_cast<uint32_t*>(workspace);
+  p.epoch = bsg::next_call_epoch();
 
   GemmConfig cfg{fmt, bn, fp8_d ? bsg::kEpiGroupedFP8 : bsg::kEpiGroupedBF16};
   cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
@@ -600,13 +611,13 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
                       !make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn)))
     return BSG_ERR_CUDA;
 
-  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (!fp8_d && cudaMemsetAsync(amax, 0, 2 * sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
   if (fp8_d && n_d % 128 != 0 && !empty) {
     // SFD_col rows 2N .. ceil(2N/128)*128 are padding the kernel never touches
     if (cudaMemsetAsync(sfd_col, 0, bsg_sf_bytes(1, n_d, valid_m, 32), s) != cudaSuccess) return BSG_ERR_CUDA;
   }
-  if (empty) return BSG_OK;
+  // no kernel runs for an empty call: its error record is cleared instead
+  if (empty) return cudaMemsetAsync(workspace, 0, 16, s) == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
 
   GemmParams p;
@@ -643,6 +654,7 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
   p.beta = beta;
   p.dprob = dprob;
   p.err = static_cast<uint32_t*>(workspace);
+  p.epoch = bsg::next_call_epoch();
 
   GemmConfig cfg{fmt, bn, fp8_d ? bsg::kEpiDswigluFP8 : bsg::kEpiDswigluF};
   cudaError_t e = pairs ? bsg::launch_gemm_pair_dswiglu(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
@@ -696,7 +708,6 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
   if (st != BSG_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
   const uint8_t* sfa = x_scale;
   const uint8_t* sfb = w_scale;
   if (scale_layout == 1) {
@@ -746,6 +757,7 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
   p.rope_sin = static_cast<const uint16_t*>(sin);
   p.qk_rope = static_cast<int>(qk_rope);
   p.err = static_cast<uint32_t*>(workspace);
+  p.epoch = bsg::next_call_epoch();
 
   GemmConfig cfg{bsg::kMXFP8, bn, bsg::kEpiRope};
   cudaError_t e = pairs ? bsg::launch_gemm_pair_rope(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
@@ -791,7 +803,6 @@ bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, con
   if (!make_operand_map(&ta, x, row_bytes, tokens, 1, 128) ||
       !make_operand_map(&tb, w, row_bytes, n, 1, pairs ? bn / 2 : bn))
     return BSG_ERR_CUDA;
-  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
 
   GemmParams p;
   memset(&p, 0, sizeof(p));
@@ -812,6 +823,7 @@ bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, con
   p.rope_sin = static_cast<const uint16_t*>(sin);
   p.qk_rope = static_cast<int>(qk_rope);
   p.err = static_cast<uint32_t*>(workspace);
+  p.epoch = bsg::next_call_epoch();
 
   GemmConfig cfg{bsg::kBF16, bn, bsg::kEpiRope};
   cudaError_t e = pairs ? bsg::launch_gemm_pair_rope(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
@@ -824,8 +836,11 @@ bsg_status bsg_read_device_error(const void* workspace, void* stream, uint32_t* 
   if (!workspace || !error_bits) return BSG_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSG_ERR_CUDA;
-  uint32_t bits = 0;
-  if (cudaMemcpy(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return BSG_ERR_CUDA;
+  // error bits, the epoch that set them, the epoch of the last call that ran: the bits are that
+  // call's only when the two epochs agree
+  uint32_t w[3] = {0, 0, 0};
+  if (cudaMemcpy(w, workspace, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BSG_ERR_CUDA;
+  const uint32_t bits = w[1] == w[2] ? w[0] : 0u;
   *error_bits = bits;
   return bits ? BSG_ERR_DEVICE : BSG_OK;
 }

@@ -47,16 +47,41 @@ __device__ __forceinline__ float ue4m3_value(uint32_t code) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));    // (1 + m/8) * 2^(e-7)
 }
 
-// Device error word: records the first error bits of a call.
-__device__ __forceinline__ void report_error(uint32_t* err, uint32_t bits) {
-  if (err != nullptr) atomicOr(err, bits);
+// Device error record in the first bytes of a call's workspace (32-bit words):
+//   words 0-1  the error bits (word 0) tagged with the epoch of the call that set them (word 1),
+//              updated together by one 64-bit atomic;
+//   word 2     the epoch of the last call whose kernel ran (every CTA stores it at its start).
+// Every call gets a fresh nonzero epoch from the library, and the host takes the bits as the
+// last call's only when words 1 and 2 agree, so no call has to clear the workspace before its
+// kernel runs.
+struct ErrSink {
+  uint32_t* ws;    // the workspace (8-byte aligned), or nullptr
+  uint32_t epoch;  // this call's epoch
+};
+
+// Marks the workspace as used by this call (any thread of every CTA may do it; same value).
+__device__ __forceinline__ void mark_call(const ErrSink& e) {
+  if (e.ws != nullptr) *reinterpret_cast<volatile uint32_t*>(e.ws + 2) = e.epoch;
+}
+
+// ORs `bits` into this call's error bits (replacing bits a previous call left behind).
+__device__ __forceinline__ void report_error(const ErrSink& e, uint32_t bits) {
+  if (e.ws == nullptr) return;
+  unsigned long long* w = reinterpret_cast<unsigned long long*>(e.ws);
+  const unsigned long long tag = static_cast<unsigned long long>(e.epoch) << 32;
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(w), assumed;
+  do {
+    assumed = old;
+    const unsigned long long nv = ((assumed >> 32) == e.epoch) ? (assumed | bits) : (tag | bits);
+    old = atomicCAS(w, assumed, nv);
+  } while (old != assumed);
 }
 
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false) when another
 // role of the CTA has aborted or after kWaitLimitNs, in which case it records a timeout
 // and raises the CTA's abort flag.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                             uint32_t* err) {
+                                             const ErrSink& err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {

@@ -733,6 +733,43 @@ __device__ __forceinline__ void epilogue_tile_rope(const GemmParams& p, int row,
   }
 }
 
+// Dense amax without a cleared output: every CTA (one thread) folds its maximum into the
+// workspace accumulator, then counts itself finished; the CTA that completes the count reads the
+// accumulator and writes *p.amax.  Both words are tagged with the call's epoch, so values a
+// previous call left behind are replaced rather than combined; the last CTA also zeroes them
+// under this epoch, so a replay of the same call (a CUDA graph) starts from zero too.
+__device__ __forceinline__ void dense_amax_finalize(const GemmParams& p, float cta_max) {
+  uint8_t* ws = reinterpret_cast<uint8_t*>(p.err);
+  unsigned long long* done = reinterpret_cast<unsigned long long*>(ws + kWsDoneByte);
+  unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws + kWsAmaxByte);
+  const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
+  if (cta_max > 0.0f) {
+    // non-negative floats order like their bit patterns
+    const uint32_t v = __float_as_uint(cta_max);
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(acc), assumed;
+    do {
+      assumed = old;
+      const bool mine = (assumed >> 32) == p.epoch;
+      const uint32_t cur = mine ? static_cast<uint32_t>(assumed) : 0u;
+      if (mine && cur >= v) break;
+      old = atomicCAS(acc, assumed, tag | (v > cur ? v : cur));
+    } while (old != assumed);
+  }
+  __threadfence();
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(done), assumed, nv;
+  do {
+    assumed = old;
+    nv = ((assumed >> 32) == p.epoch) ? assumed + 1 : (tag | 1ull);
+    old = atomicCAS(done, assumed, nv);
+  } while (old != assumed);
+  if (static_cast<uint32_t>(nv) == gridDim.x) {
+    __threadfence();
+    const unsigned long long a = atomicExch(acc, tag);  // read and zero under this epoch
+    p.amax[0] = (a >> 32) == p.epoch ? __uint_as_float(static_cast<uint32_t>(a)) : 0.0f;
+    atomicExch(done, tag);
+  }
+}
+
 // Folds one warp's running maxima of expert g into shared memory: the per-expert amax of the
 // grouped sReLU float D, or the (|ab|, |dswiglu|) pair of the dSwiGLU float D.
 template <int EPI>
@@ -988,7 +1025,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const bool bad = *bad_flag != 0;
-  if (bad && blockIdx.x == 0 && threadIdx.x == 0) report_error(p.err, kErrBadOffsets);
+  const ErrSink es{p.err, p.epoch};
+  if (threadIdx.x == 0) mark_call(es);
+  if (bad && blockIdx.x == 0 && threadIdx.x == 0) report_error(es, kErrBadOffsets);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -1008,7 +1047,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             p.sfb_ptrs ? reinterpret_cast<const uint8_t*>(p.sfb_ptrs[tc.l])
                        : p.sfb + static_cast<uint64_t>(tc.l) * p.sfb_mt * p.sf_kt * 512;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, es)) { ok = false; break; }
           const int k_left = p.k - kt * T::kElemsPerKTile;
           const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
           const int atoms = FMT == kMXFP8 ? 1 : FMT == kNVFP4 ? n_mma : 0;
@@ -1052,7 +1091,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+        if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
@@ -1065,7 +1104,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           // discarded with the error.
           // the stagers arrive after the stage's data landed and its scale factors are in TMEM
           // bf16 stages carry no scale factors: their data landing (full) is all the MMAs need
-          ok &= wait_bounded(FMT == kBF16 ? &full[stage] : &sf_ready[stage], phase, abort_flag, p.err);
+          ok &= wait_bounded(FMT == kBF16 ? &full[stage] : &sf_ready[stage], phase, abort_flag, es);
           tc_fence_after();
           const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
@@ -1112,7 +1151,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
       const int b_blk0 = ((tc.nt * BN) >> 5) & 3;  // the tile's first 32-row block within its first atom
       for (int kt = 0; kt < p.k_tiles; ++kt) {
-        ok &= wait_bounded(&full[stage], phase, abort_flag, p.err);
+        ok &= wait_bounded(&full[stage], phase, abort_flag, es);
         tc_fence_after();
         const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
         if constexpr (FMT != kBF16)
@@ -1138,7 +1177,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
       const int row = tc.mt * kTileM + quad * 32 + lane;
       if constexpr (epi_is_dswiglu(EPI)) prefetch_dswiglu_c<BN>(p, row, tc.nt * BN, half, 2);
-      if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
+      if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, es)) break;
       tc_fence_after();
       float alpha_g = 1.0f, prob_r = 0.0f;
       if (epi_is_grouped(EPI)) {
@@ -1190,11 +1229,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
+  if (EPI == kEpiDense) {
+    // every CTA folds its maximum into the workspace; the last one to finish writes the amax
+    if (threadIdx.x == 0) dense_amax_finalize(p, (!bad && *abort_flag == 0) ? s_amax[0] : 0.0f);
+  }
   if (!bad && *abort_flag == 0) {
-    // one global atomicMax per CTA (dense) or per CTA and expert touched (grouped bf16 D)
-    if (EPI == kEpiDense) {
-      if (threadIdx.x == 0 && s_amax[0] > 0.0f) atomic_max_nonneg(p.amax, s_amax[0]);
-    } else if (EPI == kEpiGroupedBF16) {
+    // one global atomicMax per CTA and expert touched (grouped float D)
+    if (EPI == kEpiGroupedBF16) {
       for (int g = threadIdx.x; g < p.l; g += kThreadsGemm)
         if (s_amax[g] > 0.0f) atomic_max_nonneg(&p.amax[g], s_amax[g]);
     } else if (EPI == kEpiDswigluF) {

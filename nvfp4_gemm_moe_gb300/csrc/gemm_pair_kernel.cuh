@@ -181,7 +181,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const bool bad = *bad_flag != 0;
-  if (bad && blockIdx.x == 0 && threadIdx.x == 0) report_error(p.err, kErrBadOffsets);
+  const ErrSink es{p.err, p.epoch};
+  if (threadIdx.x == 0) mark_call(es);
+  if (bad && blockIdx.x == 0 && threadIdx.x == 0) report_error(es, kErrBadOffsets);
   const int pair_id = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
 
@@ -207,7 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
             p.sfb_ptrs ? reinterpret_cast<const uint8_t*>(p.sfb_ptrs[tc.l])
                        : p.sfb + static_cast<uint64_t>(tc.l) * p.sfb_mt * p.sf_kt * 512;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, es)) { ok = false; break; }
           const int k_left = p.k - kt * T::kElemsPerKTile;
           const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
           const int atoms = FMT == kMXFP8 ? 1 : FMT == kNVFP4 ? n_mma : 0;
@@ -258,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
-        if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, p.err)) { ok = false; break; }
+        if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
@@ -267,7 +269,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           // stagers waited for it)
           // bf16 operands carry no scales: the even CTA's stage barrier (both CTAs' A/B bytes) is
           // all the MMAs need
-          ok &= wait_bounded(FMT == kBF16 ? &full[stage] : &sf_ready[stage], phase, abort_flag, p.err);
+          ok &= wait_bounded(FMT == kBF16 ? &full[stage] : &sf_ready[stage], phase, abort_flag, es);
           tc_fence_after();
           const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
@@ -312,7 +314,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
       const int b_blk0 = ((tc.nt * BN) >> 5) & 3;  // the tile's first 32-row block within its first atom
       for (int kt = 0; kt < p.k_tiles; ++kt) {
-        ok &= wait_bounded(&landed[stage], phase, abort_flag, p.err);
+        ok &= wait_bounded(&landed[stage], phase, abort_flag, es);
         tc_fence_after();
         const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
         // the wide B-scale gather measured faster for the RoPE tiles, slower for the dSwiGLU ones
@@ -342,7 +344,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
       const int row = tc.mt * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
       if constexpr (epi_is_dswiglu(EPI)) prefetch_dswiglu_c<BN>(p, row, tc.nt * BN, half, 2);
-      if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, p.err)) break;
+      if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, es)) break;
       tc_fence_after();
       float alpha_g = 1.0f, prob_r = 0.0f;
       if (epi_is_grouped(EPI)) {
@@ -396,10 +398,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no remote arrival or MMA into this CTA's TMEM is still pending
+  if (EPI == kEpiDense) {
+    // every CTA folds its maximum into the workspace; the last one to finish writes the amax
+    if (threadIdx.x == 0) dense_amax_finalize(p, (!bad && *abort_flag == 0) ? s_amax[0] : 0.0f);
+  }
   if (!bad && *abort_flag == 0) {
-    if (EPI == kEpiDense) {
-      if (threadIdx.x == 0 && s_amax[0] > 0.0f) atomic_max_nonneg(p.amax, s_amax[0]);
-    } else if (EPI == kEpiGroupedBF16) {
+    // one global atomicMax per CTA and expert touched (grouped float D)
+    if (EPI == kEpiGroupedBF16) {
       for (int g = threadIdx.x; g < p.l; g += kThreadsGemm)
         if (s_amax[g] > 0.0f) atomic_max_nonneg(&p.amax[g], s_amax[g]);
     } else if (EPI == kEpiDswigluF) {

@@ -10,6 +10,14 @@ namespace bsg {
 // Bytes of the per-call scratch every GEMM entry point needs (the device error word and the
 // words next to it); bsg_workspace_size() returns it.
 constexpr size_t kWorkspaceBytes = 256;
+// Byte offsets in it: 0-11 the device error record (ErrSink in common.cuh); 16-23 the dense
+// kernel's count of finished CTAs and 24-31 its amax accumulator, each a 32-bit value tagged with
+// the call's epoch in the high word (so no call has to clear them first).
+constexpr int kWsDoneByte = 16;
+constexpr int kWsAmaxByte = 24;
+
+// A fresh nonzero tag for the next call's device-side records (process-wide counter).
+uint32_t next_call_epoch();
 
 enum Fmt : int { kMXFP8 = 0, kNVFP4 = 1, kBF16 = 2 };  // kBF16: plain bf16 operands, no scale factors
 // Element types of the C / D outputs.  E4M3 and E2M1 here are plain conversions (round to
@@ -74,8 +82,9 @@ struct GemmParams {
   const uint16_t* rope_cos;
   const uint16_t* rope_sin;
   int qk_rope;
-  // device error word (workspace)
+  // device error record (workspace) and this call's epoch (see ErrSink)
   uint32_t* err;
+  uint32_t epoch;
 };
 
 struct GemmConfig {

@@ -4,8 +4,8 @@
 // code that runs under a memory plan fixed at start-up (an arena that forbids allocations
 // afterwards) and latency-critical paths that cannot afford cudaMalloc's implicit device
 // synchronisation.  For them this entry point takes the GEMM's scratch (the device error
-// word the kernel writes) from a static device array that the library itself owns.  Every
-// GPU that loads the library keeps that array until the process exits.
+// record and the amax reduction the kernel keeps) from a static device array that the library
+// itself owns.  Every GPU that loads the library keeps that array until the process exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -92,8 +92,8 @@ extern "C" bsg_status bsg_gemm_amax_noalloc(const void* a, const void* b, const 
   void* scratch = nullptr;
   const bsg_status st = current_scratch(&scratch);
   if (st != BSG_OK) return st;
-  // bsg_gemm_amax clears the error word on `stream` before the kernel runs, so the previous
-  // call's contents never leak into this one.
+  // bsg_gemm_amax tags the error record and the amax reduction in the array with a number
+  // unique to the call, so the previous call's contents never leak into this one.
   return bsg_gemm_amax(a, b, sfa, sfb, ab_dtype, sf_dtype, sf_vec_size, m, n, k, l, c, c_dtype, amax, opts,
                        scratch, BSG_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -10,16 +10,19 @@
 
 #include "bsg.h"
 #include "common.cuh"
+#include "internal.h"
 #include "ptx.cuh"
 
 namespace {
 
 constexpr uint32_t kErrSelftestCompleted = 0x80000000u;  // the wait completed: it must not
 
-__global__ void selftest_wait_kernel(uint32_t* err) {
+__global__ void selftest_wait_kernel(uint32_t* ws, uint32_t epoch) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
+  const bsg::ErrSink err{ws, epoch};
   if (threadIdx.x == 0) {
+    bsg::mark_call(err);
     bsg::mbar_init(&bar, 1);
     abort_flag = 0;
     bsg::fence_mbar_init();
@@ -43,7 +46,6 @@ extern "C" bsg_status bsg_selftest_wait_timeout(void* workspace, size_t workspac
     return BSG_ERR_CUDA;
   if (major != 10 || minor != 3) return BSG_ERR_ARCH;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return BSG_ERR_CUDA;
-  selftest_wait_kernel<<<1, 32, 0, s>>>(static_cast<uint32_t*>(workspace));
+  selftest_wait_kernel<<<1, 32, 0, s>>>(static_cast<uint32_t*>(workspace), bsg::next_call_epoch());
   return cudaGetLastError() == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
 }

@@ -152,3 +152,28 @@ def test_dense_cta_pairs_few_clusters(lib):
     """Two pairs walk many 256 x 256 tiles: stage and accumulator phases wrap around."""
     run_dense("mxfp8", 1024, 1024, 1024, 2, "bf16", cta_pair=2, max_ctas=4, boost=True)
     run_dense("nvfp4", 768, 1024, 1024, 1, "bf16", cta_pair=2, max_ctas=2)
+
+
+@pytest.mark.parametrize("cta_pair,max_ctas", [(1, 0), (1, 1), (2, 0), (2, 2)])
+def test_dense_amax_from_stale_workspace(lib, cta_pair, max_ctas):
+    """The kernel writes amax itself (the last CTA to finish) from a reduction it keeps in the
+    workspace under the call's tag: a workspace full of another call's leftovers (bytes 0xA5) and
+    a poisoned amax give the oracle's amax and no device error, twice in a row, on one CTA, one
+    pair, and full grids of CTAs and pairs."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    import nvfp4_gemm_moe_gb300 as bsg
+    fmt, m, n, k, l = "mxfp8", 640, 512, 256, 2
+    a, b = _operands(5, fmt, m, n, k, l, spread=True)
+    qa, sfa = torch_ops.quantize(torch.from_numpy(a).cuda(), fmt)
+    qb, sfb = torch_ops.quantize(torch.from_numpy(b).cuda(), fmt)
+    qa_ref, sfa_ref = oq.quantize(a, fmt)
+    qb_ref, sfb_ref = oq.quantize(b, fmt)
+    _, amax_ref = og.dense_gemm_amax(qa_ref, qb_ref, sfa_ref, sfb_ref, fmt, m, n, k, l)
+    ws = torch.full((bsg.bsg_workspace_size(),), 0xA5, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        amax = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+        torch_ops.gemm_amax(qa, qb, sfa, sfb, fmt, m, n, k, l, c_dtype=torch.float32, amax=amax, workspace=ws,
+                            cta_pair=cta_pair, max_ctas=max_ctas)
+        torch.cuda.synchronize()
+        check_amax(amax.cpu().numpy(), np.array([amax_ref]))
+        assert bsg.bsg_read_device_error(ws) == 0
