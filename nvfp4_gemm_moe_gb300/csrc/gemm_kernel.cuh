@@ -82,14 +82,18 @@ struct GemmTraits {
   // one transpose block per epilogue warp: 32 rows x 64 bytes (grouped), 32 x 32 bytes (RoPE)
   static constexpr int kXposeBlock = EPI == kEpiRope ? 1024 : kXposeBlockBytes;
   static constexpr int kXposeBytes = EPI == kEpiDense ? 0 : 8 * kXposeBlock;
-  // as many stages as shared memory and the TMEM scale-factor slots allow, at most six
+  // shared-memory ring: as many stages as fit, at most six
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
-  static constexpr int kStagesTmem = kSfStride == 0 ? 6 : (512 - kSfBase) / kSfStride;
-  static constexpr int kStages = kStagesSmem < kStagesTmem ? (kStagesSmem < 6 ? kStagesSmem : 6)
-                                                           : (kStagesTmem < 6 ? kStagesTmem : 6);
+  static constexpr int kStages = kStagesSmem < 6 ? kStagesSmem : 6;
   static_assert(kStages >= 3, "pipeline depth");
-  static constexpr int kTmemUsed = kSfBase + kStages * kSfStride;
+  // TMEM scale-factor slots: one per stage when TMEM has room, else fewer, recycled through the
+  // sf_free barriers
+  static constexpr int kSfSlotsTmem = kSfStride == 0 ? kStages : (512 - kSfBase) / kSfStride;
+  static constexpr int kSfSlots = kSfSlotsTmem < kStages ? kSfSlotsTmem : kStages;
+  static constexpr bool kSfRing = kSfSlots < kStages;
+  static_assert(kSfSlots >= 3, "TMEM scale-factor slots");
+  static constexpr int kTmemUsed = kSfBase + kSfSlots * kSfStride;
   static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                    : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM budget");
@@ -972,7 +976,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   uint64_t* tmem_empty = tmem_full + ACC;
   uint64_t* drain = tmem_empty + ACC;
   uint64_t* sf_ready = drain + 1;  // the stage's scale factors are in TMEM (four stager arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_ready + S);
+  uint64_t* sf_free = sf_ready + S;  // TMEM scale slot free again (its MMAs completed)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_free + T::kSfSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bad_flag = const_cast<int*>(abort_flag) + 1;
   int32_t* s_offs = reinterpret_cast<int32_t*>(s_bar + T::kBarBytes);
@@ -993,6 +998,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     }
     mbar_init(drain, 1);
     for (int s = 0; s < S; ++s) mbar_init(&sf_ready[s], 4);
+    for (int f = 0; f < T::kSfSlots; ++f) mbar_init(&sf_free[f], 1);
     *abort_flag = 0;
     *bad_flag = 0;
     fence_mbar_init();
@@ -1087,7 +1093,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (!bad) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, fslot = 0;
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
@@ -1106,7 +1112,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           // bf16 stages carry no scale factors: their data landing (full) is all the MMAs need
           ok &= wait_bounded(FMT == kBF16 ? &full[stage] : &sf_ready[stage], phase, abort_flag, es);
           tc_fence_after();
-          const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
+          const uint32_t sfa_t = tmem_base + T::kSfBase + fslot * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
           const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
@@ -1122,9 +1128,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
               if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
             }
             tc_commit(&empty[stage]);
+            if (T::kSfRing) tc_commit(&sf_free[fslot]);
           }
           __syncwarp();
           if (++stage == S) { stage = 0; phase ^= 1u; }
+          if (++fslot == T::kSfSlots) fslot = 0;
         }
         if (!ok) break;
         if (lane == 0) tc_commit(&tmem_full[acc]);
@@ -1142,18 +1150,21 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     }
   } else if (warp >= 10) {
     // ------------------------------------------------------------ scale-factor stagers 10..13
-    // A stage's TMEM scale columns are free once its smem stage has been refilled: the refill
-    // waited for the commit of the MMAs that read them.
+    // With one TMEM scale slot per stage, a slot is free once its smem stage has been refilled
+    // (the refill waited for the commit of the MMAs that read it); with fewer slots, the MMA
+    // thread commits each slot's release to sf_free.
     const uint32_t quad_lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0, fslot = 0, fphase = 0;
     bool ok = FMT != kBF16;  // bf16 operands have no scale factors to stage
     for (int t = blockIdx.x; !bad && ok && t < p.num_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
       const int b_blk0 = ((tc.nt * BN) >> 5) & 3;  // the tile's first 32-row block within its first atom
       for (int kt = 0; kt < p.k_tiles; ++kt) {
         ok &= wait_bounded(&full[stage], phase, abort_flag, es);
+        // with fewer TMEM slots than stages, the slot's previous MMAs must have completed
+        if (T::kSfRing) ok &= wait_bounded(&sf_free[fslot], fphase ^ 1u, abort_flag, es);
         tc_fence_after();
-        const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
+        const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + fslot * T::kSfStride;
         if constexpr (FMT != kBF16)
           stage_scale_factors<T, true>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t,
                                        sfa_t + T::kSfaCols, lane, b_blk0);
@@ -1162,6 +1173,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sf_ready[stage]);
         if (++stage == S) { stage = 0; phase ^= 1u; }
+        if (++fslot == T::kSfSlots) { fslot = 0; fphase ^= 1u; }
       }
     }
   } else {

@@ -65,12 +65,17 @@ struct PairTraits {
   static constexpr int kAmaxBytes = 4096;
   static constexpr int kXposeBlock = kXposeBlockBytes;
   static constexpr int kXposeBytes = 8 * kXposeBlock;  // one transpose block per epilogue warp
+  // shared-memory ring: as many stages as fit, at most six
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
-  static constexpr int kStagesTmem = kSfStride == 0 ? 6 : (512 - kSfBase) / kSfStride;
-  static constexpr int kStages = kStagesSmem < kStagesTmem ? (kStagesSmem < 6 ? kStagesSmem : 6)
-                                                           : (kStagesTmem < 6 ? kStagesTmem : 6);
+  static constexpr int kStages = kStagesSmem < 6 ? kStagesSmem : 6;
   static_assert(kStages >= 3, "pipeline depth");
+  // TMEM scale-factor slots: one per stage when TMEM has room, else fewer, recycled through the
+  // sf_free barriers (the two-accumulator tiles leave room for only four)
+  static constexpr int kSfSlotsTmem = kSfStride == 0 ? kStages : (512 - kSfBase) / kSfStride;
+  static constexpr int kSfSlots = kSfSlotsTmem < kStages ? kSfSlotsTmem : kStages;
+  static constexpr bool kSfRing = kSfSlots < kStages;
+  static_assert(kSfSlots >= 3 && kSfBase + kSfSlots * kSfStride <= 512, "TMEM scale-factor slots");
   static constexpr int kSmemBytes =
       1024 + kStages * kStageBytes + kBarBytes + kOffsetsBytes + kAmaxBytes + kXposeBytes;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -125,7 +130,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   uint64_t* tmem_full = sf_ready + S;
   uint64_t* tmem_empty = tmem_full + ACC;
   uint64_t* drain = tmem_empty + ACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_free = drain + 1;                        // TMEM scale slot free again (MMAs done)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_free + T::kSfSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bad_flag = const_cast<int*>(abort_flag) + 1;
   int32_t* s_offs = reinterpret_cast<int32_t*>(s_bar + T::kBarBytes);
@@ -149,6 +155,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       mbar_init(&tmem_empty[a], 16);  // eight epilogue warps in each CTA (used in the even CTA)
     }
     mbar_init(drain, 1);
+    for (int f = 0; f < T::kSfSlots; ++f) mbar_init(&sf_free[f], 1);
     *abort_flag = 0;
     *bad_flag = 0;
     fence_mbar_init();
@@ -256,7 +263,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (leader && !bad) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, fslot = 0;
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
@@ -271,7 +278,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           // all the MMAs need
           ok &= wait_bounded(FMT == kBF16 ? &full[stage] : &sf_ready[stage], phase, abort_flag, es);
           tc_fence_after();
-          const uint32_t sfa_t = tmem_base + T::kSfBase + stage * T::kSfStride;
+          const uint32_t sfa_t = tmem_base + T::kSfBase + fslot * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
           const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
@@ -286,9 +293,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
               if (n_mma == 3) issue_stage_pair<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
             }
             tc_commit_pair_multicast(&empty[stage], 0x3);
+            if (T::kSfRing) tc_commit_pair_multicast(&sf_free[fslot], 0x3);
           }
           __syncwarp();
           if (++stage == S) { stage = 0; phase ^= 1u; }
+          if (++fslot == T::kSfSlots) fslot = 0;
         }
         if (!ok) break;
         if (lane == 0) tc_commit_pair_multicast(&tmem_full[acc], 0x3);
@@ -308,15 +317,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     const uint32_t quad_lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t ready0 = mapa_shared(smem_u32(&sf_ready[0]), 0);
     uint64_t* landed = leader ? full : sf_full;
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0, fslot = 0, fphase = 0;
     bool ok = FMT != kBF16;  // bf16 operands have no scale factors to stage
     for (int t = pair_id; !bad && ok && t < p.num_tiles; t += num_pairs) {
       const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
       const int b_blk0 = ((tc.nt * BN) >> 5) & 3;  // the tile's first 32-row block within its first atom
       for (int kt = 0; kt < p.k_tiles; ++kt) {
         ok &= wait_bounded(&landed[stage], phase, abort_flag, es);
+        // with fewer TMEM slots than stages, the slot's previous MMAs must have completed (with one
+        // slot per stage the refill of the stage already waited for them)
+        if (T::kSfRing) ok &= wait_bounded(&sf_free[fslot], fphase ^ 1u, abort_flag, es);
         tc_fence_after();
-        const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + stage * T::kSfStride;
+        const uint32_t sfa_t = tmem_base + quad_lanes + T::kSfBase + fslot * T::kSfStride;
         // the wide B-scale gather measured faster for the RoPE tiles, slower for the dSwiGLU ones
         if constexpr (FMT != kBF16)
           stage_scale_factors<T, EPI == kEpiRope>(s_sfa + stage * T::kSfaBytes, s_sfb + stage * T::kSfbBytes, sfa_t,
@@ -329,6 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           else mbar_arrive_cluster_relaxed(ready0 + stage * 8);
         }
         if (++stage == S) { stage = 0; phase ^= 1u; }
+        if (++fslot == T::kSfSlots) { fslot = 0; fphase ^= 1u; }
       }
     }
   } else {
