@@ -27,9 +27,8 @@
  * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
  *   stream.  Every entry point only enqueues work (memsets, copies and kernel
  *   launches) and returns; results are valid once the stream reaches that point.
- *   Three calls synchronise `stream` first, as their comments say: a grouped call
- *   with opts->validate_offsets, bsg_grouped_gemm_srelu_discrete (it reads the
- *   experts' pointers on the host) and bsg_read_device_error.
+ *   Two calls synchronise `stream` first, as their comments say: a grouped call
+ *   with opts->validate_offsets, and bsg_read_device_error.
  * - CUDA graphs: every other compute call enqueues only kernels and memsets on
  *   `stream`, so it can be captured into a graph and replayed (inputs read, outputs
  *   written at replay time through the captured pointers).  Make one eager call of
@@ -99,6 +98,7 @@ typedef enum bsg_sf_dtype {
 /* Device error bits written to the workspace. */
 #define BSG_DEVERR_TIMEOUT 0x1u      /* a pipeline wait exceeded its time limit; the kernel gave up */
 #define BSG_DEVERR_BAD_OFFSETS 0x2u  /* padded_offsets not non-decreasing multiples of 256 ending at valid_m */
+#define BSG_DEVERR_BAD_POINTERS 0x4u /* a null or misaligned b_ptrs / sfb_ptrs entry (per-expert weights) */
 
 /* Optional launch options; pass NULL for the defaults (all fields 0). */
 typedef struct bsg_gemm_opts {
@@ -114,7 +114,10 @@ typedef struct bsg_gemm_opts {
                             2 = CTA pairs on 256-row tiles, 256 wide, or 224 wide (MXFP8) with
                             tile_n == 224 or, when tile_n is 0, an E4M3-D or dSwiGLU epilogue;
                             the RoPE projections describe their own choices */
-  int reserved[3];
+  int b_major;           /* bsg_grouped_gemm_srelu_discrete with MXFP8 operands: 0 = each expert's
+                            B is (n, k) K-major, 1 = (k, n) N-major (n contiguous, n % 16 == 0);
+                            N-major B runs on 256-wide CTA-pair or 128-wide one-CTA tiles */
+  int reserved[2];
 } bsg_gemm_opts;
 
 /* Bytes of scratch the GEMM entry points need in `workspace` (device memory,
@@ -346,16 +349,20 @@ bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, con
  *
  * Arguments and results are those of bsg_grouped_gemm_srelu except:
  * b_ptrs     device int64 (num_experts,): b_ptrs[g] is the device address of expert g's codes,
- *            (n, k) K-major, C-contiguous, 16-byte aligned.
+ *            (n, k) K-major, C-contiguous, 16-byte aligned; with MXFP8 operands and
+ *            opts->b_major == 1, (k, n) N-major instead ("Grouped GEMM + sReLU (SM100)", Support
+ *            surface and constraints: discrete B in K-major or, for FP8, N-major form).
  * sfb_ptrs   device int64 (num_experts,): sfb_ptrs[g] is the device address of expert g's SF
  *            buffer for a (1, n, k) operand (bsg_sf_bytes(1, n, k, v) bytes), 16-byte aligned.
  * workspace  at least bsg_grouped_discrete_workspace_size(num_experts) bytes, 64-byte aligned:
  *            besides the error word it holds one TMA descriptor per expert.
- * The call copies b_ptrs and sfb_ptrs to the host and synchronises `stream` once before it
- * enqueues the kernel (it builds the experts' tensor maps on the host), so it cannot be
- * captured into a CUDA graph.  A null or misaligned pointer entry returns
- * BSG_ERR_INVALID_ARG / BSG_ERR_ALIGNMENT before anything is launched.  The weight buffers
- * must stay allocated until the kernel has completed.
+ * The call never reads b_ptrs / sfb_ptrs on the host: a small kernel enqueued before the GEMM
+ * writes each expert's TMA descriptor into the workspace from a template (the shape is the same
+ * for every expert) by replacing its global address with b_ptrs[g], so the call does not
+ * synchronise and can be captured into a CUDA graph.  A null or misaligned pointer entry sets
+ * BSG_DEVERR_BAD_POINTERS (read it with bsg_read_device_error) and the GEMM then computes and
+ * writes nothing (the per-expert amax stays zeroed).  The weight buffers must stay allocated
+ * until the kernel has completed.
  */
 size_t bsg_grouped_discrete_workspace_size(int64_t num_experts);
 bsg_status bsg_grouped_gemm_srelu_discrete(const void* a, const int64_t* b_ptrs, const uint8_t* sfa,

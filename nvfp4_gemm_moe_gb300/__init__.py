@@ -17,7 +17,7 @@ from . import build as _build_mod
 E4M3, E5M2, E2M1, F32, BF16, F16 = 0, 1, 2, 3, 4, 5
 SF_UE8M0, SF_UE4M3 = 0, 1
 OK = 0
-DEVERR_TIMEOUT, DEVERR_BAD_OFFSETS = 0x1, 0x2
+DEVERR_TIMEOUT, DEVERR_BAD_OFFSETS, DEVERR_BAD_POINTERS = 0x1, 0x2, 0x4
 
 MXFP8 = (E4M3, SF_UE8M0, 32)
 NVFP4 = (E2M1, SF_UE4M3, 16)
@@ -34,7 +34,8 @@ class BsgError(RuntimeError):
 
 class bsg_gemm_opts(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("max_ctas", ctypes.c_int), ("tanh_approx", ctypes.c_int),
-                ("validate_offsets", ctypes.c_int), ("cta_pair", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("validate_offsets", ctypes.c_int), ("cta_pair", ctypes.c_int), ("b_major", ctypes.c_int),
+                ("reserved", ctypes.c_int * 2)]
 
 
 def _load():
@@ -110,10 +111,11 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _opts(tile_n=0, max_ctas=0, tanh_approx=False, validate_offsets=False, cta_pair=0):
+def _opts(tile_n=0, max_ctas=0, tanh_approx=False, validate_offsets=False, cta_pair=0, b_major="k"):
     o = bsg_gemm_opts()
     o.tile_n, o.max_ctas, o.tanh_approx, o.validate_offsets = tile_n, max_ctas, int(tanh_approx), int(validate_offsets)
     o.cta_pair = cta_pair
+    o.b_major = {"k": 0, "n": 1}[b_major]
     return o
 
 

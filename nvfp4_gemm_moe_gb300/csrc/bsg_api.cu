@@ -93,6 +93,20 @@ bool make_operand_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// N-major 8-bit operand (k rows of n bytes), loaded as 128-byte (N) x 128-row (K) boxes with the
+// 128-byte swizzle: one 128-element swizzle row of N per K row.
+bool make_operand_map_mn(CUtensorMap* m, const void* base, uint64_t n, uint64_t k) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {n, k, 1};
+  const cuuint64_t strides[2] = {n, n * k};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -258,6 +272,7 @@ bsg_status bsg_gemm_amax(const void* a, const void* b, const uint8_t* sfa, const
   if (!a || !b || !sfa || !sfb || !c || !amax) return BSG_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
   if (m < 1 || n < 1 || k < 1 || l < 1) return BSG_ERR_INVALID_ARG;
+  if (opts && opts->b_major != 0) return BSG_ERR_INVALID_ARG;  // N-major B: per-expert weights only
   if (!fits_int32(m) || !fits_int32(n) || !fits_int32(k) || !fits_int32(l)) return BSG_ERR_INVALID_ARG;
   if (k % sf_vec_size != 0) return BSG_ERR_INVALID_ARG;
   // C: f32, bf16 or f16; with FP4 operands also plain E4M3 or packed E2M1 (the pages disable FP8
@@ -387,23 +402,19 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
     if (prev != valid_m) return BSG_ERR_BAD_OFFSETS;
   }
 
-  // per-expert weights: the experts' addresses, copied to the host and checked before anything is enqueued
-  std::vector<int64_t> hb, hs;
-  if (discrete) {
-    hb.resize(static_cast<size_t>(num_experts));
-    hs.resize(static_cast<size_t>(num_experts));
-    if (cudaMemcpyAsync(hb.data(), b_ptrs, hb.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyAsync(hs.data(), sfb_ptrs, hs.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-      return BSG_ERR_CUDA;
-    for (size_t g = 0; g < hb.size(); ++g) {
-      if (!hb[g] || !hs[g]) return BSG_ERR_INVALID_ARG;
-      if ((hb[g] & 15) || (hs[g] & 15)) return BSG_ERR_ALIGNMENT;
-    }
+  // N-major B (per-expert weights, FP8): one 128-element swizzle row of N per CTA and K row, so
+  // 256-wide CTA-pair tiles or 128-wide one-CTA tiles
+  const bool b_mn = discrete && opts && opts->b_major == 1;
+  if (opts && opts->b_major != 0 && !b_mn) return BSG_ERR_INVALID_ARG;
+  if (b_mn) {
+    if (fmt != bsg::kMXFP8) return BSG_ERR_UNSUPPORTED;
+    if (opts->tile_n != 0 && opts->tile_n != 128 && opts->tile_n != 256) return BSG_ERR_UNSUPPORTED;
+    if (n % 16 != 0) return BSG_ERR_ALIGNMENT;  // the row pitch of a (k, n) B
   }
 
   // tiles and tensor maps (host only) before anything is enqueued
-  const TilePlan plan = plan_tiles(fmt, valid_m, n, 1, info.num_sms, fp8_d, opts);
+  TilePlan plan = plan_tiles(fmt, valid_m, n, 1, info.num_sms, fp8_d && !b_mn, opts);
+  if (b_mn) plan.bn = plan.pairs ? 256 : 128;
   const bool pairs = plan.pairs;
   const int bn = plan.bn;
   const int64_t m_tiles = pairs ? valid_m / 256 : valid_m / 128;
@@ -412,21 +423,14 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   if (!fits_int32(tiles)) return BSG_ERR_INVALID_ARG;
   const int elems_per_ktile = fmt == bsg::kMXFP8 ? 128 : 256;
   CUtensorMap ta, tb;
-  std::vector<CUtensorMap> maps;
   if (valid_m > 0) {
     if (!make_operand_map(&ta, a, row_bytes, valid_m, 1, 128)) return BSG_ERR_CUDA;
-    if (!discrete) {
-      if (!make_operand_map(&tb, b, row_bytes, n, num_experts, pairs ? bn / 2 : bn)) return BSG_ERR_CUDA;
-    } else {
-      // one tensor map per expert, stored in the workspace after the error word; the kernel
-      // reads them from global memory (after a tensormap-proxy acquire fence)
-      maps.resize(static_cast<size_t>(num_experts));
-      for (size_t g = 0; g < maps.size(); ++g) {
-        if (!make_operand_map(&maps[g], reinterpret_cast<const void*>(hb[g]), row_bytes, n, 1, pairs ? bn / 2 : bn))
-          return BSG_ERR_CUDA;
-      }
-      tb = maps[0];  // unused by the kernel in this form
-    }
+    // per-expert weights: a template for one expert's B, its address replaced per expert on the
+    // device (the address encoded here, a's, is never read through it)
+    const bool ok = b_mn ? make_operand_map_mn(&tb, a, n, k)
+                         : make_operand_map(&tb, discrete ? a : b, row_bytes, n, discrete ? 1 : num_experts,
+                                            pairs ? bn / 2 : bn);
+    if (!ok) return BSG_ERR_CUDA;
   }
 
   if (!fp8_d && cudaMemsetAsync(amax, 0, sizeof(float) * num_experts, s) != cudaSuccess) return BSG_ERR_CUDA;
@@ -436,13 +440,16 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   }
   // no kernel runs for an empty call: its error record is cleared instead
   if (empty) return cudaMemsetAsync(workspace, 0, 16, s) == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;
+  const uint32_t epoch = bsg::next_call_epoch();
   const CUtensorMap* b_maps = nullptr;
   if (discrete) {
-    uint8_t* dst = static_cast<uint8_t*>(workspace) + kWorkspaceBytes;
-    if (cudaMemcpyAsync(dst, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice, s) !=
-        cudaSuccess)
+    // one descriptor per expert after the 256-byte record, written by a kernel from the device
+    // pointer arrays; the GEMM kernel reads them from global memory (tensor-map proxy acquire)
+    CUtensorMap* dst = reinterpret_cast<CUtensorMap*>(static_cast<uint8_t*>(workspace) + kWorkspaceBytes);
+    if (bsg::launch_expert_maps(tb, b_ptrs, sfb_ptrs, static_cast<int>(num_experts), dst,
+                                static_cast<uint32_t*>(workspace), epoch, s) != cudaSuccess)
       return BSG_ERR_CUDA;
-    b_maps = reinterpret_cast<const CUtensorMap*>(dst);
+    b_maps = dst;
   }
   const int64_t sf_kt = cdiv(k / sf_vec_size, 4);
 
@@ -460,6 +467,7 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   p.sfb = sfb;
   p.b_maps = b_maps;
   p.sfb_ptrs = sfb_ptrs;
+  p.b_mn_major = b_mn ? 1 : 0;
   p.sfa_mt = static_cast<int>(valid_m / 128);
   p.sfb_mt = static_cast<int>(cdiv(n, 128));
   p.sf_kt = static_cast<int>(sf_kt);
@@ -481,7 +489,7 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   p.sfd_col_mt = static_cast<int>(cdiv(n, 128));
   p.sfd_col_kt = static_cast<int>(cdiv(valid_m, 128));
   p.err = static_cast<uint32_t*>(workspace);
-  p.epoch = bsg::next_call_epoch();
+  p.epoch = epoch;
 
   GemmConfig cfg{fmt, bn, fp8_d ? bsg::kEpiGroupedFP8 : bsg::kEpiGroupedBF16};
   cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
@@ -549,6 +557,7 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
       (!empty && (!a || !b || !sfa || !sfb || !alpha || !beta || !prob || !c || !d_row || !dprob)))
     return BSG_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < kWorkspaceBytes) return BSG_ERR_WORKSPACE;
+  if (opts && opts->b_major != 0) return BSG_ERR_INVALID_ARG;  // N-major B: per-expert weights only
   // N a multiple of 32: C and D are 32-column input / gate (ab / dswiglu) blocks; 2 * num_experts
   // amax values are staged in the kernel's shared memory
   if (valid_m < 0 || valid_m % 256 != 0 || n < 32 || n % 32 != 0 || k < 1 || num_experts < 1 ||

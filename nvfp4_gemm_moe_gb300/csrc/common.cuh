@@ -10,6 +10,7 @@ namespace bsg {
 
 constexpr uint32_t kErrTimeout = 0x1u;     // matches BSG_DEVERR_TIMEOUT
 constexpr uint32_t kErrBadOffsets = 0x2u;  // matches BSG_DEVERR_BAD_OFFSETS
+constexpr uint32_t kErrBadPointers = 0x4u;  // matches BSG_DEVERR_BAD_POINTERS
 
 // A pipeline wait longer than this is taken as a hang: the kernel records an error and
 // leaves instead of spinning forever.

@@ -860,9 +860,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
 // are in TMEM at sfa_t / sfb_t.  MXFP8 stages hold one scale column per row (four K blocks, one
 // per MMA, selected by the instruction descriptor's scale-factor id); NVFP4 stages hold one
 // column of four UE4M3 scales per row and MMA.  The first MMA accumulates iff acc0.
+// b_mn: B is N-major (MXFP8 only): its K advance per MMA is 32 rows of 128 bytes (four 1024-byte
+// swizzle atoms) and bit 16 of the instruction descriptor marks B as MN-major.
 template <int FMT, class T, int NM>
 __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa_t,
-                                            uint32_t sfb_t, uint32_t acc0) {
+                                            uint32_t sfb_t, uint32_t acc0, uint32_t b_mn = 0) {
+  const uint32_t b_step = b_mn ? 256u : 2u;
 #pragma unroll
   for (int j = 0; j < NM; ++j) {
     const uint32_t accumulate = j > 0 ? 1u : acc0;
@@ -870,7 +873,8 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uin
     if (FMT == kBF16) {
       tc_mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
     } else if (FMT == kMXFP8) {
-      tc_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t, sfb_t, accumulate);
+      tc_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + b_step * j, T::kIdesc | (b_mn << 16) | (j << 29) | (j << 4),
+                      sfa_t, sfb_t, accumulate);
     } else {
       tc_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4, sfb_t + j * T::kSfbColsPerMma,
                       accumulate);
@@ -1017,6 +1021,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       s_offs[i] = o;
       if ((o & 255) != 0 || o < prev || o > p.m || (i == p.l - 1 && o != p.m)) atomicOr(bad_flag, 1);
     }
+    // per-expert weights: the descriptor kernel before this one found an invalid weight pointer
+    if (p.b_maps != nullptr && threadIdx.x == 0 &&
+        reinterpret_cast<volatile uint32_t*>(p.err)[kWsBadPointersWord] == p.epoch)
+      atomicOr(bad_flag, 2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, T::kTmemCols);
@@ -1033,7 +1041,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   const bool bad = *bad_flag != 0;
   const ErrSink es{p.err, p.epoch};
   if (threadIdx.x == 0) mark_call(es);
-  if (bad && blockIdx.x == 0 && threadIdx.x == 0) report_error(es, kErrBadOffsets);
+  if ((*bad_flag & 1) && blockIdx.x == 0 && threadIdx.x == 0) report_error(es, kErrBadOffsets);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -1060,7 +1068,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           const uint32_t sf_bytes = static_cast<uint32_t>(atoms * 512 * (1 + T::kBRowGroups));
           mbar_arrive_expect_tx(&full[stage], T::kABytes + T::kBBytes + sf_bytes);
           tma_load_3d(s_a + stage * T::kABytes, &tmap_a, &full[stage], kt * kTileKBytes, tc.mt * kTileM, a_batch);
-          tma_load_3d(s_b + stage * T::kBBytes, bmap, &full[stage], kt * kTileKBytes, tc.nt * BN, b_batch);
+          if (FMT == kMXFP8 && BN == 128 && p.b_mn_major)  // N-major B: 128 bytes of N x 128 rows of K
+            tma_load_3d(s_b + stage * T::kBBytes, bmap, &full[stage], tc.nt * BN, kt * T::kElemsPerKTile, b_batch);
+          else
+            tma_load_3d(s_b + stage * T::kBBytes, bmap, &full[stage], kt * kTileKBytes, tc.nt * BN, b_batch);
           if constexpr (FMT != kBF16) {
             const uint8_t* sfa_src =
                 p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + tc.mt) * p.sf_kt +
@@ -1096,6 +1107,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, fslot = 0;
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
+      const uint32_t b_mn = (FMT == kMXFP8 && BN == 128 && p.b_mn_major) ? 1u : 0u;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es)) { ok = false; break; }
         tc_fence_after();
@@ -1115,17 +1127,19 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           const uint32_t sfa_t = tmem_base + T::kSfBase + fslot * T::kSfStride;
           const uint32_t sfb_t = sfa_t + T::kSfaCols;
           const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
+          // K-major B: rows of 128 bytes of K, 8-row groups 1024 bytes apart; N-major B (one
+          // 128-byte swizzle row of N per K row): 8-K-row atoms 1024 bytes apart
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
           const uint32_t acc0 = kt > 0 ? 1u : 0u;  // the first MMA of a tile overwrites the accumulator
           const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
           if (lane == 0) {
             if (n_mma == T::kMmasPerStage) {
-              issue_stage<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
+              issue_stage<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
             } else {
               // the last, partial K stage (K not a multiple of the stage depth)
-              if (n_mma == 1) issue_stage<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
-              if (n_mma == 2) issue_stage<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
-              if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
+              if (n_mma == 1) issue_stage<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+              if (n_mma == 2) issue_stage<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+              if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
             }
             tc_commit(&empty[stage]);
             if (T::kSfRing) tc_commit(&sf_free[fslot]);

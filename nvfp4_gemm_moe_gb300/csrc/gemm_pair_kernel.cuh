@@ -90,17 +90,19 @@ struct PairTraits {
 
 // NM pair MMAs (M = 256) of one stage, issued by one thread of the even CTA; the scale factors
 // are in both CTAs' TMEM at sfa_t / sfb_t (layout as in issue_stage).
+// b_mn: B is N-major (MXFP8, 256-wide tiles: 128 N per CTA), as in issue_stage.
 template <int FMT, class T, int NM>
 __device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa_t,
-                                                 uint32_t sfb_t, uint32_t acc0) {
+                                                 uint32_t sfb_t, uint32_t acc0, uint32_t b_mn = 0) {
+  const uint32_t b_step = b_mn ? 256u : 2u;
 #pragma unroll
   for (int j = 0; j < NM; ++j) {
     const uint32_t accumulate = j > 0 ? 1u : acc0;
     if (FMT == kBF16) {
       tc_mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
     } else if (FMT == kMXFP8) {
-      tc_mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc | (j << 29) | (j << 4), sfa_t, sfb_t,
-                           accumulate);
+      tc_mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + b_step * j, T::kIdesc | (b_mn << 16) | (j << 29) | (j << 4),
+                           sfa_t, sfb_t, accumulate);
     } else {
       tc_mma_mxf4nvf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
                            sfb_t + j * T::kSfbColsPerMma, accumulate);
@@ -173,6 +175,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       s_offs[i] = o;
       if ((o & 255) != 0 || o < prev || o > p.m || (i == p.l - 1 && o != p.m)) atomicOr(bad_flag, 1);
     }
+    // per-expert weights: the descriptor kernel before this one found an invalid weight pointer
+    if (p.b_maps != nullptr && threadIdx.x == 0 &&
+        reinterpret_cast<volatile uint32_t*>(p.err)[kWsBadPointersWord] == p.epoch)
+      atomicOr(bad_flag, 2);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, T::kTmemCols);
@@ -190,7 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   const bool bad = *bad_flag != 0;
   const ErrSink es{p.err, p.epoch};
   if (threadIdx.x == 0) mark_call(es);
-  if (bad && blockIdx.x == 0 && threadIdx.x == 0) report_error(es, kErrBadOffsets);
+  if ((*bad_flag & 1) && blockIdx.x == 0 && threadIdx.x == 0) report_error(es, kErrBadOffsets);
   const int pair_id = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
 
@@ -229,7 +235,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           else mbar_arrive_expect_tx(&sf_full[stage], sf_bytes);
           const uint32_t fbar = full0 + stage * 8;
           tma_load_3d_pair(s_a + stage * T::kABytes, &tmap_a, fbar, kt * kTileKBytes, a_row, a_batch);
-          tma_load_3d_pair(s_b + stage * T::kBBytes, bmap, fbar, kt * kTileKBytes, b_row, b_batch);
+          if (FMT == kMXFP8 && BN == 256 && p.b_mn_major)  // N-major B: 128 bytes of N x 128 rows of K
+            tma_load_3d_pair(s_b + stage * T::kBBytes, bmap, fbar, b_row, kt * T::kElemsPerKTile, b_batch);
+          else
+            tma_load_3d_pair(s_b + stage * T::kBBytes, bmap, fbar, kt * kTileKBytes, b_row, b_batch);
           if constexpr (FMT != kBF16) {
             const uint8_t* sfa_src =
                 p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + sfa_group) * p.sf_kt +
@@ -266,6 +275,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, fslot = 0;
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
+      const uint32_t b_mn = (FMT == kMXFP8 && BN == 256 && p.b_mn_major) ? 1u : 0u;
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
         if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es)) { ok = false; break; }
         tc_fence_after();
@@ -286,11 +296,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
           if (lane == 0) {
             if (n_mma == T::kMmasPerStage) {
-              issue_stage_pair<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
+              issue_stage_pair<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
             } else {
-              if (n_mma == 1) issue_stage_pair<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
-              if (n_mma == 2) issue_stage_pair<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
-              if (n_mma == 3) issue_stage_pair<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0);
+              if (n_mma == 1) issue_stage_pair<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+              if (n_mma == 2) issue_stage_pair<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+              if (n_mma == 3) issue_stage_pair<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
             }
             tc_commit_pair_multicast(&empty[stage], 0x3);
             if (T::kSfRing) tc_commit_pair_multicast(&sf_free[fslot], 0x3);

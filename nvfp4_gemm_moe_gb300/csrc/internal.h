@@ -13,8 +13,11 @@ constexpr size_t kWorkspaceBytes = 256;
 // Byte offsets in it: 0-11 the device error record (ErrSink in common.cuh); 16-23 the dense
 // kernel's count of finished CTAs and 24-31 its amax accumulator, each a 32-bit value tagged with
 // the call's epoch in the high word (so no call has to clear them first).
+// Word 3 (bytes 12-15): set to the call's epoch by the per-expert descriptor kernel when a weight
+// pointer is invalid; the GEMM kernel then computes nothing.
 constexpr int kWsDoneByte = 16;
 constexpr int kWsAmaxByte = 24;
+constexpr int kWsBadPointersWord = 3;
 
 // A fresh nonzero tag for the next call's device-side records (process-wide counter).
 uint32_t next_call_epoch();
@@ -51,6 +54,7 @@ struct GemmParams {
   const uint8_t* sfb;
   const CUtensorMap* b_maps;   // grouped with per-expert weights: one B tensor map per expert (global)
   const int64_t* sfb_ptrs;     // grouped with per-expert weights: one SFB pointer per expert
+  int b_mn_major;              // FP8 B stored N-major, (k, n) with n contiguous, per expert (128 N per CTA)
   int sfa_mt, sfb_mt;    // ceil(m/128), ceil(n/128)
   int sf_kt;             // ceil(K / (4 v)) atoms along K
   // dense epilogue
@@ -118,6 +122,12 @@ cudaError_t launch_gemm_rope(const GemmConfig& cfg, const CUtensorMap& tmap_a, c
                              const GemmParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_pair_rope(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                                   const GemmParams& p, int max_pairs, cudaStream_t stream);
+
+// Per-expert weights: writes maps[g] = `tmpl` with its global address replaced by b_ptrs[g], for
+// every expert g (device arrays b_ptrs / sfb_ptrs).  A null or misaligned entry records
+// BSG_DEVERR_BAD_POINTERS and tags workspace word kWsBadPointersWord with `epoch`.
+cudaError_t launch_expert_maps(const CUtensorMap& tmpl, const int64_t* b_ptrs, const int64_t* sfb_ptrs,
+                               int num_experts, CUtensorMap* maps, uint32_t* ws, uint32_t epoch, cudaStream_t s);
 
 // Scatters plain row-major scale bytes (rows, blocks) into the 128x4 atom layout (dst zeroed
 // first, so padding bytes hold the finite scale 0).

@@ -117,8 +117,9 @@ def grouped_gemm_srelu_discrete(a, b_ptrs, sfa, sfb_ptrs, fmt: str, padded_offse
                                 tanh_clamp_scale=None, d_dtype="bf16", c_dtype=torch.bfloat16, norm_const=None,
                                 outputs=None, workspace=None, stream=None, **opts):
     """grouped_gemm_srelu with per-expert weights: b_ptrs / sfb_ptrs are lists of the experts'
-    code tensors (n, k) / SF buffers, or device int64 tensors of their addresses. The call
-    synchronises the stream once (the experts' TMA descriptors are built on the host)."""
+    code tensors (n, k) / SF buffers, or device int64 tensors of their addresses.  The experts'
+    TMA descriptors are built on the device (no synchronisation; the call can be captured in a
+    CUDA graph); invalid addresses show up as BSG_DEVERR_BAD_POINTERS."""
     ab, sfd, v = FORMATS[fmt]
     dev = a.device
     valid_m = a.shape[0] if a.dim() == 2 else a.shape[1]

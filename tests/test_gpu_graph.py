@@ -99,3 +99,52 @@ def test_capture_and_replay_matches_eager(lib):
             assert torch.equal(got[key], v), f"{key} differs after replay (data set {seed})"
     import nvfp4_gemm_moe_gb300 as bsg
     assert all(bsg.bsg_read_device_error(wk) == 0 for wk in ws)
+
+
+def test_capture_discrete_weights(lib):
+    """The per-expert-weight call captured in a graph: its TMA descriptors are rebuilt on the
+    device from the pointer arrays at every replay, so new contents of the arrays (the experts'
+    weights in another order) take effect on replay, equal to an eager call bit for bit."""
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    dev = "cuda"
+    g = W.Grouped("graph_discrete", 3, 256, 256, 700, "fixed:300,0,400", "bf16", seed=6)
+    offs = torch.from_numpy(g.padded_offsets()).to(dev)
+    alpha = torch.from_numpy(g.alpha()).to(dev)
+    prob = torch.from_numpy(g.prob()).to(dev)
+    qa, sfa = torch_ops.quantize(_draw(30, (1, g.valid_m, g.k)).to(dev), "mxfp8")
+    experts = [torch_ops.quantize(_draw(31 + e, (1, g.n, g.k), 1 / 16).to(dev), "mxfp8") for e in range(g.experts)]
+    ws = torch.zeros(lib.bsg_grouped_discrete_workspace_size(g.experts), dtype=torch.uint8, device=dev)
+    bp = torch.empty(g.experts, dtype=torch.int64, device=dev)
+    sp = torch.empty(g.experts, dtype=torch.int64, device=dev)
+
+    def point(order):
+        bp.copy_(torch.tensor([experts[e][0].data_ptr() for e in order], dtype=torch.int64))
+        sp.copy_(torch.tensor([experts[e][1].data_ptr() for e in order], dtype=torch.int64))
+
+    outs = {}
+
+    def step():
+        outs["o"] = torch_ops.grouped_gemm_srelu_discrete(qa[0], bp, sfa, sp, "mxfp8", offs, alpha, prob, g.n, g.k,
+                                                          outputs=outs.get("o"), workspace=ws)
+
+    eager = {}
+    for order in ((0, 1, 2), (2, 0, 1)):
+        point(order)
+        step()
+        torch.cuda.synchronize()
+        eager[order] = {k2: v.clone() for k2, v in outs["o"].items() if v is not None}
+    assert not torch.equal(eager[(0, 1, 2)]["d"], eager[(2, 0, 1)]["d"])
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    torch.cuda.synchronize()
+    for order in ((2, 0, 1), (0, 1, 2), (2, 0, 1)):
+        point(order)
+        graph.replay()
+        torch.cuda.synchronize()
+        for key, v in eager[order].items():
+            assert torch.equal(outs["o"][key], v), f"{key} differs after replay (order {order})"
+    assert lib.bsg_read_device_error(ws) == 0

@@ -21,7 +21,7 @@ def _case(counts, n, k, seed=3, a_scale=1.0):
 
 
 def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0, tile_n=0, seed=3, a_scale=1.0,
-                tanh_approx=False, max_ctas=0, cta_pair=0, fmt="mxfp8", discrete=False):
+                tanh_approx=False, max_ctas=0, cta_pair=0, fmt="mxfp8", discrete=False, b_major="k"):
     from nvfp4_gemm_moe_gb300 import torch_ops
     import nvfp4_gemm_moe_gb300 as bsg
     wl, offs, a, b, alpha, prob = _case(counts, n, k, seed, a_scale)
@@ -43,14 +43,16 @@ def run_grouped(counts, n, k, d_dtype="bf16", clamp=None, c_kind="bf16", nc=1.0,
     if discrete:
         # each expert's codes and scales in an allocation of its own, allocated in reverse order
         per_sf = sfb.numel() // len(counts)
-        b_list = [qb[g].clone() for g in reversed(range(len(counts)))][::-1]
+        # N-major: expert g's codes stored (k, n), the same values transposed
+        b_list = [(qb[g].t().contiguous() if b_major == "n" else qb[g].clone())
+                  for g in reversed(range(len(counts)))][::-1]
         sfb_list = [sfb[g * per_sf:(g + 1) * per_sf].clone() for g in reversed(range(len(counts)))][::-1]
         ws = torch.zeros(bsg.bsg_grouped_discrete_workspace_size(len(counts)), dtype=torch.uint8, device="cuda")
         out = torch_ops.grouped_gemm_srelu_discrete(
             qa[0], b_list, sfa, sfb_list, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
             torch.from_numpy(prob).cuda(), n, k, tanh_clamp_scale=clamp, d_dtype=d_dtype, c_dtype=c_dtype,
             norm_const=torch.tensor([nc], dtype=torch.float32, device="cuda"), workspace=ws, tile_n=tile_n,
-            tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair, outputs=outputs)
+            tanh_approx=tanh_approx, max_ctas=max_ctas, cta_pair=cta_pair, b_major=b_major, outputs=outputs)
     else:
         out = torch_ops.grouped_gemm_srelu(
             qa[0], qb, sfa, sfb, fmt, torch.from_numpy(offs).cuda(), torch.from_numpy(alpha).cuda(),
@@ -232,8 +234,50 @@ def test_grouped_discrete_weights(lib, fmt, d_dtype, clamp, n, tile_n, cta_pair)
                 a_scale=700.0 if clamp else 1.0, discrete=True)
 
 
-def test_grouped_discrete_host_validation(lib):
-    """Null or misaligned pointer entries and a short workspace are rejected before any launch."""
+@pytest.mark.parametrize("counts,d_dtype,clamp,n,k,tile_n,cta_pair", [
+    (EDGE, "bf16", None, 512, 512, 0, 2),        # 256-wide CTA pairs (128 N per CTA)
+    (EDGE, "e4m3", None, 384, 512, 0, 2),        # E4M3 D on N-major B: pairs, ragged last N tile
+    (EDGE, "bf16", 32.0, 272, 320, 128, 1),      # one-CTA 128-wide tiles, ragged N, K tail
+    (EDGE, "e4m3", None, 256, 1024, 128, 1),
+    ([600, 900, 0, 300], "bf16", None, 768, 256, 0, 2),
+])
+def test_grouped_discrete_weights_n_major(lib, counts, d_dtype, clamp, n, k, tile_n, cta_pair):
+    """FP8 per-expert weights stored N-major, (k, n) with n contiguous ("Grouped GEMM + sReLU
+    (SM100)", Support surface and constraints), give the oracle's result."""
+    run_grouped(counts, n, k, d_dtype, clamp, "bf16", tile_n=tile_n, cta_pair=cta_pair, fmt="mxfp8",
+                a_scale=700.0 if clamp else 1.0, discrete=True, b_major="n")
+
+
+def test_grouped_discrete_n_major_rejections(lib):
+    """N-major B: MXFP8 only, per-expert weights only, 128 / 256-wide tiles, n % 16 == 0."""
+    import nvfp4_gemm_moe_gb300 as bsg
+    from nvfp4_gemm_moe_gb300 import torch_ops
+    k, n, vm = 256, 256, 256
+    qa = torch.zeros((vm, k), dtype=torch.uint8, device="cuda")
+    sfa = torch.zeros(bsg.bsg_sf_bytes(1, vm, k, 32), dtype=torch.uint8, device="cuda")
+    bs = [torch.zeros((k, n), dtype=torch.uint8, device="cuda")]
+    sfbs = [torch.zeros(bsg.bsg_sf_bytes(1, n, k, 32), dtype=torch.uint8, device="cuda")]
+    offs = torch.tensor([vm], dtype=torch.int32, device="cuda")
+    one, prob = torch.ones(1, device="cuda"), torch.ones(vm, device="cuda")
+    with pytest.raises(bsg.BsgError) as ei:
+        torch_ops.grouped_gemm_srelu_discrete(qa, bs, sfa, sfbs, "mxfp8", offs, one, prob, n, k, b_major="n",
+                                              tile_n=224, cta_pair=2)
+    assert ei.value.status == 2
+    with pytest.raises(bsg.BsgError) as ei:
+        torch_ops.grouped_gemm_srelu(qa, bs[0][None], sfa, sfbs[0], "mxfp8", offs, one, prob, n, k, b_major="n")
+    assert ei.value.status == 1
+    with pytest.raises(bsg.BsgError) as ei:
+        torch_ops.grouped_gemm_srelu_discrete(qa, [torch.zeros((k, n // 2), dtype=torch.uint8, device="cuda")], sfa,
+                                              [torch.zeros(bsg.bsg_sf_bytes(1, n, k, 16), dtype=torch.uint8,
+                                                           device="cuda")], "nvfp4", offs, one, prob, n, k,
+                                              b_major="n")
+    assert ei.value.status == 2
+
+
+def test_grouped_discrete_pointer_validation(lib):
+    """Null or misaligned pointer entries are found on the device: the call records
+    BSG_DEVERR_BAD_POINTERS and writes nothing (D stays poisoned, amax zero); a short workspace is
+    rejected on the host; the next call with good pointers on the same workspace runs clean."""
     from nvfp4_gemm_moe_gb300 import torch_ops
     import nvfp4_gemm_moe_gb300 as bsg
     k, n, vm = 256, 256, 512
@@ -246,26 +290,30 @@ def test_grouped_discrete_host_validation(lib):
     prob = torch.ones(vm, device="cuda")
     good_b = torch.tensor([t.data_ptr() for t in bs], dtype=torch.int64, device="cuda")
     good_s = torch.tensor([t.data_ptr() for t in sfbs], dtype=torch.int64, device="cuda")
-    cases = [
-        (torch.tensor([bs[0].data_ptr(), 0], dtype=torch.int64, device="cuda"), good_s, None, 1),
-        (good_b, torch.tensor([0, sfbs[1].data_ptr()], dtype=torch.int64, device="cuda"), None, 1),
-        (torch.tensor([bs[0].data_ptr() + 8, bs[1].data_ptr()], dtype=torch.int64, device="cuda"), good_s, None, 3),
-        (good_b, torch.tensor([sfbs[0].data_ptr(), sfbs[1].data_ptr() + 4], dtype=torch.int64, device="cuda"),
-         None, 3),
-        (good_b, good_s, bsg.bsg_workspace_size(), 8),
+    bad_cases = [
+        (torch.tensor([bs[0].data_ptr(), 0], dtype=torch.int64, device="cuda"), good_s),
+        (good_b, torch.tensor([0, sfbs[1].data_ptr()], dtype=torch.int64, device="cuda")),
+        (torch.tensor([bs[0].data_ptr() + 8, bs[1].data_ptr()], dtype=torch.int64, device="cuda"), good_s),
+        (good_b, torch.tensor([sfbs[0].data_ptr(), sfbs[1].data_ptr() + 4], dtype=torch.int64, device="cuda")),
     ]
-    for bp, sp, ws_bytes, status in cases:
-        ws = torch.zeros(bsg.bsg_grouped_discrete_workspace_size(2), dtype=torch.uint8, device="cuda")
-        out = {"d": torch.empty((vm, n), dtype=torch.bfloat16, device="cuda"),
-               "amax": torch.empty(2, device="cuda"), "c": None}
-        with pytest.raises(bsg.BsgError) as ei:
-            bsg.bsg_grouped_gemm_srelu_discrete(qa, bp, sfa, sp, bsg.E4M3, bsg.SF_UE8M0, 32, vm, n, k, 2, offs, ones,
-                                                prob, None, None, None, bsg.BF16, out["d"], None, bsg.BF16, None,
-                                                None, out["amax"], ws, workspace_bytes=ws_bytes)
-        assert ei.value.status == status, (status, ei.value.status)
-    # the good pointers run and give zeros
-    out = torch_ops.grouped_gemm_srelu_discrete(qa, good_b, sfa, good_s, "mxfp8", offs, ones, prob, n, k)
+    ws = torch.zeros(bsg.bsg_grouped_discrete_workspace_size(2), dtype=torch.uint8, device="cuda")
+    for bp, sp in bad_cases:
+        out = {"d": torch.full((vm, n), float("nan"), dtype=torch.bfloat16, device="cuda"),
+               "amax": torch.full((2,), -1.0, device="cuda"), "c": None}
+        bsg.bsg_grouped_gemm_srelu_discrete(qa, bp, sfa, sp, bsg.E4M3, bsg.SF_UE8M0, 32, vm, n, k, 2, offs, ones,
+                                            prob, None, None, None, bsg.BF16, out["d"], None, bsg.BF16, None,
+                                            None, out["amax"], ws)
+        assert bsg.bsg_read_device_error(ws) == bsg.DEVERR_BAD_POINTERS
+        assert torch.isnan(out["d"].float()).all() and torch.equal(out["amax"].cpu(), torch.zeros(2))
+    with pytest.raises(bsg.BsgError) as ei:
+        bsg.bsg_grouped_gemm_srelu_discrete(qa, good_b, sfa, good_s, bsg.E4M3, bsg.SF_UE8M0, 32, vm, n, k, 2, offs,
+                                            ones, prob, None, None, None, bsg.BF16, out["d"], None, bsg.BF16, None,
+                                            None, out["amax"], ws, workspace_bytes=bsg.bsg_workspace_size())
+    assert ei.value.status == 8
+    # the good pointers run on the same workspace and give zeros, with no device error
+    out = torch_ops.grouped_gemm_srelu_discrete(qa, good_b, sfa, good_s, "mxfp8", offs, ones, prob, n, k, workspace=ws)
     torch.cuda.synchronize()
+    assert bsg.bsg_read_device_error(ws) == 0
     assert float(out["d"].float().abs().max()) == 0.0
 
 
