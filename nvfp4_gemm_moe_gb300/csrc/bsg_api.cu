@@ -108,6 +108,7 @@ bool make_operand_map_mn(CUtensorMap* m, const void* base, uint64_t n, uint64_t 
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -488,6 +489,10 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   p.sfd_row_kt = static_cast<int>(cdiv(n, 128));
   p.sfd_col_mt = static_cast<int>(cdiv(n, 128));
   p.sfd_col_kt = static_cast<int>(cdiv(valid_m, 128));
+  // whole-sector row stores of C only beside the E4M3-D epilogue, which overlaps the next tile's
+  // MMAs (measured 1.2-1.5 % faster there; the exposed bf16-D epilogue was 2.6 % slower with them)
+  p.c_v8 = fp8_d && c_kind == bsg::kOutBF16 && aligned32(c) && n % 16 == 0;
+  p.d_v8 = fp8_d && aligned32(d) && aligned32(d_col);
   p.err = static_cast<uint32_t*>(workspace);
   p.epoch = epoch;
 
@@ -653,6 +658,7 @@ bsg_status bsg_grouped_gemm_dswiglu(const void* a, const void* b, const uint8_t*
   p.norm_const = norm_const;
   p.d = d_row;
   p.d_col = d_col;
+  p.d_v8 = fp8_d && aligned32(d_row) && aligned32(d_col);
   p.sfd_row = sfd_row;
   p.sfd_col = sfd_col;
   p.sfd_row_kt = static_cast<int>(cdiv(n_d, 128));
@@ -760,6 +766,7 @@ bsg_status bsg_gemm_rope_mxfp8(const uint8_t* x, const uint8_t* x_scale, const u
   p.c_kind = bsg::kOutNone;
   p.d = out_fp8_row;
   p.d_col = out_fp8_col;
+  p.d_v8 = aligned32(out_fp8_row) && aligned32(out_fp8_col);
   p.sfd_row = out_scales_row;
   p.sfd_col = out_scales_col;
   p.rope_cos = static_cast<const uint16_t*>(cos);
@@ -826,6 +833,7 @@ bsg_status bsg_gemm_rope_bf16(const void* x, const void* w, const void* cos, con
   p.c_kind = bsg::kOutNone;
   p.d = out_fp8_row;
   p.d_col = out_fp8_col;
+  p.d_v8 = aligned32(out_fp8_row) && aligned32(out_fp8_col);
   p.sfd_row = out_scales_row;
   p.sfd_col = out_scales_col;
   p.rope_cos = static_cast<const uint16_t*>(cos);

@@ -428,8 +428,11 @@ __device__ __forceinline__ void store_e4m3_block(const GemmParams& p, int row, i
     const uint32_t hi = cvt_e4m3x2(__fmul_rn(d[4 * j + 2], inv_r), __fmul_rn(d[4 * j + 3], inv_r));
     q[j] = lo | (hi << 16);
   }
-  store_rows32(s_blk, p.d, static_cast<uint64_t>(n_d), row0, dcol0, make_uint4(q[0], q[1], q[2], q[3]),
-               make_uint4(q[4], q[5], q[6], q[7]), lane);
+  if (p.d_v8)  // this thread's 32 codes are one whole sector of its row
+    st_global_v8(static_cast<uint8_t*>(p.d) + static_cast<uint64_t>(row) * n_d + dcol0, q);
+  else
+    store_rows32(s_blk, p.d, static_cast<uint64_t>(n_d), row0, dcol0, make_uint4(q[0], q[1], q[2], q[3]),
+                 make_uint4(q[4], q[5], q[6], q[7]), lane);
   // one byte per block: a tile need not start on a four-block word of the SF layout; the row's
   // last block also zeroes the padding blocks of its word
   if constexpr (kPlainScales) {
@@ -462,8 +465,11 @@ __device__ __forceinline__ void store_e4m3_block(const GemmParams& p, int row, i
     q[j] = lo | (hi << 16);
   }
   __syncwarp();  // the next block overwrites s_inv
-  store_rows32(s_blk, p.d_col, static_cast<uint64_t>(n_d), row0, dcol0, make_uint4(q[0], q[1], q[2], q[3]),
-               make_uint4(q[4], q[5], q[6], q[7]), lane);
+  if (p.d_v8)
+    st_global_v8(static_cast<uint8_t*>(p.d_col) + static_cast<uint64_t>(row) * n_d + dcol0, q);
+  else
+    store_rows32(s_blk, p.d_col, static_cast<uint64_t>(n_d), row0, dcol0, make_uint4(q[0], q[1], q[2], q[3]),
+                 make_uint4(q[4], q[5], q[6], q[7]), lane);
 }
 
 // Decodes 16-byte units of `kind` (bf16, f16, f32 or E4M3 values) into fp32 v[first ..].
@@ -835,10 +841,23 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
       // a chunk may run past N: 16-byte granules (N % 8 == 0 for 16-bit outputs, % 4 for fp32)
       // C and float D pass through the warp's transpose block (coalesced, whole-sector stores)
       if (p.c_kind != kOutNone) {
-        float cvals[32];
+        if (p.c_v8 && col0 + 32 <= p.n) {
+          // bf16 C: this thread's 32 values are two whole sectors of its row
+          uint32_t w0[8], w1[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) cvals[j] = __uint_as_float(r[j]);
-        store_block_coalesced(s_blk, p.c, p.c_kind, p.n, p.n, row - lane, col0, cvals, lane);
+          for (int j = 0; j < 8; ++j) {
+            w0[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            w1[j] = pack_bf16x2(__uint_as_float(r[16 + 2 * j]), __uint_as_float(r[16 + 2 * j + 1]));
+          }
+          uint16_t* crow = reinterpret_cast<uint16_t*>(p.c) + static_cast<uint64_t>(row) * p.n + col0;
+          st_global_v8(crow, w0);
+          st_global_v8(crow + 16, w1);
+        } else {
+          float cvals[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) cvals[j] = __uint_as_float(r[j]);
+          store_block_coalesced(s_blk, p.c, p.c_kind, p.n, p.n, row - lane, col0, cvals, lane);
+        }
       }
       if (EPI == kEpiGroupedBF16) {
         // columns past N hold zeros (zero-filled B rows), so they cannot raise the maximum

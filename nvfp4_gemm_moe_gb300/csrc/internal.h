@@ -86,6 +86,11 @@ struct GemmParams {
   const uint16_t* rope_cos;
   const uint16_t* rope_sin;
   int qk_rope;
+  // the rows of C (c_v8) or of D and D_col (d_v8) are written as whole 32-byte sectors, one
+  // 256-bit store per thread and row, instead of through the transpose block (addresses and row
+  // pitch 32-byte aligned)
+  int c_v8;
+  int d_v8;
   // device error record (workspace) and this call's epoch (see ErrSink)
   uint32_t* err;
   uint32_t epoch;
