@@ -7,9 +7,10 @@
 //              128-byte swizzle via cp.async.bulk.tensor, and the scale-factor atoms via
 //              cp.async.bulk, into a STAGES-deep shared-memory ring (full/empty mbarriers); with
 //              per-expert weights, expert g's B tensor map is read from global memory;
-//   warp 1     TMEM owner and MMA issuer: one thread issues the stage's four block-scaled
+//   warp 1     TMEM owner and MMA issuer: the warp issues the stage's four block-scaled
 //              tcgen05.mma (kind::mxf8f6f4 scale_vec::1X for MXFP8, kind::mxf4nvf4 scale_vec::4X
-//              for NVFP4) into an fp32 accumulator in TMEM, then tcgen05.commit frees the stage;
+//              for NVFP4) into an fp32 accumulator in TMEM, then tcgen05.commit frees the stage
+//              (one lane per instruction, chosen by elect.sync, with no branch around the issue);
 //   warps 2-9  epilogue: two warps per 32-lane quadrant of TMEM (= 32 rows of the tile), each
 //              taking its share of the 32-column chunks, read with tcgen05.ld, and applying the
 //              dense (C + amax), grouped sReLU (alpha, C, sReLU / tanh clamp, D, per-expert amax
@@ -875,7 +876,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
   }
 }
 
-// NM block-scaled MMAs of one stage into d_tmem, issued by one thread; the stage's scale factors
+// NM block-scaled MMAs of one stage into d_tmem, issued by the whole warp (one elected lane per
+// instruction); the stage's scale factors
 // are in TMEM at sfa_t / sfb_t.  MXFP8 stages hold one scale column per row (four K blocks, one
 // per MMA, selected by the instruction descriptor's scale-factor id); NVFP4 stages hold one
 // column of four UE4M3 scales per row and MMA.  The first MMA accumulates iff acc0.
@@ -890,12 +892,12 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uin
     const uint32_t accumulate = j > 0 ? 1u : acc0;
     // advance the start address by 32 bytes of K per MMA (encoded >> 4)
     if (FMT == kBF16) {
-      tc_mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
+      warp_mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
     } else if (FMT == kMXFP8) {
-      tc_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + b_step * j, T::kIdesc | (b_mn << 16) | (j << 29) | (j << 4),
+      warp_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + b_step * j, T::kIdesc | (b_mn << 16) | (j << 29) | (j << 4),
                       sfa_t, sfb_t, accumulate);
     } else {
-      tc_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4, sfb_t + j * T::kSfbColsPerMma,
+      warp_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4, sfb_t + j * T::kSfbColsPerMma,
                       accumulate);
     }
   }
@@ -1064,11 +1066,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && !bad) {
+    // The whole warp runs the loop and executes every copy, which elect.sync predicates to one
+    // lane (warp_* helpers); wait outcomes are made warp-uniform before they steer it.
+    if (!bad) {
       uint32_t stage = 0, phase = 0;
       uint64_t issued = 0;
       bool ok = true;
-      int fenced_l = -1;  // expert whose global tensor map this thread has acquired
+      int fenced_l = -1;  // expert whose global tensor map the warp has acquired
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
         const int a_batch = epi_is_grouped(EPI) ? 0 : tc.l;
@@ -1080,30 +1084,34 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             p.sfb_ptrs ? reinterpret_cast<const uint8_t*>(p.sfb_ptrs[tc.l])
                        : p.sfb + static_cast<uint64_t>(tc.l) * p.sfb_mt * p.sf_kt * 512;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, es)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, wait_bounded(&empty[stage], phase ^ 1u, abort_flag, es))) {
+            ok = false;
+            break;
+          }
           const int k_left = p.k - kt * T::kElemsPerKTile;
           const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
           const int atoms = FMT == kMXFP8 ? 1 : FMT == kNVFP4 ? n_mma : 0;
           const uint32_t sf_bytes = static_cast<uint32_t>(atoms * 512 * (1 + T::kBRowGroups));
-          mbar_arrive_expect_tx(&full[stage], T::kABytes + T::kBBytes + sf_bytes);
-          tma_load_3d(s_a + stage * T::kABytes, &tmap_a, &full[stage], kt * kTileKBytes, tc.mt * kTileM, a_batch);
+          warp_arrive_expect_tx(&full[stage], T::kABytes + T::kBBytes + sf_bytes);
+          warp_tma_load_3d(s_a + stage * T::kABytes, &tmap_a, &full[stage], kt * kTileKBytes, tc.mt * kTileM, a_batch);
           if (FMT == kMXFP8 && BN == 128 && p.b_mn_major)  // N-major B: 128 bytes of N x 128 rows of K
-            tma_load_3d(s_b + stage * T::kBBytes, bmap, &full[stage], tc.nt * BN, kt * T::kElemsPerKTile, b_batch);
+            warp_tma_load_3d(s_b + stage * T::kBBytes, bmap, &full[stage], tc.nt * BN, kt * T::kElemsPerKTile,
+                             b_batch);
           else
-            tma_load_3d(s_b + stage * T::kBBytes, bmap, &full[stage], kt * kTileKBytes, tc.nt * BN, b_batch);
+            warp_tma_load_3d(s_b + stage * T::kBBytes, bmap, &full[stage], kt * kTileKBytes, tc.nt * BN, b_batch);
           if constexpr (FMT != kBF16) {
             const uint8_t* sfa_src =
                 p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + tc.mt) * p.sf_kt +
                          static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
-            bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, &full[stage]);
+            warp_bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, &full[stage]);
 #pragma unroll
             for (int i = 0; i < T::kBRowGroups; ++i) {
               // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
               const int rb = min((tc.nt * BN) / 128 + i, p.sfb_mt - 1);
               const uint8_t* sfb_src = sfb_base + (static_cast<uint64_t>(rb) * p.sf_kt +
                                                    static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
-              bulk_load(s_sfb + stage * T::kSfbBytes + i * T::kAtomsPerStage * 512, sfb_src, atoms * 512,
-                        &full[stage]);
+              warp_bulk_load(s_sfb + stage * T::kSfbBytes + i * T::kAtomsPerStage * 512, sfb_src, atoms * 512,
+                             &full[stage]);
             }
           }
           ++issued;
@@ -1128,17 +1136,22 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       const uint32_t b_mn = (FMT == kMXFP8 && BN == 128 && p.b_mn_major) ? 1u : 0u;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es)) { ok = false; break; }
+        // outcomes of waits are made warp-uniform before they steer the warp-collective issue
+        if (!__all_sync(0xffffffffu, wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          // Control flow and every tcgen05 operand stay warp-uniform: the operands are computed
-          // by the whole warp and only the issue is confined to one lane, and a failed wait
-          // (timeout or abort) is recorded rather than acted on until the tile ends, so the
-          // k-loop has no data-dependent exit.  Otherwise the operands are not provably uniform
-          // and every tcgen05 instruction costs tens of cycles of extra issue work.  Issuing
-          // after a failed wait reads stale shared memory, which is harmless: the results are
-          // discarded with the error.
+          // Control flow and every tcgen05 operand stay warp-uniform: the whole warp computes
+          // the operands and executes each MMA and commit, which elect.sync predicates to one
+          // lane (no branch around the issue), and a failed wait (timeout or abort) is recorded
+          // rather than acted on until the tile ends, so the k-loop has no data-dependent exit.
+          // Issued from inside a one-lane branch, each MMA costs the issuing thread about as long
+          // as the MMA itself runs and the per-stage bookkeeping leaves the tensor pipe idle.
+          // Issuing after a failed wait reads stale shared memory, which is harmless: the
+          // results are discarded with the error.
           // the stagers arrive after the stage's data landed and its scale factors are in TMEM
           // bf16 stages carry no scale factors: their data landing (full) is all the MMAs need
           ok &= wait_bounded(FMT == kBF16 ? &full[stage] : &sf_ready[stage], phase, abort_flag, es);
@@ -1151,33 +1164,30 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
           const uint32_t acc0 = kt > 0 ? 1u : 0u;  // the first MMA of a tile overwrites the accumulator
           const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
-          if (lane == 0) {
-            if (n_mma == T::kMmasPerStage) {
-              issue_stage<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-            } else {
-              // the last, partial K stage (K not a multiple of the stage depth)
-              if (n_mma == 1) issue_stage<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-              if (n_mma == 2) issue_stage<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-              if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-            }
-            tc_commit(&empty[stage]);
-            if (T::kSfRing) tc_commit(&sf_free[fslot]);
-          }
           __syncwarp();
+          if (n_mma == T::kMmasPerStage) {
+            issue_stage<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+          } else {
+            // the last, partial K stage (K not a multiple of the stage depth)
+            if (n_mma == 1) issue_stage<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+            if (n_mma == 2) issue_stage<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+            if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+          }
+          warp_commit(&empty[stage]);
+          if (T::kSfRing) warp_commit(&sf_free[fslot]);
           if (++stage == S) { stage = 0; phase ^= 1u; }
           if (++fslot == T::kSfSlots) fslot = 0;
         }
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        if (lane == 0) tc_commit(&tmem_full[acc]);
-        __syncwarp();
+        warp_commit(&tmem_full[acc]);
         if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok) {
         // drain: wait for every MMA issued so far before TMEM is released
-        if (lane == 0) {
-          tc_commit(drain);
-          wait_bounded_plain(drain, 0);
-        }
+        __syncwarp();
+        warp_commit(drain);
+        if (lane == 0) wait_bounded_plain(drain, 0);
         __syncwarp();
       }
     }

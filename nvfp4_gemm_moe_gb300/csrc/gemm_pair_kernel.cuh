@@ -3,10 +3,10 @@
 // A cluster of two CTAs (two SMs) computes one 256 x BN output tile (BN = 256, or 224 / 192 with
 // two TMEM accumulators so that the epilogue overlaps the next tile's MMAs; 192 for the RoPE
 // projection, one head per CTA, with MXFP8 or bf16 operands), with any of the one-CTA kernel's
-// epilogues: each CTA holds 128 rows
-// of A and one BN/2-row half of B in shared memory, and one thread of the even CTA issues
-// tcgen05.mma.cta_group::2 with M = 256, N = BN, so each SM fetches its own A rows and half of
-// the B tile per K slice instead of all of B.  Each CTA's TMEM holds the fp32 accumulator of its
+// epilogues: each CTA holds 128 rows of A and one BN/2-row half of B in shared memory, and the
+// even CTA's MMA warp issues tcgen05.mma.cta_group::2 with M = 256, N = BN (one elected lane per
+// instruction), so each SM fetches its own A rows and half of the B tile per K slice instead of
+// all of B.  Each CTA's TMEM holds the fp32 accumulator of its
 // 128 rows and the scale factors of its A rows and of all BN B rows (its tensor core scales
 // every column of its rows).  Roles in each CTA (448 threads, as in the one-CTA kernel):
 //   warp 0      TMA producer: its A rows and B half with cta_group::2 tensor loads, which
@@ -14,7 +14,7 @@
 //               expecting the A/B bytes of both CTAs and its own scale atoms); its scale atoms
 //               with bulk copies on its own CTA's barrier (the even CTA's stage barrier, or the
 //               odd CTA's own sf_full barrier);
-//   warp 1      TMEM allocation in both CTAs; in the even CTA one thread waits until both CTAs'
+//   warp 1      TMEM allocation in both CTAs; in the even CTA the warp waits until both CTAs'
 //               scale factors are in TMEM, issues the pair MMAs and commits to the stage barriers
 //               of both CTAs (multicast) and, per tile, to both accumulator barriers;
 //   warps 2-9   epilogue on the CTA's own 128 rows (as in the one-CTA kernel), then an arrival
@@ -88,7 +88,8 @@ struct PairTraits {
                                      (static_cast<uint32_t>(kTileMPair >> 4) << 24);
 };
 
-// NM pair MMAs (M = 256) of one stage, issued by one thread of the even CTA; the scale factors
+// NM pair MMAs (M = 256) of one stage, issued by the even CTA's MMA warp (all lanes; one elected
+// lane issues each instruction); the scale factors
 // are in both CTAs' TMEM at sfa_t / sfb_t (layout as in issue_stage).
 // b_mn: B is N-major (MXFP8, 256-wide tiles: 128 N per CTA), as in issue_stage.
 template <int FMT, class T, int NM>
@@ -99,12 +100,12 @@ __device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc
   for (int j = 0; j < NM; ++j) {
     const uint32_t accumulate = j > 0 ? 1u : acc0;
     if (FMT == kBF16) {
-      tc_mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
+      warp_mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
     } else if (FMT == kMXFP8) {
-      tc_mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + b_step * j, T::kIdesc | (b_mn << 16) | (j << 29) | (j << 4),
+      warp_mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + b_step * j, T::kIdesc | (b_mn << 16) | (j << 29) | (j << 4),
                            sfa_t, sfb_t, accumulate);
     } else {
-      tc_mma_mxf4nvf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
+      warp_mma_mxf4nvf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
                            sfb_t + j * T::kSfbColsPerMma, accumulate);
     }
   }
@@ -202,11 +203,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
-    if (lane == 0 && !bad) {
+    // warp-collective, as in the one-CTA kernel
+    if (!bad) {
       uint32_t stage = 0, phase = 0;
       uint64_t issued = 0;
       bool ok = true;
-      int fenced_l = -1;  // expert whose global tensor map this thread has acquired
+      int fenced_l = -1;  // expert whose global tensor map the warp has acquired
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
         const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
@@ -222,7 +224,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
             p.sfb_ptrs ? reinterpret_cast<const uint8_t*>(p.sfb_ptrs[tc.l])
                        : p.sfb + static_cast<uint64_t>(tc.l) * p.sfb_mt * p.sf_kt * 512;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, es)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, wait_bounded(&empty[stage], phase ^ 1u, abort_flag, es))) {
+            ok = false;
+            break;
+          }
           const int k_left = p.k - kt * T::kElemsPerKTile;
           const int n_mma = min(T::kMmasPerStage, (k_left + T::kMmaK - 1) / T::kMmaK);
           const int atoms = FMT == kMXFP8 ? 1 : FMT == kNVFP4 ? n_mma : 0;
@@ -231,26 +236,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           // completed (its empty barrier is released after the MMAs that needed that phase), so
           // its A/B bytes always land in the phase the even CTA's arrival belongs to.
           uint64_t* sf_bar = leader ? &full[stage] : &sf_full[stage];
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (T::kABytes + T::kBBytes) + sf_bytes);
-          else mbar_arrive_expect_tx(&sf_full[stage], sf_bytes);
+          if (leader) warp_arrive_expect_tx(&full[stage], 2 * (T::kABytes + T::kBBytes) + sf_bytes);
+          else warp_arrive_expect_tx(&sf_full[stage], sf_bytes);
           const uint32_t fbar = full0 + stage * 8;
-          tma_load_3d_pair(s_a + stage * T::kABytes, &tmap_a, fbar, kt * kTileKBytes, a_row, a_batch);
+          warp_tma_load_3d_pair(s_a + stage * T::kABytes, &tmap_a, fbar, kt * kTileKBytes, a_row, a_batch);
           if (FMT == kMXFP8 && BN == 256 && p.b_mn_major)  // N-major B: 128 bytes of N x 128 rows of K
-            tma_load_3d_pair(s_b + stage * T::kBBytes, bmap, fbar, b_row, kt * T::kElemsPerKTile, b_batch);
+            warp_tma_load_3d_pair(s_b + stage * T::kBBytes, bmap, fbar, b_row, kt * T::kElemsPerKTile,
+                                  b_batch);
           else
-            tma_load_3d_pair(s_b + stage * T::kBBytes, bmap, fbar, kt * kTileKBytes, b_row, b_batch);
+            warp_tma_load_3d_pair(s_b + stage * T::kBBytes, bmap, fbar, kt * kTileKBytes, b_row, b_batch);
           if constexpr (FMT != kBF16) {
             const uint8_t* sfa_src =
                 p.sfa + ((static_cast<uint64_t>(a_batch) * p.sfa_mt + sfa_group) * p.sf_kt +
                          static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
-            bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, sf_bar);
+            warp_bulk_load(s_sfa + stage * T::kSfaBytes, sfa_src, atoms * 512, sf_bar);
 #pragma unroll
             for (int g = 0; g < T::kBRowGroups; ++g) {
               // a 128-row group past N reuses the last group's (finite) scales: its B rows are zero
               const int rb = min((tc.nt * BN) / 128 + g, p.sfb_mt - 1);
               const uint8_t* sfb_src = sfb_base + (static_cast<uint64_t>(rb) * p.sf_kt +
                                                    static_cast<uint64_t>(kt) * T::kAtomsPerStage) * 512;
-              bulk_load(s_sfb + stage * T::kSfbBytes + g * T::kAtomsPerStage * 512, sfb_src, atoms * 512, sf_bar);
+              warp_bulk_load(s_sfb + stage * T::kSfbBytes + g * T::kAtomsPerStage * 512, sfb_src, atoms * 512,
+                             sf_bar);
             }
           }
           ++issued;
@@ -277,7 +284,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       const uint32_t b_mn = (FMT == kMXFP8 && BN == 256 && p.b_mn_major) ? 1u : 0u;
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
-        if (!wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es)) { ok = false; break; }
+        // outcomes of waits are made warp-uniform before they steer the warp-collective issue
+        if (!__all_sync(0xffffffffu, wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
@@ -294,31 +305,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
           const uint32_t acc0 = kt > 0 ? 1u : 0u;
           const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
-          if (lane == 0) {
-            if (n_mma == T::kMmasPerStage) {
-              issue_stage_pair<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-            } else {
-              if (n_mma == 1) issue_stage_pair<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-              if (n_mma == 2) issue_stage_pair<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-              if (n_mma == 3) issue_stage_pair<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-            }
-            tc_commit_pair_multicast(&empty[stage], 0x3);
-            if (T::kSfRing) tc_commit_pair_multicast(&sf_free[fslot], 0x3);
-          }
+          // the whole (converged) warp issues; elect.sync picks the lane (warp-uniform branches only)
           __syncwarp();
+          if (n_mma == T::kMmasPerStage) {
+            issue_stage_pair<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+          } else {
+            if (n_mma == 1) issue_stage_pair<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+            if (n_mma == 2) issue_stage_pair<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+            if (n_mma == 3) issue_stage_pair<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+          }
+          warp_commit_pair_multicast(&empty[stage], 0x3);
+          if (T::kSfRing) warp_commit_pair_multicast(&sf_free[fslot], 0x3);
           if (++stage == S) { stage = 0; phase ^= 1u; }
           if (++fslot == T::kSfSlots) fslot = 0;
         }
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        if (lane == 0) tc_commit_pair_multicast(&tmem_full[acc], 0x3);
-        __syncwarp();
+        warp_commit_pair_multicast(&tmem_full[acc], 0x3);
         if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok) {
-        if (lane == 0) {
-          tc_commit_pair(drain);
-          wait_bounded_plain(drain, 0);
-        }
+        __syncwarp();
+        warp_commit_pair(drain);
+        if (lane == 0) wait_bounded_plain(drain, 0);
         __syncwarp();
       }
     }
