@@ -877,16 +877,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
 }
 
 // NM block-scaled MMAs of one stage into d_tmem, issued by the whole warp (one elected lane per
-// instruction); the stage's scale factors
-// are in TMEM at sfa_t / sfb_t.  MXFP8 stages hold one scale column per row (four K blocks, one
-// per MMA, selected by the instruction descriptor's scale-factor id); NVFP4 stages hold one
-// column of four UE4M3 scales per row and MMA.  The first MMA accumulates iff acc0.
-// b_mn: B is N-major (MXFP8 only): its K advance per MMA is 32 rows of 128 bytes (four 1024-byte
-// swizzle atoms) and bit 16 of the instruction descriptor marks B as MN-major.
+// instruction); the stage's scale factors are in TMEM at sfa_t / sfb_t.  MXFP8 stages hold one
+// scale column per row (four K blocks, one per MMA, selected by the instruction descriptor's
+// scale-factor id); NVFP4 stages hold one column of four UE4M3 scales per row and MMA.  The
+// first MMA accumulates iff acc0.  idesc and b_step (the B descriptor's advance per MMA) are
+// loop-invariant, computed once by the caller: for K-major B, T::kIdesc and 32 bytes (2 encoded);
+// for N-major B (MXFP8 only), bit 16 of the instruction descriptor set and 32 rows of 128 bytes
+// (four 1024-byte swizzle atoms, 256 encoded).
 template <int FMT, class T, int NM>
 __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa_t,
-                                            uint32_t sfb_t, uint32_t acc0, uint32_t b_mn = 0) {
-  const uint32_t b_step = b_mn ? 256u : 2u;
+                                            uint32_t sfb_t, uint32_t acc0, uint32_t idesc, uint32_t b_step) {
 #pragma unroll
   for (int j = 0; j < NM; ++j) {
     const uint32_t accumulate = j > 0 ? 1u : acc0;
@@ -894,11 +894,11 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t adesc, uin
     if (FMT == kBF16) {
       warp_mma_f16(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
     } else if (FMT == kMXFP8) {
-      warp_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + b_step * j, T::kIdesc | (b_mn << 16) | (j << 29) | (j << 4),
-                      sfa_t, sfb_t, accumulate);
+      warp_mma_mxf8f6f4(d_tmem, adesc + 2 * j, bdesc + b_step * j, idesc | (j << 29) | (j << 4), sfa_t, sfb_t,
+                        accumulate);
     } else {
-      warp_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4, sfb_t + j * T::kSfbColsPerMma,
-                      accumulate);
+      warp_mma_mxf4nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
+                        sfb_t + j * T::kSfbColsPerMma, accumulate);
     }
   }
 }
@@ -1135,6 +1135,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       const uint32_t b_mn = (FMT == kMXFP8 && BN == 128 && p.b_mn_major) ? 1u : 0u;
+      const uint32_t idesc = T::kIdesc | (b_mn << 16);
+      const uint32_t b_step = b_mn ? 256u : 2u;
+      // MMAs in the last K stage (fewer than a stage's when K is not a multiple of its depth)
+      const int last_mmas =
+          min(T::kMmasPerStage, (p.k - (p.k_tiles - 1) * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         // outcomes of waits are made warp-uniform before they steer the warp-collective issue
         if (!__all_sync(0xffffffffu, wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es))) {
@@ -1163,15 +1168,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           // 128-byte swizzle row of N per K row): 8-K-row atoms 1024 bytes apart
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
           const uint32_t acc0 = kt > 0 ? 1u : 0u;  // the first MMA of a tile overwrites the accumulator
-          const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
-          __syncwarp();
+          const int n_mma = kt == p.k_tiles - 1 ? last_mmas : T::kMmasPerStage;
+          // (elect.sync waits for the whole warp: no separate reconvergence is needed)
           if (n_mma == T::kMmasPerStage) {
-            issue_stage<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+            issue_stage<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, idesc, b_step);
           } else {
             // the last, partial K stage (K not a multiple of the stage depth)
-            if (n_mma == 1) issue_stage<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-            if (n_mma == 2) issue_stage<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-            if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+            if (n_mma == 1) issue_stage<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, idesc, b_step);
+            if (n_mma == 2) issue_stage<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, idesc, b_step);
+            if (n_mma == 3) issue_stage<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, idesc, b_step);
           }
           warp_commit(&empty[stage]);
           if (T::kSfRing) warp_commit(&sf_free[fslot]);

@@ -91,22 +91,21 @@ struct PairTraits {
 // NM pair MMAs (M = 256) of one stage, issued by the even CTA's MMA warp (all lanes; one elected
 // lane issues each instruction); the scale factors
 // are in both CTAs' TMEM at sfa_t / sfb_t (layout as in issue_stage).
-// b_mn: B is N-major (MXFP8, 256-wide tiles: 128 N per CTA), as in issue_stage.
+// idesc and b_step as in issue_stage (N-major B: MXFP8, 256-wide tiles, 128 N per CTA).
 template <int FMT, class T, int NM>
 __device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa_t,
-                                                 uint32_t sfb_t, uint32_t acc0, uint32_t b_mn = 0) {
-  const uint32_t b_step = b_mn ? 256u : 2u;
+                                                 uint32_t sfb_t, uint32_t acc0, uint32_t idesc, uint32_t b_step) {
 #pragma unroll
   for (int j = 0; j < NM; ++j) {
     const uint32_t accumulate = j > 0 ? 1u : acc0;
     if (FMT == kBF16) {
       warp_mma_f16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, accumulate);
     } else if (FMT == kMXFP8) {
-      warp_mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + b_step * j, T::kIdesc | (b_mn << 16) | (j << 29) | (j << 4),
-                           sfa_t, sfb_t, accumulate);
+      warp_mma_mxf8f6f4_pair(d_tmem, adesc + 2 * j, bdesc + b_step * j, idesc | (j << 29) | (j << 4), sfa_t,
+                             sfb_t, accumulate);
     } else {
       warp_mma_mxf4nvf4_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, T::kIdesc, sfa_t + j * 4,
-                           sfb_t + j * T::kSfbColsPerMma, accumulate);
+                             sfb_t + j * T::kSfbColsPerMma, accumulate);
     }
   }
 }
@@ -283,6 +282,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       bool ok = true;
       const uint32_t a_base = smem_u32(s_a), b_base = smem_u32(s_b);
       const uint32_t b_mn = (FMT == kMXFP8 && BN == 256 && p.b_mn_major) ? 1u : 0u;
+      const uint32_t idesc = T::kIdesc | (b_mn << 16);
+      const uint32_t b_step = b_mn ? 256u : 2u;
+      const int last_mmas =
+          min(T::kMmasPerStage, (p.k - (p.k_tiles - 1) * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
         // outcomes of waits are made warp-uniform before they steer the warp-collective issue
         if (!__all_sync(0xffffffffu, wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, es))) {
@@ -304,15 +307,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
           const uint64_t adesc = smem_desc(a_base + stage * T::kABytes, 16, 1024, kSwizzle128B);
           const uint64_t bdesc = smem_desc(b_base + stage * T::kBBytes, 16, 1024, kSwizzle128B);
           const uint32_t acc0 = kt > 0 ? 1u : 0u;
-          const int n_mma = min(T::kMmasPerStage, (p.k - kt * T::kElemsPerKTile + T::kMmaK - 1) / T::kMmaK);
-          // the whole (converged) warp issues; elect.sync picks the lane (warp-uniform branches only)
-          __syncwarp();
+          const int n_mma = kt == p.k_tiles - 1 ? last_mmas : T::kMmasPerStage;
+          // the whole warp issues; elect.sync picks the lane (warp-uniform branches only)
           if (n_mma == T::kMmasPerStage) {
-            issue_stage_pair<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+            issue_stage_pair<FMT, T, T::kMmasPerStage>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, idesc, b_step);
           } else {
-            if (n_mma == 1) issue_stage_pair<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-            if (n_mma == 2) issue_stage_pair<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
-            if (n_mma == 3) issue_stage_pair<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, b_mn);
+            if (n_mma == 1) issue_stage_pair<FMT, T, 1>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, idesc, b_step);
+            if (n_mma == 2) issue_stage_pair<FMT, T, 2>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, idesc, b_step);
+            if (n_mma == 3) issue_stage_pair<FMT, T, 3>(d_tmem, adesc, bdesc, sfa_t, sfb_t, acc0, idesc, b_step);
           }
           warp_commit_pair_multicast(&empty[stage], 0x3);
           if (T::kSfRing) warp_commit_pair_multicast(&sf_free[fslot], 0x3);
