@@ -107,6 +107,20 @@ bool make_operand_map_mn(CUtensorMap* m, const void* base, uint64_t n, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major bf16 output (rows x cols, cols % 8 == 0) stored by the grouped epilogue as 32 x 32
+// boxes (64 bytes of a row each) from shared-memory blocks in the 64-byte swizzled layout.
+bool make_output_map_bf16(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
@@ -495,9 +509,20 @@ bsg_status grouped_impl(const void* a, const void* b, const int64_t* b_ptrs, con
   p.d_v8 = fp8_d && aligned32(d) && aligned32(d_col);
   p.err = static_cast<uint32_t*>(workspace);
   p.epoch = epoch;
+  // bf16 D (and bf16 or no C) on 256-wide CTA pairs: the epilogue stores its 32 x 32 blocks with
+  // TMA (row pitch a multiple of 16 bytes; the maps clip the blocks at valid_m rows and N columns)
+  CUtensorMap tcm, tdm;
+  p.out_tma = pairs && bn == 256 && d_kind == bsg::kOutBF16 && (c_kind == bsg::kOutNone || c_kind == bsg::kOutBF16) &&
+              n % 8 == 0 && aligned16(d) && (c_kind == bsg::kOutNone || aligned16(c));
+  if (p.out_tma) {
+    if (!make_output_map_bf16(&tdm, d, n, valid_m)) return BSG_ERR_CUDA;
+    tcm = tdm;  // not read without C
+    if (c_kind == bsg::kOutBF16 && !make_output_map_bf16(&tcm, c, n, valid_m)) return BSG_ERR_CUDA;
+  }
 
   GemmConfig cfg{fmt, bn, fp8_d ? bsg::kEpiGroupedFP8 : bsg::kEpiGroupedBF16};
-  cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s)
+  cudaError_t e = pairs ? bsg::launch_gemm_pair(cfg, ta, tb, p, max_pairs(tiles, info.num_sms, opts), s,
+                                                p.out_tma ? &tcm : nullptr, p.out_tma ? &tdm : nullptr)
                         : bsg::launch_gemm_grouped(cfg, ta, tb, p, grid_size(tiles, info.num_sms, opts), s);
   if (e == cudaErrorInvalidValue) return BSG_ERR_UNSUPPORTED;
   return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA;

@@ -876,6 +876,68 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
   }
 }
 
+// Grouped sReLU epilogue with bf16 D and bf16 or no C, stored by TMA: for each of this warp's
+// 32-column chunks the fp32 accumulator is read from TMEM, C = alpha * acc and D are computed as
+// in epilogue_tile, and this thread's row of each 32 x 32 bf16 block is written into the warp's
+// staging blocks s_c / s_d (64 bytes per row, 16-byte granule g at granule g ^ ((row / 2) % 4):
+// the 64-byte swizzle of the tensor maps); then one elected lane stores both blocks with
+// cp.async.bulk.tensor (rows past M and columns past N are clipped by the maps).  The next chunk
+// rewrites the blocks once those stores have read them.  `release` (the accumulator-empty
+// arrival) runs as soon as the warp's last chunk has been read from TMEM, so the accumulator is
+// held neither while the last chunk is staged nor while any block travels to global memory.
+template <int BN, class Release>
+__device__ __forceinline__ void epilogue_tile_grouped_tma(const GemmParams& p, int row, int col_base,
+                                                          uint32_t tmem_acc, int lane, float alpha_g, float prob_r,
+                                                          float& run_max, int c_first, int c_step, uint8_t* s_c,
+                                                          uint8_t* s_d, const CUtensorMap* tmap_c,
+                                                          const CUtensorMap* tmap_d, Release release) {
+  const float s_clamp = p.clamp_s;
+  const float inv_s = s_clamp > 0.0f ? 1.0f / s_clamp : 0.0f;
+  const int row0 = row - lane;
+  const bool with_c = p.c_kind != kOutNone;
+  const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+  bool released = false;
+#pragma unroll 1
+  for (int c = c_first; c < BN / 32; c += c_step) {
+    const int col0 = col_base + c * 32;
+    if (col0 >= p.n) break;  // warp-uniform
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tmem_acc + c * 32, r);
+    tmem_ld_wait(r);
+    if (c + c_step >= BN / 32 || col0 + c_step * 32 >= p.n) {  // this warp's last chunk is in registers
+      release();
+      released = true;
+    }
+    uint32_t cw[16], dw[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float c0 = alpha_g * __uint_as_float(r[2 * j]);
+      const float c1 = alpha_g * __uint_as_float(r[2 * j + 1]);
+      const float d0 = srelu_clamp(c0, prob_r, s_clamp, inv_s, p.tanh_approx);
+      const float d1 = srelu_clamp(c1, prob_r, s_clamp, inv_s, p.tanh_approx);
+      // columns past N hold zeros (zero-filled B rows), so they cannot raise the maximum
+      run_max = fmaxf(run_max, fmaxf(fabsf(d0), fabsf(d1)));
+      cw[j] = pack_bf16x2(c0, c1);
+      dw[j] = pack_bf16x2(d0, d1);
+    }
+    // the previous chunk's stores have read the staging blocks
+    warp_bulk_wait_all<true>();
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t off = static_cast<uint32_t>(lane) * 64u + ((static_cast<uint32_t>(g) ^ sw) << 4);
+      if (with_c)
+        *reinterpret_cast<uint4*>(s_c + off) = make_uint4(cw[4 * g], cw[4 * g + 1], cw[4 * g + 2], cw[4 * g + 3]);
+      *reinterpret_cast<uint4*>(s_d + off) = make_uint4(dw[4 * g], dw[4 * g + 1], dw[4 * g + 2], dw[4 * g + 3]);
+    }
+    fence_async_shared();
+    __syncwarp();
+    if (with_c) warp_tma_store_2d(tmap_c, s_c, col0, row0);
+    warp_tma_store_2d(tmap_d, s_d, col0, row0);
+    warp_bulk_commit();
+  }
+  if (!released) release();
+}
+
 // NM block-scaled MMAs of one stage into d_tmem, issued by the whole warp (one elected lane per
 // instruction); the stage's scale factors are in TMEM at sfa_t / sfb_t.  MXFP8 stages hold one
 // scale column per row (four K blocks, one per MMA, selected by the instruction descriptor's

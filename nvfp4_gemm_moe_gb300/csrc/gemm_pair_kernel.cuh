@@ -63,8 +63,11 @@ struct PairTraits {
   static constexpr int kBarBytes = 1024;
   static constexpr int kOffsetsBytes = 4096;
   static constexpr int kAmaxBytes = 4096;
-  static constexpr int kXposeBlock = kXposeBlockBytes;
-  static constexpr int kXposeBytes = 8 * kXposeBlock;  // one transpose block per epilogue warp
+  // one transpose block per epilogue warp; the grouped bf16-D epilogue on 256-wide tiles stages
+  // a C and a D block per warp for its TMA stores
+  static constexpr bool kOutTma = EPI == kEpiGroupedBF16 && BN == 256;
+  static constexpr int kXposeBlock = kOutTma ? 2 * kXposeBlockBytes : kXposeBlockBytes;
+  static constexpr int kXposeBytes = 8 * kXposeBlock;
   // shared-memory ring: as many stages as fit, at most six
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
@@ -113,6 +116,7 @@ __device__ __forceinline__ void issue_stage_pair(uint32_t d_tmem, uint64_t adesc
 template <int FMT, int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_d,
                      const __grid_constant__ GemmParams p) {
   using T = PairTraits<FMT, BN, EPI>;
   constexpr int S = T::kStages;
@@ -187,6 +191,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
+    if (T::kOutTma && p.out_tma) {
+      prefetch_tmap(&tmap_c);
+      prefetch_tmap(&tmap_d);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -378,7 +386,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
       const int row = tc.mt * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
       if constexpr (epi_is_dswiglu(EPI)) prefetch_dswiglu_c<BN>(p, row, tc.nt * BN, half, 2);
-      if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, es)) break;
+      // warp-uniform outcome: the epilogues use whole-warp shuffles, syncs and elected copies
+      if (!__all_sync(0xffffffffu, wait_bounded(&tmem_full[acc], acc_phase, abort_flag, es))) break;
       tc_fence_after();
       float alpha_g = 1.0f, prob_r = 0.0f;
       if (epi_is_grouped(EPI)) {
@@ -411,6 +420,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
         epilogue_dense_bf16_early<BN, true>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release,
                                             s_xpose + (warp - 2) * T::kXposeBlock, lane);
+      } else if (T::kOutTma && p.out_tma) {
+        uint8_t* blk = s_xpose + (warp - 2) * T::kXposeBlock;
+        epilogue_tile_grouped_tma<BN>(p, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, run_max, half, 2, blk,
+                                      blk + kXposeBlockBytes, &tmap_c, &tmap_d, release);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
                                s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * T::kXposeBlock);
@@ -418,6 +431,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       }
       if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
     }
+    // the TMA stores have completed (their staging blocks are freed with the CTA)
+    if (T::kOutTma && p.out_tma) warp_bulk_wait_all<false>();
     // fold this warp's running maxima into shared memory
     if (EPI == kEpiDense) {
       float v = run_max;
@@ -457,7 +472,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
 // so fewer than #SMs / 2 pairs may fit); `max_pairs` is the caller's upper bound.
 template <int FMT, int BN, int EPI>
 cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int max_pairs,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const CUtensorMap* tc = nullptr,
+                               const CUtensorMap* td = nullptr) {
   using T = PairTraits<FMT, BN, EPI>;
   auto kern = gemm_pair_kernel<FMT, BN, EPI>;
   static std::atomic<int> resident_pairs[64];  // per device; 0 = not queried yet
@@ -481,7 +497,8 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
   }
   int pairs = max_pairs < resident ? max_pairs : resident;
   if (pairs < 1) pairs = 1;
-  kern<<<2 * pairs, kThreadsGemm, T::kSmemBytes, stream>>>(ta, tb, p);
+  // output maps only for the TMA-store epilogue; otherwise the kernel never reads them
+  kern<<<2 * pairs, kThreadsGemm, T::kSmemBytes, stream>>>(ta, tb, tc ? *tc : ta, td ? *td : ta, p);
   return cudaGetLastError();
 }
 

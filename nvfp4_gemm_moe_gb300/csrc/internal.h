@@ -91,6 +91,10 @@ struct GemmParams {
   // pitch 32-byte aligned)
   int c_v8;
   int d_v8;
+  // grouped bf16 D (and bf16 or no C) on 256-wide CTA pairs: the epilogue stages each 32 x 32
+  // block of C and D in shared memory and stores it with a TMA tensor store (the output tensor
+  // maps are kernel parameters) instead of per-thread global stores
+  int out_tma;
   // device error record (workspace) and this call's epoch (see ErrSink)
   uint32_t* err;
   uint32_t epoch;
@@ -111,9 +115,11 @@ cudaError_t launch_gemm_grouped(const GemmConfig& cfg, const CUtensorMap& tmap_a
                                 const GemmParams& p, int grid, cudaStream_t stream);
 
 // Launches the CTA-pair kernel (256 x 256 tiles on clusters of two CTAs) with at most
-// `max_pairs` clusters.
+// `max_pairs` clusters.  tmap_c / tmap_d: the output tensor maps when p.out_tma is set (else
+// unused and may be null).
 cudaError_t launch_gemm_pair(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                             const GemmParams& p, int max_pairs, cudaStream_t stream);
+                             const GemmParams& p, int max_pairs, cudaStream_t stream,
+                             const CUtensorMap* tmap_c = nullptr, const CUtensorMap* tmap_d = nullptr);
 
 // The dSwiGLU backward epilogue kernels (one-CTA and CTA-pair tiles).
 cudaError_t launch_gemm_dswiglu(const GemmConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,

@@ -91,6 +91,54 @@ __device__ __forceinline__ void warp_tma_load_3d(void* dst, const CUtensorMap* t
       : "memory");
 }
 
+// 2-D tiled store shared -> global of the box at (c0, c1) (elements past the tensor's extent are
+// not written), tracked in the elected lane's bulk async-group; warp-collective.
+__device__ __forceinline__ void warp_tma_store_2d(const CUtensorMap* tm, const void* src, int c0, int c1) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n\t"
+      "}\n" ::"l"(reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Closes the elected lane's current bulk async-group (warp-collective).
+__device__ __forceinline__ void warp_bulk_commit() {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.commit_group;\n\t"
+      "}\n" ::
+          : "memory");
+}
+
+// Waits until the elected lane's bulk stores have read their shared-memory sources (kRead) or
+// have completed; then the warp's staging buffers may be rewritten (warp-collective).
+template <bool kRead>
+__device__ __forceinline__ void warp_bulk_wait_all() {
+  if constexpr (kRead)
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.wait_group.read 0;\n\t"
+        "}\n" ::
+            : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.wait_group 0;\n\t"
+        "}\n" ::
+            : "memory");
+  __syncwarp();
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 32-byte store (one whole sector) of eight words; dst 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&q)[8]) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(q[0]), "r"(q[1]), "r"(q[2]),

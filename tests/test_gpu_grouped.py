@@ -205,6 +205,9 @@ def test_grouped_bad_offsets_detected_on_device(lib):
     ("bf16", 32.0, "f32", 264, 1.0),    # ragged N
     ("e4m3", None, "bf16", 384, 1.0),
     ("e4m3", None, None, 512, 0.75),
+    # bf16 D (with bf16 or no C) on pairs: blocks stored by TMA, clipped at ragged N
+    ("bf16", None, None, 264, 1.0),
+    ("bf16", 32.0, "bf16", 520, 1.0),
 ])
 def test_grouped_cta_pairs(lib, d_dtype, clamp, c_kind, n, nc):
     run_grouped(EDGE, n, 512, d_dtype, clamp, c_kind, nc=nc, cta_pair=2, a_scale=700.0 if clamp else 1.0)
