@@ -127,16 +127,16 @@ __device__ __forceinline__ int find_expert(const int32_t* offs, int num_experts,
   return lo;
 }
 
-// Tile t -> (batch or expert, M tile of TM rows, N tile).  Dense: batch-major, then groups of 16
+// Tile t -> (batch or expert, M tile of TM rows, N tile).  Dense: batch-major, then groups of GM
 // M tiles swept along N (neighbouring CTAs share A and B in L2); grouped: M-tile-major.
-template <int EPI, int TM = kTileM>
+template <int EPI, int TM = kTileM, int GM = 16>
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t, const int32_t* offs) {
   TileCoord tc;
   if (!epi_is_grouped(EPI)) {
     const int per_batch = p.m_tiles * p.n_tiles;
     tc.l = t / per_batch;
     const int idx = t - tc.l * per_batch;
-    constexpr int kGroupM = 16;
+    constexpr int kGroupM = GM;
     const int group = idx / (kGroupM * p.n_tiles);
     const int first_m = group * kGroupM;
     const int gm = min(kGroupM, p.m_tiles - first_m);

@@ -55,6 +55,9 @@ struct PairTraits {
   static constexpr int kSfbBytes = kBRowGroups * kAtomsPerStage * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kAcc = BN == 256 ? 1 : 2;  // 224, 192: two accumulators, epilogue overlapped
+  // dense raster: groups of M tiles swept along N (measured best: 16 for MXFP8 8192-square
+  // batches, 32 for the NVFP4 16384-square GEMM, whose B panels are then read half as often)
+  static constexpr int kRasterM = FMT == kNVFP4 ? 32 : 16;
   static constexpr int kSfaCols = kAtomsPerStage * 4;
   static constexpr int kSfbCols = kSfbColsPerMma * kAtomsPerStage;
   static constexpr int kSfStride = kAtomsPerStage == 0 ? 0 : ((kSfaCols + kSfbCols + 15) / 16) * 16;
@@ -218,7 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       int fenced_l = -1;  // expert whose global tensor map the warp has acquired
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
       for (int t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
-        const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
+        const TileCoord tc = decode_tile<EPI, 256, T::kRasterM>(p, t, s_offs);
         const int a_batch = epi_is_grouped(EPI) ? 0 : tc.l;
         const int a_row = tc.mt * 256 + static_cast<int>(rank) * 128;
         const int b_row = tc.nt * BN + static_cast<int>(rank) * T::kBHalf;
@@ -349,7 +352,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     uint32_t stage = 0, phase = 0, fslot = 0, fphase = 0;
     bool ok = FMT != kBF16;  // bf16 operands have no scale factors to stage
     for (int t = pair_id; !bad && ok && t < p.num_tiles; t += num_pairs) {
-      const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
+      const TileCoord tc = decode_tile<EPI, 256, T::kRasterM>(p, t, s_offs);
       const int b_blk0 = ((tc.nt * BN) >> 5) & 3;  // the tile's first 32-row block within its first atom
       for (int kt = 0; kt < p.k_tiles; ++kt) {
         ok &= wait_bounded(&landed[stage], phase, abort_flag, es);
@@ -383,7 +386,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
     const float nc = epi_has_fp8_d(EPI) ? *p.norm_const : 1.0f;
     const uint32_t empty_leader = mapa_shared(smem_u32(&tmem_empty[0]), 0);
     for (int t = pair_id; !bad && t < p.num_tiles; t += num_pairs) {
-      const TileCoord tc = decode_tile<EPI, 256>(p, t, s_offs);
+      const TileCoord tc = decode_tile<EPI, 256, T::kRasterM>(p, t, s_offs);
       const int row = tc.mt * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
       if constexpr (epi_is_dswiglu(EPI)) prefetch_dswiglu_c<BN>(p, row, tc.nt * BN, half, 2);
       // warp-uniform outcome: the epilogues use whole-warp shuffles, syncs and elected copies
