@@ -1,11 +1,12 @@
 // quantize.cu -- fp32 or bf16 -> MXFP8 / NVFP4 block quantiser (memory-bound).
 //
-// MXFP8: a warp takes one row at a time and walks its "units": 128 consecutive fp32 values (512 bytes,
-// one float4 per lane, fully coalesced), 4 KB of loads in flight per warp.  For MXFP8 a unit is 4 blocks of 32 (8 lanes per
-// block), for NVFP4 8 blocks of 16 (4 lanes per block).  Block maxima are reduced with
-// warp shuffles, the scale bytes of 4 consecutive blocks are adjacent in the atom layout
-// and leave as one 32-bit store, the codes as one 32-bit (E4M3) or 16-bit (E2M1) store
-// per lane.  Units of the padding rows of the last 128-row atom produce zero scale bytes.
+// A warp takes one row at a time and walks its "units", with 4 KB of loads in flight per warp.
+// MXFP8: a unit is 128 consecutive values (one float4 per lane, fully coalesced), 4 blocks of 32
+// (8 lanes per block, block maxima reduced with warp shuffles), the codes leave as one 32-bit
+// store per lane.  NVFP4: a unit is 512 values and each lane owns one block of 16 (no shuffle
+// for its maximum), its codes leave as one 64-bit store.  The scale bytes of 4 consecutive
+// blocks are adjacent in the atom layout and leave as one 32-bit store.  Units of the padding
+// rows of the last 128-row atom produce zero scale bytes.
 // bf16 inputs are widened to fp32 on load (exactly), so both input types share the arithmetic;
 // their units are the same element counts at half the bytes (8- or 16-byte loads per lane).
 #include <cuda_bf16.h>
@@ -75,37 +76,20 @@ struct QuantLoads;
 template <>
 struct QuantLoads<float> {
   static constexpr int kUnitsMx = 8;  // MXFP8 units (128 values) in flight per warp: 4 KB
-  static constexpr int kUnitsNv = 4;  // NVFP4 units (256 values) in flight per warp: 4 KB
   using Raw4 = float4;
-  struct Raw8 { float4 a, b; };
   static __device__ __forceinline__ Raw4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
   static __device__ __forceinline__ float4 widen4(const Raw4& r) { return r; }
-  static __device__ __forceinline__ Raw8 load8(const float* p) {
-    return {__ldcs(reinterpret_cast<const float4*>(p)), __ldcs(reinterpret_cast<const float4*>(p + 4))};
-  }
-  static __device__ __forceinline__ void widen8(const Raw8& r, float4& a, float4& b) { a = r.a; b = r.b; }
   static __device__ __forceinline__ Raw4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
-  static __device__ __forceinline__ Raw8 zero8() { return {zero4(), zero4()}; }
 };
 template <>
 struct QuantLoads<__nv_bfloat16> {
   static constexpr int kUnitsMx = 16;
-  static constexpr int kUnitsNv = 8;
   using Raw4 = uint2;
-  using Raw8 = uint4;
   static __device__ __forceinline__ Raw4 load4(const __nv_bfloat16* p) {
     return __ldcs(reinterpret_cast<const uint2*>(p));
   }
   static __device__ __forceinline__ float4 widen4(const Raw4& r) { return bf16x4_to_float4(r.x, r.y); }
-  static __device__ __forceinline__ Raw8 load8(const __nv_bfloat16* p) {
-    return __ldcs(reinterpret_cast<const uint4*>(p));
-  }
-  static __device__ __forceinline__ void widen8(const Raw8& r, float4& a, float4& b) {
-    a = bf16x4_to_float4(r.x, r.y);
-    b = bf16x4_to_float4(r.z, r.w);
-  }
   static __device__ __forceinline__ Raw4 zero4() { return make_uint2(0u, 0u); }
-  static __device__ __forceinline__ Raw8 zero8() { return make_uint4(0u, 0u, 0u, 0u); }
 };
 
 template <typename TIn>
@@ -162,17 +146,53 @@ __global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const TIn* __r
   }
 }
 
-// NVFP4: a unit is 256 consecutive fp32 values of one row (1 KB), eight per lane (two
-// float4 loads), so a block of 16 spans two lanes and each lane's eight codes leave as one
-// 32-bit store.  The 16 scale bytes of a unit are four 32-bit words of the atom layout,
-// stored by lanes 0, 8, 16 and 24.
+// NVFP4: a unit is 512 consecutive values of one row and lane i owns its block i (16 values:
+// four float4 loads of fp32, or two 16-byte loads of bf16), so the block maximum and the scale
+// decision are made once per block with no shuffle, and the lane's 16 codes leave as one 64-bit
+// store.  The 32 scale bytes of a unit are eight 32-bit words of the atom layout, gathered from
+// lanes 4w .. 4w + 3 and stored by lane 4w.
+// One lane's block of 16 inputs: raw loads kept in flight, widened to fp32 when processed.
+template <typename TIn>
+struct Block16;
+template <>
+struct Block16<float> {
+  float4 a[4];
+  __device__ __forceinline__ void load(const float* p, bool ok) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      a[i] = ok ? __ldcs(reinterpret_cast<const float4*>(p) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __device__ __forceinline__ void widen(float (&v)[16]) const {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[4 * i] = a[i].x; v[4 * i + 1] = a[i].y; v[4 * i + 2] = a[i].z; v[4 * i + 3] = a[i].w;
+    }
+  }
+};
+template <>
+struct Block16<__nv_bfloat16> {
+  uint4 a[2];
+  __device__ __forceinline__ void load(const __nv_bfloat16* p, bool ok) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) a[i] = ok ? __ldcs(reinterpret_cast<const uint4*>(p) + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __device__ __forceinline__ void widen(float (&v)[16]) const {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float4 lo = bf16x4_to_float4(a[i].x, a[i].y), hi = bf16x4_to_float4(a[i].z, a[i].w);
+      v[8 * i] = lo.x; v[8 * i + 1] = lo.y; v[8 * i + 2] = lo.z; v[8 * i + 3] = lo.w;
+      v[8 * i + 4] = hi.x; v[8 * i + 5] = hi.y; v[8 * i + 6] = hi.z; v[8 * i + 7] = hi.w;
+    }
+  }
+};
+
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __restrict__ x, int64_t rows, int k,
                                                                   uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                                   int64_t rows_padded, int units_per_row,
                                                                   int64_t total_rows, int64_t mt_n, int64_t kt_n) {
-  using L = QuantLoads<TIn>;
-  constexpr int kU = L::kUnitsNv;
+  // units in flight per warp: 4 KB of fp32 loads (two units) or of bf16 loads (four)
+  constexpr int kU = sizeof(TIn) == 4 ? 2 : 4;
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
@@ -183,23 +203,23 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __r
     const int64_t row_g = l * rows + r;
     const TIn* xr = x + row_g * k;
     for (int kc0 = 0; kc0 < units_per_row; kc0 += kU) {
-      typename L::Raw8 raw[kU];
+      Block16<TIn> raw[kU];
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
-        const int kk = (kc0 + j) * 256 + lane * 8;
-        const bool ok = row_ok && kc0 + j < units_per_row && kk < k;
-        raw[j] = ok ? L::load8(xr + kk) : L::zero8();
+        const int kk = (kc0 + j) * 512 + lane * 16;
+        raw[j].load(xr + kk, row_ok && kc0 + j < units_per_row && kk < k);
       }
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const int kc = kc0 + j;
         if (kc >= units_per_row) break;  // uniform across the warp
-        const int kk = kc * 256 + lane * 8;
-        float4 a0, a1;  // this lane's eight values
-        L::widen8(raw[j], a0, a1);
-        float a = fmaxf(fmaxf(fmaxf(fabsf(a0.x), fabsf(a0.y)), fmaxf(fabsf(a0.z), fabsf(a0.w))),
-                        fmaxf(fmaxf(fabsf(a1.x), fabsf(a1.y)), fmaxf(fabsf(a1.z), fabsf(a1.w))));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        const int kk = kc * 512 + lane * 16;
+        float xs[16];
+        raw[j].widen(xs);
+        float m[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m[e] = fmaxf(fabsf(xs[2 * e]), fabsf(xs[2 * e + 1]));
+        const float a = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
         const uint32_t code = ue4m3_code_of_amax_over_6(a);
         const float s = ue4m3_value(code);
         // Codes from the hardware's RNE conversion, bracketing the exact quotient v = x / s:
@@ -209,53 +229,54 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __r
         // midpoint lies between them: fp32 inputs take the exact threshold path (rare); for bf16
         // inputs v is then exactly that midpoint (x has 8 significant bits, a midpoint times s
         // at most 7: x / s is a midpoint or at least 2^-9 away from one), and the tie goes to the
-        // even code of the two.  The sign bit of x is or-ed in, so a negative value that rounds
-        // to zero gives -0 as on the exact path; s = 0 gives +0.
+        // even code of the two.  The conversion keeps the sign of x, also where the magnitude
+        // rounds to zero (-0, as on the exact path); s = 0 gives +0.
         const float inv = code != 0 ? __frcp_rn(s) : 0.0f;
         const float inv_up = inv * (1.0f + 0x1p-20f), inv_dn = inv * (1.0f - 0x1p-20f);
-        const float xs[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        uint32_t up = 0, dn = 0;
+        uint32_t up[2] = {0u, 0u}, dn[2] = {0u, 0u};
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          up |= cvt_e2m1x2(xs[e] * inv_up, xs[e + 1] * inv_up) << (4 * e);
-          dn |= cvt_e2m1x2(xs[e] * inv_dn, xs[e + 1] * inv_dn) << (4 * e);
+        for (int e = 0; e < 16; e += 2) {
+          up[e >> 3] |= cvt_e2m1x2(xs[e] * inv_up, xs[e + 1] * inv_up) << (4 * (e & 7));
+          dn[e >> 3] |= cvt_e2m1x2(xs[e] * inv_dn, xs[e + 1] * inv_dn) << (4 * (e & 7));
         }
-        uint32_t nib = up;
+        uint32_t nib[2] = {up[0], up[1]};
         bool near = false;
-        if (up != dn) {
-          if constexpr (sizeof(TIn) == 2) {
-            // nibble k differs -> bit 4k of `differs`; the two codes are neighbours, and the one
-            // whose last bit (bit 4k) is clear is the even one
-            const uint32_t diff = up ^ dn;
-            const uint32_t differs = (diff | (diff >> 1) | (diff >> 2) | (diff >> 3)) & 0x11111111u;
-            const uint32_t take_dn = (differs & up) * 0xFu;  // whole nibbles where dn is even
-            nib = (up & ~take_dn) | (dn & take_dn);
-          } else {
-            near = true;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          if (up[w] != dn[w]) {
+            if constexpr (sizeof(TIn) == 2) {
+              // nibble k differs -> bit 4k of `differs`; the two codes are neighbours, and the one
+              // whose last bit (bit 4k) is clear is the even one
+              const uint32_t diff = up[w] ^ dn[w];
+              const uint32_t differs = (diff | (diff >> 1) | (diff >> 2) | (diff >> 3)) & 0x11111111u;
+              const uint32_t take_dn = (differs & up[w]) * 0xFu;  // whole nibbles where dn is even
+              nib[w] = (up[w] & ~take_dn) | (dn[w] & take_dn);
+            } else {
+              near = true;
+            }
           }
         }
         if (!__any_sync(0xffffffffu, near)) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) nib |= (__float_as_uint(xs[e]) >> 31) << (4 * e + 3);
-          if (code == 0) nib = 0;
+          if (code == 0) nib[0] = nib[1] = 0u;
         } else {
           float t[7];
           e2m1_thresholds(s, t);
-          nib = 0;
-          if (code != 0) {
-            nib = e2m1_nibble(a0.x, t) | (e2m1_nibble(a0.y, t) << 4) | (e2m1_nibble(a0.z, t) << 8) |
-                  (e2m1_nibble(a0.w, t) << 12) | (e2m1_nibble(a1.x, t) << 16) | (e2m1_nibble(a1.y, t) << 20) |
-                  (e2m1_nibble(a1.z, t) << 24) | (e2m1_nibble(a1.w, t) << 28);
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            uint32_t n = 0u;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) n |= e2m1_nibble(xs[8 * w + e], t) << (4 * e);
+            nib[w] = code != 0 ? n : 0u;
           }
         }
-        if (row_ok && kk < k) *reinterpret_cast<uint32_t*>(q + (row_g * k + kk) / 2) = nib;
-        // block b of the unit is held by lanes 2b and 2b + 1; scale word w (blocks 4w..4w+3)
-        // gathers the codes of lanes 8w, 8w + 2, 8w + 4, 8w + 6
-        const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 2);
-        const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 4);
-        const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 6);
-        if ((lane & 7) == 0) {
-          const int64_t kb = static_cast<int64_t>(kc) * 16 + (lane >> 1);
+        if (row_ok && kk < k)
+          *reinterpret_cast<uint2*>(q + (row_g * k + kk) / 2) = make_uint2(nib[0], nib[1]);
+        // block 4w + i of the unit is held by lane 4w + i; scale word w gathers lanes 4w .. 4w + 3
+        const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 1);
+        const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 2);
+        const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 3);
+        if ((lane & 3) == 0) {
+          const int64_t kb = static_cast<int64_t>(kc) * 32 + lane;
           if ((kb >> 2) < kt_n) {
             const uint64_t off = sf_offset(r, kb, l, mt_n, kt_n);
             *reinterpret_cast<uint32_t*>(sf + off) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
@@ -281,7 +302,7 @@ cudaError_t launch_quantize(int fmt, const void* x, bool x_bf16, int64_t batch, 
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
   const unsigned grid = static_cast<unsigned>(blocks);
-  const int units_nvfp4 = static_cast<int>((k + 255) / 256);
+  const int units_nvfp4 = static_cast<int>((k + 511) / 512);
   const float* xf = static_cast<const float*>(x);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (fmt == kMXFP8 && !x_bf16) {
