@@ -1,14 +1,12 @@
 // quantize.cu -- fp32 or bf16 -> MXFP8 / NVFP4 block quantiser (memory-bound).
 //
-// A warp takes one row at a time and walks its "units", with 4 KB of loads in flight per warp.
-// MXFP8: a unit is 128 consecutive values (one float4 per lane, fully coalesced), 4 blocks of 32
-// (8 lanes per block, block maxima reduced with warp shuffles), the codes leave as one 32-bit
-// store per lane.  NVFP4: a unit is 512 values and each lane owns one block of 16 (no shuffle
-// for its maximum), its codes leave as one 64-bit store.  The scale bytes of 4 consecutive
-// blocks are adjacent in the atom layout and leave as one 32-bit store.  Units of the padding
-// rows of the last 128-row atom produce zero scale bytes.
-// bf16 inputs are widened to fp32 on load (exactly), so both input types share the arithmetic;
-// their units are the same element counts at half the bytes (8- or 16-byte loads per lane).
+// A warp takes one row at a time and walks its "units" of 32 blocks (1024 values for MXFP8, 512
+// for NVFP4), with 4 KB of loads in flight per warp.  Each lane owns one block, so its maximum
+// and its scale are decided once, without shuffles.  The scale bytes of 4 consecutive blocks are
+// adjacent in the atom layout and leave as one 32-bit store.  Units of the padding rows of the
+// last 128-row atom produce zero scale bytes.
+// bf16 inputs are widened to fp32 (exactly) when a block is processed, so both input types share
+// the arithmetic; their units are the same element counts at half the bytes, two units in flight.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -71,32 +69,61 @@ __device__ __forceinline__ float4 bf16x4_to_float4(uint32_t lo, uint32_t hi) {  
   return make_float4(__uint_as_float(lo << 16), __uint_as_float(lo & 0xffff0000u), __uint_as_float(hi << 16),
                      __uint_as_float(hi & 0xffff0000u));
 }
-template <typename TIn>
-struct QuantLoads;
-template <>
-struct QuantLoads<float> {
-  static constexpr int kUnitsMx = 8;  // MXFP8 units (128 values) in flight per warp: 4 KB
-  using Raw4 = float4;
-  static __device__ __forceinline__ Raw4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-  static __device__ __forceinline__ float4 widen4(const Raw4& r) { return r; }
-  static __device__ __forceinline__ Raw4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
-};
-template <>
-struct QuantLoads<__nv_bfloat16> {
-  static constexpr int kUnitsMx = 16;
-  using Raw4 = uint2;
-  static __device__ __forceinline__ Raw4 load4(const __nv_bfloat16* p) {
-    return __ldcs(reinterpret_cast<const uint2*>(p));
+// One lane's block of N inputs (N = 16 or 32): raw 16-byte loads kept in flight, widened to fp32
+// when the block is processed.
+template <typename TIn, int N>
+struct BlockIn;
+template <int N>
+struct BlockIn<float, N> {
+  float4 a[N / 4];
+  __device__ __forceinline__ void load(const float* p, bool ok) {
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i)
+      a[i] = ok ? __ldcs(reinterpret_cast<const float4*>(p) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  static __device__ __forceinline__ float4 widen4(const Raw4& r) { return bf16x4_to_float4(r.x, r.y); }
-  static __device__ __forceinline__ Raw4 zero4() { return make_uint2(0u, 0u); }
+  __device__ __forceinline__ void widen(float (&v)[N]) const {
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      v[4 * i] = a[i].x; v[4 * i + 1] = a[i].y; v[4 * i + 2] = a[i].z; v[4 * i + 3] = a[i].w;
+    }
+  }
+};
+template <int N>
+struct BlockIn<__nv_bfloat16, N> {
+  uint4 a[N / 8];
+  __device__ __forceinline__ void load(const __nv_bfloat16* p, bool ok) {
+#pragma unroll
+    for (int i = 0; i < N / 8; ++i)
+      a[i] = ok ? __ldcs(reinterpret_cast<const uint4*>(p) + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __device__ __forceinline__ void widen(float (&v)[N]) const {
+#pragma unroll
+    for (int i = 0; i < N / 8; ++i) {
+      const float4 lo = bf16x4_to_float4(a[i].x, a[i].y), hi = bf16x4_to_float4(a[i].z, a[i].w);
+      v[8 * i] = lo.x; v[8 * i + 1] = lo.y; v[8 * i + 2] = lo.z; v[8 * i + 3] = lo.w;
+      v[8 * i + 4] = hi.x; v[8 * i + 5] = hi.y; v[8 * i + 6] = hi.z; v[8 * i + 7] = hi.w;
+    }
+  }
 };
 
+// fp32 MXFP8 loads: one float4 per lane per 128-value unit (fully coalesced), 8 units (4 KB) in
+// flight per warp.
+struct MxLoadsF32 {
+  static constexpr int kUnits = 8;
+  static __device__ __forceinline__ float4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+};
+
+// MXFP8 from fp32: a unit is 128 consecutive values (one float4 per lane, fully coalesced), four
+// blocks of 32 held by 8 lanes each (block maxima reduced with shuffles), the codes leave as one
+// 32-bit store per lane and lane 0 stores the unit's scale word.  (One block per lane, as the
+// bf16 kernel below does, measured 15 % slower from fp32: its 128-byte lane stride spreads every
+// load instruction over 32 lines.)
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const TIn* __restrict__ x, int64_t rows, int k,
-                                                            uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                            int64_t rows_padded, int units_per_row, int64_t total_rows,
-                                                            int64_t mt_n, int64_t kt_n) {
+                                                                  uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                                  int64_t rows_padded, int units_per_row,
+                                                                  int64_t total_rows, int64_t mt_n, int64_t kt_n) {
+  static_assert(sizeof(TIn) == 4, "fp32 input");
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
@@ -109,14 +136,14 @@ __global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const TIn* __r
     const bool row_ok = r < rows;
     const int64_t row_g = l * rows + r;
     const TIn* xr = x + row_g * k;
-    using L = QuantLoads<TIn>;
-    constexpr int U = L::kUnitsMx;
+    constexpr int U = MxLoadsF32::kUnits;
     for (int kc0 = 0; kc0 < units_per_row; kc0 += U) {
-      typename L::Raw4 raw[U];
+      float4 raw[U];
 #pragma unroll
       for (int j = 0; j < U; ++j) {
         const int kk = (kc0 + j) * 128 + lane * 4;
-        raw[j] = (row_ok && kc0 + j < units_per_row && kk < k) ? L::load4(xr + kk) : L::zero4();
+        raw[j] = (row_ok && kc0 + j < units_per_row && kk < k) ? MxLoadsF32::load4(xr + kk)
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < U; ++j) {
@@ -124,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const TIn* __r
         if (kc >= units_per_row) break;  // uniform across the warp
         const int kk = kc * 128 + lane * 4;
         const bool elem_ok = row_ok && kk < k;
-        const float4 vj = L::widen4(raw[j]);
+        const float4 vj = raw[j];
         float a = fmaxf(fmaxf(fabsf(vj.x), fabsf(vj.y)), fmaxf(fabsf(vj.z), fabsf(vj.w)));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
@@ -146,46 +173,84 @@ __global__ void __launch_bounds__(kThreads) quantize_mxfp8_kernel(const TIn* __r
   }
 }
 
+// MXFP8 from bf16: a unit is 1024 consecutive values of one row and lane i owns its block i (32
+// values: four 16-byte loads), so the block maximum and the scale
+// decision are made once per block with no shuffle, and the lane's 32 codes leave as two 16-byte
+// stores.  The 32 scale bytes of a unit are eight 32-bit words of the atom layout, gathered from
+// lanes 4w .. 4w + 3 and stored by lane 4w.
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads)
+    quantize_mxfp8_bf16_kernel(const TIn* __restrict__ x, int64_t rows, int k, uint8_t* __restrict__ q,
+                               uint8_t* __restrict__ sf, int64_t rows_padded, int units_per_row, int64_t total_rows,
+                               int64_t mt_n, int64_t kt_n) {
+  static_assert(sizeof(TIn) == 2, "bf16 input");
+  constexpr int kU = 2;  // units in flight per warp: 4 KB of bf16 loads
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  // one (padded) row per warp iteration: the row's batch and index are computed once, then
+  // the warp walks the row's units
+  for (int64_t rg = warp_id; rg < total_rows; rg += num_warps) {
+    const int64_t l = rg / rows_padded;
+    const int64_t r = rg - l * rows_padded;
+    const bool row_ok = r < rows;
+    const int64_t row_g = l * rows + r;
+    const TIn* xr = x + row_g * k;
+    for (int kc0 = 0; kc0 < units_per_row; kc0 += kU) {
+      BlockIn<TIn, 32> raw[kU];
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int kk = (kc0 + j) * 1024 + lane * 32;
+        raw[j].load(xr + kk, row_ok && kc0 + j < units_per_row && kk < k);
+      }
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int kc = kc0 + j;
+        if (kc >= units_per_row) break;  // uniform across the warp
+        const int kk = kc * 1024 + lane * 32;
+        float xs[32];
+        raw[j].widen(xs);
+        float m[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) m[e] = fmaxf(fabsf(xs[2 * e]), fabsf(xs[2 * e + 1]));
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+          for (int e = 0; e < w; ++e) m[e] = fmaxf(m[e], m[e + w]);
+        }
+        const uint32_t code = e8m0_ceil_code(m[0]);
+        const float inv = e8m0_inv_scale(code);
+        uint32_t w8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          w8[e] = cvt_e4m3x2(__fmul_rn(xs[4 * e], inv), __fmul_rn(xs[4 * e + 1], inv)) |
+                  (cvt_e4m3x2(__fmul_rn(xs[4 * e + 2], inv), __fmul_rn(xs[4 * e + 3], inv)) << 16);
+        if (row_ok && kk < k) {
+          uint4* dst = reinterpret_cast<uint4*>(q + row_g * k + kk);
+          dst[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+          dst[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+        }
+        // block 4w + i of the unit is held by lane 4w + i; scale word w gathers lanes 4w .. 4w + 3
+        const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 1);
+        const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 2);
+        const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 3);
+        if ((lane & 3) == 0) {
+          const int64_t kb = static_cast<int64_t>(kc) * 32 + lane;
+          if ((kb >> 2) < kt_n) {
+            const uint64_t off = sf_offset(r, kb, l, mt_n, kt_n);
+            *reinterpret_cast<uint32_t*>(sf + off) = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+          }
+        }
+      }
+    }
+  }
+}
+
 // NVFP4: a unit is 512 consecutive values of one row and lane i owns its block i (16 values:
 // four float4 loads of fp32, or two 16-byte loads of bf16), so the block maximum and the scale
 // decision are made once per block with no shuffle, and the lane's 16 codes leave as one 64-bit
 // store.  The 32 scale bytes of a unit are eight 32-bit words of the atom layout, gathered from
 // lanes 4w .. 4w + 3 and stored by lane 4w.
-// One lane's block of 16 inputs: raw loads kept in flight, widened to fp32 when processed.
-template <typename TIn>
-struct Block16;
-template <>
-struct Block16<float> {
-  float4 a[4];
-  __device__ __forceinline__ void load(const float* p, bool ok) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      a[i] = ok ? __ldcs(reinterpret_cast<const float4*>(p) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  __device__ __forceinline__ void widen(float (&v)[16]) const {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[4 * i] = a[i].x; v[4 * i + 1] = a[i].y; v[4 * i + 2] = a[i].z; v[4 * i + 3] = a[i].w;
-    }
-  }
-};
-template <>
-struct Block16<__nv_bfloat16> {
-  uint4 a[2];
-  __device__ __forceinline__ void load(const __nv_bfloat16* p, bool ok) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) a[i] = ok ? __ldcs(reinterpret_cast<const uint4*>(p) + i) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  __device__ __forceinline__ void widen(float (&v)[16]) const {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float4 lo = bf16x4_to_float4(a[i].x, a[i].y), hi = bf16x4_to_float4(a[i].z, a[i].w);
-      v[8 * i] = lo.x; v[8 * i + 1] = lo.y; v[8 * i + 2] = lo.z; v[8 * i + 3] = lo.w;
-      v[8 * i + 4] = hi.x; v[8 * i + 5] = hi.y; v[8 * i + 6] = hi.z; v[8 * i + 7] = hi.w;
-    }
-  }
-};
-
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __restrict__ x, int64_t rows, int k,
                                                                   uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
@@ -203,7 +268,7 @@ __global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __r
     const int64_t row_g = l * rows + r;
     const TIn* xr = x + row_g * k;
     for (int kc0 = 0; kc0 < units_per_row; kc0 += kU) {
-      Block16<TIn> raw[kU];
+      BlockIn<TIn, 16> raw[kU];
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const int kk = (kc0 + j) * 512 + lane * 16;
@@ -295,7 +360,7 @@ cudaError_t launch_quantize(int fmt, const void* x, bool x_bf16, int64_t batch, 
   const int64_t mt_n = (rows + 127) / 128;
   const int64_t kt_n = (k / v + 3) / 4;
   const int64_t rows_padded = mt_n * 128;
-  const int units_per_row = static_cast<int>((k + 127) / 128);
+  const int units_per_row = static_cast<int>((k + 1023) / 1024);  // bf16 MXFP8 units
   const int64_t total_rows = batch * rows_padded;
   int64_t blocks = (total_rows + (kThreads / 32) - 1) / (kThreads / 32);
   const int64_t max_blocks = static_cast<int64_t>(num_sms) * 8;
@@ -307,10 +372,10 @@ cudaError_t launch_quantize(int fmt, const void* x, bool x_bf16, int64_t batch, 
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (fmt == kMXFP8 && !x_bf16) {
     quantize_mxfp8_kernel<<<grid, kThreads, 0, stream>>>(xf, rows, static_cast<int>(k), q, sf, rows_padded,
-                                                         units_per_row, total_rows, mt_n, kt_n);
+                                                         static_cast<int>((k + 127) / 128), total_rows, mt_n, kt_n);
   } else if (fmt == kMXFP8) {
-    quantize_mxfp8_kernel<<<grid, kThreads, 0, stream>>>(xb, rows, static_cast<int>(k), q, sf, rows_padded,
-                                                         units_per_row, total_rows, mt_n, kt_n);
+    quantize_mxfp8_bf16_kernel<<<grid, kThreads, 0, stream>>>(xb, rows, static_cast<int>(k), q, sf, rows_padded,
+                                                              units_per_row, total_rows, mt_n, kt_n);
   } else if (!x_bf16) {
     quantize_nvfp4_kernel<<<grid, kThreads, 0, stream>>>(xf, rows, static_cast<int>(k), q, sf, rows_padded,
                                                          units_nvfp4, total_rows, mt_n, kt_n);
