@@ -82,7 +82,7 @@ struct GemmTraits {
   static constexpr int kAmaxBytes = epi_is_grouped(EPI) ? 4096 : 1024;
   // one transpose block per epilogue warp: 32 rows x 64 bytes (grouped), 32 x 32 bytes (RoPE)
   static constexpr int kXposeBlock = EPI == kEpiRope ? 1024 : kXposeBlockBytes;
-  static constexpr int kXposeBytes = EPI == kEpiDense ? 0 : 8 * kXposeBlock;
+  static constexpr int kXposeBytes = 8 * kXposeBlock;
   // shared-memory ring: as many stages as fit, at most six
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
@@ -282,9 +282,11 @@ __device__ __forceinline__ void xpose_rows64(uint8_t* s_blk, const uint4 (&v)[4]
 
 // Stores this thread's 32 fp32 values v (one row chunk) as f32 / bf16 / f16 at element column
 // col0 of the warp's rows row0 .. row0 + 31 of a row-major array of `ld` elements per row and
-// `n` valid columns, through the transpose block (see store_rows64).
+// `n` valid columns (rows at or past row_end are not written), through the transpose block (see
+// store_rows64).
 __device__ __forceinline__ void store_block_coalesced(uint8_t* s_blk, void* base, int kind, int ld, int n, int row0,
-                                                      int col0, const float (&v)[32], int lane) {
+                                                      int col0, const float (&v)[32], int lane,
+                                                      int row_end = 1 << 30) {
   if (kind == kOutF32) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -293,7 +295,7 @@ __device__ __forceinline__ void store_block_coalesced(uint8_t* s_blk, void* base
       for (int j = 0; j < 4; ++j)
         u[j] = make_uint4(__float_as_uint(v[16 * h + 4 * j]), __float_as_uint(v[16 * h + 4 * j + 1]),
                           __float_as_uint(v[16 * h + 4 * j + 2]), __float_as_uint(v[16 * h + 4 * j + 3]));
-      store_rows64(s_blk, base, static_cast<uint64_t>(ld) * 4, row0, (col0 + 16 * h) * 4, n * 4, u, lane);
+      store_rows64(s_blk, base, static_cast<uint64_t>(ld) * 4, row0, (col0 + 16 * h) * 4, n * 4, u, lane, row_end);
     }
   } else {
     const bool bf = kind == kOutBF16;
@@ -306,7 +308,7 @@ __device__ __forceinline__ void store_block_coalesced(uint8_t* s_blk, void* base
                 : make_uint4(pack_f16x2(w[0], w[1]), pack_f16x2(w[2], w[3]), pack_f16x2(w[4], w[5]),
                              pack_f16x2(w[6], w[7]));
     }
-    store_rows64(s_blk, base, static_cast<uint64_t>(ld) * 2, row0, col0 * 2, n * 2, u, lane);
+    store_rows64(s_blk, base, static_cast<uint64_t>(ld) * 2, row0, col0 * 2, n * 2, u, lane, row_end);
   }
 }
 
@@ -745,39 +747,36 @@ __device__ __forceinline__ void epilogue_tile_rope(const GemmParams& p, int row,
 }
 
 // Dense amax without a cleared output: every CTA (one thread) folds its maximum into the
-// workspace accumulator, then counts itself finished; the CTA that completes the count reads the
-// accumulator and writes *p.amax.  Both words are tagged with the call's epoch, so values a
-// previous call left behind are replaced rather than combined; the last CTA also zeroes them
-// under this epoch, so a replay of the same call (a CUDA graph) starts from zero too.
+// workspace record and counts itself finished with one 128-bit compare-and-swap (lo = epoch << 32
+// | count, hi = maximum bits; non-negative floats order like their bit patterns).  A record with
+// another epoch is a previous call's and is replaced.  The CTA whose swap completes the count
+// holds the final maximum in its own result: it writes *p.amax and resets the record under this
+// epoch (count and maximum zero), so a replay of the same call (a CUDA graph) starts from zero.
 __device__ __forceinline__ void dense_amax_finalize(const GemmParams& p, float cta_max) {
-  uint8_t* ws = reinterpret_cast<uint8_t*>(p.err);
-  unsigned long long* done = reinterpret_cast<unsigned long long*>(ws + kWsDoneByte);
-  unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws + kWsAmaxByte);
-  const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
-  if (cta_max > 0.0f) {
-    // non-negative floats order like their bit patterns
-    const uint32_t v = __float_as_uint(cta_max);
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(acc), assumed;
-    do {
-      assumed = old;
-      const bool mine = (assumed >> 32) == p.epoch;
-      const uint32_t cur = mine ? static_cast<uint32_t>(assumed) : 0u;
-      if (mine && cur >= v) break;
-      old = atomicCAS(acc, assumed, tag | (v > cur ? v : cur));
-    } while (old != assumed);
+  void* rec = reinterpret_cast<uint8_t*>(p.err) + kWsAmaxRecordByte;
+  const uint64_t tag = static_cast<uint64_t>(p.epoch) << 32;
+  const uint32_t v = cta_max > 0.0f ? __float_as_uint(cta_max) : 0u;
+  const volatile uint64_t* rv = reinterpret_cast<const volatile uint64_t*>(rec);
+  uint64_t lo = rv[0], hi = rv[1];  // a guess: a torn or stale read only costs one more round
+  uint64_t new_lo, new_hi;
+  for (;;) {
+    const bool mine = (lo >> 32) == p.epoch;
+    const uint32_t count = mine ? static_cast<uint32_t>(lo) : 0u;
+    const uint32_t cur = mine ? static_cast<uint32_t>(hi) : 0u;
+    new_lo = tag | (count + 1u);
+    new_hi = v > cur ? v : cur;
+    uint64_t old_lo, old_hi;
+    atomic_cas_b128(rec, lo, hi, new_lo, new_hi, old_lo, old_hi);
+    if (old_lo == lo && old_hi == hi) break;
+    lo = old_lo;
+    hi = old_hi;
   }
-  __threadfence();
-  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(done), assumed, nv;
-  do {
-    assumed = old;
-    nv = ((assumed >> 32) == p.epoch) ? assumed + 1 : (tag | 1ull);
-    old = atomicCAS(done, assumed, nv);
-  } while (old != assumed);
-  if (static_cast<uint32_t>(nv) == gridDim.x) {
-    __threadfence();
-    const unsigned long long a = atomicExch(acc, tag);  // read and zero under this epoch
-    p.amax[0] = (a >> 32) == p.epoch ? __uint_as_float(static_cast<uint32_t>(a)) : 0.0f;
-    atomicExch(done, tag);
+  if (static_cast<uint32_t>(new_lo) == gridDim.x) {
+    p.amax[0] = __uint_as_float(static_cast<uint32_t>(new_hi));
+    // every other CTA of this call has swapped already: a plain store resets the record
+    volatile uint64_t* w = reinterpret_cast<volatile uint64_t*>(rec);
+    w[1] = 0;
+    w[0] = tag;
   }
 }
 
@@ -824,10 +823,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int l, int ro
     if (EPI == kEpiDense) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) run_max = fmaxf(run_max, fabsf(__uint_as_float(r[j])));
-      if (row_ok) {
-        float v[32];
+      float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      if (p.c_kind == kOutF32 || p.c_kind == kOutBF16 || p.c_kind == kOutF16) {
+        // whole rows of the warp's 32 x 32 block through the transpose block (coalesced)
+        const int esz = p.c_kind == kOutF32 ? 4 : 2;
+        void* batch = static_cast<uint8_t*>(p.c) + static_cast<uint64_t>(l) * p.m * p.n * esz;
+        store_block_coalesced(s_blk, batch, p.c_kind, p.n, p.n, row - lane, col0, v, lane, p.m);
+      } else if (row_ok) {
         store_row32(p.c, (static_cast<uint64_t>(l) * p.m + row) * static_cast<uint64_t>(p.n) + col0, p.c_kind, v,
                     col0, p.n);
       }
@@ -1299,7 +1303,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       const TileCoord tc = decode_tile<EPI>(p, t, s_offs);
       const int row = tc.mt * kTileM + quad * 32 + lane;
       if constexpr (epi_is_dswiglu(EPI)) prefetch_dswiglu_c<BN>(p, row, tc.nt * BN, half, 2);
-      if (!wait_bounded(&tmem_full[acc], acc_phase, abort_flag, es)) break;
+      // warp-uniform outcome: the epilogues use whole-warp shuffles and syncs
+      if (!__all_sync(0xffffffffu, wait_bounded(&tmem_full[acc], acc_phase, abort_flag, es))) break;
       tc_fence_after();
       float alpha_g = 1.0f, prob_r = 0.0f;
       if (epi_is_grouped(EPI)) {
@@ -1329,8 +1334,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                                                          s_xpose + (warp - 2) * T::kXposeBlock);
         release();
       } else if (EPI == kEpiDense && p.c_kind == kOutBF16) {
-        epilogue_dense_bf16_early<BN, false>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release, nullptr,
-                                             lane);
+        epilogue_dense_bf16_early<BN, true>(p, tc.l, row, tc.nt * BN, tmem_acc, half, run_max, release,
+                                            s_xpose + (warp - 2) * T::kXposeBlock, lane);
       } else {
         epilogue_tile<BN, EPI>(p, tc.l, row, tc.nt * BN, tmem_acc, lane, alpha_g, prob_r, nc, run_max, half, 2,
                                s_amax + (warp - 2) * 32, s_xpose + (warp - 2) * T::kXposeBlock);

@@ -10,13 +10,13 @@ namespace bsg {
 // Bytes of the per-call scratch every GEMM entry point needs (the device error word and the
 // words next to it); bsg_workspace_size() returns it.
 constexpr size_t kWorkspaceBytes = 256;
-// Byte offsets in it: 0-11 the device error record (ErrSink in common.cuh); 16-23 the dense
-// kernel's count of finished CTAs and 24-31 its amax accumulator, each a 32-bit value tagged with
-// the call's epoch in the high word (so no call has to clear them first).
+// Byte offsets in it: 0-11 the device error record (ErrSink in common.cuh); 16-31 the dense
+// kernel's amax record: the call's epoch, the count of finished CTAs and the running maximum
+// (32 bits each, one unused), updated together by one 128-bit compare-and-swap, so a record a
+// previous call left behind is recognised by its epoch and no call has to clear it first.
 // Word 3 (bytes 12-15): set to the call's epoch by the per-expert descriptor kernel when a weight
 // pointer is invalid; the GEMM kernel then computes nothing.
-constexpr int kWsDoneByte = 16;
-constexpr int kWsAmaxByte = 24;
+constexpr int kWsAmaxRecordByte = 16;
 constexpr int kWsBadPointersWord = 3;
 
 // A fresh nonzero tag for the next call's device-side records (process-wide counter).

@@ -441,6 +441,22 @@ __device__ __forceinline__ void warp_commit_pair(uint64_t* bar) {
       : "memory");
 }
 
+// 128-bit compare-and-swap on global memory (16-byte aligned): returns the previous value as
+// (lo, hi) 64-bit halves; the swap happened iff it equals (cmp_lo, cmp_hi).
+__device__ __forceinline__ void atomic_cas_b128(void* addr, uint64_t cmp_lo, uint64_t cmp_hi, uint64_t new_lo,
+                                                uint64_t new_hi, uint64_t& old_lo, uint64_t& old_hi) {
+  asm volatile(
+      "{\n\t.reg .b128 d, c, n;\n\t"
+      "mov.b128 c, {%2, %3};\n\t"
+      "mov.b128 n, {%4, %5};\n\t"
+      "atom.global.cas.b128 d, [%6], c, n;\n\t"
+      "mov.b128 {%0, %1}, d;\n\t"
+      "}\n"
+      : "=l"(old_lo), "=l"(old_hi)
+      : "l"(cmp_lo), "l"(cmp_hi), "l"(new_lo), "l"(new_hi), "l"(addr)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- conversions
 
 // Two fp32 -> packed E4M3 (round to nearest even, saturate to +-448); `lo` in bits 0-7.
