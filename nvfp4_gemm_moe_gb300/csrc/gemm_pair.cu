@@ -1,4 +1,4 @@
-// gemm_pair.cu -- instantiations of the CTA-pair (256 x 256 tile) GEMM kernel.
+// gemm_pair.cu -- instantiations of the CTA-pair GEMM kernel (256 x 256 and 256 x 224 tiles): dense and grouped.
 #include "gemm_pair_kernel.cuh"
 
 namespace bsg {
