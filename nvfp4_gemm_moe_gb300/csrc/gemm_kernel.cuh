@@ -1377,6 +1377,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   }
 }
 
+// The fewest CTAs (or CTA pairs) that still take `tiles` tiles in as many rounds as `grid` does:
+// with static round-robin tiles the launch takes ceil(tiles / grid) tile times either way, and a
+// full last round leaves the SMs that would only idle through it out of the launch.
+inline int balanced_grid(int64_t tiles, int grid) {
+  if (tiles < 1 || grid < 1) return grid < 1 ? 1 : grid;
+  const int64_t rounds = (tiles + grid - 1) / grid;
+  return static_cast<int>((tiles + rounds - 1) / rounds);
+}
+
 template <int FMT, int BN, int EPI>
 cudaError_t launch_gemm_t(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const GemmParams& p, int grid,
                           cudaStream_t stream) {
@@ -1393,6 +1402,7 @@ cudaError_t launch_gemm_t(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
+  grid = balanced_grid(p.num_tiles, grid);
   kern<<<grid, kThreadsGemm, T::kSmemBytes, stream>>>(tmap_a, tmap_b, p);
   return cudaGetLastError();
 }

@@ -500,6 +500,8 @@ cudaError_t launch_gemm_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, con
   }
   int pairs = max_pairs < resident ? max_pairs : resident;
   if (pairs < 1) pairs = 1;
+  // as few pairs as take the tiles in the same number of rounds
+  pairs = balanced_grid(p.num_tiles, pairs);
   // output maps only for the TMA-store epilogue; otherwise the kernel never reads them
   kern<<<2 * pairs, kThreadsGemm, T::kSmemBytes, stream>>>(ta, tb, tc ? *tc : ta, td ? *td : ta, p);
   return cudaGetLastError();
