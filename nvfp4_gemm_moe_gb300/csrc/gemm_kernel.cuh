@@ -710,12 +710,54 @@ __device__ __forceinline__ void rope_rotary_pair(const GemmParams& p, int row, u
   store_e4m3_block<true>(p, row, dcol0 + 32, p.n, hi, lane, s_inv, s_blk);
 }
 
+// One output block of a head's rotary pair: out[j] (kHi = false, output columns dcol0 ..
+// dcol0 + 31) or out[32 + j] (kHi, dcol0 + 32 .. dcol0 + 63) for the 32 interleaved pairs of both
+// rotary chunks (formulas as in rope_rotary_pair, the same products), then the block is quantised
+// by rows and columns.  The two halves of a quadrant's warps take one block each.
+template <bool kHi>
+__device__ __forceinline__ void rope_rotary_block(const GemmParams& p, int row, uint32_t tmem_chunk, int dcol0,
+                                                  int lane, float* s_inv, uint8_t* s_blk) {
+  uint32_t r0[32], r1[32];
+  tmem_ld_32x32b_x32(tmem_chunk, r0);
+  tmem_ld_32x32b_x32(tmem_chunk + 32, r1);
+  tmem_ld_wait(r0);
+  tmem_ld_wait(r1);
+  const int t0 = kHi ? 32 : 0;  // the block's cos / sin columns
+  const uint16_t* cs = p.rope_cos + static_cast<uint64_t>(row) * p.qk_rope + t0;
+  const uint16_t* sn = p.rope_sin + static_cast<uint64_t>(row) * p.qk_rope + t0;
+  float out[32];
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const uint32_t(&src)[32] = g == 0 ? r0 : r1;  // pairs j = 16 g .. 16 g + 15
+    uint4 cv[2], sv[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      cv[i] = __ldg(reinterpret_cast<const uint4*>(cs + 16 * g) + i);
+      sv[i] = __ldg(reinterpret_cast<const uint4*>(sn + 16 * g) + i);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const uint4& c4 = cv[jj >> 3];
+      const uint4& s4 = sv[jj >> 3];
+      const int w = (jj >> 1) & 3, hw = jj & 1;  // 32-bit word and 16-bit half within the uint4
+      const uint32_t wc = w == 0 ? c4.x : w == 1 ? c4.y : w == 2 ? c4.z : c4.w;
+      const uint32_t ws = w == 0 ? s4.x : w == 1 ? s4.y : w == 2 ? s4.z : s4.w;
+      const float c = bf16_bits_to_float(hw ? wc >> 16 : wc & 0xffffu);
+      const float sv1 = bf16_bits_to_float(hw ? ws >> 16 : ws & 0xffffu);
+      const float a = __uint_as_float(src[2 * jj]);
+      const float b = __uint_as_float(src[2 * jj + 1]);
+      out[16 * g + jj] = kHi ? fmaf(b, c, a * sv1) : fmaf(a, c, -b * sv1);
+    }
+  }
+  store_e4m3_block<true>(p, row, dcol0 + t0, p.n, out, lane, s_inv, s_blk);
+}
+
 // GEMM + RoPE + MXFP8 epilogue of one tile ("GEMM + RoPE + MXFP8 Projection (SM100)",
 // Equations) for the rows (tokens) of one warp: output columns col_base .. col_base + BN - 1
 // of the (tokens, heads x 192) projection.  Global 32-column chunk g is chunk g % 6 of head
 // g / 6; chunks 4 and 5 of a head are rotary (RoPE, rope_rotary_pair), the rest pass unchanged.
-// BN = 192 (one head per tile): half 0 of a quadrant's warps takes chunks 0-2, half 1 chunk 3
-// and the rotary pair.  BN = 256: the tile's chunks go in pairs (0,1), (2,3), (4,5), (6,7), half
+// BN = 192 (one head per tile): half 0 of a quadrant's warps takes chunks 0-1 and the rotary
+// pair's first output block, half 1 chunks 2-3 and its second block (equal work).  BN = 256: the tile's chunks go in pairs (0,1), (2,3), (4,5), (6,7), half
 // 0 taking the first and third, half 1 the others; a pair starts at an even global chunk, so
 // it is either two plain chunks or one head's rotary pair (g % 6 == 4), never split.
 template <int BN>
@@ -724,13 +766,11 @@ __device__ __forceinline__ void epilogue_tile_rope(const GemmParams& p, int row,
   static_assert(BN == 192 || BN == 256, "RoPE tiles");
   if constexpr (BN == 192) {
     // col_base = head * 192: chunks 0-3 plain, 4-5 rotary
-    if (half == 0) {
+    const int c0 = 2 * half;
 #pragma unroll 1
-      for (int c = 0; c < 3; ++c) rope_plain_chunk(p, row, tmem_acc + c * 32, col_base + c * 32, lane, s_inv, s_blk);
-    } else {
-      rope_plain_chunk(p, row, tmem_acc + 3 * 32, col_base + 3 * 32, lane, s_inv, s_blk);
-      rope_rotary_pair(p, row, tmem_acc + 4 * 32, col_base + 4 * 32, lane, s_inv, s_blk);
-    }
+    for (int c = c0; c < c0 + 2; ++c) rope_plain_chunk(p, row, tmem_acc + c * 32, col_base + c * 32, lane, s_inv, s_blk);
+    if (half == 0) rope_rotary_block<false>(p, row, tmem_acc + 4 * 32, col_base + 4 * 32, lane, s_inv, s_blk);
+    else rope_rotary_block<true>(p, row, tmem_acc + 4 * 32, col_base + 4 * 32, lane, s_inv, s_blk);
   } else {
 #pragma unroll 1
     for (int q = half; q < 4; q += 2) {
