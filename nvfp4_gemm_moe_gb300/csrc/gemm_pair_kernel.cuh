@@ -71,10 +71,13 @@ struct PairTraits {
   static constexpr bool kOutTma = EPI == kEpiGroupedBF16 && BN == 256;
   static constexpr int kXposeBlock = kOutTma ? 2 * kXposeBlockBytes : kXposeBlockBytes;
   static constexpr int kXposeBytes = 8 * kXposeBlock;
-  // shared-memory ring: as many stages as fit, at most six
+  // shared-memory ring: as many stages as fit, at most six (five for RoPE tiles)
   static constexpr int kStagesSmem =
       (232448 - 1024 - kBarBytes - kOffsetsBytes - kAmaxBytes - kXposeBytes) / kStageBytes;
-  static constexpr int kStages = kStagesSmem < 6 ? kStagesSmem : 6;
+  // the RoPE tiles stop at five (measured faster: their epilogue reads the cos / sin rows through
+  // L1, which gets the shared memory a sixth stage would take)
+  static constexpr int kMaxStages = EPI == kEpiRope ? 5 : 6;
+  static constexpr int kStages = kStagesSmem < kMaxStages ? kStagesSmem : kMaxStages;
   static_assert(kStages >= 3, "pipeline depth");
   // TMEM scale-factor slots: one per stage when TMEM has room, else fewer, recycled through the
   // sf_free barriers (the two-accumulator tiles leave room for only four)
