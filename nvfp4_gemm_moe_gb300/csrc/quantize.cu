@@ -252,10 +252,12 @@ __global__ void __launch_bounds__(kThreads)
 // store.  The 32 scale bytes of a unit are eight 32-bit words of the atom layout, gathered from
 // lanes 4w .. 4w + 3 and stored by lane 4w.
 template <typename TIn>
-__global__ void __launch_bounds__(kThreads) quantize_nvfp4_kernel(const TIn* __restrict__ x, int64_t rows, int k,
-                                                                  uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                                  int64_t rows_padded, int units_per_row,
-                                                                  int64_t total_rows, int64_t mt_n, int64_t kt_n) {
+// fp32 input: four blocks resident per SM (64 registers, 72 without the bound; measured 10 %
+// faster: more loads in flight); bf16 input: two (its 4-unit items need the registers)
+__global__ void __launch_bounds__(kThreads, sizeof(TIn) == 4 ? 4 : 2)
+    quantize_nvfp4_kernel(const TIn* __restrict__ x, int64_t rows, int k, uint8_t* __restrict__ q,
+                          uint8_t* __restrict__ sf, int64_t rows_padded, int units_per_row, int64_t total_rows,
+                          int64_t mt_n, int64_t kt_n) {
   // units in flight per warp: 4 KB of fp32 loads (two units) or of bf16 loads (four)
   constexpr int kU = sizeof(TIn) == 4 ? 2 : 4;
   const int lane = threadIdx.x & 31;
