@@ -104,7 +104,9 @@ typedef enum bsg_sf_dtype {
 typedef struct bsg_gemm_opts {
   int tile_n;            /* output tile width: 0 = automatic, else 128 or 256 (MXFP8 also 192 or
                             224: two accumulators in TMEM); other values mean automatic */
-  int max_ctas;          /* 0 = one persistent CTA per SM, else at most this many CTAs */
+  int max_ctas;          /* 0 = up to one persistent CTA per SM, else at most this many CTAs; the
+                            launch uses the fewest CTAs (CTA pairs) that take the tiles in the
+                            same number of rounds */
   int tanh_approx;       /* grouped only: 1 = tanh.approx.f32 in the soft clamp, 0 = tanhf */
   int validate_offsets;  /* grouped only: 1 = copy padded_offsets to the host and check them
                             before launching (synchronises the stream) */
